@@ -1,0 +1,115 @@
+"""fp64 CPU oracle for fused candidate scoring -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never calls it and
+shares no code with it; the only thing both sides share is the seeded input
+generator in ``similarity_softmax_candidate_gb300.workloads``, which holds
+none of the method's arithmetic.
+
+The arithmetic lives in ``oracle.c`` (plain loops, double accumulation in
+index order). This module compiles it with gcc, loads it with ctypes and
+wraps it for numpy arrays.
+
+Method source: PR #69 "cuda: add a fused candidate-scoring kernel for CLM
+and Kev" (the opening table of the two models' similarities, and the section
+"What is fused, precisely"). Parity pins: tests/test_oracle_pins.py and the
+hand cases under tests/golden/.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+#: The norm clamp of the cosine similarity. The page gives no value; each
+#: norm is clamped on its own at this floor (plainest cosine convention).
+EPS = 1e-8
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, no fast-math,
+    no FMA contraction so the rounding is the same on x86 and Arm)."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fno-fast-math", "-ffp-contract=off",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            f, d, l, i, p = (ctypes.c_void_p, ctypes.c_double, ctypes.c_long,
+                             ctypes.c_int, ctypes.c_void_p)
+            lib.oracle_logits.argtypes = [f, f, l, l, l, i, d, d, d, p]
+            lib.oracle_logits.restype = i
+            lib.oracle_softmax.argtypes = [p, l, l, p]
+            lib.oracle_softmax.restype = i
+            lib.oracle_score_batch.argtypes = [f, f, l, l, l, i, d, d, d, p]
+            lib.oracle_score_batch.restype = i
+            _lib = lib
+    return _lib
+
+
+def _shapes(Q, C):
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    if Q.ndim == 1:
+        Q = Q[None, :]
+    if C.ndim == 2:
+        C = C[None, :, :]
+    B, D = Q.shape
+    if C.shape[0] != B or C.shape[2] != D:
+        raise ValueError(f"shape mismatch: Q {Q.shape}, C {C.shape}")
+    return Q, C, B, C.shape[1], D
+
+
+def logits(Q, C, normalize, scale, temperature, eps=EPS):
+    """Similarity logits z[B,K] (float64) for Q[B,D] (or q[D]) and
+    C[B,K,D] (or C[K,D])."""
+    Q, C, B, K, D = _shapes(Q, C)
+    z = np.empty((B, K), dtype=np.float64)
+    rc = _load().oracle_logits(Q.ctypes.data, C.ctypes.data, B, K, D, int(normalize),
+                               float(scale), float(temperature), float(eps), z.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_logits: bad size")
+    return z
+
+
+def softmax(z):
+    """Row-wise softmax of z[B,K] (or z[K]) in float64."""
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    one = z.ndim == 1
+    z2 = z[None, :] if one else z
+    p = np.empty_like(z2)
+    rc = _load().oracle_softmax(z2.ctypes.data, z2.shape[0], z2.shape[1], p.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_softmax: bad size")
+    return p[0] if one else p
+
+
+def score_batch(Q, C, normalize, scale, temperature, eps=EPS):
+    """Softmax probabilities p[B,K] (float64) of the whole readout."""
+    Q, C, B, K, D = _shapes(Q, C)
+    p = np.empty((B, K), dtype=np.float64)
+    rc = _load().oracle_score_batch(Q.ctypes.data, C.ctypes.data, B, K, D, int(normalize),
+                                    float(scale), float(temperature), float(eps), p.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_score_batch: bad size")
+    return p
