@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark of fused candidate scoring on GB300.
+
+Headline workload: 16384 questions, K=255 candidates of D=512 float32
+features each (8.6 GB of candidates, larger than the 129 MB L2), CLM cosine
+scoring with scale 1/0.07 and temperature 1, scored as four launches over
+consecutive slices of 4096 questions. One "step" is those four launches.
+The same workload is also timed with Kev dot scoring (scale 1/16).
+
+Printed on one JSON line (rank 0):
+  value      questions/s of the whole job, inputs resident in HBM
+  e2e        the same metric with inputs streamed from pinned host memory
+             and the probabilities copied back, every step
+  roofline   the streaming kernel's algorithmic bytes per launch / its mean
+             launch time (CUDA events on its stream), against the measured
+             HBM copy bandwidth
+  cpu_baseline  the fp64 oracle timed on a bounded sample on the host cores
+  extra      dot scoring, and single-question latency (us/call, direct and
+             CUDA-graph replay) for the page's five shapes
+
+--impl reference times the fp64 oracle (the only reference there is) on
+bounded samples of the same workload, on the host cores.
+
+Under torchrun each rank runs the whole workload on its own GPU (replicas:
+questions are independent, there is nothing to exchange); timing is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+B_TOTAL = 16384
+CHUNK = 4096
+K = 255
+D = 512
+BYTES_PER_QUESTION = 4 * (K * D + D + K)  # C row block + q read once, p written once
+
+# The page's five shapes (PR #69, "What it is worth"), RTX 4090 fused times in us.
+PAGE_SHAPES = [
+    ("clm-cosine-5x512", 1, 5, 512, 1, 9.2),
+    ("clm-cosine-64x512", 1, 64, 512, 1, 12.1),
+    ("clm-cosine-255x512", 1, 255, 512, 1, 23.6),
+    ("clm-cosine-batch8-255x512", 8, 255, 512, 1, 23.8),
+    ("kev-dot-255x2560", 1, 255, 2560, 0, 55.3),
+]
+
+METRIC = "questions/s (K=255, D=512, cosine, 16384 questions in 4 launches)"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peak_hbm():
+    path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _traffic_from_profile(kernel_src_sha):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(_ROOT, "profiles", "stream_kernel_throughput_k255_d512.txt")
+    try:
+        fields = {}
+        for line in open(path):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != kernel_src_sha:
+            return None
+        return float(fields["dram_bytes_per_4096_question_launch"])
+    except Exception:
+        return None
+
+
+def _kernel_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("kernels.cu", "internal.h"):
+        with open(os.path.join(_ROOT, "similarity_softmax_candidate_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during timed regions."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.windows = []
+        self.file = tempfile.NamedTemporaryFile(prefix="clocks_", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def window(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.close()
+        rows = []
+        import datetime
+        for line in open(self.file.name):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except Exception:
+                continue
+        os.unlink(self.file.name)
+        sel = [r for r in rows if any(a - 0.06 <= r[0] <= b + 0.06 for a, b in self.windows)] or rows
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in sel:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": sorted(reasons), "samples": len(sel)}
+
+
+def _time_oracle(sample_Q, sample_C, normalize, scale):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.score_batch(sample_Q, sample_C, normalize, scale, 1.0)
+    return time.perf_counter() - t0
+
+
+def _host_sample(n, seed=4):
+    """n questions of the throughput workload's shape and distribution,
+    drawn on the host (float32 N(0,1))."""
+    from similarity_softmax_candidate_gb300 import workloads
+    wl = workloads.random_case(n, K, D, 1, workloads.CLM_SCALE, seed, "cpu")
+    return wl.Q.numpy(), wl.C.numpy()
+
+
+def cpu_baseline(target_s=10.0):
+    """The oracle as it stands (single-threaded C, fp64) on a bounded sample."""
+    from similarity_softmax_candidate_gb300 import workloads
+    Qp, Cp = _host_sample(8)
+    t_probe = _time_oracle(Qp, Cp, 1, workloads.CLM_SCALE) / 8
+    n = int(max(8, min(2048, target_s / max(t_probe, 1e-6))))
+    Qs, Cs = _host_sample(n, seed=5)
+    dt = _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
+    return {"value": n / dt, "unit": "questions/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} questions of the K=255, D=512 cosine workload (host-drawn N(0,1)), "
+                      f"fp64 C oracle, single thread, {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    from similarity_softmax_candidate_gb300 import workloads
+    Qp, Cp = _host_sample(8)
+    t_q = _time_oracle(Qp, Cp, 1, workloads.CLM_SCALE) / 8
+    budget = 60.0
+    n = int(max(1, min(1024, budget / max(t_q, 1e-6) / max(1, args.steps + args.warmup))))
+    Qs, Cs = _host_sample(n, seed=6)
+    for _ in range(args.warmup):
+        _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
+    qps = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": qps, "unit": "questions/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"throughput: cosine, K={K}, D={D}; each step a bounded sample of {n} questions",
+                   "B": n, "K": K, "D": D},
+        "cpu_baseline": {"value": qps, "unit": "questions/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} questions per step, host-drawn N(0,1), fp64 C oracle, single thread"},
+        "e2e": {"value": qps, "unit": "questions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--latency-calls", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--skip-extra", action="store_true", help="only the headline throughput and its roofline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = _dist()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import similarity_softmax_candidate_gb300 as cs
+    from similarity_softmax_candidate_gb300 import _build, workloads
+    _build.build_library()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    wls = workloads.throughput(dev)
+    wl_cos, wl_dot = wls
+    out = torch.empty((B_TOTAL, K), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    plan = cs.cs_query_plan(wl_cos.Q[:CHUNK], wl_cos.C[:CHUNK], 1)
+
+    def step(wl):
+        for b0 in range(0, B_TOTAL, CHUNK):
+            cs.cs_score_candidates_batch(wl.Q[b0:b0 + CHUNK], wl.C[b0:b0 + CHUNK], wl.normalize, wl.scale,
+                                         wl.temperature, out=out[b0:b0 + CHUNK], stream=stream)
+
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local)
+    clocks.start()
+
+    def timed(wl):
+        for _ in range(args.warmup):
+            step(wl)
+        barrier()
+        n_launch = args.steps * (B_TOTAL // CHUNK)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_launch)]
+        t_wall = time.time()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        i = 0
+        for _ in range(args.steps):
+            for b0 in range(0, B_TOTAL, CHUNK):
+                ev[i].record(stream)
+                cs.cs_score_candidates_batch(wl.Q[b0:b0 + CHUNK], wl.C[b0:b0 + CHUNK], wl.normalize, wl.scale,
+                                             wl.temperature, out=out[b0:b0 + CHUNK], stream=stream)
+                ev[i + 1].record(stream)
+                i += 2
+        stop.record(stream)
+        barrier()
+        clocks.window(t_wall, time.time())
+        ms = max_over_ranks(start.elapsed_time(stop))
+        launch_ms = [ev[j].elapsed_time(ev[j + 1]) for j in range(0, 2 * n_launch, 2)]
+        return ms, launch_ms, n_launch
+
+    ms_cos, launches_cos, n_launch = timed(wl_cos)
+    ms_dot, launches_dot, _ = timed(wl_dot)
+    clock_info = clocks.stop()
+
+    ms_per_step = ms_cos / args.steps
+    value = world * B_TOTAL / (ms_per_step / 1e3)
+    peak, peak_kind = _peak_hbm()
+    launch_bytes = CHUNK * BYTES_PER_QUESTION
+    mean_launch_ms = sum(launches_cos) / len(launches_cos)
+    achieved = launch_bytes / (mean_launch_ms / 1e3) / 1e9
+    traffic = _traffic_from_profile(_kernel_sha())
+    dot_ms_step = ms_dot / args.steps
+    dot_launch_ms = sum(launches_dot) / len(launches_dot)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "questions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "throughput: 16384 questions x K=255 x D=512 fp32 N(0,1), CLM cosine "
+                               "(scale 1/0.07, T=1), 4 launches of 4096 questions per step",
+                   "B": B_TOTAL, "K": K, "D": D, "launches_per_step": B_TOTAL // CHUNK,
+                   "l2": "inputs (8.6 GB per rank) larger than L2 (129 MB); no flush",
+                   "plan": plan, "parallelism": f"replicas x{world}"},
+        "gpu_launches": n_launch,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "stream_kernel (STREAM plan), one launch = 4096 questions",
+                     "algorithmic_bytes_per_launch": launch_bytes, "mean_launch_ms": mean_launch_ms,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+        "clocks": clock_info,
+        "extra": {
+            "hbm_gbs_step": world * B_TOTAL * BYTES_PER_QUESTION / (ms_per_step / 1e3) / 1e9,
+            "frac_of_8tbs_nominal": achieved / 8000.0,
+            "dot": {"questions_per_s": world * B_TOTAL / (dot_ms_step / 1e3), "ms_per_step": dot_ms_step,
+                    "launch_gbs": launch_bytes / (dot_launch_ms / 1e3) / 1e9,
+                    "frac": launch_bytes / (dot_launch_ms / 1e3) / 1e9 / peak},
+        },
+    }
+
+    if not args.skip_extra:
+        line["extra"]["latency_b1"] = latency_table(cs, workloads, dev, args.latency_calls)
+        line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
+    del wls, wl_cos, wl_dot
+    torch.cuda.empty_cache()
+
+    if rank == 0:
+        try:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        except Exception as e:  # the oracle is optional for the GPU numbers
+            line["cpu_baseline"] = {"value": None, "unit": "questions/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {e}"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def latency_table(cs, workloads, dev, calls):
+    """us per call for the page's shapes: back-to-back direct calls, graph
+    replay of a one-call graph, and single calls with L2 flushed before each."""
+    import torch
+    rows = []
+    flush = torch.empty(64 * 1024 * 1024, device=dev)  # 256 MB > L2
+    for name, B, k, d, normalize, page_us in PAGE_SHAPES:
+        wl = workloads.random_case(B, k, d, normalize, workloads.CLM_SCALE if normalize else workloads.KEV_SCALE,
+                                   90 + k, dev)
+        out = torch.empty(B, k, device=dev)
+        s = torch.cuda.current_stream(dev)
+
+        def call():
+            if B == 1:
+                cs.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=out[0], stream=s)
+            else:
+                cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=s)
+
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(calls):
+                call()
+            b.record(s)
+            torch.cuda.synchronize()
+            reps.append(1e3 * a.elapsed_time(b) / calls)
+        direct = statistics.median(reps)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call_in = torch.cuda.current_stream(dev)
+            if B == 1:
+                cs.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=out[0], stream=call_in)
+            else:
+                cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=call_in)
+        for _ in range(20):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(calls):
+                g.replay()
+            b.record(s)
+            torch.cuda.synchronize()
+            reps.append(1e3 * a.elapsed_time(b) / calls)
+        graph = statistics.median(reps)
+        cold = []
+        for _ in range(200):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            call()
+            b.record(s)
+            torch.cuda.synchronize()
+            cold.append(1e3 * a.elapsed_time(b))
+        plan = cs.cs_query_plan(wl.Q, wl.C, normalize)
+        rows.append({"shape": name, "B": B, "K": k, "D": d, "direct_us": direct, "graph_us": graph,
+                     "cold_l2_us": statistics.median(cold), "plan": plan["plan"], "cluster": plan["cluster"],
+                     "ctas": plan["ctas"], "rtx4090_fused_us_context": page_us})
+        del g
+    return rows
+
+
+def e2e(cs, wl, dev, args, world, barrier, max_over_ranks):
+    """questions/s with the inputs in pinned host memory: every step copies
+    Q and C host->device (two chunk buffers, copies overlapped with compute
+    on a second stream) and the probabilities device->host."""
+    import torch
+    Qh = wl.Q.cpu().pin_memory()
+    Ch = torch.empty(wl.C.shape, dtype=torch.float32, pin_memory=True)
+    for b0 in range(0, B_TOTAL, CHUNK):
+        Ch[b0:b0 + CHUNK].copy_(wl.C[b0:b0 + CHUNK])
+    outh = torch.empty((B_TOTAL, K), dtype=torch.float32, pin_memory=True)
+    dQ = [torch.empty((CHUNK, D), device=dev) for _ in range(2)]
+    dC = [torch.empty((CHUNK, K, D), device=dev) for _ in range(2)]
+    dO = [torch.empty((CHUNK, K), device=dev) for _ in range(2)]
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+
+    def one_step():
+        n = B_TOTAL // CHUNK
+        for i in range(n):
+            j = i % 2
+            b0 = i * CHUNK
+            with torch.cuda.stream(copy):
+                if i >= 2:
+                    copy.wait_event(freed[j])
+                dQ[j].copy_(Qh[b0:b0 + CHUNK], non_blocking=True)
+                dC[j].copy_(Ch[b0:b0 + CHUNK], non_blocking=True)
+                loaded[j].record(copy)
+            comp.wait_event(loaded[j])
+            cs.cs_score_candidates_batch(dQ[j], dC[j], wl.normalize, wl.scale, wl.temperature, out=dO[j],
+                                         stream=comp)
+            outh[b0:b0 + CHUNK].copy_(dO[j], non_blocking=True)
+            freed[j].record(comp)
+        comp.synchronize()
+
+    for _ in range(2):
+        one_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one_step()
+    barrier()
+    dt = max_over_ranks(time.perf_counter() - t0)
+    h2d = (Qh.numel() + Ch.numel()) * 4
+    d2h = outh.numel() * 4
+    del Ch, Qh, outh, dQ, dC, dO
+    return {"value": world * B_TOTAL * args.e2e_steps / dt, "unit": "questions/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "h2d_gbs": h2d * args.e2e_steps / dt / 1e9}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

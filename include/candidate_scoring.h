@@ -1,0 +1,148 @@
+/*
+ * candidate_scoring.h -- C ABI of the GB300 (sm_103a) fused candidate-scoring
+ * library, libcandidate_scoring.so.
+ *
+ * The operation (PR #69 "cuda: add a fused candidate-scoring kernel for CLM
+ * and Kev"; its opening table gives the two similarities and "What is fused,
+ * precisely" the fusion): for each question b, given a query q_b[D] and K
+ * candidates C_b[K,D],
+ *
+ *   sim_k = cos(q_b, c_k)   normalize = 1  (CLM; each norm clamped at 1e-8)
+ *   sim_k = c_k . q_b       normalize = 0  (Kev)
+ *   z_k   = scale * sim_k / temperature
+ *   p_k   = exp(z_k - max_j z_j) / sum_j exp(z_j - max_j z_j)
+ *
+ * and only p is written: the similarities never reach global memory, and each
+ * candidate row is read from memory once (its dot with q and its squared norm
+ * come from the same load).
+ *
+ * Conventions shared by every entry point below:
+ *   - All array pointers are CUDA DEVICE pointers to float32 data the caller
+ *     owns (cudaMalloc, or a torch CUDA tensor). Host pointers are not
+ *     detected; passing one is undefined (the kernel faults).
+ *   - Layout is dense row-major: Q is [B][D], C is [B][K][D], out is [B][K].
+ *     out must not overlap Q or C. Inputs are only read.
+ *   - The work is queued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream). Calls are asynchronous: they never synchronize,
+ *     allocate, free or memset, and one call enqueues exactly one kernel, so
+ *     it captures into a CUDA graph as one node (PR #69, "Through a CUDA
+ *     Graph" and "Verified on hardware").
+ *   - The first call on a device does one-time set-up (kernel attributes and
+ *     an occupancy query); make one ordinary call per device before starting
+ *     a stream capture.
+ *   - Invalid arguments return a nonzero status BEFORE any CUDA call: nothing
+ *     is launched and out is untouched (PR #69, "Verified on hardware", the
+ *     rejected-arguments group). A failed launch returns CS_ERR_LAUNCH.
+ *     Faults inside the kernel surface, as usual in CUDA, at the caller's
+ *     next synchronizing call.
+ *   - Results are deterministic: the same call on the same device gives
+ *     bit-identical output, directly or replayed from a graph.
+ */
+#ifndef CANDIDATE_SCORING_H
+#define CANDIDATE_SCORING_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *cs_stream_t;
+
+/* Largest number of candidates per question. The softmax runs over an
+ * on-chip array of this many logits; a larger K is refused rather than
+ * truncated (PR #69, "Verified on hardware": scoring only the first 255
+ * would give a confident wrong answer). */
+#define CS_MAX_K 255
+
+typedef enum {
+    CS_OK = 0,
+    CS_ERR_NULL_POINTER = 1,   /* Q, C or out is NULL */
+    CS_ERR_K_ZERO = 2,         /* K <= 0: no candidates */
+    CS_ERR_K_TOO_LARGE = 3,    /* K > CS_MAX_K */
+    CS_ERR_D_ZERO = 4,         /* D <= 0 */
+    CS_ERR_BAD_SCALE = 5,      /* scale == 0, NaN or infinite */
+    CS_ERR_BAD_TEMPERATURE = 6,/* temperature <= 0, NaN or infinite */
+    CS_ERR_BAD_BATCH = 7,      /* B <= 0 */
+    CS_ERR_BAD_SIMILARITY = 8, /* normalize is neither 0 nor 1 */
+    CS_ERR_LAUNCH = 9,         /* a CUDA call failed; nothing useful was queued */
+    CS_ERR_ALIAS = 10,         /* out overlaps Q or C */
+    CS_ERR_TOO_LARGE = 11,     /* B*K*D elements do not fit the 64-bit index space */
+    CS_ERR_BAD_PLAN = 12       /* cs_score_candidates_batch_plan: plan not feasible */
+} cs_status;
+
+/* ABI version of this header and library: 1. */
+int cs_abi_version(void);
+
+/* Static English text for a status code (never NULL). */
+const char *cs_status_string(int status);
+
+/*
+ * One question: q[D], C[K][D] -> out[K]. Identical to
+ * cs_score_candidates_batch with B = 1.
+ *   normalize   1 = cosine (CLM), 0 = dot (Kev)
+ *   scale       multiplies the similarity; for CLM pass exp(logit_scale),
+ *               for Kev 1/sqrt(256). Any finite nonzero value.
+ *   temperature divides the scaled similarity; finite and > 0.
+ */
+int cs_score_candidates(const float *q, const float *C, int K, int D,
+                        int normalize, float scale, float temperature,
+                        float *out, cs_stream_t stream);
+
+/*
+ * B questions in one launch (a grid over questions, not a loop of launches;
+ * PR #69, "What is fused, precisely"): Q[B][D], C[B][K][D] -> out[B][K].
+ * K is the same for every question. Arguments as cs_score_candidates.
+ */
+int cs_score_candidates_batch(const float *Q, const float *C, int B, int K,
+                              int D, int normalize, float scale,
+                              float temperature, float *out,
+                              cs_stream_t stream);
+
+/* Execution plans (kernel choices) the library picks between. */
+#define CS_PLAN_AUTO 0
+#define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions */
+#define CS_PLAN_CLUSTER 2  /* one thread-block cluster per question, rows split */
+#define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment */
+
+/*
+ * The plan cs_score_candidates_batch would use for these arguments.
+ * Arguments are validated exactly as there (status on failure). On CS_OK,
+ * every non-NULL output pointer receives: plan (CS_PLAN_*), cluster (CTAs
+ * per cluster, 1 = none), ctas (CTAs launched), smem_bytes (dynamic shared
+ * memory per CTA). Needs a CUDA device (it queries the current one).
+ */
+int cs_query_plan(const float *Q, const float *C, int B, int K, int D,
+                  int normalize, int *plan, int *cluster, int *ctas,
+                  int *smem_bytes);
+
+/*
+ * cs_score_candidates_batch with the plan chosen by the caller, for tests
+ * and tuning. plan is CS_PLAN_*; cluster (CS_PLAN_CLUSTER: 1..16, at most
+ * K) and ctas (CS_PLAN_STREAM: 1..B) may be 0 for the automatic choice.
+ * Returns CS_ERR_BAD_PLAN when the plan cannot run these arguments (e.g.
+ * CS_PLAN_STREAM or CS_PLAN_CLUSTER with D % 4 != 0 or unaligned pointers).
+ * The result equals the automatic plan's within float32 rounding.
+ */
+int cs_score_candidates_batch_plan(const float *Q, const float *C, int B,
+                                   int K, int D, int normalize, float scale,
+                                   float temperature, float *out,
+                                   cs_stream_t stream, int plan, int cluster,
+                                   int ctas);
+
+/* Device status word bits (see cs_device_status). */
+#define CS_DEVERR_WAIT_TIMEOUT 1u  /* an on-chip wait gave up after ~1 s */
+
+/*
+ * Reads (and, if clear != 0, resets) the status word the kernels of this
+ * library set on the current device when one of their bounded waits gives
+ * up. A kernel that gives up stops early and leaves NaN in the results it
+ * could not finish. Synchronizes the device; not for the hot path.
+ */
+int cs_device_status(unsigned *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CANDIDATE_SCORING_H */

@@ -1,0 +1,191 @@
+"""Thin Python binding of libcandidate_scoring.so (ctypes).
+
+Argument marshalling only: every step of the readout runs in the library's
+CUDA kernels. Function names match the C ABI in include/candidate_scoring.h.
+Tensors must be float32, contiguous and on a CUDA device (a host buffer
+passed as a device pointer faults the kernel, the first defect listed in
+PR #69 "cuda: add a fused candidate-scoring kernel for CLM and Kev",
+"Defects the GPU found, in order"; the binding refuses one up front).
+
+If the library has not been built, every call raises: there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+CS_MAX_K = 255
+CS_PLAN_AUTO, CS_PLAN_STREAM, CS_PLAN_CLUSTER, CS_PLAN_GENERIC = 0, 1, 2, 3
+PLAN_NAMES = {CS_PLAN_STREAM: "stream", CS_PLAN_CLUSTER: "cluster", CS_PLAN_GENERIC: "generic"}
+
+STATUS = {
+    0: "CS_OK", 1: "CS_ERR_NULL_POINTER", 2: "CS_ERR_K_ZERO", 3: "CS_ERR_K_TOO_LARGE",
+    4: "CS_ERR_D_ZERO", 5: "CS_ERR_BAD_SCALE", 6: "CS_ERR_BAD_TEMPERATURE", 7: "CS_ERR_BAD_BATCH",
+    8: "CS_ERR_BAD_SIMILARITY", 9: "CS_ERR_LAUNCH", 10: "CS_ERR_ALIAS", 11: "CS_ERR_TOO_LARGE",
+    12: "CS_ERR_BAD_PLAN",
+}
+globals().update({name: code for code, name in STATUS.items()})
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CSError(RuntimeError):
+    """A nonzero cs_status from the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)} ({cs_status_string(self.status)})")
+
+
+def library() -> ctypes.CDLL:
+    """The loaded library with argument types declared. Raises RuntimeError
+    if it has not been built (call ``_build.build_library()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"{_build.LIB_NAME} is not built; run __graft_entry__.build() or "
+                               "python -m similarity_softmax_candidate_gb300._build")
+        lib = ctypes.CDLL(_build.LIB_PATH)
+        P, I, F, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_uint)
+        IP = ctypes.POINTER(ctypes.c_int)
+        lib.cs_abi_version.argtypes = []
+        lib.cs_abi_version.restype = I
+        lib.cs_status_string.argtypes = [I]
+        lib.cs_status_string.restype = ctypes.c_char_p
+        lib.cs_score_candidates.argtypes = [P, P, I, I, I, F, F, P, P]
+        lib.cs_score_candidates.restype = I
+        lib.cs_score_candidates_batch.argtypes = [P, P, I, I, I, I, F, F, P, P]
+        lib.cs_score_candidates_batch.restype = I
+        lib.cs_score_candidates_batch_plan.argtypes = [P, P, I, I, I, I, F, F, P, P, I, I, I]
+        lib.cs_score_candidates_batch_plan.restype = I
+        lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
+        lib.cs_query_plan.restype = I
+        lib.cs_device_status.argtypes = [U, I]
+        lib.cs_device_status.restype = I
+        _lib = lib
+        return lib
+
+
+def cs_abi_version() -> int:
+    return int(library().cs_abi_version())
+
+
+def cs_status_string(status: int) -> str:
+    return library().cs_status_string(int(status)).decode()
+
+
+def _check(t, name, ndim):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (host memory cannot be read by the kernel)")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def cs_score_candidates(q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
+    """One question: q[D], C[K,D] -> out[K] (float32, CUDA)."""
+    import torch
+    qp = _check(q, "q", 1)
+    cp = _check(C, "C", 2)
+    K, D = int(C.shape[0]), int(C.shape[1])
+    if q.shape[0] != D or q.device != C.device:
+        raise ValueError(f"q {tuple(q.shape)} does not match C {tuple(C.shape)}")
+    if out is None:
+        out = torch.empty(K, device=C.device, dtype=torch.float32)
+    op = _check(out, "out", 1)
+    if out.shape[0] != K or out.device != C.device:
+        raise ValueError(f"out must be [K={K}] on {C.device}")
+    with torch.cuda.device(C.device):
+        s = library().cs_score_candidates(qp, cp, K, D, int(normalize), float(scale), float(temperature),
+                                          op, _stream_handle(stream))
+    if s != 0:
+        raise CSError(s, "cs_score_candidates")
+    return out
+
+
+def _batch_ptrs(Q, C, out):
+    import torch
+    qp = _check(Q, "Q", 2)
+    cp = _check(C, "C", 3)
+    B, K, D = (int(x) for x in C.shape)
+    if tuple(Q.shape) != (B, D) or Q.device != C.device:
+        raise ValueError(f"Q {tuple(Q.shape)} does not match C {tuple(C.shape)}")
+    if out is None:
+        out = torch.empty((B, K), device=C.device, dtype=torch.float32)
+    op = _check(out, "out", 2)
+    if tuple(out.shape) != (B, K) or out.device != C.device:
+        raise ValueError(f"out must be [B={B}, K={K}] on {C.device}")
+    return qp, cp, op, out, B, K, D
+
+
+def cs_score_candidates_batch(Q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
+    """B questions: Q[B,D], C[B,K,D] -> out[B,K] (float32, CUDA), one launch."""
+    import torch
+    qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
+    with torch.cuda.device(C.device):
+        s = library().cs_score_candidates_batch(qp, cp, B, K, D, int(normalize), float(scale),
+                                                float(temperature), op, _stream_handle(stream))
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_batch")
+    return out
+
+
+def cs_score_candidates_batch_plan(Q, C, normalize: int, scale: float, temperature: float, plan: int,
+                                   cluster: int = 0, ctas: int = 0, out=None, stream=None):
+    """cs_score_candidates_batch with a caller-chosen plan (tests, tuning)."""
+    import torch
+    qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
+    with torch.cuda.device(C.device):
+        s = library().cs_score_candidates_batch_plan(qp, cp, B, K, D, int(normalize), float(scale),
+                                                     float(temperature), op, _stream_handle(stream),
+                                                     int(plan), int(cluster), int(ctas))
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_batch_plan")
+    return out
+
+
+def cs_query_plan(Q, C, normalize: int) -> dict:
+    """The automatic plan for these tensors: kind, cluster, ctas, smem_bytes."""
+    import torch
+    qp = _check(Q, "Q", 2)
+    cp = _check(C, "C", 3)
+    B, K, D = (int(x) for x in C.shape)
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    with torch.cuda.device(C.device):
+        s = library().cs_query_plan(qp, cp, B, K, D, int(normalize), *[ctypes.byref(v) for v in vals])
+    if s != 0:
+        raise CSError(s, "cs_query_plan")
+    kind, cluster, ctas, smem = (v.value for v in vals)
+    return {"plan": PLAN_NAMES.get(kind, kind), "kind": kind, "cluster": cluster, "ctas": ctas,
+            "smem_bytes": smem}
+
+
+def cs_device_status(clear: bool = False) -> int:
+    """The device status word of the current device (synchronizes)."""
+    v = ctypes.c_uint(0)
+    s = library().cs_device_status(ctypes.byref(v), int(bool(clear)))
+    if s != 0:
+        raise CSError(s, "cs_device_status")
+    return int(v.value)

@@ -1,0 +1,308 @@
+// C ABI of the candidate-scoring library: argument validation, plan choice
+// and the single kernel launch per call. See include/candidate_scoring.h for
+// the contract of every entry point.
+//
+// Validation follows the rejected-arguments group of PR #69 "cuda: add a
+// fused candidate-scoring kernel for CLM and Kev" (section "Verified on
+// hardware"): K above 255, K of zero, D of zero, a zero scale, a negative
+// temperature and a null query are errors, not answers. It runs before any
+// CUDA call, so a rejected call launches nothing and writes nothing.
+#include "candidate_scoring.h"
+#include "internal.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
+
+namespace {
+
+using cs::Plan;
+using cs::Problem;
+
+// Bytes of candidate rows per bulk-copy stage the planner aims for.
+constexpr int kStageTargetBytes = 16384;
+// Most candidate rows per stage, and most stages per ring.
+constexpr int kMaxRowsPerStage = 32;
+constexpr int kMaxStages = 32;
+// Per-CTA candidate bytes below which splitting a question further over a
+// cluster stops paying.
+constexpr long long kSplitMinBytes = 16384;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    std::map<std::pair<int, long long>, int> clusters;  // (cluster, smem|nq4|cos) -> max active
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// out == nullptr with has_out == false validates everything but the output.
+int validate(const float* Q, const float* C, long long B, int K, int D, int normalize, const float* out,
+             bool has_out, bool check_scalars, float scale, float temperature) {
+    if (!Q || !C || (has_out && !out)) return CS_ERR_NULL_POINTER;
+    if (B <= 0) return CS_ERR_BAD_BATCH;
+    if (K <= 0) return CS_ERR_K_ZERO;
+    if (K > CS_MAX_K) return CS_ERR_K_TOO_LARGE;
+    if (D <= 0) return CS_ERR_D_ZERO;
+    if (normalize != 0 && normalize != 1) return CS_ERR_BAD_SIMILARITY;
+    if (check_scalars) {
+        if (!std::isfinite(scale) || scale == 0.0f) return CS_ERR_BAD_SCALE;
+        if (!std::isfinite(temperature) || !(temperature > 0.0f)) return CS_ERR_BAD_TEMPERATURE;
+    }
+    // B*K*D elements, as bytes, must fit comfortably in 64 bits.
+    const unsigned long long bk = static_cast<unsigned long long>(B) * static_cast<unsigned long long>(K);
+    if (bk > (1ull << 60) / static_cast<unsigned long long>(D)) return CS_ERR_TOO_LARGE;
+    if (has_out) {
+        const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + bk * 4ull;
+        const uintptr_t q0 = reinterpret_cast<uintptr_t>(Q),
+                        q1 = q0 + static_cast<unsigned long long>(B) * static_cast<unsigned long long>(D) * 4ull;
+        const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), c1 = c0 + bk * static_cast<unsigned long long>(D) * 4ull;
+        if ((o0 < q1 && q0 < o1) || (o0 < c1 && c0 < o1)) return CS_ERR_ALIAS;
+    }
+    return CS_OK;
+}
+
+// Per-device facts and one-time kernel attributes. Returns a CUDA error.
+cudaError_t device_state(DeviceState** st) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        e = cs::configure_device_kernels(d.smem_optin);
+        if (e != cudaSuccess) return e;
+        d.ready = true;
+    }
+    *st = &d;
+    return cudaSuccess;
+}
+
+int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize) {
+    const long long key2 = (static_cast<long long>(smem) << 8) | (nq4 << 1) | normalize;
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = d.clusters.find({cluster, key2});
+    if (it != d.clusters.end()) return it->second;
+    const int n = cs::max_active_clusters(cluster, smem, nq4, normalize);
+    d.clusters[{cluster, key2}] = n;
+    return n;
+}
+
+bool tma_eligible(const Problem& p) {
+    return (p.D % 4) == 0 && (reinterpret_cast<uintptr_t>(p.Q) % 16) == 0 &&
+           (reinterpret_cast<uintptr_t>(p.C) % 16) == 0;
+}
+
+int nq4_for(int D) {
+    const int d4 = D / 4;
+    if (d4 <= 32) return 1;
+    if (d4 <= 64) return 2;
+    if (d4 <= 128) return 4;
+    if (d4 <= 256) return 8;
+    return 0;  // q read from shared memory
+}
+
+// Ring geometry for D: rows per stage, and how many stages fit in shared
+// memory. Returns false when not even two stages fit.
+bool ring_geometry(const DeviceState& d, int D, int* rows_per_stage, int* max_stages) {
+    const long long row_bytes = 4ll * D;
+    long long R = kStageTargetBytes / row_bytes;
+    if (R < 1) R = 1;
+    if (R > kMaxRowsPerStage) R = kMaxRowsPerStage;
+    const size_t fixed = cs::smem_layout(0, static_cast<int>(R), D).total;
+    if (fixed >= static_cast<size_t>(d.smem_optin)) return false;
+    long long ns = static_cast<long long>(d.smem_optin - fixed) / (R * row_bytes);
+    // The barrier array grows by 16 bytes per stage as well.
+    while (ns > 0 && cs::smem_layout(static_cast<int>(ns), static_cast<int>(R), D).total >
+                         static_cast<size_t>(d.smem_optin))
+        --ns;
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns < 2) return false;
+    *rows_per_stage = static_cast<int>(R);
+    *max_stages = static_cast<int>(ns);
+    return true;
+}
+
+// STREAM plan with `ctas` persistent CTAs (0 = one per SM, at most B).
+void stream_plan(const DeviceState& d, const Problem& p, int R, int max_ns, int ctas, Plan* plan) {
+    if (ctas <= 0) ctas = d.sms;
+    if (ctas > p.B) ctas = static_cast<int>(p.B);
+    // Stages one CTA ever needs: no point reserving more ring than that.
+    const long long qpc = (p.B + ctas - 1) / ctas;
+    const long long need = qpc * ((p.K + R - 1) / R);
+    const int ns = need < max_ns ? static_cast<int>(need < 2 ? 2 : need) : max_ns;
+    plan->kind = cs::kPlanStream;
+    plan->cluster = 1;
+    plan->ctas = ctas;
+    plan->rows_per_stage = R;
+    plan->stages = ns;
+    plan->nq4 = nq4_for(p.D);
+    plan->smem = cs::smem_layout(ns, R, p.D).total;
+}
+
+void cluster_plan(const Problem& p, int G, int R, int max_ns, Plan* plan) {
+    const int rows = (p.K + G - 1) / G;
+    const int need = (rows + R - 1) / R;
+    const int ns = need < max_ns ? (need < 2 ? 2 : need) : max_ns;
+    plan->kind = cs::kPlanCluster;
+    plan->cluster = G;
+    plan->ctas = G * static_cast<int>(p.B);
+    plan->rows_per_stage = R;
+    plan->stages = ns;
+    plan->nq4 = nq4_for(p.D);
+    plan->smem = cs::smem_layout(ns, R, p.D).total;
+}
+
+void generic_plan(const Problem& p, Plan* plan) {
+    plan->kind = cs::kPlanGeneric;
+    plan->cluster = 1;
+    plan->ctas = static_cast<int>(p.B);
+    plan->rows_per_stage = 0;
+    plan->stages = 0;
+    plan->nq4 = 0;
+    plan->smem = 0;
+}
+
+// Chooses (or checks a forced) plan. Returns a cs_status.
+int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas, Plan* plan) {
+    int R = 0, max_ns = 0;
+    const bool fast = tma_eligible(p) && ring_geometry(d, p.D, &R, &max_ns);
+    if (kind == cs::kPlanGeneric) {
+        generic_plan(p, plan);
+        return CS_OK;
+    }
+    if (kind == cs::kPlanStream) {
+        if (!fast || ctas < 0 || ctas > p.B) return CS_ERR_BAD_PLAN;
+        stream_plan(d, p, R, max_ns, ctas, plan);
+        return CS_OK;
+    }
+    if (kind == cs::kPlanCluster) {
+        if (!fast || p.B > 65535 || cluster < 0 || cluster > cs::kMaxCluster || cluster > p.K)
+            return CS_ERR_BAD_PLAN;
+        if (cluster == 0) {
+            cluster = 1;
+            while (cluster * 2 <= cs::kMaxCluster && cluster * 2 <= p.K) cluster *= 2;
+        }
+        if (cluster == 1) {  // one CTA per question: the STREAM kernel, B CTAs
+            stream_plan(d, p, R, max_ns, static_cast<int>(p.B), plan);
+            return CS_OK;
+        }
+        cluster_plan(p, cluster, R, max_ns, plan);
+        if (cached_max_clusters(d, cluster, plan->smem, plan->nq4, p.normalize) < 1) return CS_ERR_BAD_PLAN;
+        return CS_OK;
+    }
+    // automatic choice
+    if (!fast) {
+        generic_plan(p, plan);
+        return CS_OK;
+    }
+    if (p.B * 2 <= d.sms) {
+        // Few questions: split each over a cluster so one question is not
+        // confined to one SM (the page's 256-thread lesson, "What it is worth").
+        const long long q_bytes = 4ll * p.K * p.D;
+        int G = 1;
+        while (G * 2 <= cs::kMaxCluster && G * 2 <= p.K && (G * 2) * p.B <= d.sms &&
+               q_bytes / (G * 2) >= kSplitMinBytes)
+            G *= 2;
+        while (G > 1) {
+            cluster_plan(p, G, R, max_ns, plan);
+            if (cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize) >= p.B) return CS_OK;
+            G /= 2;
+        }
+    }
+    stream_plan(d, p, R, max_ns, 0, plan);
+    return CS_OK;
+}
+
+int run(const float* Q, const float* C, long long B, int K, int D, int normalize, float scale, float temperature,
+        float* out, cs_stream_t stream, int kind, int cluster, int ctas) {
+    const int v = validate(Q, C, B, K, D, normalize, out, true, true, scale, temperature);
+    if (v != CS_OK) return v;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature};
+    Plan plan{};
+    const int s = make_plan(*d, p, kind, cluster, ctas, &plan);
+    if (s != CS_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = plan.kind == cs::kPlanGeneric ? cs::launch_generic(p, st) : cs::launch_stream(p, plan, st);
+    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cs_abi_version(void) { return 1; }
+
+const char* cs_status_string(int status) {
+    switch (status) {
+        case CS_OK: return "ok";
+        case CS_ERR_NULL_POINTER: return "null pointer (Q, C or out)";
+        case CS_ERR_K_ZERO: return "K must be at least 1";
+        case CS_ERR_K_TOO_LARGE: return "K exceeds CS_MAX_K (255)";
+        case CS_ERR_D_ZERO: return "D must be at least 1";
+        case CS_ERR_BAD_SCALE: return "scale must be finite and nonzero";
+        case CS_ERR_BAD_TEMPERATURE: return "temperature must be finite and positive";
+        case CS_ERR_BAD_BATCH: return "B must be at least 1";
+        case CS_ERR_BAD_SIMILARITY: return "normalize must be 0 (dot) or 1 (cosine)";
+        case CS_ERR_LAUNCH: return "CUDA launch failed";
+        case CS_ERR_ALIAS: return "out overlaps Q or C";
+        case CS_ERR_TOO_LARGE: return "B*K*D is too large";
+        case CS_ERR_BAD_PLAN: return "requested plan cannot run these arguments";
+        default: return "unknown status";
+    }
+}
+
+int cs_score_candidates(const float* q, const float* C, int K, int D, int normalize, float scale, float temperature,
+                        float* out, cs_stream_t stream) {
+    return run(q, C, 1, K, D, normalize, scale, temperature, out, stream, cs::kPlanAuto, 0, 0);
+}
+
+int cs_score_candidates_batch(const float* Q, const float* C, int B, int K, int D, int normalize, float scale,
+                              float temperature, float* out, cs_stream_t stream) {
+    return run(Q, C, B, K, D, normalize, scale, temperature, out, stream, cs::kPlanAuto, 0, 0);
+}
+
+int cs_score_candidates_batch_plan(const float* Q, const float* C, int B, int K, int D, int normalize, float scale,
+                                   float temperature, float* out, cs_stream_t stream, int plan, int cluster,
+                                   int ctas) {
+    if (plan < CS_PLAN_AUTO || plan > CS_PLAN_GENERIC) return CS_ERR_BAD_PLAN;
+    return run(Q, C, B, K, D, normalize, scale, temperature, out, stream, plan, cluster, ctas);
+}
+
+int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int normalize, int* plan, int* cluster,
+                  int* ctas, int* smem_bytes) {
+    const int v = validate(Q, C, B, K, D, normalize, nullptr, false, false, 1.f, 1.f);
+    if (v != CS_OK) return v;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
+    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f};
+    Plan pl{};
+    const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &pl);
+    if (s != CS_OK) return s;
+    if (plan) *plan = pl.kind;
+    if (cluster) *cluster = pl.cluster;
+    if (ctas) *ctas = pl.ctas;
+    if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);
+    return CS_OK;
+}
+
+int cs_device_status(unsigned* flags, int clear) {
+    if (!flags) return CS_ERR_NULL_POINTER;
+    return cs::read_device_status(flags, clear != 0) == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Internal interface between the C ABI (abi.cpp) and the kernels
+// (kernels.cu): launch arguments, plans and the shared-memory layout, which
+// the host sizes and the device carves up with the same function.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace cs {
+
+// Consumer warps per CTA of the streaming kernels; one more warp issues the
+// bulk copies.
+constexpr int kConsumerWarps = 8;
+constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+// On-chip logits per question (K <= 255), one buffer per question in flight.
+constexpr int kLogitSlots = 256;
+// Largest cluster the split plan uses (non-portable size on sm_100-class parts).
+constexpr int kMaxCluster = 16;
+// Threads of the scalar fallback kernel.
+constexpr int kGenericThreads = 256;
+
+// The float32 arguments of one readout, after validation.
+struct Problem {
+    const float* Q;    // [B][D]
+    const float* C;    // [B][K][D]
+    float* out;        // [B][K]
+    long long B;
+    int K;
+    int D;
+    int normalize;     // 1 cosine, 0 dot
+    float scale;       // multiplies the similarity
+    float temperature; // divides the scaled similarity
+};
+
+enum PlanKind { kPlanAuto = 0, kPlanStream = 1, kPlanCluster = 2, kPlanGeneric = 3 };
+
+struct Plan {
+    int kind;          // PlanKind
+    int cluster;       // CTAs per cluster (split plan), else 1
+    int ctas;          // CTAs launched in total
+    int rows_per_stage;// candidate rows per bulk-copy stage
+    int stages;        // stages in the shared-memory ring
+    int nq4;           // float4s of q per lane held in registers (0: read q from smem)
+    size_t smem;       // dynamic shared memory per CTA
+};
+
+// Shared-memory carve-up of the streaming kernels. All offsets are bytes
+// from the (128-byte aligned) dynamic shared-memory base.
+struct SmemLayout {
+    size_t ring;     // stages * rows_per_stage * D floats
+    size_t qbuf;     // 2 slots of D floats
+    size_t logits;   // 2 * kLogitSlots floats
+    size_t xch;      // one float2 (local max, local sum) for the cluster exchange
+    size_t bars;     // full[stages], empty[stages], qfull[2], qempty[2] (8 B each)
+    size_t flag;     // int: this CTA gave up waiting
+    size_t total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage, int D) {
+    SmemLayout L;
+    size_t off = 0;
+    L.ring = off;   off += (size_t)stages * rows_per_stage * D * sizeof(float);
+    L.qbuf = off;   off += 2 * (size_t)D * sizeof(float);
+    L.logits = off; off += 2 * (size_t)kLogitSlots * sizeof(float);
+    L.xch = off;    off += 16;
+    L.bars = off;   off += (2 * (size_t)stages + 4) * 8;
+    L.flag = off;   off += 16;
+    L.total = off;
+    return L;
+}
+
+// Launchers (kernels.cu). Each enqueues exactly one kernel on `stream` and
+// returns the launch status; none synchronizes or allocates.
+cudaError_t launch_stream(const Problem& p, const Plan& plan, cudaStream_t stream);
+cudaError_t launch_generic(const Problem& p, cudaStream_t stream);
+
+// One-time per-device kernel attributes (dynamic smem ceiling, cluster size).
+cudaError_t configure_device_kernels(int smem_optin);
+
+// Clusters of `cluster` CTAs with `smem` bytes each that fit on the device
+// at once (0 if none).
+int max_active_clusters(int cluster, size_t smem, int nq4, int normalize);
+
+// Device status word (bounded-wait give-ups).
+cudaError_t read_device_status(unsigned* flags, bool clear);
+
+}  // namespace cs

@@ -1,0 +1,162 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+function its header declares, and rejects bad arguments before any CUDA call
+(so nothing is launched and the output is untouched).
+
+Source of the rejected arguments: PR #69 "cuda: add a fused candidate-scoring
+kernel for CLM and Kev", section "Verified on hardware" (K above 255, K of
+zero, D of zero, a zero scale, a negative temperature, a null query).
+"""
+from __future__ import annotations
+
+import ctypes
+import glob
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from similarity_softmax_candidate_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# Fake device addresses: validation must never dereference them.
+Q_ADDR, C_ADDR, OUT_ADDR = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(cs_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("cs_abi_version", "cs_status_string", "cs_score_candidates", "cs_score_candidates_batch"):
+        assert n in names
+
+
+@pytest.mark.parametrize("name", _declared_functions())
+def test_library_exports_declared_symbol(host_lib, name):
+    assert hasattr(host_lib, name), f"{name} declared in include/*.h but not exported"
+
+
+def test_abi_version(host_lib):
+    assert host_lib.cs_abi_version() == 1
+
+
+def test_status_strings(host_lib):
+    for code in range(13):
+        s = host_lib.cs_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert host_lib.cs_status_string(999).decode() == "unknown status"
+
+
+def _batch(lib, Q=Q_ADDR, C=C_ADDR, B=1, K=5, D=512, normalize=1, scale=14.2857, temperature=1.0, out=OUT_ADDR):
+    return lib.cs_score_candidates_batch(Q, C, B, K, D, normalize, scale, temperature, out, None)
+
+
+def _single(lib, q=Q_ADDR, C=C_ADDR, K=5, D=512, normalize=1, scale=14.2857, temperature=1.0, out=OUT_ADDR):
+    return lib.cs_score_candidates(q, C, K, D, normalize, scale, temperature, out, None)
+
+
+REJECTS = [
+    ("k_above_255", dict(K=256), binding.CS_ERR_K_TOO_LARGE),
+    ("k_far_above", dict(K=100000), binding.CS_ERR_K_TOO_LARGE),
+    ("k_zero", dict(K=0), binding.CS_ERR_K_ZERO),
+    ("k_negative", dict(K=-3), binding.CS_ERR_K_ZERO),
+    ("d_zero", dict(D=0), binding.CS_ERR_D_ZERO),
+    ("d_negative", dict(D=-1), binding.CS_ERR_D_ZERO),
+    ("scale_zero", dict(scale=0.0), binding.CS_ERR_BAD_SCALE),
+    ("scale_neg_zero", dict(scale=-0.0), binding.CS_ERR_BAD_SCALE),
+    ("scale_nan", dict(scale=math.nan), binding.CS_ERR_BAD_SCALE),
+    ("scale_inf", dict(scale=math.inf), binding.CS_ERR_BAD_SCALE),
+    ("temperature_negative", dict(temperature=-1.0), binding.CS_ERR_BAD_TEMPERATURE),
+    ("temperature_zero", dict(temperature=0.0), binding.CS_ERR_BAD_TEMPERATURE),
+    ("temperature_nan", dict(temperature=math.nan), binding.CS_ERR_BAD_TEMPERATURE),
+    ("temperature_inf", dict(temperature=math.inf), binding.CS_ERR_BAD_TEMPERATURE),
+    ("null_query", dict(Q=None), binding.CS_ERR_NULL_POINTER),
+    ("null_candidates", dict(C=None), binding.CS_ERR_NULL_POINTER),
+    ("null_out", dict(out=None), binding.CS_ERR_NULL_POINTER),
+    ("similarity_2", dict(normalize=2), binding.CS_ERR_BAD_SIMILARITY),
+    ("similarity_neg", dict(normalize=-1), binding.CS_ERR_BAD_SIMILARITY),
+]
+
+
+@pytest.mark.parametrize("name,kw,status", REJECTS, ids=[r[0] for r in REJECTS])
+def test_batch_rejects(host_lib, name, kw, status):
+    assert _batch(host_lib, **kw) == status
+
+
+@pytest.mark.parametrize("name,kw,status", REJECTS, ids=[r[0] for r in REJECTS])
+def test_single_rejects(host_lib, name, kw, status):
+    kw = {("q" if k == "Q" else k): v for k, v in kw.items()}
+    assert _single(host_lib, **kw) == status
+
+
+@pytest.mark.parametrize("B", [0, -1, -(2 ** 31)])
+def test_batch_rejects_bad_batch(host_lib, B):
+    assert _batch(host_lib, B=B) == binding.CS_ERR_BAD_BATCH
+
+
+def test_rejects_out_overlapping_inputs(host_lib):
+    B, K, D = 4, 8, 16
+    # out starting inside C, and out starting inside Q
+    assert _batch(host_lib, B=B, K=K, D=D, out=C_ADDR + 4 * 100) == binding.CS_ERR_ALIAS
+    assert _batch(host_lib, B=B, K=K, D=D, out=Q_ADDR + 4 * (B * D - 1)) == binding.CS_ERR_ALIAS
+    # out ending exactly where Q starts does not overlap (would go on to CUDA, so not called here)
+
+
+def test_rejects_oversized_problem(host_lib):
+    assert _batch(host_lib, B=2 ** 31 - 1, K=255, D=2 ** 31 - 1) == binding.CS_ERR_TOO_LARGE
+
+
+def test_first_failing_check_wins(host_lib):
+    # the page lists each reject on its own; with several bad arguments the
+    # library reports pointers, then B, K, D, similarity, scale, temperature
+    assert _batch(host_lib, Q=None, K=0) == binding.CS_ERR_NULL_POINTER
+    assert _batch(host_lib, K=0, D=0) == binding.CS_ERR_K_ZERO
+    assert _batch(host_lib, D=0, scale=0.0) == binding.CS_ERR_D_ZERO
+    assert _batch(host_lib, scale=0.0, temperature=-1.0) == binding.CS_ERR_BAD_SCALE
+
+
+def test_rejected_call_leaves_output_untouched(host_lib):
+    """Validation returns before any CUDA call, so even a host buffer passed
+    as out is never written by a rejected call."""
+    out = np.full(64, 12345.0, dtype=np.float32)
+    before = out.copy()
+    for _, kw, status in REJECTS:
+        if "out" in kw:
+            continue
+        assert _batch(host_lib, out=out.ctypes.data, **kw) == status
+    np.testing.assert_array_equal(out, before)
+
+
+def test_plan_entry_rejects_unknown_plan(host_lib):
+    f = host_lib.cs_score_candidates_batch_plan
+    assert f(Q_ADDR, C_ADDR, 1, 5, 512, 1, 1.0, 1.0, OUT_ADDR, None, 7, 0, 0) == binding.CS_ERR_BAD_PLAN
+    assert f(Q_ADDR, C_ADDR, 1, 5, 512, 1, 1.0, 1.0, OUT_ADDR, None, -1, 0, 0) == binding.CS_ERR_BAD_PLAN
+    assert f(Q_ADDR, C_ADDR, 1, 0, 512, 1, 1.0, 1.0, OUT_ADDR, None, 1, 0, 0) == binding.CS_ERR_K_ZERO
+
+
+def test_query_plan_validates(host_lib):
+    i = ctypes.c_int()
+    r = ctypes.byref(i)
+    assert host_lib.cs_query_plan(Q_ADDR, C_ADDR, 1, 256, 512, 1, r, r, r, r) == binding.CS_ERR_K_TOO_LARGE
+    assert host_lib.cs_query_plan(None, C_ADDR, 1, 5, 512, 1, r, r, r, r) == binding.CS_ERR_NULL_POINTER
+
+
+def test_device_status_null(host_lib):
+    assert host_lib.cs_device_status(None, 0) == binding.CS_ERR_NULL_POINTER
+
+
+def test_binding_refuses_host_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(8)
+    C = torch.zeros(3, 8)
+    with pytest.raises(ValueError, match="CUDA device"):
+        binding.cs_score_candidates(q, C, 1, 1.0, 1.0)

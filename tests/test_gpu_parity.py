@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the fp64
+oracle on the same seeded inputs.
+
+Groups follow PR #69 "cuda: add a fused candidate-scoring kernel for CLM and
+Kev", "Verified on hardware": the fixed cases (single candidate, identical
+candidates, zero candidate, overflow), the batch path (1, 8, 4 and 3
+questions with K up to 255 and D up to 256, single-question calls through
+cs_score_candidates), plus every execution plan on shapes with ragged tails,
+the workloads of "What it is worth" at their full sizes, and output guards.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from similarity_softmax_candidate_gb300 import binding, workloads
+from tests._util import ATOL, assert_parity, oracle_probs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _run(wl, entry="auto", out=None):
+    Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+    if entry == "single" or (entry == "auto" and wl.B == 1):
+        o = binding.cs_score_candidates(Q[0], C[0], wl.normalize, wl.scale, wl.temperature,
+                                        out=None if out is None else out[0])
+        torch.cuda.synchronize()
+        return o[None, :]
+    o = binding.cs_score_candidates_batch(Q, C, wl.normalize, wl.scale, wl.temperature, out=out)
+    torch.cuda.synchronize()
+    return o
+
+
+def _config_cases():
+    cases = []
+    for name in ("clm_k5", "clm_k64", "clm_batch8", "kev_k255"):
+        for wl in workloads.CONFIGS[name]("cpu"):
+            cases.append(wl)
+    return cases
+
+
+CONFIG_CASES = _config_cases()
+
+
+@pytest.mark.parametrize("wl", CONFIG_CASES, ids=[w.name for w in CONFIG_CASES])
+def test_workload_parity(cuda_lib, wl):
+    p = _run(wl)
+    assert_parity(p, oracle_probs(wl.Q, wl.C, wl.normalize, wl.scale, wl.temperature), wl.name)
+
+
+def test_single_and_batch_entry_points_agree(cuda_lib):
+    for wl in CONFIG_CASES:
+        if wl.B != 1:
+            continue
+        ref = oracle_probs(wl.Q, wl.C, wl.normalize, wl.scale, wl.temperature)
+        ps = _run(wl, "single")
+        pb = _run(wl, "batch")
+        assert_parity(ps, ref, wl.name + " single")
+        assert_parity(pb, ref, wl.name + " batch")
+        assert torch.max(torch.abs(ps - pb)).item() <= ATOL
+
+
+def test_degenerate_cases(cuda_lib):
+    # K = 1 gives exactly 1; identical candidates give 1/K; zero query gives uniform
+    single = workloads.random_case(3, 1, 512, 1, workloads.CLM_SCALE, 11)
+    p = _run(single)
+    assert torch.all(p == 1.0)
+    for normalize in (0, 1):
+        same = workloads.random_case(2, 64, 512, normalize, workloads.CLM_SCALE, 12)
+        same.C[:] = same.C[:, :1, :].clone()
+        p = _run(same)
+        assert torch.max(torch.abs(p - 1.0 / 64)).item() <= 1e-7
+        zq = workloads.random_case(2, 255, 512, normalize, workloads.CLM_SCALE, 13)
+        zq.Q.zero_()
+        p = _run(zq)
+        assert torch.max(torch.abs(p - 1.0 / 255)).item() <= 1e-7
+    # all-zero candidates under cosine: every logit is 0
+    zc = workloads.random_case(2, 17, 512, 1, workloads.CLM_SCALE, 14)
+    zc.C.zero_()
+    assert torch.max(torch.abs(_run(zc) - 1.0 / 17)).item() <= 1e-7
+
+
+def test_golden_hand_cases(cuda_lib):
+    import json
+    import os
+    from scipy.special import softmax
+    with open(os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        q = torch.tensor(c["q"], dtype=torch.float32, device=DEV)
+        C = torch.tensor(c["C"], dtype=torch.float32, device=DEV)
+        p = binding.cs_score_candidates(q, C, c["normalize"], c["scale"], c["temperature"])
+        torch.cuda.synchronize()
+        expected = softmax(np.array(c["expected_logits"], dtype=np.float64))
+        assert_parity(p[None, :], expected[None, :], c["name"])
+
+
+@pytest.mark.parametrize("B", [1, 8, 4, 3])
+def test_page_batch_group(cuda_lib, B):
+    """The page's batch group: K up to 255 and D up to 256; B = 1 goes
+    through the single-question entry point, the rest through the batch one."""
+    rng = np.random.default_rng(B)
+    for normalize in (0, 1):
+        for K, D in ((255, 256), (int(rng.integers(1, 256)), int(rng.integers(1, 257))), (7, 3)):
+            wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 100 + K + D)
+            p = _run(wl)
+            assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0), f"B={B} K={K} D={D}")
+
+
+PLAN_SHAPES = [
+    (3, 255, 512), (2, 37, 132), (5, 1, 4), (1, 64, 2560), (2, 200, 1028), (4, 17, 4100),
+    (7, 255, 128), (3, 33, 12), (2, 255, 1024), (1, 255, 2560), (9, 100, 16),
+]
+
+PLANS = [
+    ("stream_auto", binding.CS_PLAN_STREAM, 0, 0),
+    ("stream_1cta", binding.CS_PLAN_STREAM, 0, 1),
+    ("stream_2cta", binding.CS_PLAN_STREAM, 0, 2),
+    ("cluster_auto", binding.CS_PLAN_CLUSTER, 0, 0),
+    ("cluster_1", binding.CS_PLAN_CLUSTER, 1, 0),
+    ("cluster_2", binding.CS_PLAN_CLUSTER, 2, 0),
+    ("cluster_3", binding.CS_PLAN_CLUSTER, 3, 0),
+    ("cluster_8", binding.CS_PLAN_CLUSTER, 8, 0),
+    ("cluster_16", binding.CS_PLAN_CLUSTER, 16, 0),
+    ("generic", binding.CS_PLAN_GENERIC, 0, 0),
+]
+
+
+@pytest.mark.parametrize("plan", PLANS, ids=[p[0] for p in PLANS])
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_every_plan(cuda_lib, plan, normalize):
+    _, kind, cluster, ctas = plan
+    for B, K, D in PLAN_SHAPES:
+        if cluster > K or ctas > B:
+            continue
+        wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 1000 + B * K + D)
+        Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+        p = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, kind, cluster, ctas)
+        torch.cuda.synchronize()
+        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0), f"{plan[0]} B={B} K={K} D={D}")
+
+
+def test_unaligned_and_odd_shapes_use_scalar_path(cuda_lib):
+    for normalize in (0, 1):
+        # odd D
+        wl = workloads.random_case(3, 255, 513, normalize, 2.0, 21)
+        Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+        assert binding.cs_query_plan(Q, C, normalize)["plan"] == "generic"
+        assert_parity(_run(wl), oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "odd D")
+        # pointers 4 bytes past a 16-byte boundary, D a multiple of 4
+        wl = workloads.random_case(2, 64, 512, normalize, 2.0, 22)
+        Qb = torch.empty(wl.B * wl.D + 1, device=DEV)
+        Cb = torch.empty(wl.B * wl.K * wl.D + 1, device=DEV)
+        Q = Qb[1:].view(wl.B, wl.D)
+        C = Cb[1:].view(wl.B, wl.K, wl.D)
+        Q.copy_(wl.Q)
+        C.copy_(wl.C)
+        assert binding.cs_query_plan(Q, C, normalize)["plan"] == "generic"
+        p = binding.cs_score_candidates_batch(Q, C, normalize, 2.0, 1.0)
+        torch.cuda.synchronize()
+        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "unaligned")
+        with pytest.raises(binding.CSError):
+            binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_STREAM)
+
+
+def test_large_d(cuda_lib):
+    """D large enough that q sits in shared memory, and beyond what the
+    shared-memory ring holds (scalar path)."""
+    for D in (12288, 20000):
+        for normalize in (0, 1):
+            wl = workloads.random_case(2, 9, D, normalize, 3.0, 31)
+            assert_parity(_run(wl), oracle_probs(wl.Q, wl.C, normalize, 3.0, 1.0), f"D={D}")
+
+
+def test_automatic_plans(cuda_lib):
+    def plan(B, K, D):
+        Q = torch.empty(B, D, device=DEV)
+        C = torch.empty(B, K, D, device=DEV)
+        return binding.cs_query_plan(Q, C, 1)
+    one = plan(1, 255, 512)
+    assert one["plan"] == "cluster" and one["cluster"] >= 2, one
+    assert plan(1, 255, 2560)["plan"] == "cluster"
+    big = plan(4096, 255, 512)
+    assert big["plan"] == "stream" and big["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan(2, 255, 511)["plan"] == "generic"
+
+
+def test_throughput_workload_full_size(cuda_lib):
+    """16384 questions, K=255, D=512 (8.6 GB of candidates), scored as four
+    launches over consecutive slices of 4096 questions, exactly as timed by
+    the benchmark. Every row is checked to sum to 1 and be finite; a
+    deterministic sample of questions (every 64th, plus the first and last of
+    each slice) is compared with the oracle."""
+    wls = workloads.throughput(DEV)
+    out = torch.empty((workloads.THROUGHPUT_B, 255), device=DEV)
+    chunk = workloads.THROUGHPUT_CHUNK
+    for wl in wls:
+        for b0 in range(0, wl.B, chunk):
+            binding.cs_score_candidates_batch(wl.Q[b0:b0 + chunk], wl.C[b0:b0 + chunk], wl.normalize,
+                                              wl.scale, wl.temperature, out=out[b0:b0 + chunk])
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all()
+        sums = out.double().sum(dim=1)
+        assert torch.max(torch.abs(sums - 1.0)).item() <= 1e-5
+        idx = sorted(set(range(0, wl.B, 64)) | {b + o for b in range(0, wl.B, chunk) for o in (0, chunk - 1)})
+        sel = torch.tensor(idx, device=DEV)
+        ref = oracle_probs(wl.Q.index_select(0, sel), wl.C.index_select(0, sel), wl.normalize, wl.scale,
+                           wl.temperature)
+        assert_parity(out.index_select(0, sel), ref, wl.name)
+    del wls
+    torch.cuda.empty_cache()
+
+
+def test_deterministic(cuda_lib):
+    for B, K, D in ((1, 255, 512), (300, 255, 512), (2, 255, 2560)):
+        wl = workloads.random_case(B, K, D, 1, 14.2857, 41, DEV)
+        a = binding.cs_score_candidates_batch(wl.Q, wl.C, 1, wl.scale, 1.0)
+        b = binding.cs_score_candidates_batch(wl.Q, wl.C, 1, wl.scale, 1.0)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+
+
+def test_output_guards_untouched(cuda_lib):
+    """Sentinels around out survive every plan, and a rejected call leaves out
+    exactly as it was."""
+    sentinel = 7777.0
+    for B, K, D, kind, cl in ((1, 255, 512, 0, 0), (5, 37, 512, 1, 0), (3, 64, 512, 2, 8), (2, 33, 100, 3, 0)):
+        wl = workloads.random_case(B, K, D, 1, 2.0, 51, DEV)
+        pad = 64
+        buf = torch.full((pad + B * K + pad,), sentinel, device=DEV)
+        out = buf[pad:pad + B * K].view(B, K)
+        binding.cs_score_candidates_batch_plan(wl.Q, wl.C, 1, 2.0, 1.0, kind, cl, 0, out=out)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == sentinel) and torch.all(buf[pad + B * K:] == sentinel)
+        assert_parity(out, oracle_probs(wl.Q, wl.C, 1, 2.0, 1.0), f"guards plan {kind}")
+    before = buf.clone()
+    with pytest.raises(binding.CSError):
+        binding.cs_score_candidates_batch(wl.Q, wl.C, 1, 0.0, 1.0, out=out)
+    with pytest.raises(binding.CSError):
+        binding.cs_score_candidates_batch(wl.Q, wl.C, 1, 1.0, -1.0, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(buf, before)
+
+
+def test_rejects_on_device(cuda_lib):
+    q = torch.randn(512, device=DEV)
+    C = torch.randn(256, 512, device=DEV)
+    with pytest.raises(binding.CSError) as e:
+        binding.cs_score_candidates(q, C, 1, 1.0, 1.0)
+    assert e.value.status == binding.CS_ERR_K_TOO_LARGE
+
+
+def test_nondefault_stream(cuda_lib):
+    wl = workloads.random_case(4, 255, 512, 1, 14.2857, 61, DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        p = binding.cs_score_candidates_batch(wl.Q, wl.C, 1, wl.scale, 1.0, stream=s)
+    s.synchronize()
+    assert_parity(p, oracle_probs(wl.Q, wl.C, 1, wl.scale, 1.0), "side stream")
+
+
+def test_no_wait_gave_up(cuda_lib):
+    torch.cuda.synchronize()
+    assert binding.cs_device_status() == 0
