@@ -56,7 +56,7 @@ PAGE_SHAPES = [
     ("kev-dot-255x2560", 1, 255, 2560, 0, 55.3),
 ]
 
-METRIC = "questions/s (K=255, D=512, cosine, 16384 questions in 4 launches)"
+METRIC = "questions/s (K=255, D=512, cosine, 16384 questions in 4 launches of 4096)"
 
 
 def _dist():
@@ -96,7 +96,7 @@ def _traffic_from_profile(kernel_src_sha):
 def _kernel_sha():
     import hashlib
     h = hashlib.sha256()
-    for name in ("kernels.cu", "internal.h"):
+    for name in ("kernels.cu", "internal.h", "abi.cpp"):
         with open(os.path.join(_ROOT, "similarity_softmax_candidate_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -221,6 +221,7 @@ def run_reference(args):
 
 
 def main():
+    global B_TOTAL, CHUNK
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -230,6 +231,10 @@ def main():
     ap.add_argument("--latency-calls", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extra", action="store_true", help="only the headline throughput and its roofline")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle's CPU baseline")
+    ap.add_argument("--questions", type=int, default=B_TOTAL,
+                    help="questions per step (default 16384; smaller only for profiling captures)")
+    ap.add_argument("--chunk", type=int, default=CHUNK, help="questions per launch (default 4096)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -263,7 +268,10 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    wls = workloads.throughput(dev)
+    B_TOTAL, CHUNK = args.questions, args.chunk
+    if B_TOTAL % CHUNK:
+        ap.error("--questions must be a multiple of --chunk")
+    wls = workloads.throughput(dev, B=B_TOTAL)
     wl_cos, wl_dot = wls
     out = torch.empty((B_TOTAL, K), device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -312,6 +320,8 @@ def main():
     mean_launch_ms = sum(launches_cos) / len(launches_cos)
     achieved = launch_bytes / (mean_launch_ms / 1e3) / 1e9
     traffic = _traffic_from_profile(_kernel_sha())
+    if traffic is not None:
+        traffic *= CHUNK / 4096.0
     dot_ms_step = ms_dot / args.steps
     dot_launch_ms = sum(launches_dot) / len(launches_dot)
 
@@ -319,15 +329,15 @@ def main():
         "metric": METRIC, "value": value, "unit": "questions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "throughput: 16384 questions x K=255 x D=512 fp32 N(0,1), CLM cosine "
-                               "(scale 1/0.07, T=1), 4 launches of 4096 questions per step",
+        "config": {"workload": f"throughput: {B_TOTAL} questions x K=255 x D=512 fp32 N(0,1), CLM cosine "
+                               f"(scale 1/0.07, T=1), {B_TOTAL // CHUNK} launches of {CHUNK} questions per step",
                    "B": B_TOTAL, "K": K, "D": D, "launches_per_step": B_TOTAL // CHUNK,
-                   "l2": "inputs (8.6 GB per rank) larger than L2 (129 MB); no flush",
+                   "l2": f"inputs ({B_TOTAL * K * D * 4 / 1e9:.1f} GB per rank) larger than L2 (129 MB); no flush",
                    "plan": plan, "parallelism": f"replicas x{world}"},
         "gpu_launches": n_launch,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "stream_kernel (STREAM plan), one launch = 4096 questions",
+                     "kernel": f"stream_kernel (STREAM plan), one launch = {CHUNK} questions",
                      "algorithmic_bytes_per_launch": launch_bytes, "mean_launch_ms": mean_launch_ms,
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
         "clocks": clock_info,
@@ -346,12 +356,13 @@ def main():
     del wls, wl_cos, wl_dot
     torch.cuda.empty_cache()
 
-    if rank == 0:
+    if rank == 0 and not args.no_cpu:
         try:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         except Exception as e:  # the oracle is optional for the GPU numbers
             line["cpu_baseline"] = {"value": None, "unit": "questions/s", "cores": 1, "kind": "oracle",
                                     "sample": f"failed: {e}"}
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

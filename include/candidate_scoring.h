@@ -132,6 +132,7 @@ int cs_score_candidates_batch_plan(const float *Q, const float *C, int B,
 
 /* Device status word bits (see cs_device_status). */
 #define CS_DEVERR_WAIT_TIMEOUT 1u  /* an on-chip wait gave up after ~1 s */
+#define CS_DEVERR_BAD_CONFIG 2u    /* a kernel refused an inconsistent launch plan */
 
 /*
  * Reads (and, if clear != 0, resets) the status word the kernels of this

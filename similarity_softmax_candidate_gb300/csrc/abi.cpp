@@ -23,10 +23,9 @@ namespace {
 using cs::Plan;
 using cs::Problem;
 
-// Bytes of candidate rows per bulk-copy stage the planner aims for.
+// Bytes of candidate rows per bulk-copy stage the planner aims for, and the
+// most stages per ring.
 constexpr int kStageTargetBytes = 16384;
-// Most candidate rows per stage, and most stages per ring.
-constexpr int kMaxRowsPerStage = 32;
 constexpr int kMaxStages = 32;
 // Per-CTA candidate bytes below which splitting a question further over a
 // cluster stops paying.
@@ -114,35 +113,61 @@ int nq4_for(int D) {
     return 0;  // q read from shared memory
 }
 
-// Ring geometry for D: rows per stage, and how many stages fit in shared
-// memory. Returns false when not even two stages fit.
-bool ring_geometry(const DeviceState& d, int D, int* rows_per_stage, int* max_stages) {
-    const long long row_bytes = 4ll * D;
-    long long R = kStageTargetBytes / row_bytes;
+// Rows per stage that make a stage of about kStageTargetBytes (1..8).
+int stage_rows(int D) {
+    long long R = kStageTargetBytes / (4ll * D);
     if (R < 1) R = 1;
-    if (R > kMaxRowsPerStage) R = kMaxRowsPerStage;
-    const size_t fixed = cs::smem_layout(0, static_cast<int>(R), D).total;
-    if (fixed >= static_cast<size_t>(d.smem_optin)) return false;
-    long long ns = static_cast<long long>(d.smem_optin - fixed) / (R * row_bytes);
-    // The barrier array grows by 16 bytes per stage as well.
-    while (ns > 0 && cs::smem_layout(static_cast<int>(ns), static_cast<int>(R), D).total >
-                         static_cast<size_t>(d.smem_optin))
-        --ns;
+    if (R > cs::kMaxRowsPerStage) R = cs::kMaxRowsPerStage;
+    return static_cast<int>(R);
+}
+
+// The most stages of R rows of D floats that fit in shared memory, as a
+// multiple of the consumer-warp count (at most kMaxStages); 0 if not even
+// one stage per consumer warp fits. Stage g lives in slot g % NS and belongs
+// to warp g % kConsumerWarps, so with NS a multiple of the warp count every
+// slot always has the same owner, which consumes its uses in order: a
+// parity wait on a slot can then never see a phase two uses old.
+int max_stages(const DeviceState& d, int R, int D) {
+    const long long stage_bytes = 4ll * R * D;
+    const size_t fixed = cs::smem_layout(0, R, D).total;
+    if (fixed >= static_cast<size_t>(d.smem_optin)) return 0;
+    long long ns = static_cast<long long>(d.smem_optin - fixed) / stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
-    if (ns < 2) return false;
-    *rows_per_stage = static_cast<int>(R);
-    *max_stages = static_cast<int>(ns);
-    return true;
+    ns -= ns % cs::kConsumerWarps;
+    // The barrier array grows by 16 bytes per stage as well.
+    while (ns > 0 && cs::smem_layout(static_cast<int>(ns), R, D).total > static_cast<size_t>(d.smem_optin))
+        ns -= cs::kConsumerWarps;
+    return ns > 0 ? static_cast<int>(ns) : 0;
+}
+
+// Ring stages for `need` stages of work: enough for all of it if that fits,
+// rounded up to whole rounds of consumer warps.
+int ring_stages(long long need, int max_ns) {
+    long long ns = (need + cs::kConsumerWarps - 1) / cs::kConsumerWarps * cs::kConsumerWarps;
+    return ns < max_ns ? static_cast<int>(ns) : max_ns;
 }
 
 // STREAM plan with `ctas` persistent CTAs (0 = one per SM, at most B).
-void stream_plan(const DeviceState& d, const Problem& p, int R, int max_ns, int ctas, Plan* plan) {
+// Picks rows per stage R <= stage_rows(D) that keeps the most bytes in
+// flight (larger R on ties). Returns false if no ring fits.
+bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
+    int R = 0, max_ns = 0;
+    long long best = 0;
+    for (int r = stage_rows(p.D); r >= 1; --r) {
+        const int ns = max_stages(d, r, p.D);
+        const long long bytes = 4ll * r * p.D * ns;
+        if (bytes > best) {
+            best = bytes;
+            R = r;
+            max_ns = ns;
+        }
+    }
+    if (max_ns == 0) return false;
     if (ctas <= 0) ctas = d.sms;
     if (ctas > p.B) ctas = static_cast<int>(p.B);
     // Stages one CTA ever needs: no point reserving more ring than that.
     const long long qpc = (p.B + ctas - 1) / ctas;
-    const long long need = qpc * ((p.K + R - 1) / R);
-    const int ns = need < max_ns ? static_cast<int>(need < 2 ? 2 : need) : max_ns;
+    const int ns = ring_stages(qpc * ((p.K + R - 1) / R), max_ns);
     plan->kind = cs::kPlanStream;
     plan->cluster = 1;
     plan->ctas = ctas;
@@ -150,12 +175,19 @@ void stream_plan(const DeviceState& d, const Problem& p, int R, int max_ns, int 
     plan->stages = ns;
     plan->nq4 = nq4_for(p.D);
     plan->smem = cs::smem_layout(ns, R, p.D).total;
+    return true;
 }
 
-void cluster_plan(const Problem& p, int G, int R, int max_ns, Plan* plan) {
+// CLUSTER plan with G CTAs per question: each CTA's rows spread over all
+// consumer warps (one stage each) when the ring holds them.
+bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     const int rows = (p.K + G - 1) / G;
-    const int need = (rows + R - 1) / R;
-    const int ns = need < max_ns ? (need < 2 ? 2 : need) : max_ns;
+    int R = (rows + cs::kConsumerWarps - 1) / cs::kConsumerWarps;
+    const int Rmax = stage_rows(p.D);
+    if (R > Rmax) R = Rmax;
+    const int max_ns = max_stages(d, R, p.D);
+    if (max_ns == 0) return false;
+    const int ns = ring_stages((rows + R - 1) / R, max_ns);
     plan->kind = cs::kPlanCluster;
     plan->cluster = G;
     plan->ctas = G * static_cast<int>(p.B);
@@ -163,6 +195,7 @@ void cluster_plan(const Problem& p, int G, int R, int max_ns, Plan* plan) {
     plan->stages = ns;
     plan->nq4 = nq4_for(p.D);
     plan->smem = cs::smem_layout(ns, R, p.D).total;
+    return true;
 }
 
 void generic_plan(const Problem& p, Plan* plan) {
@@ -177,38 +210,30 @@ void generic_plan(const Problem& p, Plan* plan) {
 
 // Chooses (or checks a forced) plan. Returns a cs_status.
 int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas, Plan* plan) {
-    int R = 0, max_ns = 0;
-    const bool fast = tma_eligible(p) && ring_geometry(d, p.D, &R, &max_ns);
+    const bool aligned = tma_eligible(p);
     if (kind == cs::kPlanGeneric) {
         generic_plan(p, plan);
         return CS_OK;
     }
     if (kind == cs::kPlanStream) {
-        if (!fast || ctas < 0 || ctas > p.B) return CS_ERR_BAD_PLAN;
-        stream_plan(d, p, R, max_ns, ctas, plan);
-        return CS_OK;
+        if (!aligned || ctas < 0 || ctas > p.B) return CS_ERR_BAD_PLAN;
+        return stream_plan(d, p, ctas, plan) ? CS_OK : CS_ERR_BAD_PLAN;
     }
     if (kind == cs::kPlanCluster) {
-        if (!fast || p.B > 65535 || cluster < 0 || cluster > cs::kMaxCluster || cluster > p.K)
+        if (!aligned || p.B > 65535 || cluster < 0 || cluster > cs::kMaxCluster || cluster > p.K)
             return CS_ERR_BAD_PLAN;
         if (cluster == 0) {
             cluster = 1;
             while (cluster * 2 <= cs::kMaxCluster && cluster * 2 <= p.K) cluster *= 2;
         }
-        if (cluster == 1) {  // one CTA per question: the STREAM kernel, B CTAs
-            stream_plan(d, p, R, max_ns, static_cast<int>(p.B), plan);
-            return CS_OK;
-        }
-        cluster_plan(p, cluster, R, max_ns, plan);
+        if (cluster == 1)  // one CTA per question: the STREAM kernel with B CTAs
+            return stream_plan(d, p, static_cast<int>(p.B), plan) ? CS_OK : CS_ERR_BAD_PLAN;
+        if (!cluster_plan(d, p, cluster, plan)) return CS_ERR_BAD_PLAN;
         if (cached_max_clusters(d, cluster, plan->smem, plan->nq4, p.normalize) < 1) return CS_ERR_BAD_PLAN;
         return CS_OK;
     }
     // automatic choice
-    if (!fast) {
-        generic_plan(p, plan);
-        return CS_OK;
-    }
-    if (p.B * 2 <= d.sms) {
+    if (aligned && p.B * 2 <= d.sms) {
         // Few questions: split each over a cluster so one question is not
         // confined to one SM (the page's 256-thread lesson, "What it is worth").
         const long long q_bytes = 4ll * p.K * p.D;
@@ -216,13 +241,14 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         while (G * 2 <= cs::kMaxCluster && G * 2 <= p.K && (G * 2) * p.B <= d.sms &&
                q_bytes / (G * 2) >= kSplitMinBytes)
             G *= 2;
-        while (G > 1) {
-            cluster_plan(p, G, R, max_ns, plan);
-            if (cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize) >= p.B) return CS_OK;
-            G /= 2;
+        for (; G > 1; G /= 2) {
+            if (cluster_plan(d, p, G, plan) &&
+                cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize) >= p.B)
+                return CS_OK;
         }
     }
-    stream_plan(d, p, R, max_ns, 0, plan);
+    if (aligned && stream_plan(d, p, 0, plan)) return CS_OK;
+    generic_plan(p, plan);
     return CS_OK;
 }
 

@@ -13,8 +13,11 @@ namespace cs {
 // bulk copies.
 constexpr int kConsumerWarps = 8;
 constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
-// On-chip logits per question (K <= 255), one buffer per question in flight.
+// On-chip per-row results per question (K <= 255), one buffer per question
+// in flight.
 constexpr int kLogitSlots = 256;
+// Most candidate rows in one ring stage; one warp reduces a whole stage.
+constexpr int kMaxRowsPerStage = 8;
 // Largest cluster the split plan uses (non-portable size on sm_100-class parts).
 constexpr int kMaxCluster = 16;
 // Threads of the scalar fallback kernel.
@@ -50,7 +53,7 @@ struct Plan {
 struct SmemLayout {
     size_t ring;     // stages * rows_per_stage * D floats
     size_t qbuf;     // 2 slots of D floats
-    size_t logits;   // 2 * kLogitSlots floats
+    size_t tn;       // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
     size_t xch;      // one float2 (local max, local sum) for the cluster exchange
     size_t bars;     // full[stages], empty[stages], qfull[2], qempty[2] (8 B each)
     size_t flag;     // int: this CTA gave up waiting
@@ -62,7 +65,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
     size_t off = 0;
     L.ring = off;   off += (size_t)stages * rows_per_stage * D * sizeof(float);
     L.qbuf = off;   off += 2 * (size_t)D * sizeof(float);
-    L.logits = off; off += 2 * (size_t)kLogitSlots * sizeof(float);
+    L.tn = off;     off += 4 * (size_t)kLogitSlots * sizeof(float);
     L.xch = off;    off += 16;
     L.bars = off;   off += (2 * (size_t)stages + 4) * 8;
     L.flag = off;   off += 16;

@@ -11,9 +11,12 @@
 // sm_89; none of that is kept beyond "softmax in shared memory"):
 //   * stream_kernel -- a warp-specialised CTA: one elected thread issues 1-D
 //     bulk copies (cp.async.bulk, TMA engine) of whole candidate rows into a
-//     ring of shared-memory stages tracked by mbarriers; eight consumer warps
-//     compute one row each per stage with float4 shared loads, q held in
-//     registers, and warp-shuffle reductions.
+//     ring of shared-memory stages tracked by mbarriers. Stage g (up to 8
+//     rows) belongs to consumer warp g % 8, which computes the dots and
+//     squared norms of all its rows from float4 shared loads against q held
+//     in registers, then reduces them together with one transposed butterfly
+//     of warp shuffles. The per-row cosine and the softmax run later, one
+//     lane per row, in the warp that finishes the question.
 //       - STREAM plan: persistent, one CTA per SM, each CTA streams a
 //         contiguous run of questions, prefetching the next question while a
 //         single warp finishes the previous question's softmax.
@@ -156,16 +159,24 @@ __device__ __forceinline__ float logit_of(float t, float n, float qn, float scal
     return scale * sim / temperature;
 }
 
-// Softmax of lg[0..n) (n <= 256) by one warp, written to dst[0..n).
-__device__ __forceinline__ void softmax_store(const float* lg, int n, float* __restrict__ dst, int lane) {
-    float z[kLogitSlots / 32];
-    float m = -INFINITY;
+// Logits of rows lane, lane+32, ... (< n) from their dot t and squared norm
+// n_sq; -inf beyond n.
+template <bool COS>
+__device__ __forceinline__ void load_logits(const float* t, const float* n_sq, int n, float qn, float scale,
+                                            float temperature, int lane, float (&z)[kLogitSlots / 32]) {
 #pragma unroll
     for (int j = 0; j < kLogitSlots / 32; ++j) {
         const int k = lane + 32 * j;
-        z[j] = k < n ? lg[k] : -INFINITY;
-        m = fmaxf(m, z[j]);
+        z[j] = k < n ? logit_of(t[k], COS ? n_sq[k] : 0.f, qn, scale, temperature, COS) : -INFINITY;
     }
+}
+
+// Softmax of z over one warp (rows lane + 32 j < n), written to dst[0..n).
+__device__ __forceinline__ void softmax_store(float (&z)[kLogitSlots / 32], int n, float* __restrict__ dst,
+                                              int lane) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kLogitSlots / 32; ++j) m = fmaxf(m, z[j]);
     m = warp_max(m);
     float s = 0.f;
 #pragma unroll
@@ -182,76 +193,121 @@ __device__ __forceinline__ void softmax_store(const float* lg, int n, float* __r
     }
 }
 
+// Sums each of the V values v[0..V) over the 32 lanes of a warp with V - 1
+// + (5 - log2 V) shuffles: at each butterfly level a lane keeps half of its
+// values and receives the matching half from its partner, so the values are
+// spread over the lanes instead of every lane reducing all of them. Returns
+// the full sum of value *idx; every lane whose low (5 - log2 V) bits are zero
+// holds a distinct value.
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane, int* idx) {
+    static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two <= 32");
+    int id = 0;
+#pragma unroll
+    for (int h = V / 2, o = 16; h >= 1; h >>= 1, o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? v[i] : v[i + h];
+            const float keep = upper ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        if (upper) id += h;
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = 16 / V; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    *idx = id;
+    return x;
+}
+
 // ------------------------------------------------------------------ stream kernel
 
 struct StreamArgs {
     Problem p;
-    int rows_per_stage;  // R
+    int rows_per_stage;  // R <= kMaxRowsPerStage
     int stages;          // NS
     int cluster;         // G: CTAs per question (1 = STREAM plan)
 };
 
-// Dot (and squared norm) of one candidate row in shared memory with q held
-// in registers: lane handles float4 columns lane, lane+32, ...
+// Dots (and squared norms) of the nr <= kMaxRowsPerStage rows of one stage.
+// Lane handles float4 columns lane, lane+32, ...; q comes from registers
+// (NQ4 > 0) or from shared memory (NQ4 == 0, large D). Accumulators v hold
+// t_r at v[VPR*r] and, for the cosine, the squared norm at v[VPR*r + 1].
 template <int NQ4, bool COS>
-__device__ __forceinline__ void row_dot_regs(const float4* __restrict__ row, const float4 (&qv)[NQ4], int D4,
-                                             int lane, float& t, float& n) {
-    float t0 = 0.f, t1 = 0.f, n0 = 0.f, n1 = 0.f;
+__device__ __forceinline__ void stage_dots(const float4* __restrict__ st, int nr, int D4, const float4 (&qv)[NQ4 > 0 ? NQ4 : 1],
+                                           const float4* __restrict__ q4, int lane,
+                                           float (&v)[(COS ? 2 : 1) * kMaxRowsPerStage]) {
+    constexpr int VPR = COS ? 2 : 1;
 #pragma unroll
-    for (int j = 0; j < NQ4; ++j) {
-        const int i = lane + 32 * j;
-        if (i < D4) {
-            const float4 c = row[i];
-            t0 = fmaf(c.x, qv[j].x, t0);
-            t1 = fmaf(c.y, qv[j].y, t1);
-            t0 = fmaf(c.z, qv[j].z, t0);
-            t1 = fmaf(c.w, qv[j].w, t1);
-            if (COS) {
-                n0 = fmaf(c.x, c.x, n0);
-                n1 = fmaf(c.y, c.y, n1);
-                n0 = fmaf(c.z, c.z, n0);
-                n1 = fmaf(c.w, c.w, n1);
+    for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = 0.f;
+    if constexpr (NQ4 > 0) {
+#pragma unroll
+        for (int j = 0; j < NQ4; ++j) {
+            const int i = lane + 32 * j;
+            if (i < D4) {
+                const float4 q = qv[j];
+#pragma unroll
+                for (int r = 0; r < kMaxRowsPerStage; ++r) {
+                    if (r < nr) {
+                        const float4 c = st[r * D4 + i];
+                        float t = v[VPR * r];
+                        t = fmaf(c.x, q.x, t);
+                        t = fmaf(c.y, q.y, t);
+                        t = fmaf(c.z, q.z, t);
+                        t = fmaf(c.w, q.w, t);
+                        v[VPR * r] = t;
+                        if (COS) {
+                            float n = v[VPR * r + 1];
+                            n = fmaf(c.x, c.x, n);
+                            n = fmaf(c.y, c.y, n);
+                            n = fmaf(c.z, c.z, n);
+                            n = fmaf(c.w, c.w, n);
+                            v[VPR * r + 1] = n;
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        for (int i = lane; i < D4; i += 32) {
+            const float4 q = q4[i];
+#pragma unroll
+            for (int r = 0; r < kMaxRowsPerStage; ++r) {
+                if (r < nr) {
+                    const float4 c = st[r * D4 + i];
+                    float t = v[VPR * r];
+                    t = fmaf(c.x, q.x, t);
+                    t = fmaf(c.y, q.y, t);
+                    t = fmaf(c.z, q.z, t);
+                    t = fmaf(c.w, q.w, t);
+                    v[VPR * r] = t;
+                    if (COS) {
+                        float n = v[VPR * r + 1];
+                        n = fmaf(c.x, c.x, n);
+                        n = fmaf(c.y, c.y, n);
+                        n = fmaf(c.z, c.z, n);
+                        n = fmaf(c.w, c.w, n);
+                        v[VPR * r + 1] = n;
+                    }
+                }
             }
         }
     }
-    t = t0 + t1;
-    n = n0 + n1;
-}
-
-// Same with q read from shared memory (large D).
-template <bool COS>
-__device__ __forceinline__ void row_dot_smem(const float4* __restrict__ row, const float4* __restrict__ q4, int D4,
-                                             int lane, float& t, float& n) {
-    float t0 = 0.f, t1 = 0.f, n0 = 0.f, n1 = 0.f;
-#pragma unroll 4
-    for (int i = lane; i < D4; i += 32) {
-        const float4 c = row[i];
-        const float4 q = q4[i];
-        t0 = fmaf(c.x, q.x, t0);
-        t1 = fmaf(c.y, q.y, t1);
-        t0 = fmaf(c.z, q.z, t0);
-        t1 = fmaf(c.w, q.w, t1);
-        if (COS) {
-            n0 = fmaf(c.x, c.x, n0);
-            n1 = fmaf(c.y, c.y, n1);
-            n0 = fmaf(c.z, c.z, n0);
-            n1 = fmaf(c.w, c.w, n1);
-        }
-    }
-    t = t0 + t1;
-    n = n0 + n1;
 }
 
 template <int NQ4, bool COS>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamArgs args) {
     extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int VPR = COS ? 2 : 1;
+    constexpr int V = VPR * kMaxRowsPerStage;
     const Problem& p = args.p;
     const int K = p.K, D = p.D, D4 = p.D >> 2;
     const int R = args.rows_per_stage, NS = args.stages, G = args.cluster;
     const SmemLayout L = smem_layout(NS, R, D);
     float* ring = reinterpret_cast<float*>(smem + L.ring);
     float* qbuf = reinterpret_cast<float*>(smem + L.qbuf);
-    float* logits = reinterpret_cast<float*>(smem + L.logits);
+    float* tn = reinterpret_cast<float*>(smem + L.tn);
     float2* xch = reinterpret_cast<float2*>(smem + L.xch);
     volatile int* give_up = reinterpret_cast<volatile int*>(smem + L.flag);
     const uint32_t full0 = smem_u32(smem + L.bars);
@@ -261,17 +317,33 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(full0 + 8u * s, 1);
-            mbar_init(empty0 + 8u * s, kConsumerWarps);
+    // The ring must hold whole rounds of consumer warps (slot s is always
+    // owned by warp s % kConsumerWarps) and a stage at most kMaxRowsPerStage
+    // rows; the host plans it so. Every CTA sees the same arguments, so a bad
+    // plan makes every CTA of every cluster leave here, before any barrier.
+    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || R < 1 || R > kMaxRowsPerStage || 2 * NS + 4 > kStreamThreads) {
+        if (threadIdx.x == 0) atomicOr(&g_status, 2u);
+        return;
+    }
+
+    // Barrier set-up, one barrier per thread: full[s] and empty[s] complete
+    // once per use of stage slot s (one producer arrival + the copy's bytes;
+    // one arrival of the owning consumer warp), qfull/qempty per q slot.
+    {
+        const int t = threadIdx.x;
+        bool did = false;
+        if (t < 2 * NS) {
+            mbar_init(full0 + 8u * t, 1);
+            did = true;
+        } else if (t < 2 * NS + 2) {
+            mbar_init(qfull0 + 8u * (t - 2 * NS), 1);
+            did = true;
+        } else if (t < 2 * NS + 4) {
+            mbar_init(qempty0 + 8u * (t - 2 * NS - 2), kConsumerWarps);
+            did = true;
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(qfull0 + 8u * s, 1);
-            mbar_init(qempty0 + 8u * s, kConsumerWarps);
-        }
-        *give_up = 0;
-        fence_mbar_init();
+        if (t == 0) *give_up = 0;
+        if (did) fence_mbar_init();
     }
     __syncthreads();
 
@@ -293,6 +365,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     const int nrows = khi - klo;
     const int nst = (nrows + R - 1) / R;
     const uint32_t row_bytes = static_cast<uint32_t>(D) * 4u;
+    float qn = 1.f;  // clamped query norm of the current question (cosine)
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one elected thread issues every copy
@@ -331,7 +404,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         }
         __syncwarp();
     } else {
-        // ---------------- consumers
+        // ---------------- consumers: stage gst belongs to warp gst % kConsumerWarps
         uint32_t gst = 0;
         long long nq = 0;
         for (long long b = qb; b < qe; ++b, ++nq) {
@@ -339,7 +412,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
             const float4* q4 = reinterpret_cast<const float4*>(qbuf + qs * D);
             float4 qv[NQ4 > 0 ? NQ4 : 1];
-            float qn = 1.f;
             if constexpr (NQ4 > 0) {
                 float sq = 0.f;
 #pragma unroll
@@ -356,34 +428,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             } else if (COS) {
                 float sq = 0.f;
                 for (int i = lane; i < D4; i += 32) {
-                    const float4 v = q4[i];
-                    sq += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                    const float4 x = q4[i];
+                    sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
                 }
                 qn = fmaxf(sqrtf(warp_sum(sq)), kEps);
             }
 
-            float* lg = logits + (nq & 1) * kLogitSlots;
+            float* tb = tn + (nq & 1) * 2 * kLogitSlots;  // dots
+            float* nb = tb + kLogitSlots;                 // squared norms
             for (int s = 0; s < nst; ++s, ++gst) {
+                if (static_cast<int>(gst % kConsumerWarps) != warp) continue;
                 const uint32_t slot = gst % NS, par = (gst / NS) & 1u;
-                const bool ok = wait_phase(full0 + 8u * slot, par, give_up);
-                good = good && ok;
+                const bool ok = wait_phase(full0 + 8u * slot, par, give_up) && good;
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
-                const float* st = ring + static_cast<size_t>(slot) * R * D;
-                // rows r of this stage with (k0 + r) % kConsumerWarps == warp
-                int r = warp - (k0 % kConsumerWarps);
-                if (r < 0) r += kConsumerWarps;
-                for (; r < nr; r += kConsumerWarps) {
-                    const float4* row = reinterpret_cast<const float4*>(st + static_cast<size_t>(r) * D);
-                    float t, n;
-                    if constexpr (NQ4 > 0)
-                        row_dot_regs<NQ4, COS>(row, qv, D4, lane, t, n);
-                    else
-                        row_dot_smem<COS>(row, q4, D4, lane, t, n);
-                    t = warp_sum(t);
-                    if (COS) n = warp_sum(n);
-                    if (lane == 0)
-                        lg[k0 + r] = good ? logit_of(t, n, qn, p.scale, p.temperature, COS) : __int_as_float(0x7fc00000);
+                float v[V];
+                stage_dots<NQ4, COS>(reinterpret_cast<const float4*>(ring + static_cast<size_t>(slot) * R * D), nr, D4,
+                                     qv, q4, lane, v);
+                int idx;
+                const float sum = transpose_reduce<V>(v, lane, &idx);
+                if ((lane & (32 / V - 1)) == 0) {
+                    const int r = idx / VPR;
+                    if (r < nr) (VPR == 2 && (idx & 1) ? nb : tb)[k0 + r] = ok ? sum : __int_as_float(0x7fc00000);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8u * slot);
@@ -392,22 +458,29 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
             }
-            consumer_bar_sync();  // all logits of question b are in lg
-            if (G == 1 && warp == static_cast<int>(nq % kConsumerWarps))
-                softmax_store(lg, nrows, p.out + static_cast<size_t>(b) * K, lane);
+            consumer_bar_sync();  // every row of question b has its dot (and norm)
+            if (G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
+                float z[kLogitSlots / 32];
+                load_logits<COS>(tb, nb, nrows, qn, p.scale, p.temperature, lane, z);
+                softmax_store(z, nrows, p.out + static_cast<size_t>(b) * K, lane);
+            }
         }
     }
 
     if (G > 1) {
         // Cluster plan: one question per cluster; combine (local max, local
         // sum of exp) of every CTA through distributed shared memory.
-        const float* lg = logits;
+        float z[kLogitSlots / 32];
         if (warp == 0) {
+            load_logits<COS>(tn, tn + kLogitSlots, nrows, qn, p.scale, p.temperature, lane, z);
             float m = -INFINITY;
-            for (int k = lane; k < nrows; k += 32) m = fmaxf(m, lg[k]);
+#pragma unroll
+            for (int j = 0; j < kLogitSlots / 32; ++j) m = fmaxf(m, z[j]);
             m = warp_max(m);
             float s = 0.f;
-            for (int k = lane; k < nrows; k += 32) s += expf(lg[k] - m);
+#pragma unroll
+            for (int j = 0; j < kLogitSlots / 32; ++j)
+                if (lane + 32 * j < nrows) s += expf(z[j] - m);
             s = warp_sum(s);
             if (lane == 0) *xch = make_float2(m, s);
         }
@@ -416,14 +489,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         if (warp == 0) {
             float mj = -INFINITY, sj = 0.f;
             if (lane < G) {
-                const float2 v = ld_peer_f2(xch, static_cast<uint32_t>(lane));
-                mj = v.x;
-                sj = v.y;
+                const float2 x = ld_peer_f2(xch, static_cast<uint32_t>(lane));
+                mj = x.x;
+                sj = x.y;
             }
             const float M = warp_max(mj);
             const float S = warp_sum(lane < G ? sj * expf(mj - M) : 0.f);
             float* dst = p.out + static_cast<size_t>(qb) * K + klo;
-            for (int k = lane; k < nrows; k += 32) dst[k] = expf(lg[k] - M) / S;
+#pragma unroll
+            for (int j = 0; j < kLogitSlots / 32; ++j) {
+                const int k = lane + 32 * j;
+                if (k < nrows) dst[k] = expf(z[j] - M) / S;
+            }
         }
         __syncwarp();
         cluster_sync_all();  // no CTA leaves while a peer may still read its xch
@@ -474,7 +551,12 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         if (lane == 0) lg[k] = logit_of(t, n, qn, p.scale, p.temperature, COS);
     }
     __syncthreads();
-    if (warp == 0) softmax_store(lg, K, p.out + static_cast<size_t>(b) * K, lane);
+    if (warp == 0) {
+        float z[kLogitSlots / 32];
+#pragma unroll
+        for (int j = 0; j < kLogitSlots / 32; ++j) z[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
+        softmax_store(z, K, p.out + static_cast<size_t>(b) * K, lane);
+    }
 }
 
 // ------------------------------------------------------------------ dispatch
