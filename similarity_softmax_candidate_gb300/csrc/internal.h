@@ -9,10 +9,12 @@
 
 namespace cs {
 
-// Consumer warps per CTA of the streaming kernels; one more warp issues the
-// bulk copies.
+// Consumer warps per CTA of the streaming kernels. Two more warps issue the
+// bulk copies: kConsumerWarps lanes of one warp the candidate stages (lane l
+// fills exactly the ring slots consumer warp l drains), one lane of the
+// other the query rows.
 constexpr int kConsumerWarps = 8;
-constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStreamThreads = (kConsumerWarps + 2) * 32;
 // On-chip per-row results per question (K <= 255), one buffer per question
 // in flight.
 constexpr int kLogitSlots = 256;
@@ -54,8 +56,8 @@ struct SmemLayout {
     size_t ring;     // stages * rows_per_stage * D floats
     size_t qbuf;     // 2 slots of D floats
     size_t tn;       // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
-    size_t xch;      // one float2 (local max, local sum) for the cluster exchange
-    size_t bars;     // full[stages], empty[stages], qfull[2], qempty[2] (8 B each)
+    size_t xch;      // kMaxCluster float2 (max, sum) received from the cluster's CTAs
+    size_t bars;     // full[stages], empty[stages], qfull[2], qempty[2], xbar (8 B each)
     size_t flag;     // int: this CTA gave up waiting
     size_t total;
 };
@@ -66,8 +68,8 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
     L.ring = off;   off += (size_t)stages * rows_per_stage * D * sizeof(float);
     L.qbuf = off;   off += 2 * (size_t)D * sizeof(float);
     L.tn = off;     off += 4 * (size_t)kLogitSlots * sizeof(float);
-    L.xch = off;    off += 16;
-    L.bars = off;   off += (2 * (size_t)stages + 4) * 8;
+    L.xch = off;    off += (size_t)kMaxCluster * 8;
+    L.bars = off;   off += (2 * (size_t)stages + 5) * 8;
     L.flag = off;   off += 16;
     L.total = off;
     return L;

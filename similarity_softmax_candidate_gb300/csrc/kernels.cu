@@ -5,14 +5,16 @@
 //   z_k = scale * sim(q_b, c_k) / temperature,  p = softmax_k(z)
 // with sim the cosine (each norm clamped at 1e-8) or the plain dot. Each
 // candidate row is read once: its dot with q and its squared norm accumulate
-// from the same registers. Logits live only in shared memory.
+// from the same registers. Per-row results live only in shared memory.
 //
 // GB300 design (the page's kernel was one 1024-thread block per question on
-// sm_89; none of that is kept beyond "softmax in shared memory"):
-//   * stream_kernel -- a warp-specialised CTA: one elected thread issues 1-D
-//     bulk copies (cp.async.bulk, TMA engine) of whole candidate rows into a
-//     ring of shared-memory stages tracked by mbarriers. Stage g (up to 8
-//     rows) belongs to consumer warp g % 8, which computes the dots and
+// sm_89; of that only "softmax over shared memory" is kept):
+//   * stream_kernel -- a warp-specialised CTA: eight lanes of a producer
+//     warp issue 1-D bulk copies (cp.async.bulk, TMA engine) of whole
+//     candidate rows into a ring of shared-memory stages tracked by
+//     mbarriers, a second producer warp the query rows. Stage g (up to 8
+//     rows) is issued by lane g % 8 and belongs to consumer warp g % 8 --
+//     eight independent pipelines per CTA -- which computes the dots and
 //     squared norms of all its rows from float4 shared loads against q held
 //     in registers, then reduces them together with one transposed butterfly
 //     of warp shuffles. The per-row cosine and the softmax run later, one
@@ -21,9 +23,10 @@
 //         contiguous run of questions, prefetching the next question while a
 //         single warp finishes the previous question's softmax.
 //       - CLUSTER plan: one thread-block cluster (up to 16 CTAs) per
-//         question, the K rows striped over the CTAs; each CTA reduces its
-//         rows to (local max, local sum) and the CTAs combine them through
-//         distributed shared memory, so a single question uses 16 SMs.
+//         question, the K rows split over the CTAs; each CTA reduces its rows
+//         to (local max, local sum of exp) and pushes the pair into every
+//         peer's shared memory with st.async, completing on the peer's
+//         mbarrier, so one question uses up to 16 SMs.
 //   * generic_kernel -- scalar loads, any D and any alignment.
 // Every on-chip wait is bounded (about 1 s); a CTA that gives up sets a
 // device status bit, writes NaN where it could not finish, waits (bounded)
@@ -38,8 +41,10 @@ __device__ unsigned int g_status;
 
 namespace {
 
-constexpr float kEps = 1e-8f;                       // norm clamp of the cosine
+constexpr float kEps = 1e-8f;        // norm clamp of the cosine
+constexpr float kEps2 = 1e-16f;      // kEps squared: max(|c|, eps) = sqrt(max(|c|^2, eps^2))
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
+constexpr int kSlotsPerLane = kLogitSlots / 32;
 
 // ------------------------------------------------------------------ PTX
 
@@ -97,17 +102,28 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float2 ld_peer_f2(const void* local, uint32_t rank) {
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
-    return v;
+    return remote;
+}
+
+// Store a float2 into a peer CTA's shared memory; the 8 bytes complete as
+// transactions on the peer's mbarrier.
+__device__ __forceinline__ void st_async_peer(uint32_t remote_dst, float2 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     remote_dst),
+                 "f"(v.x), "f"(v.y), "r"(remote_bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ void consumer_bar_sync() {
@@ -154,42 +170,42 @@ __device__ __forceinline__ void wait_phase_until(uint32_t bar, uint32_t parity, 
     }
 }
 
-__device__ __forceinline__ float logit_of(float t, float n, float qn, float scale, float temperature, bool cos) {
-    float sim = cos ? t / (qn * fmaxf(sqrtf(n), kEps)) : t;
-    return scale * sim / temperature;
+// Logit factor of a question: z = a * t (dot) or a * t / max(|c|, eps)
+// (cosine, with a already divided by max(|q|, eps)).
+__device__ __forceinline__ float logit_factor(float qn, float scale, float temperature, bool cos) {
+    return cos ? scale / (temperature * qn) : scale / temperature;
 }
 
-// Logits of rows lane, lane+32, ... (< n) from their dot t and squared norm
+// Logits of rows lane, lane+32, ... (< n) from their dots t and squared norms
 // n_sq; -inf beyond n.
 template <bool COS>
-__device__ __forceinline__ void load_logits(const float* t, const float* n_sq, int n, float qn, float scale,
-                                            float temperature, int lane, float (&z)[kLogitSlots / 32]) {
+__device__ __forceinline__ void load_logits(const float* t, const float* n_sq, int n, float a, int lane,
+                                            float (&z)[kSlotsPerLane]) {
 #pragma unroll
-    for (int j = 0; j < kLogitSlots / 32; ++j) {
+    for (int j = 0; j < kSlotsPerLane; ++j) {
         const int k = lane + 32 * j;
-        z[j] = k < n ? logit_of(t[k], COS ? n_sq[k] : 0.f, qn, scale, temperature, COS) : -INFINITY;
+        z[j] = -INFINITY;
+        if (k < n) z[j] = COS ? a * t[k] * rsqrtf(fmaxf(n_sq[k], kEps2)) : a * t[k];
     }
 }
 
 // Softmax of z over one warp (rows lane + 32 j < n), written to dst[0..n).
-__device__ __forceinline__ void softmax_store(float (&z)[kLogitSlots / 32], int n, float* __restrict__ dst,
-                                              int lane) {
+__device__ __forceinline__ void softmax_store(float (&z)[kSlotsPerLane], int n, float* __restrict__ dst, int lane) {
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kLogitSlots / 32; ++j) m = fmaxf(m, z[j]);
+    for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
     m = warp_max(m);
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < kLogitSlots / 32; ++j) {
-        const int k = lane + 32 * j;
-        z[j] = k < n ? expf(z[j] - m) : 0.f;
+    for (int j = 0; j < kSlotsPerLane; ++j) {
+        z[j] = lane + 32 * j < n ? __expf(z[j] - m) : 0.f;
         s += z[j];
     }
-    s = warp_sum(s);
+    const float inv = 1.0f / warp_sum(s);
 #pragma unroll
-    for (int j = 0; j < kLogitSlots / 32; ++j) {
+    for (int j = 0; j < kSlotsPerLane; ++j) {
         const int k = lane + 32 * j;
-        if (k < n) dst[k] = z[j] / s;
+        if (k < n) dst[k] = z[j] * inv;
     }
 }
 
@@ -226,8 +242,10 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane, int* 
 struct StreamArgs {
     Problem p;
     int rows_per_stage;  // R <= kMaxRowsPerStage
-    int stages;          // NS
+    int stages;          // NS, a multiple of kConsumerWarps
     int cluster;         // G: CTAs per question (1 = STREAM plan)
+    int q_per_cta;       // STREAM plan: CTA c takes q_per_cta (+1 if c < q_rem) questions
+    int q_rem;
 };
 
 // Dots (and squared norms) of the nr <= kMaxRowsPerStage rows of one stage.
@@ -235,9 +253,9 @@ struct StreamArgs {
 // (NQ4 > 0) or from shared memory (NQ4 == 0, large D). Accumulators v hold
 // t_r at v[VPR*r] and, for the cosine, the squared norm at v[VPR*r + 1].
 template <int NQ4, bool COS>
-__device__ __forceinline__ void stage_dots(const float4* __restrict__ st, int nr, int D4, const float4 (&qv)[NQ4 > 0 ? NQ4 : 1],
-                                           const float4* __restrict__ q4, int lane,
-                                           float (&v)[(COS ? 2 : 1) * kMaxRowsPerStage]) {
+__device__ __forceinline__ void stage_dots(const float4* __restrict__ st, int nr, int D4,
+                                           const float4 (&qv)[NQ4 > 0 ? NQ4 : 1], const float4* __restrict__ q4,
+                                           int lane, float (&v)[(COS ? 2 : 1) * kMaxRowsPerStage]) {
     constexpr int VPR = COS ? 2 : 1;
 #pragma unroll
     for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = 0.f;
@@ -304,48 +322,49 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     const Problem& p = args.p;
     const int K = p.K, D = p.D, D4 = p.D >> 2;
     const int R = args.rows_per_stage, NS = args.stages, G = args.cluster;
-    const SmemLayout L = smem_layout(NS, R, D);
-    float* ring = reinterpret_cast<float*>(smem + L.ring);
-    float* qbuf = reinterpret_cast<float*>(smem + L.qbuf);
-    float* tn = reinterpret_cast<float*>(smem + L.tn);
-    float2* xch = reinterpret_cast<float2*>(smem + L.xch);
-    volatile int* give_up = reinterpret_cast<volatile int*>(smem + L.flag);
-    const uint32_t full0 = smem_u32(smem + L.bars);
-    const uint32_t empty0 = full0 + 8u * NS;
-    const uint32_t qfull0 = empty0 + 8u * NS;
-    const uint32_t qempty0 = qfull0 + 16u;
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // The ring must hold whole rounds of consumer warps (slot s is always
     // owned by warp s % kConsumerWarps) and a stage at most kMaxRowsPerStage
     // rows; the host plans it so. Every CTA sees the same arguments, so a bad
     // plan makes every CTA of every cluster leave here, before any barrier.
-    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || R < 1 || R > kMaxRowsPerStage || 2 * NS + 4 > kStreamThreads) {
+    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || R < 1 || R > kMaxRowsPerStage || G < 1 ||
+        G > kMaxCluster) {
         if (threadIdx.x == 0) atomicOr(&g_status, 2u);
         return;
     }
 
-    // Barrier set-up, one barrier per thread: full[s] and empty[s] complete
-    // once per use of stage slot s (one producer arrival + the copy's bytes;
-    // one arrival of the owning consumer warp), qfull/qempty per q slot.
-    {
-        const int t = threadIdx.x;
-        bool did = false;
-        if (t < 2 * NS) {
-            mbar_init(full0 + 8u * t, 1);
-            did = true;
-        } else if (t < 2 * NS + 2) {
-            mbar_init(qfull0 + 8u * (t - 2 * NS), 1);
-            did = true;
-        } else if (t < 2 * NS + 4) {
-            mbar_init(qempty0 + 8u * (t - 2 * NS - 2), kConsumerWarps);
-            did = true;
+    const SmemLayout L = smem_layout(NS, R, D);
+    float* ring = reinterpret_cast<float*>(smem + L.ring);
+    float* qbuf = reinterpret_cast<float*>(smem + L.qbuf);
+    float* tn = reinterpret_cast<float*>(smem + L.tn);
+    float2* xch = reinterpret_cast<float2*>(smem + L.xch);
+    volatile int* give_up = reinterpret_cast<volatile int*>(smem + L.flag);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8u * NS;
+    const uint32_t qfull0 = empty0 + 8u * NS;
+    const uint32_t qempty0 = qfull0 + 16u;
+    uint64_t* xbar = bars + 2 * NS + 4;
+
+    // Barrier set-up by warp 0: full[s] completes once per use of slot s
+    // (the producer's arrival plus the copy's bytes), empty[s] once its owner
+    // warp is done with it; qfull/qempty per q slot; xbar when every CTA of
+    // the cluster has pushed its (max, sum) here.
+    if (warp == 0) {
+        const int nbars = 2 * NS + 5;
+        for (int i = lane; i < nbars; i += 32) {
+            const uint32_t count = (i >= 2 * NS + 2 && i < 2 * NS + 4) ? kConsumerWarps : 1u;
+            mbar_init(full0 + 8u * i, count);
         }
-        if (t == 0) *give_up = 0;
-        if (did) fence_mbar_init();
+        if (lane == 0) *give_up = 0;
+        fence_mbar_init();
+        __syncwarp();
+        if (lane == 0 && G > 1) mbar_arrive_expect_tx(smem_u32(xbar), 8u * G);
     }
     __syncthreads();
+    // Cluster: announce "my barriers exist"; waited on before the first push.
+    if (G > 1) cluster_arrive_release();
 
     // Questions [qb, qe) and candidate rows [klo, khi) of this CTA.
     long long qb, qe;
@@ -357,61 +376,94 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         klo = rank * K / G;
         khi = (rank + 1) * K / G;
     } else {
-        qb = static_cast<long long>(blockIdx.x) * p.B / gridDim.x;
-        qe = static_cast<long long>(blockIdx.x + 1) * p.B / gridDim.x;
+        const int c = blockIdx.x;
+        qb = static_cast<long long>(c) * args.q_per_cta + min(c, args.q_rem);
+        qe = qb + args.q_per_cta + (c < args.q_rem ? 1 : 0);
         klo = 0;
         khi = K;
     }
     const int nrows = khi - klo;
     const int nst = (nrows + R - 1) / R;
     const uint32_t row_bytes = static_cast<uint32_t>(D) * 4u;
-    float qn = 1.f;  // clamped query norm of the current question (cosine)
+    float a = 1.f;  // logit factor of the current question
 
     if (warp == kConsumerWarps) {
-        // ---------------- producer: one elected thread issues every copy
+        // ---------------- stage producers: lane l issues stages g = l, l + 8, ...
+        // into slots l, l + 8, ... (the slots consumer warp l drains), so each
+        // lane reuses its own slots in order; eight lanes issue in parallel.
+        if (lane < kConsumerWarps) {
+            const long long nqs = qe - qb;
+            uint32_t slot = lane, phase = 0;
+            unsigned long long issued = 0;
+            long long n = 0;  // question of this lane's next stage, relative to qb
+            int s = lane;     // its stage index within that question
+            while (s >= nst) {
+                s -= nst;
+                ++n;
+            }
+            for (; n < nqs; ++issued) {
+                const uint32_t bar_e = empty0 + 8u * slot, bar_f = full0 + 8u * slot;
+                if (lane + kConsumerWarps * issued >= static_cast<unsigned long long>(NS) &&
+                    !wait_phase(bar_e, phase ^ 1u, give_up))
+                    break;
+                const int k0 = s * R;
+                const uint32_t bytes = static_cast<uint32_t>(min(R, nrows - k0)) * row_bytes;
+                mbar_arrive_expect_tx(bar_f, bytes);
+                bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * R * D),
+                         p.C + ((static_cast<size_t>(qb + n)) * K + klo + k0) * D, bytes, bar_f);
+                slot += kConsumerWarps;
+                if (slot >= static_cast<uint32_t>(NS)) {
+                    slot -= NS;
+                    phase ^= 1u;
+                }
+                s += kConsumerWarps;
+                while (s >= nst) {
+                    s -= nst;
+                    ++n;
+                }
+            }
+            if (*give_up) {
+                // Let this lane's copies in flight land before the CTA exits.
+                const unsigned long long deadline = globaltimer() + kWaitLimitNs;
+                const unsigned long long per_lane = static_cast<unsigned long long>(NS / kConsumerWarps);
+                for (unsigned long long m = issued > per_lane ? issued - per_lane : 0; m < issued; ++m) {
+                    const unsigned long long g = lane + kConsumerWarps * m;
+                    wait_phase_until(full0 + 8u * static_cast<uint32_t>(g % NS),
+                                     static_cast<uint32_t>((g / NS) & 1u), deadline);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kConsumerWarps + 1) {
+        // ---------------- query producer: one lane issues every question's q
         if (lane == 0) {
-            uint32_t gst = 0;
             long long nq = 0;
             for (long long b = qb; b < qe; ++b, ++nq) {
                 const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
-                if (!wait_phase(qempty0 + 8u * qs, qpar ^ 1u, give_up)) break;
+                if (nq >= 2 && !wait_phase(qempty0 + 8u * qs, qpar ^ 1u, give_up)) break;
                 mbar_arrive_expect_tx(qfull0 + 8u * qs, row_bytes);
                 bulk_g2s(smem_u32(qbuf + qs * D), p.Q + static_cast<size_t>(b) * D, row_bytes, qfull0 + 8u * qs);
-                bool stop = false;
-                for (int s = 0; s < nst; ++s, ++gst) {
-                    const uint32_t slot = gst % NS, par = (gst / NS) & 1u;
-                    if (!wait_phase(empty0 + 8u * slot, par ^ 1u, give_up)) { stop = true; break; }
-                    const int k0 = klo + s * R;
-                    const int nr = min(R, khi - k0);
-                    const uint32_t bytes = static_cast<uint32_t>(nr) * row_bytes;
-                    mbar_arrive_expect_tx(full0 + 8u * slot, bytes);
-                    bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * R * D),
-                             p.C + (static_cast<size_t>(b) * K + k0) * D, bytes, full0 + 8u * slot);
-                }
-                if (stop) { ++nq; break; }
             }
             if (*give_up) {
-                // Let this CTA's copies in flight land before it exits.
                 const unsigned long long deadline = globaltimer() + kWaitLimitNs;
-                const uint32_t last = gst < static_cast<uint32_t>(NS) ? gst : static_cast<uint32_t>(NS);
-                for (uint32_t u = gst - last; u < gst; ++u)
-                    wait_phase_until(full0 + 8u * (u % NS), (u / NS) & 1u, deadline);
-                const long long qlast = nq < 2 ? nq : 2;
-                for (long long u = nq - qlast; u < nq; ++u)
+                for (long long u = nq > 2 ? nq - 2 : 0; u < nq; ++u)
                     wait_phase_until(qfull0 + 8u * static_cast<uint32_t>(u & 1),
                                      static_cast<uint32_t>((u >> 1) & 1), deadline);
             }
         }
         __syncwarp();
     } else {
-        // ---------------- consumers: stage gst belongs to warp gst % kConsumerWarps
-        uint32_t gst = 0;
+        // ---------------- consumers: stage g belongs to warp g % kConsumerWarps;
+        // this warp's slots are warp, warp + 8, ... (NS is a multiple of 8)
+        uint32_t gst0 = 0;                // global index of the question's first stage
+        uint32_t slot = warp, phase = 0;  // this warp's next slot and its phase
         long long nq = 0;
-        for (long long b = qb; b < qe; ++b, ++nq) {
+        for (long long b = qb; b < qe; ++b, ++nq, gst0 += nst) {
             const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
             bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
             const float4* q4 = reinterpret_cast<const float4*>(qbuf + qs * D);
             float4 qv[NQ4 > 0 ? NQ4 : 1];
+            float qn = 1.f;
             if constexpr (NQ4 > 0) {
                 float sq = 0.f;
 #pragma unroll
@@ -433,13 +485,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 }
                 qn = fmaxf(sqrtf(warp_sum(sq)), kEps);
             }
+            a = logit_factor(qn, p.scale, p.temperature, COS);
 
             float* tb = tn + (nq & 1) * 2 * kLogitSlots;  // dots
             float* nb = tb + kLogitSlots;                 // squared norms
-            for (int s = 0; s < nst; ++s, ++gst) {
-                if (static_cast<int>(gst % kConsumerWarps) != warp) continue;
-                const uint32_t slot = gst % NS, par = (gst / NS) & 1u;
-                const bool ok = wait_phase(full0 + 8u * slot, par, give_up) && good;
+            // first stage of this question owned by this warp
+            int s = static_cast<int>((static_cast<uint32_t>(warp) + kConsumerWarps - gst0 % kConsumerWarps) %
+                                     kConsumerWarps);
+            for (; s < nst; s += kConsumerWarps) {
+                const uint32_t bar_f = full0 + 8u * slot, bar_e = empty0 + 8u * slot;
+                const bool ok = wait_phase(bar_f, phase, give_up) && good;
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
                 float v[V];
@@ -452,7 +507,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     if (r < nr) (VPR == 2 && (idx & 1) ? nb : tb)[k0 + r] = ok ? sum : __int_as_float(0x7fc00000);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+                if (lane == 0) mbar_arrive(bar_e);
+                slot += kConsumerWarps;
+                if (slot >= static_cast<uint32_t>(NS)) {
+                    slot -= NS;
+                    phase ^= 1u;
+                }
             }
             if constexpr (NQ4 == 0) {
                 __syncwarp();
@@ -460,50 +520,57 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             }
             consumer_bar_sync();  // every row of question b has its dot (and norm)
             if (G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
-                float z[kLogitSlots / 32];
-                load_logits<COS>(tb, nb, nrows, qn, p.scale, p.temperature, lane, z);
+                float z[kSlotsPerLane];
+                load_logits<COS>(tb, nb, nrows, a, lane, z);
                 softmax_store(z, nrows, p.out + static_cast<size_t>(b) * K, lane);
             }
         }
     }
 
     if (G > 1) {
-        // Cluster plan: one question per cluster; combine (local max, local
-        // sum of exp) of every CTA through distributed shared memory.
-        float z[kLogitSlots / 32];
+        // Cluster plan (one question per cluster): warp 0 reduces this CTA's
+        // rows to (m, s) = (max z, sum exp(z - m)), pushes the pair into slot
+        // `rank` of every peer's xch (completing on the peer's xbar), waits
+        // for all G pairs to arrive here, and writes p = exp(z - M) / S with
+        // M = max m_g and S = sum s_g exp(m_g - M).
+        cluster_wait();  // every CTA of the cluster has initialised its barriers
         if (warp == 0) {
-            load_logits<COS>(tn, tn + kLogitSlots, nrows, qn, p.scale, p.temperature, lane, z);
+            const uint32_t rank = cluster_ctarank();
+            float z[kSlotsPerLane];
+            load_logits<COS>(tn, tn + kLogitSlots, nrows, a, lane, z);
             float m = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kLogitSlots / 32; ++j) m = fmaxf(m, z[j]);
+            for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
             m = warp_max(m);
             float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < kLogitSlots / 32; ++j)
-                if (lane + 32 * j < nrows) s += expf(z[j] - m);
+            for (int j = 0; j < kSlotsPerLane; ++j)
+                if (lane + 32 * j < nrows) s += __expf(z[j] - m);
             s = warp_sum(s);
-            if (lane == 0) *xch = make_float2(m, s);
-        }
-        __syncwarp();
-        cluster_sync_all();  // every CTA's (m, s) is visible cluster-wide
-        if (warp == 0) {
+            if (lane < G)
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
+                              peer_addr(xbar, static_cast<uint32_t>(lane)));
+            const bool ok = wait_phase(smem_u32(xbar), 0, give_up);
             float mj = -INFINITY, sj = 0.f;
             if (lane < G) {
-                const float2 x = ld_peer_f2(xch, static_cast<uint32_t>(lane));
+                const float2 x = xch[lane];
                 mj = x.x;
                 sj = x.y;
             }
             const float M = warp_max(mj);
-            const float S = warp_sum(lane < G ? sj * expf(mj - M) : 0.f);
+            const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
             float* dst = p.out + static_cast<size_t>(qb) * K + klo;
 #pragma unroll
-            for (int j = 0; j < kLogitSlots / 32; ++j) {
+            for (int j = 0; j < kSlotsPerLane; ++j) {
                 const int k = lane + 32 * j;
-                if (k < nrows) dst[k] = expf(z[j] - M) / S;
+                if (k < nrows) dst[k] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
             }
         }
         __syncwarp();
-        cluster_sync_all();  // no CTA leaves while a peer may still read its xch
+        // Leave only when every CTA has received every pair: no push into a
+        // CTA that has exited, none left in flight.
+        cluster_arrive_release();
+        cluster_wait();
     }
 }
 
@@ -528,6 +595,7 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         }
         qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // whole norm per warp, never summed across warps
     }
+    const float a = logit_factor(qn, p.scale, p.temperature, COS);
     for (int k = warp; k < K; k += nwarps) {
         const float* __restrict__ c = p.C + (static_cast<size_t>(b) * K + k) * D;
         float t0 = 0.f, t1 = 0.f, n0 = 0.f, n1 = 0.f;
@@ -548,13 +616,13 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         }
         const float t = warp_sum(t0 + t1);
         const float n = COS ? warp_sum(n0 + n1) : 0.f;
-        if (lane == 0) lg[k] = logit_of(t, n, qn, p.scale, p.temperature, COS);
+        if (lane == 0) lg[k] = COS ? a * t * rsqrtf(fmaxf(n, kEps2)) : a * t;
     }
     __syncthreads();
     if (warp == 0) {
-        float z[kLogitSlots / 32];
+        float z[kSlotsPerLane];
 #pragma unroll
-        for (int j = 0; j < kLogitSlots / 32; ++j) z[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
+        for (int j = 0; j < kSlotsPerLane; ++j) z[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
         softmax_store(z, K, p.out + static_cast<size_t>(b) * K, lane);
     }
 }
@@ -630,6 +698,9 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, cudaStream_t strea
     a.rows_per_stage = plan.rows_per_stage;
     a.stages = plan.stages;
     a.cluster = plan.kind == kPlanCluster ? plan.cluster : 1;
+    const long long ctas = plan.kind == kPlanCluster ? 1 : plan.ctas;
+    a.q_per_cta = static_cast<int>(p.B / ctas);
+    a.q_rem = static_cast<int>(p.B % ctas);
     return p.normalize ? launch_stream_c<true>(a, plan, stream) : launch_stream_c<false>(a, plan, stream);
 }
 
