@@ -82,26 +82,38 @@ def cs_status_string(status: int) -> str:
 
 def _check(t, name, ndim):
     import torch
-    if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be on a CUDA device (host memory cannot be read by the kernel)")
-    if t.dtype != torch.float32:
-        raise TypeError(f"{name} must be float32, got {t.dtype}")
-    if not t.is_contiguous():
+    try:
+        ok = t.is_cuda and t.dtype == torch.float32 and t.dim() == ndim and t.is_contiguous()
+    except AttributeError:
+        raise TypeError(f"{name} must be a torch.Tensor") from None
+    if not ok:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device (host memory cannot be read by the kernel)")
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32, got {t.dtype}")
+        if t.dim() != ndim:
+            raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
         raise ValueError(f"{name} must be contiguous")
-    if t.dim() != ndim:
-        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
     return t.data_ptr()
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device):
     import torch
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def _call(fn, device, args, stream):
+    """Call fn(*args, stream) with `device` current (the library launches on
+    the current device); switches device only when it has to."""
+    import torch
+    if device.index == torch.cuda.current_device():
+        return fn(*args, _stream_handle(stream, device))
+    with torch.cuda.device(device):
+        return fn(*args, _stream_handle(stream, device))
 
 
 def cs_score_candidates(q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
@@ -117,9 +129,8 @@ def cs_score_candidates(q, C, normalize: int, scale: float, temperature: float, 
     op = _check(out, "out", 1)
     if out.shape[0] != K or out.device != C.device:
         raise ValueError(f"out must be [K={K}] on {C.device}")
-    with torch.cuda.device(C.device):
-        s = library().cs_score_candidates(qp, cp, K, D, int(normalize), float(scale), float(temperature),
-                                          op, _stream_handle(stream))
+    s = _call(library().cs_score_candidates, C.device,
+              (qp, cp, K, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates")
     return out
@@ -144,9 +155,8 @@ def cs_score_candidates_batch(Q, C, normalize: int, scale: float, temperature: f
     """B questions: Q[B,D], C[B,K,D] -> out[B,K] (float32, CUDA), one launch."""
     import torch
     qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
-    with torch.cuda.device(C.device):
-        s = library().cs_score_candidates_batch(qp, cp, B, K, D, int(normalize), float(scale),
-                                                float(temperature), op, _stream_handle(stream))
+    s = _call(library().cs_score_candidates_batch, C.device,
+              (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_batch")
     return out
@@ -157,10 +167,9 @@ def cs_score_candidates_batch_plan(Q, C, normalize: int, scale: float, temperatu
     """cs_score_candidates_batch with a caller-chosen plan (tests, tuning)."""
     import torch
     qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
-    with torch.cuda.device(C.device):
-        s = library().cs_score_candidates_batch_plan(qp, cp, B, K, D, int(normalize), float(scale),
-                                                     float(temperature), op, _stream_handle(stream),
-                                                     int(plan), int(cluster), int(ctas))
+    lib = library()
+    s = _call(lambda *a: lib.cs_score_candidates_batch_plan(*a, int(plan), int(cluster), int(ctas)), C.device,
+              (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_batch_plan")
     return out
