@@ -47,13 +47,14 @@ K = 255
 D = 512
 BYTES_PER_QUESTION = 4 * (K * D + D + K)  # C row block + q read once, p written once
 
-# The page's five shapes (PR #69, "What it is worth"), RTX 4090 fused times in us.
+# The page's five shapes (PR #69, "What it is worth"): RTX 4090 fused time in
+# us and fused/unfused speed-up, quoted as context.
 PAGE_SHAPES = [
-    ("clm-cosine-5x512", 1, 5, 512, 1, 9.2),
-    ("clm-cosine-64x512", 1, 64, 512, 1, 12.1),
-    ("clm-cosine-255x512", 1, 255, 512, 1, 23.6),
-    ("clm-cosine-batch8-255x512", 8, 255, 512, 1, 23.8),
-    ("kev-dot-255x2560", 1, 255, 2560, 0, 55.3),
+    ("clm-cosine-5x512", 1, 5, 512, 1, 9.2, 1.22),
+    ("clm-cosine-64x512", 1, 64, 512, 1, 12.1, 1.51),
+    ("clm-cosine-255x512", 1, 255, 512, 1, 23.6, 1.79),
+    ("clm-cosine-batch8-255x512", 8, 255, 512, 1, 23.8, 1.84),
+    ("kev-dot-255x2560", 1, 255, 2560, 0, 55.3, 1.81),
 ]
 
 METRIC = "questions/s (K=255, D=512, cosine, 16384 questions in 4 launches of 4096)"
@@ -313,6 +314,32 @@ def main():
     ms_dot, launches_dot, _ = timed(wl_dot)
     clock_info = clocks.stop()
 
+    # The unfused baseline on the same workload (two launches per slice).
+    staged = torch.empty((B_TOTAL, K), device=dev)
+    unfused = {}
+    for wl in (wl_cos, wl_dot):
+        def ustep(wl=wl):
+            for b0 in range(0, B_TOTAL, CHUNK):
+                cs.cs_score_candidates_batch_unfused(wl.Q[b0:b0 + CHUNK], wl.C[b0:b0 + CHUNK], wl.normalize,
+                                                     wl.scale, wl.temperature, staged=staged[b0:b0 + CHUNK],
+                                                     out=out[b0:b0 + CHUNK], stream=stream)
+        for _ in range(args.warmup):
+            ustep()
+        barrier()
+        ua, ub = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        usteps = max(3, args.steps // 4)
+        ua.record(stream)
+        for _ in range(usteps):
+            ustep()
+        ub.record(stream)
+        barrier()
+        ums = max_over_ranks(ua.elapsed_time(ub)) / usteps
+        fused_ms = (ms_cos if wl.normalize else ms_dot) / args.steps
+        unfused["cos" if wl.normalize else "dot"] = {
+            "questions_per_s": world * B_TOTAL / (ums / 1e3), "ms_per_step": ums,
+            "fused_over_unfused": ums / fused_ms, "steps": usteps}
+    del staged
+
     ms_per_step = ms_cos / args.steps
     value = world * B_TOTAL / (ms_per_step / 1e3)
     peak, peak_kind = _peak_hbm()
@@ -347,6 +374,7 @@ def main():
             "dot": {"questions_per_s": world * B_TOTAL / (dot_ms_step / 1e3), "ms_per_step": dot_ms_step,
                     "launch_gbs": launch_bytes / (dot_launch_ms / 1e3) / 1e9,
                     "frac": launch_bytes / (dot_launch_ms / 1e3) / 1e9 / peak},
+            "unfused_baseline": unfused,
         },
     }
 
@@ -375,7 +403,7 @@ def latency_table(cs, workloads, dev, calls):
     import torch
     rows = []
     flush = torch.empty(64 * 1024 * 1024, device=dev)  # 256 MB > L2
-    for name, B, k, d, normalize, page_us in PAGE_SHAPES:
+    for name, B, k, d, normalize, page_us, page_ratio in PAGE_SHAPES:
         wl = workloads.random_case(B, k, d, normalize, workloads.CLM_SCALE if normalize else workloads.KEV_SCALE,
                                    90 + k, dev)
         out = torch.empty(B, k, device=dev)
@@ -420,6 +448,37 @@ def latency_table(cs, workloads, dev, calls):
             torch.cuda.synchronize()
             reps.append(1e3 * a.elapsed_time(b) / calls)
         graph = statistics.median(reps)
+
+        def graph_loop_us(fn, n=50):
+            gl = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gl):
+                for _ in range(n):
+                    fn(torch.cuda.current_stream(dev))
+            for _ in range(3):
+                gl.replay()
+            torch.cuda.synchronize()
+            vals = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                for _ in range(20):
+                    gl.replay()
+                b.record(s)
+                torch.cuda.synchronize()
+                vals.append(1e3 * a.elapsed_time(b) / (20 * n))
+            del gl
+            return statistics.median(vals)
+
+        staged = torch.empty(B, k, device=dev)
+
+        def fused_on(st):
+            cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=st)
+
+        def unfused_on(st):
+            cs.cs_score_candidates_batch_unfused(wl.Q, wl.C, normalize, wl.scale, 1.0, staged=staged, out=out,
+                                                 stream=st)
+        fused_loop = graph_loop_us(fused_on)
+        unfused_loop = graph_loop_us(unfused_on)
         cold = []
         for _ in range(200):
             flush.fill_(1.0)
@@ -431,8 +490,10 @@ def latency_table(cs, workloads, dev, calls):
             cold.append(1e3 * a.elapsed_time(b))
         plan = cs.cs_query_plan(wl.Q, wl.C, normalize)
         rows.append({"shape": name, "B": B, "K": k, "D": d, "direct_us": direct, "graph_us": graph,
-                     "cold_l2_us": statistics.median(cold), "plan": plan["plan"], "cluster": plan["cluster"],
-                     "ctas": plan["ctas"], "rtx4090_fused_us_context": page_us})
+                     "graph_loop_us": fused_loop, "cold_l2_us": statistics.median(cold),
+                     "unfused_graph_loop_us": unfused_loop, "fused_over_unfused": unfused_loop / fused_loop,
+                     "plan": plan["plan"], "cluster": plan["cluster"], "ctas": plan["ctas"],
+                     "rtx4090_fused_us_context": page_us, "rtx4090_ratio_context": page_ratio})
         del g
     return rows
 

@@ -130,6 +130,26 @@ int cs_score_candidates_batch_plan(const float *Q, const float *C, int B,
                                    cs_stream_t stream, int plan, int cluster,
                                    int ctas);
 
+/*
+ * The unfused baseline, for comparison with the fused readout (PR #69,
+ * "What it is worth": a separate norm pass plus the scoring block with the
+ * row norm loaded from a staged array, reading C twice; for the dot, whose
+ * similarity has no norm to fuse, the same split costs a second kernel and a
+ * global round trip of the similarities, "What is fused, precisely").
+ *   pass 1: staged[b][k] = |c_bk| (cosine) or c_bk . q_b (dot)
+ *   pass 2: cosine: the scoring kernel again, dots recomputed from C, norms
+ *           read from staged; dot: softmax of scale * staged / temperature.
+ * Same arguments and result as cs_score_candidates_batch (within float32
+ * rounding), plus `staged`: a caller-owned device buffer of B*K floats that
+ * must not overlap Q, C or out; its contents on return are pass 1's values.
+ * Two kernels are enqueued on `stream` (two graph nodes when captured).
+ * Needs D % 4 == 0 and 16-byte aligned Q and C (CS_ERR_BAD_PLAN otherwise).
+ */
+int cs_score_candidates_batch_unfused(const float *Q, const float *C, int B,
+                                      int K, int D, int normalize, float scale,
+                                      float temperature, float *staged,
+                                      float *out, cs_stream_t stream);
+
 /* Device status word bits (see cs_device_status). */
 #define CS_DEVERR_WAIT_TIMEOUT 1u  /* an on-chip wait gave up after ~1 s */
 #define CS_DEVERR_BAD_CONFIG 2u    /* a kernel refused an inconsistent launch plan */

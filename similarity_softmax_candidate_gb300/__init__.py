@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     cs_score_candidates,
     cs_score_candidates_batch,
     cs_score_candidates_batch_plan,
+    cs_score_candidates_batch_unfused,
     cs_status_string,
     library,
 )

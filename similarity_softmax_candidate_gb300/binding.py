@@ -64,6 +64,8 @@ def library() -> ctypes.CDLL:
         lib.cs_score_candidates_batch.restype = I
         lib.cs_score_candidates_batch_plan.argtypes = [P, P, I, I, I, I, F, F, P, P, I, I, I]
         lib.cs_score_candidates_batch_plan.restype = I
+        lib.cs_score_candidates_batch_unfused.argtypes = [P, P, I, I, I, I, F, F, P, P, P]
+        lib.cs_score_candidates_batch_unfused.restype = I
         lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
         lib.cs_query_plan.restype = I
         lib.cs_device_status.argtypes = [U, I]
@@ -172,6 +174,26 @@ def cs_score_candidates_batch_plan(Q, C, normalize: int, scale: float, temperatu
               (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_batch_plan")
+    return out
+
+
+def cs_score_candidates_batch_unfused(Q, C, normalize: int, scale: float, temperature: float, staged=None,
+                                      out=None, stream=None):
+    """The unfused baseline (two launches): pass 1 stages one float per row
+    in `staged` [B,K] (allocated here by torch when None), pass 2 scores from
+    it. Same result as cs_score_candidates_batch within float32 rounding."""
+    import torch
+    qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
+    if staged is None:
+        staged = torch.empty((B, K), device=C.device, dtype=torch.float32)
+    sp = _check(staged, "staged", 2)
+    if tuple(staged.shape) != (B, K) or staged.device != C.device:
+        raise ValueError(f"staged must be [B={B}, K={K}] on {C.device}")
+    lib = library()
+    s = _call(lambda *a: lib.cs_score_candidates_batch_unfused(*a[:8], sp, op, a[8]), C.device,
+              (qp, cp, B, K, D, int(normalize), float(scale), float(temperature)), stream)
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_batch_unfused")
     return out
 
 

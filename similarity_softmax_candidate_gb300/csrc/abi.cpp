@@ -258,12 +258,44 @@ int run(const float* Q, const float* C, long long B, int K, int D, int normalize
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, scale, temperature};
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, nullptr};
     Plan plan{};
     const int s = make_plan(*d, p, kind, cluster, ctas, &plan);
     if (s != CS_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = plan.kind == cs::kPlanGeneric ? cs::launch_generic(p, st) : cs::launch_stream(p, plan, st);
+    const cudaError_t e = plan.kind == cs::kPlanGeneric
+                              ? cs::launch_generic(p, st)
+                              : cs::launch_stream(p, plan, normalize ? cs::kFusedCos : cs::kFusedDot, st);
+    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
+bool overlaps(const void* a, unsigned long long abytes, const void* b, unsigned long long bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// The unfused baseline: pass 1 stages one value per row in `staged`, pass 2
+// scores from it. Two launches on `stream`.
+int run_unfused(const float* Q, const float* C, long long B, int K, int D, int normalize, float scale,
+                float temperature, float* staged, float* out, cs_stream_t stream) {
+    const int v = validate(Q, C, B, K, D, normalize, out, true, true, scale, temperature);
+    if (v != CS_OK) return v;
+    if (!staged) return CS_ERR_NULL_POINTER;
+    const unsigned long long bk4 = static_cast<unsigned long long>(B) * K * 4ull;
+    if (overlaps(staged, bk4, out, bk4) || overlaps(staged, bk4, Q, static_cast<unsigned long long>(B) * D * 4ull) ||
+        overlaps(staged, bk4, C, bk4 * static_cast<unsigned long long>(D)))
+        return CS_ERR_ALIAS;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, staged};
+    Plan plan{};
+    const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
+    if (s != CS_OK) return s;
+    if (plan.kind == cs::kPlanGeneric) return CS_ERR_BAD_PLAN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cs::launch_stream(p, plan, normalize ? cs::kRowNorm : cs::kRowDot, st);
+    if (e == cudaSuccess)
+        e = normalize ? cs::launch_stream(p, plan, cs::kStagedCos, st) : cs::launch_staged_softmax(p, st);
     return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
 }
 
@@ -309,13 +341,19 @@ int cs_score_candidates_batch_plan(const float* Q, const float* C, int B, int K,
     return run(Q, C, B, K, D, normalize, scale, temperature, out, stream, plan, cluster, ctas);
 }
 
+int cs_score_candidates_batch_unfused(const float* Q, const float* C, int B, int K, int D, int normalize,
+                                      float scale, float temperature, float* staged, float* out,
+                                      cs_stream_t stream) {
+    return run_unfused(Q, C, B, K, D, normalize, scale, temperature, staged, out, stream);
+}
+
 int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int normalize, int* plan, int* cluster,
                   int* ctas, int* smem_bytes) {
     const int v = validate(Q, C, B, K, D, normalize, nullptr, false, false, 1.f, 1.f);
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f};
+    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f, nullptr};
     Plan pl{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &pl);
     if (s != CS_OK) return s;

@@ -36,6 +36,7 @@ struct Problem {
     int normalize;     // 1 cosine, 0 dot
     float scale;       // multiplies the similarity
     float temperature; // divides the scaled similarity
+    float* staged;     // unfused baseline only: one float per row [B][K]
 };
 
 enum PlanKind { kPlanAuto = 0, kPlanStream = 1, kPlanCluster = 2, kPlanGeneric = 3 };
@@ -75,10 +76,21 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
     return L;
 }
 
+// What one launch of the streaming kernel computes.
+enum StreamMode {
+    kFusedCos = 0,   // the fused readout, cosine
+    kFusedDot = 1,   // the fused readout, dot
+    kRowNorm = 2,    // unfused baseline pass 1 (cosine): staged[row] = |c|
+    kRowDot = 3,     // unfused baseline pass 1 (dot):    staged[row] = c . q
+    kStagedCos = 4,  // unfused baseline pass 2 (cosine): dots, norms read from staged, softmax
+};
+
 // Launchers (kernels.cu). Each enqueues exactly one kernel on `stream` and
 // returns the launch status; none synchronizes or allocates.
-cudaError_t launch_stream(const Problem& p, const Plan& plan, cudaStream_t stream);
+cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStream_t stream);
 cudaError_t launch_generic(const Problem& p, cudaStream_t stream);
+// Unfused baseline pass 2 (dot): softmax of scale * staged / temperature.
+cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream);
 
 // One-time per-device kernel attributes (dynamic smem ceiling, cluster size).
 cudaError_t configure_device_kernels(int smem_optin);

@@ -28,6 +28,12 @@
 //         peer's shared memory with st.async, completing on the peer's
 //         mbarrier, so one question uses up to 16 SMs.
 //   * generic_kernel -- scalar loads, any D and any alignment.
+//   * the unfused baseline (PR #69, "What it is worth": a separate norm pass
+//     and a scoring block that loads the norm from a staged array) reuses
+//     stream_kernel: pass 1 writes one value per row (the norm, or for the dot
+//     the similarity) to a staged array in global memory; pass 2 is the
+//     scoring block reading the staged norms (cosine) or staged_softmax_kernel
+//     (dot).
 // Every on-chip wait is bounded (about 1 s); a CTA that gives up sets a
 // device status bit, writes NaN where it could not finish, waits (bounded)
 // for its own copies in flight, and exits.
@@ -45,6 +51,13 @@ constexpr float kEps = 1e-8f;        // norm clamp of the cosine
 constexpr float kEps2 = 1e-16f;      // kEps squared: max(|c|, eps) = sqrt(max(|c|^2, eps^2))
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 constexpr int kSlotsPerLane = kLogitSlots / 32;
+
+// What a StreamMode accumulates per row and what it finishes with.
+__host__ __device__ constexpr bool acc_norm(int m) { return m == kFusedCos || m == kRowNorm; }  // c . c
+__host__ __device__ constexpr bool acc_dot(int m) { return m != kRowNorm; }                     // c . q
+__host__ __device__ constexpr int values_per_row(int m) { return acc_norm(m) && acc_dot(m) ? 2 : 1; }
+__host__ __device__ constexpr bool does_softmax(int m) { return m == kFusedCos || m == kFusedDot || m == kStagedCos; }
+__host__ __device__ constexpr bool cos_logits(int m) { return m == kFusedCos || m == kStagedCos; }
 
 // ------------------------------------------------------------------ PTX
 
@@ -176,16 +189,24 @@ __device__ __forceinline__ float logit_factor(float qn, float scale, float tempe
     return cos ? scale / (temperature * qn) : scale / temperature;
 }
 
-// Logits of rows lane, lane+32, ... (< n) from their dots t and squared norms
-// n_sq; -inf beyond n.
-template <bool COS>
-__device__ __forceinline__ void load_logits(const float* t, const float* n_sq, int n, float a, int lane,
-                                            float (&z)[kSlotsPerLane]) {
+// Logits of rows lane, lane+32, ... (< n) from their dots t and, for the
+// fused cosine, squared norms n_sq, or, for the staged cosine, norms read
+// from the staged array; -inf beyond n.
+template <int MODE>
+__device__ __forceinline__ void load_logits(const float* t, const float* n_sq, const float* staged_norm, int n,
+                                            float a, int lane, float (&z)[kSlotsPerLane]) {
 #pragma unroll
     for (int j = 0; j < kSlotsPerLane; ++j) {
         const int k = lane + 32 * j;
         z[j] = -INFINITY;
-        if (k < n) z[j] = COS ? a * t[k] * rsqrtf(fmaxf(n_sq[k], kEps2)) : a * t[k];
+        if (k < n) {
+            if (MODE == kFusedCos)
+                z[j] = a * t[k] * rsqrtf(fmaxf(n_sq[k], kEps2));
+            else if (MODE == kStagedCos)
+                z[j] = a * t[k] / fmaxf(staged_norm[k], kEps);
+            else
+                z[j] = a * t[k];
+        }
     }
 }
 
@@ -248,77 +269,63 @@ struct StreamArgs {
     int q_rem;
 };
 
-// Dots (and squared norms) of the nr <= kMaxRowsPerStage rows of one stage.
-// Lane handles float4 columns lane, lane+32, ...; q comes from registers
-// (NQ4 > 0) or from shared memory (NQ4 == 0, large D). Accumulators v hold
-// t_r at v[VPR*r] and, for the cosine, the squared norm at v[VPR*r + 1].
-template <int NQ4, bool COS>
+// Per-row sums of the nr <= kMaxRowsPerStage rows of one stage. Lane
+// handles float4 columns lane, lane+32, ...; q comes from registers
+// (NQ4 > 0) or from shared memory (NQ4 == 0, large D). With two values per
+// row (fused cosine) v[2r] = c_r . q and v[2r + 1] = c_r . c_r; with one,
+// v[r] = c_r . q, or c_r . c_r for the norm pass.
+template <int NQ4, int MODE>
 __device__ __forceinline__ void stage_dots(const float4* __restrict__ st, int nr, int D4,
                                            const float4 (&qv)[NQ4 > 0 ? NQ4 : 1], const float4* __restrict__ q4,
-                                           int lane, float (&v)[(COS ? 2 : 1) * kMaxRowsPerStage]) {
-    constexpr int VPR = COS ? 2 : 1;
+                                           int lane, float (&v)[values_per_row(MODE) * kMaxRowsPerStage]) {
+    constexpr int VPR = values_per_row(MODE);
 #pragma unroll
     for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = 0.f;
+    auto accumulate = [&](const float4& c, const float4& q, int r) {
+        if (acc_dot(MODE)) {
+            float t = v[VPR * r];
+            t = fmaf(c.x, q.x, t);
+            t = fmaf(c.y, q.y, t);
+            t = fmaf(c.z, q.z, t);
+            t = fmaf(c.w, q.w, t);
+            v[VPR * r] = t;
+        }
+        if (acc_norm(MODE)) {
+            const int i = VPR * r + VPR - 1;
+            float n = v[i];
+            n = fmaf(c.x, c.x, n);
+            n = fmaf(c.y, c.y, n);
+            n = fmaf(c.z, c.z, n);
+            n = fmaf(c.w, c.w, n);
+            v[i] = n;
+        }
+    };
     if constexpr (NQ4 > 0) {
 #pragma unroll
         for (int j = 0; j < NQ4; ++j) {
             const int i = lane + 32 * j;
             if (i < D4) {
-                const float4 q = qv[j];
 #pragma unroll
-                for (int r = 0; r < kMaxRowsPerStage; ++r) {
-                    if (r < nr) {
-                        const float4 c = st[r * D4 + i];
-                        float t = v[VPR * r];
-                        t = fmaf(c.x, q.x, t);
-                        t = fmaf(c.y, q.y, t);
-                        t = fmaf(c.z, q.z, t);
-                        t = fmaf(c.w, q.w, t);
-                        v[VPR * r] = t;
-                        if (COS) {
-                            float n = v[VPR * r + 1];
-                            n = fmaf(c.x, c.x, n);
-                            n = fmaf(c.y, c.y, n);
-                            n = fmaf(c.z, c.z, n);
-                            n = fmaf(c.w, c.w, n);
-                            v[VPR * r + 1] = n;
-                        }
-                    }
-                }
+                for (int r = 0; r < kMaxRowsPerStage; ++r)
+                    if (r < nr) accumulate(st[r * D4 + i], qv[j], r);
             }
         }
     } else {
         for (int i = lane; i < D4; i += 32) {
             const float4 q = q4[i];
 #pragma unroll
-            for (int r = 0; r < kMaxRowsPerStage; ++r) {
-                if (r < nr) {
-                    const float4 c = st[r * D4 + i];
-                    float t = v[VPR * r];
-                    t = fmaf(c.x, q.x, t);
-                    t = fmaf(c.y, q.y, t);
-                    t = fmaf(c.z, q.z, t);
-                    t = fmaf(c.w, q.w, t);
-                    v[VPR * r] = t;
-                    if (COS) {
-                        float n = v[VPR * r + 1];
-                        n = fmaf(c.x, c.x, n);
-                        n = fmaf(c.y, c.y, n);
-                        n = fmaf(c.z, c.z, n);
-                        n = fmaf(c.w, c.w, n);
-                        v[VPR * r + 1] = n;
-                    }
-                }
-            }
+            for (int r = 0; r < kMaxRowsPerStage; ++r)
+                if (r < nr) accumulate(st[r * D4 + i], q, r);
         }
     }
 }
 
-template <int NQ4, bool COS>
+template <int NQ4, int MODE>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamArgs args) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int VPR = COS ? 2 : 1;
+    constexpr int VPR = values_per_row(MODE);
     constexpr int V = VPR * kMaxRowsPerStage;
+    constexpr bool COS = cos_logits(MODE);
     const Problem& p = args.p;
     const int K = p.K, D = p.D, D4 = p.D >> 2;
     const int R = args.rows_per_stage, NS = args.stages, G = args.cluster;
@@ -360,11 +367,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         if (lane == 0) *give_up = 0;
         fence_mbar_init();
         __syncwarp();
-        if (lane == 0 && G > 1) mbar_arrive_expect_tx(smem_u32(xbar), 8u * G);
+        if (lane == 0 && G > 1 && does_softmax(MODE)) mbar_arrive_expect_tx(smem_u32(xbar), 8u * G);
     }
     __syncthreads();
     // Cluster: announce "my barriers exist"; waited on before the first push.
-    if (G > 1) cluster_arrive_release();
+    if (G > 1 && does_softmax(MODE)) cluster_arrive_release();
 
     // Questions [qb, qe) and candidate rows [klo, khi) of this CTA.
     long long qb, qe;
@@ -498,13 +505,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
                 float v[V];
-                stage_dots<NQ4, COS>(reinterpret_cast<const float4*>(ring + static_cast<size_t>(slot) * R * D), nr, D4,
-                                     qv, q4, lane, v);
+                stage_dots<NQ4, MODE>(reinterpret_cast<const float4*>(ring + static_cast<size_t>(slot) * R * D), nr,
+                                      D4, qv, q4, lane, v);
                 int idx;
                 const float sum = transpose_reduce<V>(v, lane, &idx);
                 if ((lane & (32 / V - 1)) == 0) {
                     const int r = idx / VPR;
-                    if (r < nr) (VPR == 2 && (idx & 1) ? nb : tb)[k0 + r] = ok ? sum : __int_as_float(0x7fc00000);
+                    const float val = ok ? sum : __int_as_float(0x7fc00000);
+                    if (r < nr) {
+                        if constexpr (does_softmax(MODE))
+                            (VPR == 2 && (idx & 1) ? nb : tb)[k0 + r] = val;
+                        else
+                            p.staged[static_cast<size_t>(b) * K + klo + k0 + r] = MODE == kRowNorm ? sqrtf(val) : val;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_e);
@@ -519,15 +532,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
             }
             consumer_bar_sync();  // every row of question b has its dot (and norm)
-            if (G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
+            if (does_softmax(MODE) && G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
                 float z[kSlotsPerLane];
-                load_logits<COS>(tb, nb, nrows, a, lane, z);
+                load_logits<MODE>(tb, nb, MODE == kStagedCos ? p.staged + static_cast<size_t>(b) * K : nullptr,
+                                  nrows, a, lane, z);
                 softmax_store(z, nrows, p.out + static_cast<size_t>(b) * K, lane);
             }
         }
     }
 
-    if (G > 1) {
+    if (G > 1 && does_softmax(MODE)) {
         // Cluster plan (one question per cluster): warp 0 reduces this CTA's
         // rows to (m, s) = (max z, sum exp(z - m)), pushes the pair into slot
         // `rank` of every peer's xch (completing on the peer's xbar), waits
@@ -537,7 +551,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         if (warp == 0) {
             const uint32_t rank = cluster_ctarank();
             float z[kSlotsPerLane];
-            load_logits<COS>(tn, tn + kLogitSlots, nrows, a, lane, z);
+            load_logits<MODE>(tn, tn + kLogitSlots,
+                              MODE == kStagedCos ? p.staged + static_cast<size_t>(qb) * K + klo : nullptr, nrows, a,
+                              lane, z);
             float m = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
@@ -627,9 +643,26 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     }
 }
 
+// Unfused baseline pass 2 (dot): one warp per question, softmax of
+// scale * staged / temperature over the question's K staged similarities.
+__global__ void __launch_bounds__(256) staged_softmax_kernel(const Problem p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long b = static_cast<long long>(blockIdx.x) * 8 + warp;
+    if (b >= p.B) return;
+    const float a = p.scale / p.temperature;
+    const float* t = p.staged + static_cast<size_t>(b) * p.K;
+    float z[kSlotsPerLane];
+#pragma unroll
+    for (int j = 0; j < kSlotsPerLane; ++j) {
+        const int k = lane + 32 * j;
+        z[j] = k < p.K ? a * t[k] : -INFINITY;
+    }
+    softmax_store(z, p.K, p.out + static_cast<size_t>(b) * p.K, lane);
+}
+
 // ------------------------------------------------------------------ dispatch
 
-template <int NQ4, bool COS>
+template <int NQ4, int MODE>
 cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -649,50 +682,47 @@ cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t 
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, stream_kernel<NQ4, COS>, a);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<NQ4, MODE>, a);
 }
 
-template <bool COS>
-cudaError_t launch_stream_c(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
+template <int MODE>
+cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     switch (plan.nq4) {
-        case 1: return launch_stream_t<1, COS>(a, plan, stream);
-        case 2: return launch_stream_t<2, COS>(a, plan, stream);
-        case 4: return launch_stream_t<4, COS>(a, plan, stream);
-        case 8: return launch_stream_t<8, COS>(a, plan, stream);
-        case 0: return launch_stream_t<0, COS>(a, plan, stream);
+        case 1: return launch_stream_t<1, MODE>(a, plan, stream);
+        case 2: return launch_stream_t<2, MODE>(a, plan, stream);
+        case 4: return launch_stream_t<4, MODE>(a, plan, stream);
+        case 8: return launch_stream_t<8, MODE>(a, plan, stream);
+        case 0: return launch_stream_t<0, MODE>(a, plan, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int NQ4, bool COS>
-const void* stream_fn() {
-    return reinterpret_cast<const void*>(stream_kernel<NQ4, COS>);
+template <int MODE>
+const void* stream_fn_m(int nq4) {
+    switch (nq4) {
+        case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE>);
+        case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE>);
+        case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE>);
+        case 8: return reinterpret_cast<const void*>(stream_kernel<8, MODE>);
+        case 0: return reinterpret_cast<const void*>(stream_kernel<0, MODE>);
+    }
+    return nullptr;
 }
 
-const void* stream_fn_for(int nq4, int normalize) {
-    if (normalize) {
-        switch (nq4) {
-            case 1: return stream_fn<1, true>();
-            case 2: return stream_fn<2, true>();
-            case 4: return stream_fn<4, true>();
-            case 8: return stream_fn<8, true>();
-            case 0: return stream_fn<0, true>();
-        }
-    } else {
-        switch (nq4) {
-            case 1: return stream_fn<1, false>();
-            case 2: return stream_fn<2, false>();
-            case 4: return stream_fn<4, false>();
-            case 8: return stream_fn<8, false>();
-            case 0: return stream_fn<0, false>();
-        }
+const void* stream_fn_for(int nq4, int mode) {
+    switch (mode) {
+        case kFusedCos: return stream_fn_m<kFusedCos>(nq4);
+        case kFusedDot: return stream_fn_m<kFusedDot>(nq4);
+        case kRowNorm: return stream_fn_m<kRowNorm>(nq4);
+        case kRowDot: return stream_fn_m<kRowDot>(nq4);
+        case kStagedCos: return stream_fn_m<kStagedCos>(nq4);
     }
     return nullptr;
 }
 
 }  // namespace
 
-cudaError_t launch_stream(const Problem& p, const Plan& plan, cudaStream_t stream) {
+cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStream_t stream) {
     StreamArgs a;
     a.p = p;
     a.rows_per_stage = plan.rows_per_stage;
@@ -701,7 +731,20 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, cudaStream_t strea
     const long long ctas = plan.kind == kPlanCluster ? 1 : plan.ctas;
     a.q_per_cta = static_cast<int>(p.B / ctas);
     a.q_rem = static_cast<int>(p.B % ctas);
-    return p.normalize ? launch_stream_c<true>(a, plan, stream) : launch_stream_c<false>(a, plan, stream);
+    switch (mode) {
+        case kFusedCos: return launch_stream_m<kFusedCos>(a, plan, stream);
+        case kFusedDot: return launch_stream_m<kFusedDot>(a, plan, stream);
+        case kRowNorm: return launch_stream_m<kRowNorm>(a, plan, stream);
+        case kRowDot: return launch_stream_m<kRowDot>(a, plan, stream);
+        case kStagedCos: return launch_stream_m<kStagedCos>(a, plan, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>((p.B + 7) / 8)), block(256);
+    staged_softmax_kernel<<<grid, block, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_generic(const Problem& p, cudaStream_t stream) {
@@ -715,9 +758,9 @@ cudaError_t launch_generic(const Problem& p, cudaStream_t stream) {
 
 cudaError_t configure_device_kernels(int smem_optin) {
     const int nq4s[5] = {1, 2, 4, 8, 0};
-    for (int c = 0; c < 2; ++c) {
+    for (int m = kFusedCos; m <= kStagedCos; ++m) {
         for (int i = 0; i < 5; ++i) {
-            const void* f = stream_fn_for(nq4s[i], c);
+            const void* f = stream_fn_for(nq4s[i], m);
             cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -728,7 +771,7 @@ cudaError_t configure_device_kernels(int smem_optin) {
 }
 
 int max_active_clusters(int cluster, size_t smem, int nq4, int normalize) {
-    const void* f = stream_fn_for(nq4, normalize);
+    const void* f = stream_fn_for(nq4, normalize ? kFusedCos : kFusedDot);
     if (!f) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

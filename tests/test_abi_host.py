@@ -160,3 +160,24 @@ def test_binding_refuses_host_tensors():
     C = torch.zeros(3, 8)
     with pytest.raises(ValueError, match="CUDA device"):
         binding.cs_score_candidates(q, C, 1, 1.0, 1.0)
+
+
+STAGED_ADDR = 0x7F3000000000
+
+
+def _unfused(lib, Q=Q_ADDR, C=C_ADDR, B=1, K=5, D=512, normalize=1, scale=14.2857, temperature=1.0,
+             staged=STAGED_ADDR, out=OUT_ADDR):
+    return lib.cs_score_candidates_batch_unfused(Q, C, B, K, D, normalize, scale, temperature, staged, out, None)
+
+
+@pytest.mark.parametrize("name,kw,status", REJECTS, ids=[r[0] for r in REJECTS])
+def test_unfused_rejects(host_lib, name, kw, status):
+    assert _unfused(host_lib, **kw) == status
+
+
+def test_unfused_rejects_null_or_overlapping_staged(host_lib):
+    assert _unfused(host_lib, staged=None) == binding.CS_ERR_NULL_POINTER
+    B, K, D = 4, 8, 16
+    assert _unfused(host_lib, B=B, K=K, D=D, staged=C_ADDR + 64) == binding.CS_ERR_ALIAS
+    assert _unfused(host_lib, B=B, K=K, D=D, staged=OUT_ADDR + 4 * (B * K - 1)) == binding.CS_ERR_ALIAS
+    assert _unfused(host_lib, B=B, K=K, D=D, staged=Q_ADDR) == binding.CS_ERR_ALIAS
