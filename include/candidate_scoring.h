@@ -68,7 +68,8 @@ typedef enum {
     CS_ERR_LAUNCH = 9,         /* a CUDA call failed; nothing useful was queued */
     CS_ERR_ALIAS = 10,         /* out overlaps Q or C */
     CS_ERR_TOO_LARGE = 11,     /* B*K*D elements do not fit the 64-bit index space */
-    CS_ERR_BAD_PLAN = 12       /* cs_score_candidates_batch_plan: plan not feasible */
+    CS_ERR_BAD_PLAN = 12,      /* cs_score_candidates_batch_plan: plan not feasible */
+    CS_ERR_SCRATCH_TOO_SMALL = 13 /* B*K above CS_NOALLOC_MAX_ROWS (no-allocation entry) */
 } cs_status;
 
 /* ABI version of this header and library: 1. */
@@ -149,6 +150,34 @@ int cs_score_candidates_batch_unfused(const float *Q, const float *C, int B,
                                       int K, int D, int normalize, float scale,
                                       float temperature, float *staged,
                                       float *out, cs_stream_t stream);
+
+/*
+ * cs_score_candidates_batch_unfused without the `staged` argument: the
+ * staged array is a buffer built into the library, so the call allocates
+ * nothing and needs no scratch from the caller. The page has no counterpart
+ * of this entry point; it serves callers that cannot call cudaMalloc -- code
+ * running under a host framework that owns all device memory through its
+ * own pool and forbids raw allocations, or latency-critical code that cannot
+ * afford cudaMalloc's implicit device-wide synchronization.
+ *   - B*K must not exceed CS_NOALLOC_MAX_ROWS (CS_ERR_SCRATCH_TOO_SMALL
+ *     otherwise, before any CUDA call).
+ *   - The buffer takes 4 MiB of device memory on every GPU that loads the
+ *     library, until the process exits.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before
+ *     starting any stream capture on that device.
+ *   - Every call shares the one buffer and leaves its own pass-1 values in
+ *     it. Nothing in it needs to start at zero (pass 1 writes every row that
+ *     pass 2 reads), but calls that overlap on the GPU -- e.g. on two streams
+ *     at once -- race on it: serialize them.
+ * Other arguments, requirements and results as cs_score_candidates_batch_unfused.
+ */
+#define CS_NOALLOC_MAX_ROWS 1048576
+int cs_score_candidates_batch_unfused_noalloc(const float *Q, const float *C,
+                                              int B, int K, int D,
+                                              int normalize, float scale,
+                                              float temperature, float *out,
+                                              cs_stream_t stream);
 
 /* Device status word bits (see cs_device_status). */
 #define CS_DEVERR_WAIT_TIMEOUT 1u  /* an on-chip wait gave up after ~1 s */

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     cs_score_candidates_batch,
     cs_score_candidates_batch_plan,
     cs_score_candidates_batch_unfused,
+    cs_score_candidates_batch_unfused_noalloc,
     cs_status_string,
     library,
 )

@@ -25,8 +25,9 @@ STATUS = {
     0: "CS_OK", 1: "CS_ERR_NULL_POINTER", 2: "CS_ERR_K_ZERO", 3: "CS_ERR_K_TOO_LARGE",
     4: "CS_ERR_D_ZERO", 5: "CS_ERR_BAD_SCALE", 6: "CS_ERR_BAD_TEMPERATURE", 7: "CS_ERR_BAD_BATCH",
     8: "CS_ERR_BAD_SIMILARITY", 9: "CS_ERR_LAUNCH", 10: "CS_ERR_ALIAS", 11: "CS_ERR_TOO_LARGE",
-    12: "CS_ERR_BAD_PLAN",
+    12: "CS_ERR_BAD_PLAN", 13: "CS_ERR_SCRATCH_TOO_SMALL",
 }
+CS_NOALLOC_MAX_ROWS = 1 << 20
 globals().update({name: code for code, name in STATUS.items()})
 
 _lock = threading.Lock()
@@ -66,6 +67,8 @@ def library() -> ctypes.CDLL:
         lib.cs_score_candidates_batch_plan.restype = I
         lib.cs_score_candidates_batch_unfused.argtypes = [P, P, I, I, I, I, F, F, P, P, P]
         lib.cs_score_candidates_batch_unfused.restype = I
+        lib.cs_score_candidates_batch_unfused_noalloc.argtypes = [P, P, I, I, I, I, F, F, P, P]
+        lib.cs_score_candidates_batch_unfused_noalloc.restype = I
         lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
         lib.cs_query_plan.restype = I
         lib.cs_device_status.argtypes = [U, I]
@@ -194,6 +197,22 @@ def cs_score_candidates_batch_unfused(Q, C, normalize: int, scale: float, temper
               (qp, cp, B, K, D, int(normalize), float(scale), float(temperature)), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_batch_unfused")
+    return out
+
+
+def cs_score_candidates_batch_unfused_noalloc(Q, C, normalize: int, scale: float, temperature: float, out,
+                                              stream=None):
+    """The unfused baseline with the library's built-in staged buffer, for
+    callers that cannot allocate device memory: nothing is allocated here or
+    in the library, so `out` [B,K] must be given. B*K <= CS_NOALLOC_MAX_ROWS;
+    calls share the buffer, so calls overlapping on the GPU race."""
+    if out is None:
+        raise ValueError("out is required: this entry point allocates nothing")
+    qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
+    s = _call(library().cs_score_candidates_batch_unfused_noalloc, C.device,
+              (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_batch_unfused_noalloc")
     return out
 
 

@@ -320,6 +320,8 @@ const char* cs_status_string(int status) {
         case CS_ERR_ALIAS: return "out overlaps Q or C";
         case CS_ERR_TOO_LARGE: return "B*K*D is too large";
         case CS_ERR_BAD_PLAN: return "requested plan cannot run these arguments";
+        case CS_ERR_SCRATCH_TOO_SMALL:
+            return "B*K exceeds the built-in scratch of the no-allocation entry point (1048576 rows)";
         default: return "unknown status";
     }
 }
@@ -344,6 +346,19 @@ int cs_score_candidates_batch_plan(const float* Q, const float* C, int B, int K,
 int cs_score_candidates_batch_unfused(const float* Q, const float* C, int B, int K, int D, int normalize,
                                       float scale, float temperature, float* staged, float* out,
                                       cs_stream_t stream) {
+    return run_unfused(Q, C, B, K, D, normalize, scale, temperature, staged, out, stream);
+}
+
+int cs_score_candidates_batch_unfused_noalloc(const float* Q, const float* C, int B, int K, int D, int normalize,
+                                              float scale, float temperature, float* out, cs_stream_t stream) {
+    const int v = validate(Q, C, B, K, D, normalize, out, true, true, scale, temperature);
+    if (v != CS_OK) return v;
+    if (static_cast<unsigned long long>(B) * static_cast<unsigned long long>(K) > cs::kNoAllocStagedFloats)
+        return CS_ERR_SCRATCH_TOO_SMALL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CS_ERR_LAUNCH;
+    float* staged = nullptr;
+    if (cs::noalloc_staged_address(dev, &staged) != cudaSuccess) return CS_ERR_LAUNCH;
     return run_unfused(Q, C, B, K, D, normalize, scale, temperature, staged, out, stream);
 }
 

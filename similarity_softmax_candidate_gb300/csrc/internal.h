@@ -92,6 +92,13 @@ cudaError_t launch_generic(const Problem& p, cudaStream_t stream);
 // Unfused baseline pass 2 (dot): softmax of scale * staged / temperature.
 cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream);
 
+// Size, in floats, of the built-in staged array of the no-allocation
+// unfused entry point (4 MiB): it serves calls with B*K up to this many rows.
+constexpr unsigned long long kNoAllocStagedFloats = 1ull << 20;
+// Device address of that array on `device` (which must be current), looked
+// up once per device with cudaGetSymbolAddress and then cached.
+cudaError_t noalloc_staged_address(int device, float** ptr);
+
 // One-time per-device kernel attributes (dynamic smem ceiling, cluster size).
 cudaError_t configure_device_kernels(int smem_optin);
 

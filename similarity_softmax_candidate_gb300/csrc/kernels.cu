@@ -41,6 +41,8 @@
 
 #include <math.h>
 
+#include <mutex>
+
 namespace cs {
 
 __device__ unsigned int g_status;
@@ -790,6 +792,29 @@ int max_active_clusters(int cluster, size_t smem, int nq4, int normalize) {
         return 0;
     }
     return n;
+}
+
+// Built-in staged array for cs_score_candidates_batch_unfused_noalloc, for
+// callers that cannot allocate device memory themselves. It takes 4 MiB on
+// every device that loads this library, for the life of the process. Host
+// code must not pass the symbol itself to a kernel (on the host it names a
+// shadow, not device memory): noalloc_staged_address looks up the real
+// device address once per device.
+static __device__ __align__(256) float g_noalloc_staged[kNoAllocStagedFloats];
+
+cudaError_t noalloc_staged_address(int device, float** ptr) {
+    static std::mutex mu;
+    static float* addr[64] = {};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[device]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_staged);
+        if (e != cudaSuccess) return e;
+        addr[device] = static_cast<float*>(p);
+    }
+    *ptr = addr[device];
+    return cudaSuccess;
 }
 
 cudaError_t read_device_status(unsigned* flags, bool clear) {
