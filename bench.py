@@ -314,6 +314,34 @@ def main():
     ms_dot, launches_dot, _ = timed(wl_dot)
     clock_info = clocks.stop()
 
+    # The same workload with the candidates stored as bfloat16 (half the bytes).
+    bf16 = {}
+    Cb = torch.empty(wl_cos.C.shape, device=dev, dtype=torch.bfloat16)
+    for b0 in range(0, B_TOTAL, CHUNK):
+        Cb[b0:b0 + CHUNK].copy_(wl_cos.C[b0:b0 + CHUNK])
+    bytes_q_bf16 = 2 * K * D + 4 * D + 4 * K
+    for wl in (wl_cos, wl_dot):
+        def bstep(wl=wl):
+            for b0 in range(0, B_TOTAL, CHUNK):
+                cs.cs_score_candidates_batch_bf16(wl.Q[b0:b0 + CHUNK], Cb[b0:b0 + CHUNK], wl.normalize, wl.scale,
+                                                  wl.temperature, out=out[b0:b0 + CHUNK], stream=stream)
+        for _ in range(args.warmup):
+            bstep()
+        barrier()
+        ba, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        bsteps = max(3, args.steps // 2)
+        ba.record(stream)
+        for _ in range(bsteps):
+            bstep()
+        bb.record(stream)
+        barrier()
+        bms = max_over_ranks(ba.elapsed_time(bb)) / bsteps
+        gbs = world * B_TOTAL * bytes_q_bf16 / (bms / 1e3) / 1e9
+        bf16["cos" if wl.normalize else "dot"] = {
+            "questions_per_s": world * B_TOTAL / (bms / 1e3), "ms_per_step": bms, "hbm_gbs": gbs,
+            "frac": gbs / _peak_hbm()[0], "algorithmic_bytes_per_question": bytes_q_bf16, "steps": bsteps}
+    del Cb
+
     # The unfused baseline on the same workload (two launches per slice).
     staged = torch.empty((B_TOTAL, K), device=dev)
     unfused = {}
@@ -375,6 +403,7 @@ def main():
                     "launch_gbs": launch_bytes / (dot_launch_ms / 1e3) / 1e9,
                     "frac": launch_bytes / (dot_launch_ms / 1e3) / 1e9 / peak},
             "unfused_baseline": unfused,
+            "bf16_candidates": bf16,
         },
     }
 

@@ -41,6 +41,8 @@
 #ifndef CANDIDATE_SCORING_H
 #define CANDIDATE_SCORING_H
 
+#include <stdint.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -99,6 +101,25 @@ int cs_score_candidates_batch(const float *Q, const float *C, int B, int K,
                               int D, int normalize, float scale,
                               float temperature, float *out,
                               cs_stream_t stream);
+
+/*
+ * The same readouts with the candidates stored as bfloat16 (C holds the
+ * 16-bit patterns, [B][K][D] row-major), half the bytes of the float32
+ * layout on a path whose time is the reading of C. Each element is widened
+ * exactly to float32 and accumulated in float32, so the result is the
+ * float32 readout of the bfloat16-rounded candidates. q and out stay
+ * float32. The fast plans need D % 8 == 0 and 16-byte aligned Q and C;
+ * other shapes take the scalar plan. Arguments, errors and conventions as
+ * cs_score_candidates / cs_score_candidates_batch. (bfloat16 storage is our
+ * extension; the page's kernel reads float32.)
+ */
+int cs_score_candidates_bf16(const float *q, const uint16_t *C, int K, int D,
+                             int normalize, float scale, float temperature,
+                             float *out, cs_stream_t stream);
+int cs_score_candidates_batch_bf16(const float *Q, const uint16_t *C, int B,
+                                   int K, int D, int normalize, float scale,
+                                   float temperature, float *out,
+                                   cs_stream_t stream);
 
 /* Execution plans (kernel choices) the library picks between. */
 #define CS_PLAN_AUTO 0

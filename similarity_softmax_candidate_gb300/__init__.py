@@ -21,7 +21,9 @@ from .binding import (  # noqa: F401
     cs_device_status,
     cs_query_plan,
     cs_score_candidates,
+    cs_score_candidates_bf16,
     cs_score_candidates_batch,
+    cs_score_candidates_batch_bf16,
     cs_score_candidates_batch_plan,
     cs_score_candidates_batch_unfused,
     cs_score_candidates_batch_unfused_noalloc,

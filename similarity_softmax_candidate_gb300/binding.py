@@ -69,6 +69,10 @@ def library() -> ctypes.CDLL:
         lib.cs_score_candidates_batch_unfused.restype = I
         lib.cs_score_candidates_batch_unfused_noalloc.argtypes = [P, P, I, I, I, I, F, F, P, P]
         lib.cs_score_candidates_batch_unfused_noalloc.restype = I
+        lib.cs_score_candidates_bf16.argtypes = [P, P, I, I, I, F, F, P, P]
+        lib.cs_score_candidates_bf16.restype = I
+        lib.cs_score_candidates_batch_bf16.argtypes = [P, P, I, I, I, I, F, F, P, P]
+        lib.cs_score_candidates_batch_bf16.restype = I
         lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
         lib.cs_query_plan.restype = I
         lib.cs_device_status.argtypes = [U, I]
@@ -85,17 +89,18 @@ def cs_status_string(status: int) -> str:
     return library().cs_status_string(int(status)).decode()
 
 
-def _check(t, name, ndim):
+def _check(t, name, ndim, dtype=None):
     import torch
+    dtype = torch.float32 if dtype is None else dtype
     try:
-        ok = t.is_cuda and t.dtype == torch.float32 and t.dim() == ndim and t.is_contiguous()
+        ok = t.is_cuda and t.dtype == dtype and t.dim() == ndim and t.is_contiguous()
     except AttributeError:
         raise TypeError(f"{name} must be a torch.Tensor") from None
     if not ok:
         if not t.is_cuda:
             raise ValueError(f"{name} must be on a CUDA device (host memory cannot be read by the kernel)")
-        if t.dtype != torch.float32:
-            raise TypeError(f"{name} must be float32, got {t.dtype}")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
         if t.dim() != ndim:
             raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
         raise ValueError(f"{name} must be contiguous")
@@ -141,10 +146,10 @@ def cs_score_candidates(q, C, normalize: int, scale: float, temperature: float, 
     return out
 
 
-def _batch_ptrs(Q, C, out):
+def _batch_ptrs(Q, C, out, c_dtype=None):
     import torch
     qp = _check(Q, "Q", 2)
-    cp = _check(C, "C", 3)
+    cp = _check(C, "C", 3, c_dtype)
     B, K, D = (int(x) for x in C.shape)
     if tuple(Q.shape) != (B, D) or Q.device != C.device:
         raise ValueError(f"Q {tuple(Q.shape)} does not match C {tuple(C.shape)}")
@@ -213,6 +218,39 @@ def cs_score_candidates_batch_unfused_noalloc(Q, C, normalize: int, scale: float
               (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_batch_unfused_noalloc")
+    return out
+
+
+def cs_score_candidates_bf16(q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
+    """One question with bfloat16 candidates: q[D] float32, C[K,D] bfloat16
+    -> out[K] float32 (CUDA)."""
+    import torch
+    qp = _check(q, "q", 1)
+    cp = _check(C, "C", 2, torch.bfloat16)
+    K, D = int(C.shape[0]), int(C.shape[1])
+    if q.shape[0] != D or q.device != C.device:
+        raise ValueError(f"q {tuple(q.shape)} does not match C {tuple(C.shape)}")
+    if out is None:
+        out = torch.empty(K, device=C.device, dtype=torch.float32)
+    op = _check(out, "out", 1)
+    if out.shape[0] != K or out.device != C.device:
+        raise ValueError(f"out must be [K={K}] on {C.device}")
+    s = _call(library().cs_score_candidates_bf16, C.device,
+              (qp, cp, K, D, int(normalize), float(scale), float(temperature), op), stream)
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_bf16")
+    return out
+
+
+def cs_score_candidates_batch_bf16(Q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
+    """B questions with bfloat16 candidates: Q[B,D] float32, C[B,K,D]
+    bfloat16 -> out[B,K] float32 (CUDA), one launch."""
+    import torch
+    qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out, torch.bfloat16)
+    s = _call(library().cs_score_candidates_batch_bf16, C.device,
+              (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_batch_bf16")
     return out
 
 

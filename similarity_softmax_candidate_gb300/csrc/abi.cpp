@@ -43,8 +43,8 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 // out == nullptr with has_out == false validates everything but the output.
-int validate(const float* Q, const float* C, long long B, int K, int D, int normalize, const float* out,
-             bool has_out, bool check_scalars, float scale, float temperature) {
+int validate(const float* Q, const void* C, long long B, int K, int D, int normalize, const float* out,
+             bool has_out, bool check_scalars, float scale, float temperature, int c_bytes = 4) {
     if (!Q || !C || (has_out && !out)) return CS_ERR_NULL_POINTER;
     if (B <= 0) return CS_ERR_BAD_BATCH;
     if (K <= 0) return CS_ERR_K_ZERO;
@@ -62,7 +62,8 @@ int validate(const float* Q, const float* C, long long B, int K, int D, int norm
         const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + bk * 4ull;
         const uintptr_t q0 = reinterpret_cast<uintptr_t>(Q),
                         q1 = q0 + static_cast<unsigned long long>(B) * static_cast<unsigned long long>(D) * 4ull;
-        const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), c1 = c0 + bk * static_cast<unsigned long long>(D) * 4ull;
+        const uintptr_t c0 = reinterpret_cast<uintptr_t>(C),
+                        c1 = c0 + bk * static_cast<unsigned long long>(D) * static_cast<unsigned long long>(c_bytes);
         if ((o0 < q1 && q0 < o1) || (o0 < c1 && c0 < o1)) return CS_ERR_ALIAS;
     }
     return CS_OK;
@@ -89,33 +90,38 @@ cudaError_t device_state(DeviceState** st) {
     return cudaSuccess;
 }
 
-int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize) {
-    const long long key2 = (static_cast<long long>(smem) << 8) | (nq4 << 1) | normalize;
+int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16) {
+    const long long key2 = (static_cast<long long>(smem) << 8) | (nq4 << 2) | (c_bf16 << 1) | normalize;
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = d.clusters.find({cluster, key2});
     if (it != d.clusters.end()) return it->second;
-    const int n = cs::max_active_clusters(cluster, smem, nq4, normalize);
+    const int n = cs::max_active_clusters(cluster, smem, nq4, normalize, c_bf16);
     d.clusters[{cluster, key2}] = n;
     return n;
 }
 
+// Bulk copies move whole rows: a row of C and of Q must be a multiple of 16
+// bytes and start 16-byte aligned.
 bool tma_eligible(const Problem& p) {
-    return (p.D % 4) == 0 && (reinterpret_cast<uintptr_t>(p.Q) % 16) == 0 &&
+    const int per_chunk = 16 / cs::c_elem_bytes(p);
+    return (p.D % per_chunk) == 0 && (reinterpret_cast<uintptr_t>(p.Q) % 16) == 0 &&
            (reinterpret_cast<uintptr_t>(p.C) % 16) == 0;
 }
 
-int nq4_for(int D) {
-    const int d4 = D / 4;
-    if (d4 <= 32) return 1;
-    if (d4 <= 64) return 2;
-    if (d4 <= 128) return 4;
-    if (d4 <= 256) return 8;
-    return 0;  // q read from shared memory
+// 16-byte chunks of a C row each lane handles, when q for them fits in 32
+// registers per lane (0: q is read from shared memory instead).
+int nq4_for(const Problem& p) {
+    const int per_chunk = 16 / cs::c_elem_bytes(p);
+    const int dc = p.D / per_chunk;
+    const int max_nqc = 32 / per_chunk;  // 8 for float32, 4 for bfloat16
+    for (int n = 1; n <= max_nqc; n *= 2)
+        if (dc <= 32 * n) return n;
+    return 0;
 }
 
 // Rows per stage that make a stage of about kStageTargetBytes (1..8).
-int stage_rows(int D) {
-    long long R = kStageTargetBytes / (4ll * D);
+int stage_rows(long long row_bytes) {
+    long long R = kStageTargetBytes / row_bytes;
     if (R < 1) R = 1;
     if (R > cs::kMaxRowsPerStage) R = cs::kMaxRowsPerStage;
     return static_cast<int>(R);
@@ -127,15 +133,15 @@ int stage_rows(int D) {
 // to warp g % kConsumerWarps, so with NS a multiple of the warp count every
 // slot always has the same owner, which consumes its uses in order: a
 // parity wait on a slot can then never see a phase two uses old.
-int max_stages(const DeviceState& d, int R, int D) {
-    const long long stage_bytes = 4ll * R * D;
-    const size_t fixed = cs::smem_layout(0, R, D).total;
+int max_stages(const DeviceState& d, int R, int D, int c_bytes) {
+    const long long stage_bytes = static_cast<long long>(c_bytes) * R * D;
+    const size_t fixed = cs::smem_layout(0, R, D, c_bytes).total;
     if (fixed >= static_cast<size_t>(d.smem_optin)) return 0;
     long long ns = static_cast<long long>(d.smem_optin - fixed) / stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     ns -= ns % cs::kConsumerWarps;
     // The barrier array grows by 16 bytes per stage as well.
-    while (ns > 0 && cs::smem_layout(static_cast<int>(ns), R, D).total > static_cast<size_t>(d.smem_optin))
+    while (ns > 0 && cs::smem_layout(static_cast<int>(ns), R, D, c_bytes).total > static_cast<size_t>(d.smem_optin))
         ns -= cs::kConsumerWarps;
     return ns > 0 ? static_cast<int>(ns) : 0;
 }
@@ -151,11 +157,12 @@ int ring_stages(long long need, int max_ns) {
 // Picks rows per stage R <= stage_rows(D) that keeps the most bytes in
 // flight (larger R on ties). Returns false if no ring fits.
 bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
+    const int cb = cs::c_elem_bytes(p);
     int R = 0, max_ns = 0;
     long long best = 0;
-    for (int r = stage_rows(p.D); r >= 1; --r) {
-        const int ns = max_stages(d, r, p.D);
-        const long long bytes = 4ll * r * p.D * ns;
+    for (int r = stage_rows(static_cast<long long>(cb) * p.D); r >= 1; --r) {
+        const int ns = max_stages(d, r, p.D, cb);
+        const long long bytes = static_cast<long long>(cb) * r * p.D * ns;
         if (bytes > best) {
             best = bytes;
             R = r;
@@ -173,19 +180,20 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     plan->ctas = ctas;
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = nq4_for(p.D);
-    plan->smem = cs::smem_layout(ns, R, p.D).total;
+    plan->nq4 = nq4_for(p);
+    plan->smem = cs::smem_layout(ns, R, p.D, cb).total;
     return true;
 }
 
 // CLUSTER plan with G CTAs per question: each CTA's rows spread over all
 // consumer warps (one stage each) when the ring holds them.
 bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
+    const int cb = cs::c_elem_bytes(p);
     const int rows = (p.K + G - 1) / G;
     int R = (rows + cs::kConsumerWarps - 1) / cs::kConsumerWarps;
-    const int Rmax = stage_rows(p.D);
+    const int Rmax = stage_rows(static_cast<long long>(cb) * p.D);
     if (R > Rmax) R = Rmax;
-    const int max_ns = max_stages(d, R, p.D);
+    const int max_ns = max_stages(d, R, p.D, cb);
     if (max_ns == 0) return false;
     const int ns = ring_stages((rows + R - 1) / R, max_ns);
     plan->kind = cs::kPlanCluster;
@@ -193,8 +201,8 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     plan->ctas = G * static_cast<int>(p.B);
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = nq4_for(p.D);
-    plan->smem = cs::smem_layout(ns, R, p.D).total;
+    plan->nq4 = nq4_for(p);
+    plan->smem = cs::smem_layout(ns, R, p.D, cb).total;
     return true;
 }
 
@@ -229,21 +237,21 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         if (cluster == 1)  // one CTA per question: the STREAM kernel with B CTAs
             return stream_plan(d, p, static_cast<int>(p.B), plan) ? CS_OK : CS_ERR_BAD_PLAN;
         if (!cluster_plan(d, p, cluster, plan)) return CS_ERR_BAD_PLAN;
-        if (cached_max_clusters(d, cluster, plan->smem, plan->nq4, p.normalize) < 1) return CS_ERR_BAD_PLAN;
+        if (cached_max_clusters(d, cluster, plan->smem, plan->nq4, p.normalize, p.c_bf16) < 1) return CS_ERR_BAD_PLAN;
         return CS_OK;
     }
     // automatic choice
     if (aligned && p.B * 2 <= d.sms) {
         // Few questions: split each over a cluster so one question is not
         // confined to one SM (the page's 256-thread lesson, "What it is worth").
-        const long long q_bytes = 4ll * p.K * p.D;
+        const long long q_bytes = static_cast<long long>(cs::c_elem_bytes(p)) * p.K * p.D;
         int G = 1;
         while (G * 2 <= cs::kMaxCluster && G * 2 <= p.K && (G * 2) * p.B <= d.sms &&
                q_bytes / (G * 2) >= kSplitMinBytes)
             G *= 2;
         for (; G > 1; G /= 2) {
             if (cluster_plan(d, p, G, plan) &&
-                cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize) >= p.B)
+                cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize, p.c_bf16) >= p.B)
                 return CS_OK;
         }
     }
@@ -252,13 +260,13 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
     return CS_OK;
 }
 
-int run(const float* Q, const float* C, long long B, int K, int D, int normalize, float scale, float temperature,
-        float* out, cs_stream_t stream, int kind, int cluster, int ctas) {
-    const int v = validate(Q, C, B, K, D, normalize, out, true, true, scale, temperature);
+int run(const float* Q, const void* C, long long B, int K, int D, int normalize, float scale, float temperature,
+        float* out, cs_stream_t stream, int kind, int cluster, int ctas, int c_bf16 = 0) {
+    const int v = validate(Q, C, B, K, D, normalize, out, true, true, scale, temperature, c_bf16 ? 2 : 4);
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, nullptr};
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, nullptr, c_bf16};
     Plan plan{};
     const int s = make_plan(*d, p, kind, cluster, ctas, &plan);
     if (s != CS_OK) return s;
@@ -287,7 +295,7 @@ int run_unfused(const float* Q, const float* C, long long B, int K, int D, int n
         return CS_ERR_ALIAS;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, staged};
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, staged, 0};
     Plan plan{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
     if (s != CS_OK) return s;
@@ -362,13 +370,23 @@ int cs_score_candidates_batch_unfused_noalloc(const float* Q, const float* C, in
     return run_unfused(Q, C, B, K, D, normalize, scale, temperature, staged, out, stream);
 }
 
+int cs_score_candidates_bf16(const float* q, const uint16_t* C, int K, int D, int normalize, float scale,
+                             float temperature, float* out, cs_stream_t stream) {
+    return run(q, C, 1, K, D, normalize, scale, temperature, out, stream, cs::kPlanAuto, 0, 0, 1);
+}
+
+int cs_score_candidates_batch_bf16(const float* Q, const uint16_t* C, int B, int K, int D, int normalize, float scale,
+                                   float temperature, float* out, cs_stream_t stream) {
+    return run(Q, C, B, K, D, normalize, scale, temperature, out, stream, cs::kPlanAuto, 0, 0, 1);
+}
+
 int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int normalize, int* plan, int* cluster,
                   int* ctas, int* smem_bytes) {
     const int v = validate(Q, C, B, K, D, normalize, nullptr, false, false, 1.f, 1.f);
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f, nullptr};
+    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f, nullptr, 0};
     Plan pl{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &pl);
     if (s != CS_OK) return s;

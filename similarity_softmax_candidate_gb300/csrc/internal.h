@@ -28,7 +28,7 @@ constexpr int kGenericThreads = 256;
 // The float32 arguments of one readout, after validation.
 struct Problem {
     const float* Q;    // [B][D]
-    const float* C;    // [B][K][D]
+    const void* C;     // [B][K][D], float32 or bfloat16 (see c_bf16)
     float* out;        // [B][K]
     long long B;
     int K;
@@ -37,7 +37,11 @@ struct Problem {
     float scale;       // multiplies the similarity
     float temperature; // divides the scaled similarity
     float* staged;     // unfused baseline only: one float per row [B][K]
+    int c_bf16;        // 1: C holds bfloat16 bit patterns (2 bytes each)
 };
+
+// Bytes of one element of C.
+inline int c_elem_bytes(const Problem& p) { return p.c_bf16 ? 2 : 4; }
 
 enum PlanKind { kPlanAuto = 0, kPlanStream = 1, kPlanCluster = 2, kPlanGeneric = 3 };
 
@@ -47,14 +51,14 @@ struct Plan {
     int ctas;          // CTAs launched in total
     int rows_per_stage;// candidate rows per bulk-copy stage
     int stages;        // stages in the shared-memory ring
-    int nq4;           // float4s of q per lane held in registers (0: read q from smem)
+    int nq4;           // 16-byte chunks of a C row per lane whose q sits in registers (0: q read from smem)
     size_t smem;       // dynamic shared memory per CTA
 };
 
 // Shared-memory carve-up of the streaming kernels. All offsets are bytes
 // from the (128-byte aligned) dynamic shared-memory base.
 struct SmemLayout {
-    size_t ring;     // stages * rows_per_stage * D floats
+    size_t ring;     // stages * rows_per_stage * D elements of C
     size_t qbuf;     // 2 slots of D floats
     size_t tn;       // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
     size_t xch;      // kMaxCluster float2 (max, sum) received from the cluster's CTAs
@@ -63,10 +67,11 @@ struct SmemLayout {
     size_t total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage, int D) {
+// c_bytes: bytes of one element of C (4 float32, 2 bfloat16).
+__host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage, int D, int c_bytes) {
     SmemLayout L;
     size_t off = 0;
-    L.ring = off;   off += (size_t)stages * rows_per_stage * D * sizeof(float);
+    L.ring = off;   off += (size_t)stages * rows_per_stage * D * c_bytes;
     L.qbuf = off;   off += 2 * (size_t)D * sizeof(float);
     L.tn = off;     off += 4 * (size_t)kLogitSlots * sizeof(float);
     L.xch = off;    off += (size_t)kMaxCluster * 8;
@@ -104,7 +109,7 @@ cudaError_t configure_device_kernels(int smem_optin);
 
 // Clusters of `cluster` CTAs with `smem` bytes each that fit on the device
 // at once (0 if none).
-int max_active_clusters(int cluster, size_t smem, int nq4, int normalize);
+int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16);
 
 // Device status word (bounded-wait give-ups).
 cudaError_t read_device_status(unsigned* flags, bool clear);

@@ -61,6 +61,35 @@ __host__ __device__ constexpr int values_per_row(int m) { return acc_norm(m) && 
 __host__ __device__ constexpr bool does_softmax(int m) { return m == kFusedCos || m == kFusedDot || m == kStagedCos; }
 __host__ __device__ constexpr bool cos_logits(int m) { return m == kFusedCos || m == kStagedCos; }
 
+// Elements of C. The streaming kernel moves rows as 16-byte chunks: 4
+// float32 or 8 bfloat16 (stored as their 16-bit patterns). A chunk widens to
+// QF4 float4s, matched against the same number of float4s of q.
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static constexpr int kPerChunk = 4;
+    static constexpr int kQF4 = 1;
+    __device__ __forceinline__ static void widen(const uint4& c, float4 (&f)[1]) {
+        f[0] = make_float4(__uint_as_float(c.x), __uint_as_float(c.y), __uint_as_float(c.z), __uint_as_float(c.w));
+    }
+    __device__ __forceinline__ static float value(const float* row, int d) { return __ldg(row + d); }
+};
+template <>
+struct Elem<uint16_t> {  // bfloat16: the high half of a float32
+    static constexpr int kPerChunk = 8;
+    static constexpr int kQF4 = 2;
+    __device__ __forceinline__ static void widen(const uint4& c, float4 (&f)[2]) {
+        f[0] = make_float4(__uint_as_float(c.x << 16), __uint_as_float(c.x & 0xffff0000u), __uint_as_float(c.y << 16),
+                           __uint_as_float(c.y & 0xffff0000u));
+        f[1] = make_float4(__uint_as_float(c.z << 16), __uint_as_float(c.z & 0xffff0000u), __uint_as_float(c.w << 16),
+                           __uint_as_float(c.w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static float value(const uint16_t* row, int d) {
+        return __uint_as_float(static_cast<uint32_t>(__ldg(row + d)) << 16);
+    }
+};
+
 // ------------------------------------------------------------------ PTX
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -271,16 +300,19 @@ struct StreamArgs {
     int q_rem;
 };
 
-// Per-row sums of the nr <= kMaxRowsPerStage rows of one stage. Lane
-// handles float4 columns lane, lane+32, ...; q comes from registers
-// (NQ4 > 0) or from shared memory (NQ4 == 0, large D). With two values per
-// row (fused cosine) v[2r] = c_r . q and v[2r + 1] = c_r . c_r; with one,
-// v[r] = c_r . q, or c_r . c_r for the norm pass.
-template <int NQ4, int MODE>
-__device__ __forceinline__ void stage_dots(const float4* __restrict__ st, int nr, int D4,
-                                           const float4 (&qv)[NQ4 > 0 ? NQ4 : 1], const float4* __restrict__ q4,
-                                           int lane, float (&v)[values_per_row(MODE) * kMaxRowsPerStage]) {
+// Per-row sums of the nr <= kMaxRowsPerStage rows of one stage (rows of DC
+// 16-byte chunks each). Lane handles chunks lane, lane+32, ...; q comes from
+// registers (NQC > 0: qv holds the q float4s of those chunks) or from shared
+// memory (NQC == 0, large D). With two values per row (fused cosine)
+// v[2r] = c_r . q and v[2r + 1] = c_r . c_r; with one, v[r] = c_r . q, or
+// c_r . c_r for the norm pass.
+template <int NQC, int MODE, typename T>
+__device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr, int DC,
+                                           const float4 (&qv)[(NQC > 0 ? NQC : 1) * Elem<T>::kQF4],
+                                           const float4* __restrict__ q4, int lane,
+                                           float (&v)[values_per_row(MODE) * kMaxRowsPerStage]) {
     constexpr int VPR = values_per_row(MODE);
+    constexpr int QF4 = Elem<T>::kQF4;
 #pragma unroll
     for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = 0.f;
     auto accumulate = [&](const float4& c, const float4& q, int r) {
@@ -302,34 +334,51 @@ __device__ __forceinline__ void stage_dots(const float4* __restrict__ st, int nr
             v[i] = n;
         }
     };
-    if constexpr (NQ4 > 0) {
+    if constexpr (NQC > 0) {
 #pragma unroll
-        for (int j = 0; j < NQ4; ++j) {
+        for (int j = 0; j < NQC; ++j) {
             const int i = lane + 32 * j;
-            if (i < D4) {
+            if (i < DC) {
 #pragma unroll
-                for (int r = 0; r < kMaxRowsPerStage; ++r)
-                    if (r < nr) accumulate(st[r * D4 + i], qv[j], r);
+                for (int r = 0; r < kMaxRowsPerStage; ++r) {
+                    if (r < nr) {
+                        float4 c[QF4];
+                        Elem<T>::widen(st[r * DC + i], c);
+#pragma unroll
+                        for (int h = 0; h < QF4; ++h) accumulate(c[h], qv[j * QF4 + h], r);
+                    }
+                }
             }
         }
     } else {
-        for (int i = lane; i < D4; i += 32) {
-            const float4 q = q4[i];
+        for (int i = lane; i < DC; i += 32) {
+            float4 q[QF4];
 #pragma unroll
-            for (int r = 0; r < kMaxRowsPerStage; ++r)
-                if (r < nr) accumulate(st[r * D4 + i], q, r);
+            for (int h = 0; h < QF4; ++h) q[h] = q4[i * QF4 + h];
+#pragma unroll
+            for (int r = 0; r < kMaxRowsPerStage; ++r) {
+                if (r < nr) {
+                    float4 c[QF4];
+                    Elem<T>::widen(st[r * DC + i], c);
+#pragma unroll
+                    for (int h = 0; h < QF4; ++h) accumulate(c[h], q[h], r);
+                }
+            }
         }
     }
 }
 
-template <int NQ4, int MODE>
+template <int NQC, int MODE, typename T>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamArgs args) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VPR = values_per_row(MODE);
     constexpr int V = VPR * kMaxRowsPerStage;
     constexpr bool COS = cos_logits(MODE);
+    constexpr int QF4 = Elem<T>::kQF4;
     const Problem& p = args.p;
-    const int K = p.K, D = p.D, D4 = p.D >> 2;
+    const int K = p.K, D = p.D;
+    const int DC = D / Elem<T>::kPerChunk;  // 16-byte chunks per row of C
+    const T* Cg = static_cast<const T*>(p.C);
     const int R = args.rows_per_stage, NS = args.stages, G = args.cluster;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -343,8 +392,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         return;
     }
 
-    const SmemLayout L = smem_layout(NS, R, D);
-    float* ring = reinterpret_cast<float*>(smem + L.ring);
+    const SmemLayout L = smem_layout(NS, R, D, static_cast<int>(sizeof(T)));
+    unsigned char* ring = smem + L.ring;
+    const uint32_t stage_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(D) * sizeof(T);
     float* qbuf = reinterpret_cast<float*>(smem + L.qbuf);
     float* tn = reinterpret_cast<float*>(smem + L.tn);
     float2* xch = reinterpret_cast<float2*>(smem + L.xch);
@@ -393,7 +443,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     }
     const int nrows = khi - klo;
     const int nst = (nrows + R - 1) / R;
-    const uint32_t row_bytes = static_cast<uint32_t>(D) * 4u;
+    const uint32_t row_bytes = static_cast<uint32_t>(D) * sizeof(T);  // a row of C
+    const uint32_t q_bytes = static_cast<uint32_t>(D) * 4u;
     float a = 1.f;  // logit factor of the current question
 
     if (warp == kConsumerWarps) {
@@ -418,8 +469,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;
                 const uint32_t bytes = static_cast<uint32_t>(min(R, nrows - k0)) * row_bytes;
                 mbar_arrive_expect_tx(bar_f, bytes);
-                bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * R * D),
-                         p.C + ((static_cast<size_t>(qb + n)) * K + klo + k0) * D, bytes, bar_f);
+                bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * stage_bytes),
+                         Cg + ((static_cast<size_t>(qb + n)) * K + klo + k0) * D, bytes, bar_f);
                 slot += kConsumerWarps;
                 if (slot >= static_cast<uint32_t>(NS)) {
                     slot -= NS;
@@ -450,8 +501,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             for (long long b = qb; b < qe; ++b, ++nq) {
                 const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
                 if (nq >= 2 && !wait_phase(qempty0 + 8u * qs, qpar ^ 1u, give_up)) break;
-                mbar_arrive_expect_tx(qfull0 + 8u * qs, row_bytes);
-                bulk_g2s(smem_u32(qbuf + qs * D), p.Q + static_cast<size_t>(b) * D, row_bytes, qfull0 + 8u * qs);
+                mbar_arrive_expect_tx(qfull0 + 8u * qs, q_bytes);
+                bulk_g2s(smem_u32(qbuf + qs * D), p.Q + static_cast<size_t>(b) * D, q_bytes, qfull0 + 8u * qs);
             }
             if (*give_up) {
                 const unsigned long long deadline = globaltimer() + kWaitLimitNs;
@@ -471,15 +522,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
             bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
             const float4* q4 = reinterpret_cast<const float4*>(qbuf + qs * D);
-            float4 qv[NQ4 > 0 ? NQ4 : 1];
+            float4 qv[(NQC > 0 ? NQC : 1) * QF4];
             float qn = 1.f;
-            if constexpr (NQ4 > 0) {
+            if constexpr (NQC > 0) {
                 float sq = 0.f;
 #pragma unroll
-                for (int j = 0; j < NQ4; ++j) {
+                for (int j = 0; j < NQC; ++j) {
                     const int i = lane + 32 * j;
-                    qv[j] = i < D4 ? q4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (COS) sq += qv[j].x * qv[j].x + qv[j].y * qv[j].y + qv[j].z * qv[j].z + qv[j].w * qv[j].w;
+#pragma unroll
+                    for (int h = 0; h < QF4; ++h) {
+                        float4& x = qv[j * QF4 + h];
+                        x = i < DC ? q4[i * QF4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (COS) sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
@@ -488,7 +543,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 if (COS) qn = fmaxf(sqrtf(warp_sum(sq)), kEps);
             } else if (COS) {
                 float sq = 0.f;
-                for (int i = lane; i < D4; i += 32) {
+                for (int i = lane; i < D / 4; i += 32) {
                     const float4 x = q4[i];
                     sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
                 }
@@ -507,8 +562,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
                 float v[V];
-                stage_dots<NQ4, MODE>(reinterpret_cast<const float4*>(ring + static_cast<size_t>(slot) * R * D), nr,
-                                      D4, qv, q4, lane, v);
+                stage_dots<NQC, MODE, T>(reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes),
+                                         nr, DC, qv, q4, lane, v);
                 int idx;
                 const float sum = transpose_reduce<V>(v, lane, &idx);
                 if ((lane & (32 / V - 1)) == 0) {
@@ -529,7 +584,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     phase ^= 1u;
                 }
             }
-            if constexpr (NQ4 == 0) {
+            if constexpr (NQC == 0) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
             }
@@ -596,7 +651,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
 
 // One CTA per question, one warp per candidate row, scalar coalesced loads:
 // any D, any alignment.
-template <bool COS>
+template <bool COS, typename T>
 __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem p) {
     __shared__ float lg[kLogitSlots];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -615,11 +670,11 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     }
     const float a = logit_factor(qn, p.scale, p.temperature, COS);
     for (int k = warp; k < K; k += nwarps) {
-        const float* __restrict__ c = p.C + (static_cast<size_t>(b) * K + k) * D;
+        const T* __restrict__ c = static_cast<const T*>(p.C) + (static_cast<size_t>(b) * K + k) * D;
         float t0 = 0.f, t1 = 0.f, n0 = 0.f, n1 = 0.f;
         int d = lane;
         for (; d + 32 < D; d += 64) {
-            const float c0 = __ldg(c + d), c1 = __ldg(c + d + 32);
+            const float c0 = Elem<T>::value(c, d), c1 = Elem<T>::value(c, d + 32);
             t0 = fmaf(c0, __ldg(q + d), t0);
             t1 = fmaf(c1, __ldg(q + d + 32), t1);
             if (COS) {
@@ -628,7 +683,7 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
             }
         }
         if (d < D) {
-            const float c0 = __ldg(c + d);
+            const float c0 = Elem<T>::value(c, d);
             t0 = fmaf(c0, __ldg(q + d), t0);
             if (COS) n0 = fmaf(c0, c0, n0);
         }
@@ -664,7 +719,7 @@ __global__ void __launch_bounds__(256) staged_softmax_kernel(const Problem p) {
 
 // ------------------------------------------------------------------ dispatch
 
-template <int NQ4, int MODE>
+template <int NQC, int MODE, typename T>
 cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -684,40 +739,50 @@ cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t 
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, stream_kernel<NQ4, MODE>, a);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<NQC, MODE, T>, a);
 }
 
-template <int MODE>
+template <int MODE, typename T>
 cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     switch (plan.nq4) {
-        case 1: return launch_stream_t<1, MODE>(a, plan, stream);
-        case 2: return launch_stream_t<2, MODE>(a, plan, stream);
-        case 4: return launch_stream_t<4, MODE>(a, plan, stream);
-        case 8: return launch_stream_t<8, MODE>(a, plan, stream);
-        case 0: return launch_stream_t<0, MODE>(a, plan, stream);
+        case 1: return launch_stream_t<1, MODE, T>(a, plan, stream);
+        case 2: return launch_stream_t<2, MODE, T>(a, plan, stream);
+        case 4: return launch_stream_t<4, MODE, T>(a, plan, stream);
+        case 8: return launch_stream_t<8, MODE, T>(a, plan, stream);
+        case 0: return launch_stream_t<0, MODE, T>(a, plan, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int MODE>
-const void* stream_fn_m(int nq4) {
-    switch (nq4) {
-        case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE>);
-        case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE>);
-        case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE>);
-        case 8: return reinterpret_cast<const void*>(stream_kernel<8, MODE>);
-        case 0: return reinterpret_cast<const void*>(stream_kernel<0, MODE>);
+template <int MODE, typename T>
+const void* stream_fn_m(int nqc) {
+    switch (nqc) {
+        case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE, T>);
+        case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE, T>);
+        case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE, T>);
+        case 8: return reinterpret_cast<const void*>(stream_kernel<8, MODE, T>);
+        case 0: return reinterpret_cast<const void*>(stream_kernel<0, MODE, T>);
     }
     return nullptr;
 }
 
-const void* stream_fn_for(int nq4, int mode) {
+// Kernels exist for every mode over float32 C, and for the fused modes over
+// bfloat16 C (nqc 8 is never planned for bfloat16: q would take 64 registers).
+const void* stream_fn_for(int nqc, int mode, int c_bf16) {
+    if (c_bf16) {
+        if (nqc == 8) return nullptr;
+        switch (mode) {
+            case kFusedCos: return stream_fn_m<kFusedCos, uint16_t>(nqc);
+            case kFusedDot: return stream_fn_m<kFusedDot, uint16_t>(nqc);
+        }
+        return nullptr;
+    }
     switch (mode) {
-        case kFusedCos: return stream_fn_m<kFusedCos>(nq4);
-        case kFusedDot: return stream_fn_m<kFusedDot>(nq4);
-        case kRowNorm: return stream_fn_m<kRowNorm>(nq4);
-        case kRowDot: return stream_fn_m<kRowDot>(nq4);
-        case kStagedCos: return stream_fn_m<kStagedCos>(nq4);
+        case kFusedCos: return stream_fn_m<kFusedCos, float>(nqc);
+        case kFusedDot: return stream_fn_m<kFusedDot, float>(nqc);
+        case kRowNorm: return stream_fn_m<kRowNorm, float>(nqc);
+        case kRowDot: return stream_fn_m<kRowDot, float>(nqc);
+        case kStagedCos: return stream_fn_m<kStagedCos, float>(nqc);
     }
     return nullptr;
 }
@@ -733,12 +798,20 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
     const long long ctas = plan.kind == kPlanCluster ? 1 : plan.ctas;
     a.q_per_cta = static_cast<int>(p.B / ctas);
     a.q_rem = static_cast<int>(p.B % ctas);
+    if (p.c_bf16) {
+        if (plan.nq4 == 8) return cudaErrorInvalidValue;
+        switch (mode) {
+            case kFusedCos: return launch_stream_m<kFusedCos, uint16_t>(a, plan, stream);
+            case kFusedDot: return launch_stream_m<kFusedDot, uint16_t>(a, plan, stream);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (mode) {
-        case kFusedCos: return launch_stream_m<kFusedCos>(a, plan, stream);
-        case kFusedDot: return launch_stream_m<kFusedDot>(a, plan, stream);
-        case kRowNorm: return launch_stream_m<kRowNorm>(a, plan, stream);
-        case kRowDot: return launch_stream_m<kRowDot>(a, plan, stream);
-        case kStagedCos: return launch_stream_m<kStagedCos>(a, plan, stream);
+        case kFusedCos: return launch_stream_m<kFusedCos, float>(a, plan, stream);
+        case kFusedDot: return launch_stream_m<kFusedDot, float>(a, plan, stream);
+        case kRowNorm: return launch_stream_m<kRowNorm, float>(a, plan, stream);
+        case kRowDot: return launch_stream_m<kRowDot, float>(a, plan, stream);
+        case kStagedCos: return launch_stream_m<kStagedCos, float>(a, plan, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -751,29 +824,39 @@ cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream) {
 
 cudaError_t launch_generic(const Problem& p, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(p.B)), block(kGenericThreads);
-    if (p.normalize)
-        generic_kernel<true><<<grid, block, 0, stream>>>(p);
-    else
-        generic_kernel<false><<<grid, block, 0, stream>>>(p);
+    if (p.c_bf16) {
+        if (p.normalize)
+            generic_kernel<true, uint16_t><<<grid, block, 0, stream>>>(p);
+        else
+            generic_kernel<false, uint16_t><<<grid, block, 0, stream>>>(p);
+    } else {
+        if (p.normalize)
+            generic_kernel<true, float><<<grid, block, 0, stream>>>(p);
+        else
+            generic_kernel<false, float><<<grid, block, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 
 cudaError_t configure_device_kernels(int smem_optin) {
     const int nq4s[5] = {1, 2, 4, 8, 0};
-    for (int m = kFusedCos; m <= kStagedCos; ++m) {
-        for (int i = 0; i < 5; ++i) {
-            const void* f = stream_fn_for(nq4s[i], m);
-            cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
-            if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
+    for (int bf = 0; bf < 2; ++bf) {
+        for (int m = kFusedCos; m <= kStagedCos; ++m) {
+            for (int i = 0; i < 5; ++i) {
+                const void* f = stream_fn_for(nq4s[i], m, bf);
+                if (!f) continue;
+                cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+                if (e != cudaSuccess) return e;
+                e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
         }
     }
     return cudaSuccess;
 }
 
-int max_active_clusters(int cluster, size_t smem, int nq4, int normalize) {
-    const void* f = stream_fn_for(nq4, normalize ? kFusedCos : kFusedDot);
+int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16) {
+    const void* f = stream_fn_for(nq4, normalize ? kFusedCos : kFusedDot, c_bf16);
     if (!f) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

@@ -181,3 +181,18 @@ def test_unfused_rejects_null_or_overlapping_staged(host_lib):
     assert _unfused(host_lib, B=B, K=K, D=D, staged=C_ADDR + 64) == binding.CS_ERR_ALIAS
     assert _unfused(host_lib, B=B, K=K, D=D, staged=OUT_ADDR + 4 * (B * K - 1)) == binding.CS_ERR_ALIAS
     assert _unfused(host_lib, B=B, K=K, D=D, staged=Q_ADDR) == binding.CS_ERR_ALIAS
+
+
+@pytest.mark.parametrize("name,kw,status", REJECTS, ids=[r[0] for r in REJECTS])
+def test_bf16_batch_rejects(host_lib, name, kw, status):
+    kw = {**dict(Q=Q_ADDR, C=C_ADDR, B=1, K=5, D=512, normalize=1, scale=14.2857, temperature=1.0, out=OUT_ADDR), **kw}
+    assert host_lib.cs_score_candidates_batch_bf16(kw["Q"], kw["C"], kw["B"], kw["K"], kw["D"], kw["normalize"],
+                                                   kw["scale"], kw["temperature"], kw["out"], None) == status
+
+
+def test_bf16_alias_uses_two_byte_elements(host_lib):
+    B, K, D = 4, 8, 16
+    # C holds B*K*D*2 = 1 KB: an out 1100 bytes past C's start does not
+    # overlap it, one 1000 bytes past does
+    assert host_lib.cs_score_candidates_batch_bf16(Q_ADDR, C_ADDR, B, K, D, 1, 1.0, 1.0, C_ADDR + 1000,
+                                                   None) == binding.CS_ERR_ALIAS
