@@ -342,6 +342,30 @@ def main():
             "frac": gbs / _peak_hbm()[0], "algorithmic_bytes_per_question": bytes_q_bf16, "steps": bsteps}
     del Cb
 
+    # A ragged batch of the same size: K_b uniform in [1, 255], one launch.
+    rw = workloads.ragged(B_TOTAL, D, 1, workloads.CLM_SCALE, 12, dev)
+    rout = torch.empty(rw.total_rows, device=dev)
+    ragged_bytes = 4 * (rw.total_rows * D + B_TOTAL * D + rw.total_rows)
+
+    def rstep():
+        cs.cs_score_candidates_ragged(rw.Q, rw.C, rw.offsets, 1, rw.scale, 1.0, out=rout, stream=stream)
+    for _ in range(args.warmup):
+        rstep()
+    barrier()
+    ra, rb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rsteps = max(3, args.steps // 2)
+    ra.record(stream)
+    for _ in range(rsteps):
+        rstep()
+    rb.record(stream)
+    barrier()
+    rms = max_over_ranks(ra.elapsed_time(rb)) / rsteps
+    ragged_info = {"questions_per_s": world * B_TOTAL / (rms / 1e3), "ms_per_call": rms,
+                   "hbm_gbs": world * ragged_bytes / (rms / 1e3) / 1e9,
+                   "frac": world * ragged_bytes / (rms / 1e3) / 1e9 / _peak_hbm()[0],
+                   "total_rows": rw.total_rows, "K_range": [1, 255], "steps": rsteps}
+    del rw, rout
+
     # The unfused baseline on the same workload (two launches per slice).
     staged = torch.empty((B_TOTAL, K), device=dev)
     unfused = {}
@@ -404,6 +428,7 @@ def main():
                     "frac": launch_bytes / (dot_launch_ms / 1e3) / 1e9 / peak},
             "unfused_baseline": unfused,
             "bf16_candidates": bf16,
+            "ragged_cosine": ragged_info,
         },
     }
 

@@ -121,6 +121,35 @@ int cs_score_candidates_batch_bf16(const float *Q, const uint16_t *C, int B,
                                    float temperature, float *out,
                                    cs_stream_t stream);
 
+/*
+ * Ragged batches: question b has its own K_b candidates (1 <= K_b <= 255).
+ * C holds all candidate rows back to back, [total_rows][D] (float32, or
+ * bfloat16 bit patterns for the _bf16 form); question b owns rows
+ * offsets[b] .. offsets[b+1]-1, and out [total_rows] receives its
+ * probabilities at the same rows. offsets is a DEVICE array of B+1 int64
+ * with offsets[0] = 0 and offsets[B] = total_rows; Q is [B][D] as before.
+ * One launch, as cs_score_candidates_batch (work is split by rows, not by
+ * questions, so mixed K_b stays balanced).
+ * The host cannot read offsets without synchronizing, so it checks only
+ * what it is given (B >= 1, B <= total_rows <= 255*B, pointers, scalars,
+ * overlaps of out with Q, C and offsets -- the usual status codes). Each
+ * question's own offsets are checked by the kernel: a question with K_b
+ * outside [1, 255] or rows outside [0, total_rows) is skipped (its rows of
+ * out are not written) and CS_DEVERR_BAD_OFFSETS is set in the device status
+ * word (cs_device_status). The ragged layout is our extension; the page's
+ * call takes one K for the whole batch.
+ */
+int cs_score_candidates_ragged(const float *Q, const float *C,
+                               const long long *offsets, int B,
+                               long long total_rows, int D, int normalize,
+                               float scale, float temperature, float *out,
+                               cs_stream_t stream);
+int cs_score_candidates_ragged_bf16(const float *Q, const uint16_t *C,
+                                    const long long *offsets, int B,
+                                    long long total_rows, int D, int normalize,
+                                    float scale, float temperature, float *out,
+                                    cs_stream_t stream);
+
 /* Execution plans (kernel choices) the library picks between. */
 #define CS_PLAN_AUTO 0
 #define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions */
@@ -203,6 +232,7 @@ int cs_score_candidates_batch_unfused_noalloc(const float *Q, const float *C,
 /* Device status word bits (see cs_device_status). */
 #define CS_DEVERR_WAIT_TIMEOUT 1u  /* an on-chip wait gave up after ~1 s */
 #define CS_DEVERR_BAD_CONFIG 2u    /* a kernel refused an inconsistent launch plan */
+#define CS_DEVERR_BAD_OFFSETS 4u   /* a ragged question had invalid offsets and was skipped */
 
 /*
  * Reads (and, if clear != 0, resets) the status word the kernels of this

@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     cs_score_candidates_batch_plan,
     cs_score_candidates_batch_unfused,
     cs_score_candidates_batch_unfused_noalloc,
+    cs_score_candidates_ragged,
     cs_status_string,
     library,
 )

@@ -73,6 +73,11 @@ def library() -> ctypes.CDLL:
         lib.cs_score_candidates_bf16.restype = I
         lib.cs_score_candidates_batch_bf16.argtypes = [P, P, I, I, I, I, F, F, P, P]
         lib.cs_score_candidates_batch_bf16.restype = I
+        LL = ctypes.c_longlong
+        lib.cs_score_candidates_ragged.argtypes = [P, P, P, I, LL, I, I, F, F, P, P]
+        lib.cs_score_candidates_ragged.restype = I
+        lib.cs_score_candidates_ragged_bf16.argtypes = [P, P, P, I, LL, I, I, F, F, P, P]
+        lib.cs_score_candidates_ragged_bf16.restype = I
         lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
         lib.cs_query_plan.restype = I
         lib.cs_device_status.argtypes = [U, I]
@@ -251,6 +256,33 @@ def cs_score_candidates_batch_bf16(Q, C, normalize: int, scale: float, temperatu
               (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_batch_bf16")
+    return out
+
+
+def cs_score_candidates_ragged(Q, C, offsets, normalize: int, scale: float, temperature: float, out=None,
+                               stream=None):
+    """Ragged batch: Q[B,D] float32, C[total_rows,D] (float32 or bfloat16),
+    offsets[B+1] int64 on the device (question b owns rows
+    offsets[b]..offsets[b+1]-1) -> out[total_rows] float32, one launch."""
+    import torch
+    qp = _check(Q, "Q", 2)
+    bf16 = getattr(C, "dtype", None) == torch.bfloat16
+    cp = _check(C, "C", 2, torch.bfloat16 if bf16 else torch.float32)
+    op_ = _check(offsets, "offsets", 1, torch.int64)
+    B, D = int(Q.shape[0]), int(Q.shape[1])
+    total = int(C.shape[0])
+    if int(C.shape[1]) != D or int(offsets.shape[0]) != B + 1 or Q.device != C.device or offsets.device != C.device:
+        raise ValueError(f"shapes do not match: Q {tuple(Q.shape)}, C {tuple(C.shape)}, offsets {tuple(offsets.shape)}")
+    if out is None:
+        out = torch.empty(total, device=C.device, dtype=torch.float32)
+    op = _check(out, "out", 1)
+    if out.shape[0] != total or out.device != C.device:
+        raise ValueError(f"out must be [total_rows={total}] on {C.device}")
+    lib = library()
+    fn = lib.cs_score_candidates_ragged_bf16 if bf16 else lib.cs_score_candidates_ragged
+    s = _call(fn, C.device, (qp, cp, op_, B, total, D, int(normalize), float(scale), float(temperature), op), stream)
+    if s != 0:
+        raise CSError(s, "cs_score_candidates_ragged")
     return out
 
 

@@ -244,9 +244,10 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
     if (aligned && p.B * 2 <= d.sms) {
         // Few questions: split each over a cluster so one question is not
         // confined to one SM (the page's 256-thread lesson, "What it is worth").
-        const long long q_bytes = static_cast<long long>(cs::c_elem_bytes(p)) * p.K * p.D;
+        const long long avg_k = p.offsets ? (p.total_rows + p.B - 1) / p.B : p.K;
+        const long long q_bytes = static_cast<long long>(cs::c_elem_bytes(p)) * avg_k * p.D;
         int G = 1;
-        while (G * 2 <= cs::kMaxCluster && G * 2 <= p.K && (G * 2) * p.B <= d.sms &&
+        while (G * 2 <= cs::kMaxCluster && G * 2 <= avg_k && (G * 2) * p.B <= d.sms &&
                q_bytes / (G * 2) >= kSplitMinBytes)
             G *= 2;
         for (; G > 1; G /= 2) {
@@ -266,7 +267,7 @@ int run(const float* Q, const void* C, long long B, int K, int D, int normalize,
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, nullptr, c_bf16};
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, nullptr, c_bf16, nullptr, 0};
     Plan plan{};
     const int s = make_plan(*d, p, kind, cluster, ctas, &plan);
     if (s != CS_OK) return s;
@@ -282,6 +283,39 @@ bool overlaps(const void* a, unsigned long long abytes, const void* b, unsigned 
     return a0 < b0 + bbytes && b0 < a0 + abytes;
 }
 
+// Ragged batches: question b owns rows offsets[b] .. offsets[b+1]-1 of C and
+// of out. The offsets live in device memory, so only what the host knows is
+// checked here (B, total_rows, D, pointers, scalars, overlaps); the kernels
+// check each question's own offsets.
+int run_ragged(const float* Q, const void* C, const long long* offsets, long long B, long long total_rows, int D,
+               int normalize, float scale, float temperature, float* out, cs_stream_t stream, int c_bf16) {
+    if (!Q || !C || !offsets || !out) return CS_ERR_NULL_POINTER;
+    if (B <= 0) return CS_ERR_BAD_BATCH;
+    if (total_rows < B) return CS_ERR_K_ZERO;
+    if (total_rows > static_cast<long long>(CS_MAX_K) * B) return CS_ERR_K_TOO_LARGE;
+    if (D <= 0) return CS_ERR_D_ZERO;
+    if (normalize != 0 && normalize != 1) return CS_ERR_BAD_SIMILARITY;
+    if (!std::isfinite(scale) || scale == 0.0f) return CS_ERR_BAD_SCALE;
+    if (!std::isfinite(temperature) || !(temperature > 0.0f)) return CS_ERR_BAD_TEMPERATURE;
+    const unsigned long long cb = c_bf16 ? 2ull : 4ull, rows = static_cast<unsigned long long>(total_rows);
+    if (rows > (1ull << 60) / static_cast<unsigned long long>(D)) return CS_ERR_TOO_LARGE;
+    const unsigned long long out_b = rows * 4ull, q_b = static_cast<unsigned long long>(B) * D * 4ull,
+                             c_b = rows * D * cb, o_b = (static_cast<unsigned long long>(B) + 1ull) * 8ull;
+    if (overlaps(out, out_b, Q, q_b) || overlaps(out, out_b, C, c_b) || overlaps(out, out_b, offsets, o_b))
+        return CS_ERR_ALIAS;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
+    Problem p{Q, C, out, B, CS_MAX_K, D, normalize, scale, temperature, nullptr, c_bf16, offsets, total_rows};
+    Plan plan{};
+    const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
+    if (s != CS_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = plan.kind == cs::kPlanGeneric
+                              ? cs::launch_generic(p, st)
+                              : cs::launch_stream(p, plan, normalize ? cs::kFusedCos : cs::kFusedDot, st);
+    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
 // The unfused baseline: pass 1 stages one value per row in `staged`, pass 2
 // scores from it. Two launches on `stream`.
 int run_unfused(const float* Q, const float* C, long long B, int K, int D, int normalize, float scale,
@@ -295,7 +329,7 @@ int run_unfused(const float* Q, const float* C, long long B, int K, int D, int n
         return CS_ERR_ALIAS;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, staged, 0};
+    Problem p{Q, C, out, B, K, D, normalize, scale, temperature, staged, 0, nullptr, 0};
     Plan plan{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
     if (s != CS_OK) return s;
@@ -380,13 +414,24 @@ int cs_score_candidates_batch_bf16(const float* Q, const uint16_t* C, int B, int
     return run(Q, C, B, K, D, normalize, scale, temperature, out, stream, cs::kPlanAuto, 0, 0, 1);
 }
 
+int cs_score_candidates_ragged(const float* Q, const float* C, const long long* offsets, int B, long long total_rows,
+                               int D, int normalize, float scale, float temperature, float* out, cs_stream_t stream) {
+    return run_ragged(Q, C, offsets, B, total_rows, D, normalize, scale, temperature, out, stream, 0);
+}
+
+int cs_score_candidates_ragged_bf16(const float* Q, const uint16_t* C, const long long* offsets, int B,
+                                    long long total_rows, int D, int normalize, float scale, float temperature,
+                                    float* out, cs_stream_t stream) {
+    return run_ragged(Q, C, offsets, B, total_rows, D, normalize, scale, temperature, out, stream, 1);
+}
+
 int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int normalize, int* plan, int* cluster,
                   int* ctas, int* smem_bytes) {
     const int v = validate(Q, C, B, K, D, normalize, nullptr, false, false, 1.f, 1.f);
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f, nullptr, 0};
+    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f, nullptr, 0, nullptr, 0};
     Plan pl{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &pl);
     if (s != CS_OK) return s;

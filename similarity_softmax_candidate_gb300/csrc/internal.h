@@ -38,6 +38,11 @@ struct Problem {
     float temperature; // divides the scaled similarity
     float* staged;     // unfused baseline only: one float per row [B][K]
     int c_bf16;        // 1: C holds bfloat16 bit patterns (2 bytes each)
+    // Ragged batches: question b owns rows offsets[b] .. offsets[b+1]-1 of C
+    // (and of out); offsets has B+1 entries and total_rows = offsets[B].
+    // nullptr: every question has K rows (row b*K + k).
+    const long long* offsets;
+    long long total_rows;
 };
 
 // Bytes of one element of C.
@@ -63,6 +68,7 @@ struct SmemLayout {
     size_t tn;       // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
     size_t xch;      // kMaxCluster float2 (max, sum) received from the cluster's CTAs
     size_t bars;     // full[stages], empty[stages], qfull[2], qempty[2], xbar (8 B each)
+    size_t range;    // two long longs: this CTA's question range (ragged STREAM plan)
     size_t flag;     // int: this CTA gave up waiting
     size_t total;
 };
@@ -76,6 +82,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
     L.tn = off;     off += 4 * (size_t)kLogitSlots * sizeof(float);
     L.xch = off;    off += (size_t)kMaxCluster * 8;
     L.bars = off;   off += (2 * (size_t)stages + 5) * 8;
+    L.range = off;  off += 16;
     L.flag = off;   off += 16;
     L.total = off;
     return L;

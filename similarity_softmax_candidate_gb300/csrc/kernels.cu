@@ -289,6 +289,61 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane, int* 
     return x;
 }
 
+// ------------------------------------------------------------------ questions and rows
+
+constexpr int kMaxK = 255;
+
+// The rows of question b this CTA handles (CTA `rank` of G on the question):
+// row0 is the index in C (and in out) of the first, n how many. A ragged
+// question whose offsets are out of range -- K_b outside [1, 255], or rows
+// outside [0, total_rows) -- gets n = 0 and bad = true: it is skipped, and
+// nothing outside the buffers is ever read or written.
+struct QRows {
+    long long row0;
+    int n;
+    bool bad;
+};
+
+__device__ __forceinline__ QRows question_rows(const Problem& p, long long b, int rank, int G) {
+    long long o0 = b * p.K, kb = p.K;
+    bool bad = false;
+    if (p.offsets) {
+        o0 = p.offsets[b];
+        const long long o1 = p.offsets[b + 1];
+        kb = o1 - o0;
+        if (!(o0 >= 0 && kb >= 1 && kb <= kMaxK && o1 <= p.total_rows)) {
+            o0 = 0;
+            kb = 0;
+            bad = true;
+        }
+    }
+    const int k = static_cast<int>(kb);
+    const int lo = rank * k / G, hi = (rank + 1) * k / G;
+    return QRows{o0 + lo, hi - lo, bad};
+}
+
+// First index b in [0, n] with off[b] >= target, position n counting as
+// satisfied without being read; off must be non-decreasing for the answer to
+// mean anything, but every read stays in [0, n) whatever it holds. One warp
+// probes 32 positions per round, so n = 16384 takes three dependent rounds.
+__device__ long long lower_bound_warp(const long long* off, long long n, long long target, int lane) {
+    long long lo = 0, hi = n;  // the answer lies in [lo, hi]; hi always satisfies
+    for (;;) {
+        const long long span = hi - lo;
+        const long long step = span <= 31 ? 1 : (span + 30) / 31;  // lo + 31 step >= hi
+        long long pos = lo + step * lane;
+        if (pos > hi) pos = hi;
+        const bool ge = pos == n || off[pos] >= target;
+        const unsigned m = __ballot_sync(0xffffffffu, ge);
+        const int f = __ffs(m) - 1;  // m != 0: the lanes at hi satisfy
+        long long pf = lo + step * f;
+        if (pf > hi) pf = hi;
+        if (f == 0 || step == 1) return pf;
+        lo = lo + step * (f - 1) + 1;
+        hi = pf;
+    }
+}
+
 // ------------------------------------------------------------------ stream kernel
 
 struct StreamArgs {
@@ -376,7 +431,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     constexpr bool COS = cos_logits(MODE);
     constexpr int QF4 = Elem<T>::kQF4;
     const Problem& p = args.p;
-    const int K = p.K, D = p.D;
+    const int D = p.D;
     const int DC = D / Elem<T>::kPerChunk;  // 16-byte chunks per row of C
     const T* Cg = static_cast<const T*>(p.C);
     const int R = args.rows_per_stage, NS = args.stages, G = args.cluster;
@@ -399,6 +454,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     float* tn = reinterpret_cast<float*>(smem + L.tn);
     float2* xch = reinterpret_cast<float2*>(smem + L.xch);
     volatile int* give_up = reinterpret_cast<volatile int*>(smem + L.flag);
+    long long* range = reinterpret_cast<long long*>(smem + L.range);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8u * NS;
@@ -420,32 +476,44 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         fence_mbar_init();
         __syncwarp();
         if (lane == 0 && G > 1 && does_softmax(MODE)) mbar_arrive_expect_tx(smem_u32(xbar), 8u * G);
+        if (G == 1 && p.offsets) {
+            // Ragged STREAM plan: CTA c takes the questions whose first row
+            // falls in [c T / grid, (c+1) T / grid), T = total rows. CTA 0
+            // starts at 0, the last CTA ends at B, and a CTA never ends before
+            // it starts, so every question has a CTA even if offsets are bad.
+            const long long c = blockIdx.x, grid = gridDim.x, rows = p.total_rows;
+            long long qb0 = c == 0 ? 0 : lower_bound_warp(p.offsets, p.B, c * rows / grid, lane);
+            long long qe0 = c + 1 == grid ? p.B : lower_bound_warp(p.offsets, p.B, (c + 1) * rows / grid, lane);
+            if (qe0 < qb0) qe0 = qb0;
+            if (lane == 0) {
+                range[0] = qb0;
+                range[1] = qe0;
+            }
+        }
     }
     __syncthreads();
     // Cluster: announce "my barriers exist"; waited on before the first push.
     if (G > 1 && does_softmax(MODE)) cluster_arrive_release();
 
-    // Questions [qb, qe) and candidate rows [klo, khi) of this CTA.
+    // Questions [qb, qe) of this CTA, and its rank among the CTAs of a question.
     long long qb, qe;
-    int klo, khi;
+    int rank = 0;
     if (G > 1) {
-        const int rank = static_cast<int>(cluster_ctarank());
+        rank = static_cast<int>(cluster_ctarank());
         qb = blockIdx.y;
         qe = qb + 1;
-        klo = rank * K / G;
-        khi = (rank + 1) * K / G;
+    } else if (p.offsets) {
+        qb = range[0];
+        qe = range[1];
     } else {
         const int c = blockIdx.x;
         qb = static_cast<long long>(c) * args.q_per_cta + min(c, args.q_rem);
         qe = qb + args.q_per_cta + (c < args.q_rem ? 1 : 0);
-        klo = 0;
-        khi = K;
     }
-    const int nrows = khi - klo;
-    const int nst = (nrows + R - 1) / R;
     const uint32_t row_bytes = static_cast<uint32_t>(D) * sizeof(T);  // a row of C
     const uint32_t q_bytes = static_cast<uint32_t>(D) * 4u;
     float a = 1.f;  // logit factor of the current question
+    QRows last{0, 0, false};  // rows of the last question (the cluster plan's only one)
 
     if (warp == kConsumerWarps) {
         // ---------------- stage producers: lane l issues stages g = l, l + 8, ...
@@ -457,9 +525,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             unsigned long long issued = 0;
             long long n = 0;  // question of this lane's next stage, relative to qb
             int s = lane;     // its stage index within that question
-            while (s >= nst) {
+            QRows qr = nqs > 0 ? question_rows(p, qb, rank, G) : QRows{0, 0, false};
+            int nst = (qr.n + R - 1) / R;
+            while (n < nqs && s >= nst) {
                 s -= nst;
-                ++n;
+                if (++n < nqs) {
+                    qr = question_rows(p, qb + n, rank, G);
+                    nst = (qr.n + R - 1) / R;
+                }
             }
             for (; n < nqs; ++issued) {
                 const uint32_t bar_e = empty0 + 8u * slot, bar_f = full0 + 8u * slot;
@@ -467,19 +540,22 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     !wait_phase(bar_e, phase ^ 1u, give_up))
                     break;
                 const int k0 = s * R;
-                const uint32_t bytes = static_cast<uint32_t>(min(R, nrows - k0)) * row_bytes;
+                const uint32_t bytes = static_cast<uint32_t>(min(R, qr.n - k0)) * row_bytes;
                 mbar_arrive_expect_tx(bar_f, bytes);
                 bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * stage_bytes),
-                         Cg + ((static_cast<size_t>(qb + n)) * K + klo + k0) * D, bytes, bar_f);
+                         Cg + static_cast<size_t>(qr.row0 + k0) * D, bytes, bar_f);
                 slot += kConsumerWarps;
                 if (slot >= static_cast<uint32_t>(NS)) {
                     slot -= NS;
                     phase ^= 1u;
                 }
                 s += kConsumerWarps;
-                while (s >= nst) {
+                while (n < nqs && s >= nst) {
                     s -= nst;
-                    ++n;
+                    if (++n < nqs) {
+                        qr = question_rows(p, qb + n, rank, G);
+                        nst = (qr.n + R - 1) / R;
+                    }
                 }
             }
             if (*give_up) {
@@ -518,7 +594,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         uint32_t gst0 = 0;                // global index of the question's first stage
         uint32_t slot = warp, phase = 0;  // this warp's next slot and its phase
         long long nq = 0;
-        for (long long b = qb; b < qe; ++b, ++nq, gst0 += nst) {
+        QRows qr = qb < qe ? question_rows(p, qb, rank, G) : QRows{0, 0, false};
+        for (long long b = qb; b < qe; ++b, ++nq) {
+            // the next question's rows: loaded now, used next round
+            const QRows qr_next = b + 1 < qe ? question_rows(p, b + 1, rank, G) : QRows{0, 0, false};
+            const int nrows = qr.n;
+            const int nst = (nrows + R - 1) / R;
+            if (qr.bad && warp == 0 && lane == 0) atomicOr(&g_status, 4u);
             const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
             bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
             const float4* q4 = reinterpret_cast<const float4*>(qbuf + qs * D);
@@ -573,7 +655,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                         if constexpr (does_softmax(MODE))
                             (VPR == 2 && (idx & 1) ? nb : tb)[k0 + r] = val;
                         else
-                            p.staged[static_cast<size_t>(b) * K + klo + k0 + r] = MODE == kRowNorm ? sqrtf(val) : val;
+                            p.staged[qr.row0 + k0 + r] = MODE == kRowNorm ? sqrtf(val) : val;
                     }
                 }
                 __syncwarp();
@@ -591,10 +673,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             consumer_bar_sync();  // every row of question b has its dot (and norm)
             if (does_softmax(MODE) && G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
                 float z[kSlotsPerLane];
-                load_logits<MODE>(tb, nb, MODE == kStagedCos ? p.staged + static_cast<size_t>(b) * K : nullptr,
-                                  nrows, a, lane, z);
-                softmax_store(z, nrows, p.out + static_cast<size_t>(b) * K, lane);
+                load_logits<MODE>(tb, nb, MODE == kStagedCos ? p.staged + qr.row0 : nullptr, nrows, a, lane, z);
+                softmax_store(z, nrows, p.out + qr.row0, lane);
             }
+            gst0 += nst;
+            last = qr;
+            qr = qr_next;
         }
     }
 
@@ -608,8 +692,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         if (warp == 0) {
             const uint32_t rank = cluster_ctarank();
             float z[kSlotsPerLane];
-            load_logits<MODE>(tn, tn + kLogitSlots,
-                              MODE == kStagedCos ? p.staged + static_cast<size_t>(qb) * K + klo : nullptr, nrows, a,
+            const int nrows = last.n;
+            load_logits<MODE>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr, nrows, a,
                               lane, z);
             float m = -INFINITY;
 #pragma unroll
@@ -632,7 +716,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             }
             const float M = warp_max(mj);
             const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
-            float* dst = p.out + static_cast<size_t>(qb) * K + klo;
+            float* dst = p.out + last.row0;
 #pragma unroll
             for (int j = 0; j < kSlotsPerLane; ++j) {
                 const int k = lane + 32 * j;
@@ -657,7 +741,12 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = kGenericThreads / 32;
     const long long b = blockIdx.x;
-    const int K = p.K, D = p.D;
+    const QRows qr = question_rows(p, b, 0, 1);
+    if (qr.bad) {
+        if (threadIdx.x == 0) atomicOr(&g_status, 4u);
+        return;
+    }
+    const int K = qr.n, D = p.D;
     const float* __restrict__ q = p.Q + static_cast<size_t>(b) * D;
     float qn = 1.f;
     if (COS) {
@@ -670,7 +759,7 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     }
     const float a = logit_factor(qn, p.scale, p.temperature, COS);
     for (int k = warp; k < K; k += nwarps) {
-        const T* __restrict__ c = static_cast<const T*>(p.C) + (static_cast<size_t>(b) * K + k) * D;
+        const T* __restrict__ c = static_cast<const T*>(p.C) + static_cast<size_t>(qr.row0 + k) * D;
         float t0 = 0.f, t1 = 0.f, n0 = 0.f, n1 = 0.f;
         int d = lane;
         for (; d + 32 < D; d += 64) {
@@ -696,7 +785,7 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         float z[kSlotsPerLane];
 #pragma unroll
         for (int j = 0; j < kSlotsPerLane; ++j) z[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
-        softmax_store(z, K, p.out + static_cast<size_t>(b) * K, lane);
+        softmax_store(z, K, p.out + qr.row0, lane);
     }
 }
 

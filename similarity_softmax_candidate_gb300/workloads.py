@@ -19,6 +19,8 @@ distribution, so Gaussian features stand in for them:
   kev_overflow the same with C scaled by 1e3 (raw logits far beyond exp range)
   throughput   16384 questions, K=255, D=512, q, C ~ N(0,1), scored as four
                consecutive slices of 4096 questions, cosine and dot
+  ragged       B questions with K_b uniform in [kmin, kmax] (the serving mix
+               of short and long candidate lists), rows back to back
 
 CLM's logit_scale is ln(1/0.07), so its scale exp(logit_scale) is 1/0.07;
 Kev's is 1/sqrt(256) = 1/16. The temperature is 1. Scales are rounded to
@@ -134,6 +136,44 @@ def throughput(device="cuda", seed=4, B=THROUGHPUT_B, K=MAX_K, D=512):
         C[b0:b1].normal_(generator=g)
     return [Workload("throughput_cos", Q, C, 1, CLM_SCALE),
             Workload("throughput_dot", Q, C, 0, KEV_SCALE)]
+
+
+@dataclasses.dataclass
+class RaggedWorkload:
+    """A ragged batch: question b owns rows offsets[b]..offsets[b+1]-1 of C."""
+    name: str
+    Q: torch.Tensor        # [B, D] float32
+    C: torch.Tensor        # [total_rows, D] float32
+    offsets: torch.Tensor  # [B + 1] int64
+    normalize: int
+    scale: float
+    temperature: float = TEMPERATURE
+
+    @property
+    def B(self) -> int:
+        return int(self.Q.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.C.shape[0])
+
+
+def ragged(B, D, normalize, scale, seed, device="cpu", kmin=1, kmax=MAX_K, name=None) -> RaggedWorkload:
+    """B questions with K_b drawn uniformly from [kmin, kmax] (the serving
+    mix of short and long candidate lists), q and C ~ N(0,1)."""
+    g = _gen(seed, "cpu")
+    k = torch.randint(kmin, kmax + 1, (B,), generator=g, dtype=torch.int64)
+    offsets = torch.zeros(B + 1, dtype=torch.int64)
+    offsets[1:] = torch.cumsum(k, 0)
+    total = int(offsets[-1])
+    Q = normal((B, D), seed + 1, device)
+    C = torch.empty((total, D), device=device, dtype=torch.float32)
+    gc = _gen(seed + 2, device)
+    step = max(1, (1 << 28) // D)
+    for r0 in range(0, total, step):
+        C[r0:r0 + step].normal_(generator=gc)
+    return RaggedWorkload(name or f"ragged_b{B}_d{D}_{'cos' if normalize else 'dot'}", Q, C, offsets.to(device),
+                          int(normalize), float(scale))
 
 
 CONFIGS = {

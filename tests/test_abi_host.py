@@ -196,3 +196,28 @@ def test_bf16_alias_uses_two_byte_elements(host_lib):
     # overlap it, one 1000 bytes past does
     assert host_lib.cs_score_candidates_batch_bf16(Q_ADDR, C_ADDR, B, K, D, 1, 1.0, 1.0, C_ADDR + 1000,
                                                    None) == binding.CS_ERR_ALIAS
+
+
+OFF_ADDR = 0x7F4000000000
+
+
+def _ragged(lib, Q=Q_ADDR, C=C_ADDR, offsets=OFF_ADDR, B=4, total=40, D=512, normalize=1, scale=2.0,
+            temperature=1.0, out=OUT_ADDR):
+    return lib.cs_score_candidates_ragged(Q, C, offsets, B, total, D, normalize, scale, temperature, out, None)
+
+
+def test_ragged_rejects(host_lib):
+    E = binding
+    assert _ragged(host_lib, offsets=None) == E.CS_ERR_NULL_POINTER
+    assert _ragged(host_lib, Q=None) == E.CS_ERR_NULL_POINTER
+    assert _ragged(host_lib, B=0) == E.CS_ERR_BAD_BATCH
+    assert _ragged(host_lib, B=4, total=3) == E.CS_ERR_K_ZERO          # some question would have no row
+    assert _ragged(host_lib, B=4, total=4 * 255 + 1) == E.CS_ERR_K_TOO_LARGE
+    assert _ragged(host_lib, D=0) == E.CS_ERR_D_ZERO
+    assert _ragged(host_lib, normalize=3) == E.CS_ERR_BAD_SIMILARITY
+    assert _ragged(host_lib, scale=0.0) == E.CS_ERR_BAD_SCALE
+    assert _ragged(host_lib, temperature=-2.0) == E.CS_ERR_BAD_TEMPERATURE
+    assert _ragged(host_lib, out=OFF_ADDR + 8) == E.CS_ERR_ALIAS         # out over the offsets
+    assert _ragged(host_lib, out=C_ADDR + 4 * 512 * 39) == E.CS_ERR_ALIAS
+    assert host_lib.cs_score_candidates_ragged_bf16(Q_ADDR, C_ADDR, OFF_ADDR, 4, 40, 512, 1, 2.0, 1.0,
+                                                    C_ADDR + 2 * 512 * 39, None) == E.CS_ERR_ALIAS
