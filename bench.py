@@ -67,6 +67,23 @@ def _dist():
     return rank, world, local
 
 
+def reduce_max(x, device=None):
+    """Maximum of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, max_ms, world):
+    """Units per second of the whole job: every rank processed
+    units_per_rank, the slowest in max_ms."""
+    return world * units_per_rank / (max_ms / 1e3)
+
+
 def _peak_hbm():
     path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
     try:
@@ -263,11 +280,7 @@ def main():
         torch.cuda.synchronize()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dev)
 
     B_TOTAL, CHUNK = args.questions, args.chunk
     if B_TOTAL % CHUNK:
@@ -393,7 +406,7 @@ def main():
     del staged
 
     ms_per_step = ms_cos / args.steps
-    value = world * B_TOTAL / (ms_per_step / 1e3)
+    value = whole_job_rate(B_TOTAL, ms_per_step, world)
     peak, peak_kind = _peak_hbm()
     launch_bytes = CHUNK * BYTES_PER_QUESTION
     mean_launch_ms = sum(launches_cos) / len(launches_cos)

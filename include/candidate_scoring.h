@@ -242,6 +242,17 @@ int cs_score_candidates_batch_unfused_noalloc(const float *Q, const float *C,
  */
 int cs_device_status(unsigned *flags, int clear);
 
+/*
+ * Self-test of the kernels' bounded waits: enqueues one tiny kernel whose
+ * single thread waits, with the same wait routine the scoring kernels use,
+ * on an on-chip barrier nothing will complete. After limit_us microseconds
+ * (1 .. 1000000; CS_ERR_BAD_PLAN otherwise) it gives up, sets
+ * CS_DEVERR_WAIT_TIMEOUT in the device status word and exits, leaving the
+ * context usable. For tests and health checks: it shows that a wait that
+ * never completes ends in a status, not a hang.
+ */
+int cs_selftest_bounded_wait(int limit_us, cs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,6 +80,8 @@ def library() -> ctypes.CDLL:
         lib.cs_score_candidates_ragged_bf16.restype = I
         lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
         lib.cs_query_plan.restype = I
+        lib.cs_selftest_bounded_wait.argtypes = [I, P]
+        lib.cs_selftest_bounded_wait.restype = I
         lib.cs_device_status.argtypes = [U, I]
         lib.cs_device_status.restype = I
         _lib = lib

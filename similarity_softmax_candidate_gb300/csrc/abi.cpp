@@ -442,6 +442,13 @@ int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int norma
     return CS_OK;
 }
 
+int cs_selftest_bounded_wait(int limit_us, cs_stream_t stream) {
+    if (limit_us < 1 || limit_us > 1000000) return CS_ERR_BAD_PLAN;
+    const cudaError_t e = cs::launch_selftest_wait(static_cast<unsigned long long>(limit_us) * 1000ull,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
 int cs_device_status(unsigned* flags, int clear) {
     if (!flags) return CS_ERR_NULL_POINTER;
     return cs::read_device_status(flags, clear != 0) == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;

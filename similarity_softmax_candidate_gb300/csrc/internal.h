@@ -118,6 +118,9 @@ cudaError_t configure_device_kernels(int smem_optin);
 // at once (0 if none).
 int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16);
 
+// Bounded-wait self-test: one wait that nothing completes, limit_ns long.
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
+
 // Device status word (bounded-wait give-ups).
 cudaError_t read_device_status(unsigned* flags, bool clear);
 

@@ -191,14 +191,15 @@ __device__ __forceinline__ float warp_max(float v) {
 // Bounded wait on an mbarrier phase. Returns false if this CTA has given up
 // (now or earlier); the first thread to hit the limit raises the CTA's flag
 // and the device status bit.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* give_up) {
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* give_up,
+                                           unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*give_up) return false;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*give_up) return false;
-        if ((it & 31u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+        if ((it & 31u) == 0 && globaltimer() - t0 > limit_ns) {
             *give_up = 1;
             atomicOr(&g_status, 1u);
             return false;
@@ -806,6 +807,21 @@ __global__ void __launch_bounds__(256) staged_softmax_kernel(const Problem p) {
     softmax_store(z, p.K, p.out + static_cast<size_t>(b) * p.K, lane);
 }
 
+// Self-test of the bounded wait: one thread waits, with the kernels' own
+// wait_phase, on an mbarrier nothing will ever arrive at; after limit_ns it
+// gives up, sets the device status bit and returns. Nothing is copied into
+// shared memory, so nothing is in flight when it leaves.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int flag;
+    if (threadIdx.x == 0) {
+        flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+        (void)wait_phase(smem_u32(&bar), 0, reinterpret_cast<volatile int*>(&flag), limit_ns);
+    }
+}
+
 // ------------------------------------------------------------------ dispatch
 
 template <int NQC, int MODE, typename T>
@@ -903,6 +919,11 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
         case kStagedCos: return launch_stream_m<kStagedCos, float>(a, plan, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream) {
