@@ -193,6 +193,7 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     int R = (rows + cs::kConsumerWarps - 1) / cs::kConsumerWarps;
     const int Rmax = stage_rows(static_cast<long long>(cb) * p.D);
     if (R > Rmax) R = Rmax;
+    while (R > 1 && max_stages(d, R, p.D, cb) == 0) --R;  // a ring of 8 stages must fit
     const int max_ns = max_stages(d, R, p.D, cb);
     if (max_ns == 0) return false;
     const int ns = ring_stages((rows + R - 1) / R, max_ns);
