@@ -556,13 +556,38 @@ def latency_table(cs, workloads, dev, calls):
             torch.cuda.synchronize()
             cold.append(1e3 * a.elapsed_time(b))
         plan = cs.cs_query_plan(wl.Q, wl.C, normalize)
-        rows.append({"shape": name, "B": B, "K": k, "D": d, "direct_us": direct, "graph_us": graph,
+        native = native_latency(B, k, d, normalize, calls)
+        rows.append({"shape": name, "B": B, "K": k, "D": d, "c_abi": native, "direct_us": direct, "graph_us": graph,
                      "graph_loop_us": fused_loop, "cold_l2_us": statistics.median(cold),
                      "unfused_graph_loop_us": unfused_loop, "fused_over_unfused": unfused_loop / fused_loop,
                      "plan": plan["plan"], "cluster": plan["cluster"], "ctas": plan["ctas"],
                      "rtx4090_fused_us_context": page_us, "rtx4090_ratio_context": page_ratio})
         del g
     return rows
+
+
+def native_latency(B, K, D, normalize, calls):
+    """us per call from native code (cs_latency: the C ABI called from C++,
+    no Python between calls): direct back-to-back calls, a one-call graph
+    replayed, and 50 calls in one graph; fused and unfused."""
+    from similarity_softmax_candidate_gb300 import _build
+    try:
+        tool = _build.build_latency_tool()
+        res = {}
+        for unfused in (0, 1):
+            r = subprocess.run([tool, str(B), str(K), str(D), str(normalize), str(calls), str(unfused)],
+                               capture_output=True, text=True, timeout=120)
+            if r.returncode != 0:
+                return {"error": r.stderr.strip()[-200:]}
+            d = json.loads(r.stdout.strip().splitlines()[-1])
+            tag = "unfused_" if unfused else ""
+            for key in ("direct_us", "graph1_us", "graph50_us"):
+                res[tag + key] = d[key]
+        res["fused_over_unfused_graph50"] = res["unfused_graph50_us"] / res["graph50_us"]
+        res["fused_over_unfused_direct"] = res["unfused_direct_us"] / res["direct_us"]
+        return res
+    except Exception as e:  # the Python-side numbers stand without it
+        return {"error": str(e)[:200]}
 
 
 def e2e(cs, wl, dev, args, world, barrier, max_over_ranks):

@@ -17,12 +17,18 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libcandidate_scoring.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
+# Native latency harness (calls the C ABI from C++; see csrc/latency_main.cu).
+LATENCY_NAME = "cs_latency"
+LATENCY_PATH = os.path.join(PKG, LATENCY_NAME)
+LATENCY_SRC = os.path.join(CSRC, "latency_main.cu")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    """Library sources: every .cu/.cpp in csrc except programs (*_main.cu)."""
+    files = glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp"))
+    return sorted(f for f in files if not f.endswith("_main.cu"))
 
 
 def _inputs():
@@ -77,5 +83,23 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+def build_latency_tool(force: bool = False) -> str:
+    """Compile the native latency harness next to the library (linked to
+    it, found at run time through an $ORIGIN rpath)."""
+    build_library()
+    if not force and os.path.exists(LATENCY_PATH) and \
+            os.path.getmtime(LATENCY_PATH) >= max(os.path.getmtime(LATENCY_SRC), os.path.getmtime(LIB_PATH)):
+        return LATENCY_PATH
+    staged = LATENCY_PATH + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), "-O2", "-std=c++17", *ARCH_FLAGS, "-I", INCLUDE, LATENCY_SRC, "-o", staged, "-L", PKG,
+           "-lcandidate_scoring", "-Xlinker", "-rpath,$ORIGIN"]
+    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout.decode(errors='replace')}")
+    os.replace(staged, LATENCY_PATH)
+    return LATENCY_PATH
+
+
 if __name__ == "__main__":
     print(build_library(force=True, verbose=True))
+    print(build_latency_tool(force=True))
