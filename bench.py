@@ -195,16 +195,21 @@ def _host_sample(n, seed=4):
 
 
 def cpu_baseline(target_s=10.0):
-    """The oracle as it stands (single-threaded C, fp64) on a bounded sample."""
+    """The oracle as it stands (single-threaded C, fp64) on a bounded sample:
+    passes over up to 2048 host-drawn questions until about target_s of CPU
+    time has been spent."""
     from similarity_softmax_candidate_gb300 import workloads
     Qp, Cp = _host_sample(8)
     t_probe = _time_oracle(Qp, Cp, 1, workloads.CLM_SCALE) / 8
     n = int(max(8, min(2048, target_s / max(t_probe, 1e-6))))
     Qs, Cs = _host_sample(n, seed=5)
-    dt = _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
-    return {"value": n / dt, "unit": "questions/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} questions of the K=255, D=512 cosine workload (host-drawn N(0,1)), "
-                      f"fp64 C oracle, single thread, {dt:.1f} s"}
+    dt, done = 0.0, 0
+    while dt < target_s or done == 0:
+        dt += _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
+        done += n
+    return {"value": done / dt, "unit": "questions/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} question scorings ({done // n} passes over {n} questions of the K=255, D=512 "
+                      f"cosine workload, host-drawn N(0,1)), fp64 C oracle, single thread, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -327,7 +332,74 @@ def main():
     ms_dot, launches_dot, _ = timed(wl_dot)
     clock_info = clocks.stop()
 
-    # The same workload with the candidates stored as bfloat16 (half the bytes).
+    bf16, ragged_info, unfused = {}, {}, {}
+    if not args.skip_extra:
+        bf16, ragged_info, unfused = extras(cs, workloads, wl_cos, wl_dot, out, dev, stream, args, world, barrier,
+                                            max_over_ranks, ms_cos, ms_dot)
+
+    ms_per_step = ms_cos / args.steps
+    value = whole_job_rate(B_TOTAL, ms_per_step, world)
+    peak, peak_kind = _peak_hbm()
+    launch_bytes = CHUNK * BYTES_PER_QUESTION
+    mean_launch_ms = sum(launches_cos) / len(launches_cos)
+    achieved = launch_bytes / (mean_launch_ms / 1e3) / 1e9
+    traffic = _traffic_from_profile(_kernel_sha())
+    if traffic is not None:
+        traffic *= CHUNK / 4096.0
+    dot_ms_step = ms_dot / args.steps
+    dot_launch_ms = sum(launches_dot) / len(launches_dot)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "questions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"throughput: {B_TOTAL} questions x K=255 x D=512 fp32 N(0,1), CLM cosine "
+                               f"(scale 1/0.07, T=1), {B_TOTAL // CHUNK} launches of {CHUNK} questions per step",
+                   "B": B_TOTAL, "K": K, "D": D, "launches_per_step": B_TOTAL // CHUNK,
+                   "l2": f"inputs ({B_TOTAL * K * D * 4 / 1e9:.1f} GB per rank) larger than L2 (129 MB); no flush",
+                   "plan": plan, "parallelism": f"replicas x{world}"},
+        "gpu_launches": n_launch,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": f"stream_kernel (STREAM plan), one launch = {CHUNK} questions",
+                     "algorithmic_bytes_per_launch": launch_bytes, "mean_launch_ms": mean_launch_ms,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+        "clocks": clock_info,
+        "extra": {
+            "hbm_gbs_step": world * B_TOTAL * BYTES_PER_QUESTION / (ms_per_step / 1e3) / 1e9,
+            "frac_of_8tbs_nominal": achieved / 8000.0,
+            "dot": {"questions_per_s": world * B_TOTAL / (dot_ms_step / 1e3), "ms_per_step": dot_ms_step,
+                    "launch_gbs": launch_bytes / (dot_launch_ms / 1e3) / 1e9,
+                    "frac": launch_bytes / (dot_launch_ms / 1e3) / 1e9 / peak},
+            "unfused_baseline": unfused,
+            "bf16_candidates": bf16,
+            "ragged_cosine": ragged_info,
+        },
+    }
+
+    if not args.skip_extra:
+        line["extra"]["latency_b1"] = latency_table(cs, workloads, dev, args.latency_calls)
+        line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
+    del wls, wl_cos, wl_dot
+    torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_cpu:
+        try:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        except Exception as e:  # the oracle is optional for the GPU numbers
+            line["cpu_baseline"] = {"value": None, "unit": "questions/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {e}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def extras(cs, workloads, wl_cos, wl_dot, out, dev, stream, args, world, barrier, max_over_ranks, ms_cos, ms_dot):
+    """bfloat16 candidates, a ragged batch and the unfused baseline on the
+    throughput workload's sizes (extra keys of the JSON line)."""
+    import torch
     bf16 = {}
     Cb = torch.empty(wl_cos.C.shape, device=dev, dtype=torch.bfloat16)
     for b0 in range(0, B_TOTAL, CHUNK):
@@ -405,63 +477,7 @@ def main():
             "fused_over_unfused": ums / fused_ms, "steps": usteps}
     del staged
 
-    ms_per_step = ms_cos / args.steps
-    value = whole_job_rate(B_TOTAL, ms_per_step, world)
-    peak, peak_kind = _peak_hbm()
-    launch_bytes = CHUNK * BYTES_PER_QUESTION
-    mean_launch_ms = sum(launches_cos) / len(launches_cos)
-    achieved = launch_bytes / (mean_launch_ms / 1e3) / 1e9
-    traffic = _traffic_from_profile(_kernel_sha())
-    if traffic is not None:
-        traffic *= CHUNK / 4096.0
-    dot_ms_step = ms_dot / args.steps
-    dot_launch_ms = sum(launches_dot) / len(launches_dot)
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "questions/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"throughput: {B_TOTAL} questions x K=255 x D=512 fp32 N(0,1), CLM cosine "
-                               f"(scale 1/0.07, T=1), {B_TOTAL // CHUNK} launches of {CHUNK} questions per step",
-                   "B": B_TOTAL, "K": K, "D": D, "launches_per_step": B_TOTAL // CHUNK,
-                   "l2": f"inputs ({B_TOTAL * K * D * 4 / 1e9:.1f} GB per rank) larger than L2 (129 MB); no flush",
-                   "plan": plan, "parallelism": f"replicas x{world}"},
-        "gpu_launches": n_launch,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"stream_kernel (STREAM plan), one launch = {CHUNK} questions",
-                     "algorithmic_bytes_per_launch": launch_bytes, "mean_launch_ms": mean_launch_ms,
-                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
-        "clocks": clock_info,
-        "extra": {
-            "hbm_gbs_step": world * B_TOTAL * BYTES_PER_QUESTION / (ms_per_step / 1e3) / 1e9,
-            "frac_of_8tbs_nominal": achieved / 8000.0,
-            "dot": {"questions_per_s": world * B_TOTAL / (dot_ms_step / 1e3), "ms_per_step": dot_ms_step,
-                    "launch_gbs": launch_bytes / (dot_launch_ms / 1e3) / 1e9,
-                    "frac": launch_bytes / (dot_launch_ms / 1e3) / 1e9 / peak},
-            "unfused_baseline": unfused,
-            "bf16_candidates": bf16,
-            "ragged_cosine": ragged_info,
-        },
-    }
-
-    if not args.skip_extra:
-        line["extra"]["latency_b1"] = latency_table(cs, workloads, dev, args.latency_calls)
-        line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
-    del wls, wl_cos, wl_dot
-    torch.cuda.empty_cache()
-
-    if rank == 0 and not args.no_cpu:
-        try:
-            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
-        except Exception as e:  # the oracle is optional for the GPU numbers
-            line["cpu_baseline"] = {"value": None, "unit": "questions/s", "cores": 1, "kind": "oracle",
-                                    "sample": f"failed: {e}"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+    return bf16, ragged_info, unfused
 
 
 def latency_table(cs, workloads, dev, calls):
