@@ -63,6 +63,8 @@ def _load():
             lib.oracle_softmax.restype = i
             lib.oracle_score_batch.argtypes = [f, f, l, l, l, i, d, d, d, p]
             lib.oracle_score_batch.restype = i
+            lib.oracle_project.argtypes = [f, f, l, l, l, p]
+            lib.oracle_project.restype = i
             _lib = lib
     return _lib
 
@@ -113,3 +115,30 @@ def score_batch(Q, C, normalize, scale, temperature, eps=EPS):
     if rc != 0:
         raise ValueError("oracle_score_batch: bad size")
     return p
+
+
+def project(H, W):
+    """P = H W^T in float64 for H[R, Din] and W[D, Din] (float32 values, e.g.
+    bfloat16 weights and features widened exactly)."""
+    H = np.ascontiguousarray(H, dtype=np.float32)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    if H.ndim != 2 or W.ndim != 2 or H.shape[1] != W.shape[1]:
+        raise ValueError(f"shape mismatch: H {H.shape}, W {W.shape}")
+    P = np.empty((H.shape[0], W.shape[0]), dtype=np.float64)
+    rc = _load().oracle_project(H.ctypes.data, W.ctypes.data, H.shape[0], H.shape[1], W.shape[0], P.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_project: bad size")
+    return P
+
+
+def project_score_batch(Hq, Wq, Hc, Wc, normalize, scale, temperature, eps=EPS):
+    """The readout with caller-side projections: q_b = Wq hq_b, c_bk = Wc
+    hc_bk, then score_batch on the projected vectors (each projected value is
+    rounded once to float32, the precision the scorer takes). Hq [B, Din],
+    Hc [B, K, Din]; returns p [B, K] float64."""
+    Hq = np.asarray(Hq, dtype=np.float32)
+    Hc = np.asarray(Hc, dtype=np.float32)
+    B, K, Din = Hc.shape
+    q = project(Hq, Wq).astype(np.float32)
+    c = project(Hc.reshape(B * K, Din), Wc).astype(np.float32).reshape(B, K, -1)
+    return score_batch(q, c, normalize, scale, temperature, eps)

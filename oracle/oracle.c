@@ -96,3 +96,24 @@ int oracle_score_batch(const float *Q, const float *C, long B, long K, long D,
      * except for the in-place exp, which reads z[b,k] before writing p[b,k]. */
     return oracle_softmax(p, B, K, p);
 }
+
+/* Projection of feature rows by a weight matrix (the caller-side heads of
+ * PR #69's opening table: CLM's state_head / action_head, Kev's k() / q()):
+ *   P[r][n] = sum_i H[r][i] * W[n][i]
+ * H is [R][Din], W is [D][Din] (one output feature per row of W), P is
+ * [R][D]; float inputs (the values the GPU sees), double accumulation in
+ * index order. Returns 0, or -1 for a bad size. */
+int oracle_project(const float *H, const float *W, long R, long Din, long D, double *P)
+{
+    if (R < 0 || Din < 0 || D < 0) return -1;
+    for (long r = 0; r < R; ++r) {
+        const float *h = H + (size_t)r * (size_t)Din;
+        for (long n = 0; n < D; ++n) {
+            const float *w = W + (size_t)n * (size_t)Din;
+            double acc = 0.0;
+            for (long i = 0; i < Din; ++i) acc += (double)h[i] * (double)w[i];
+            P[(size_t)r * (size_t)D + (size_t)n] = acc;
+        }
+    }
+    return 0;
+}

@@ -265,3 +265,51 @@ def test_query_norm_is_not_multiplied():
     cos = 1.0 - cdist(q[None].astype(np.float64), C.astype(np.float64), "cosine")[0]
     np.testing.assert_allclose(z, cos, rtol=1e-10, atol=1e-14)
     assert np.max(np.abs(z - cos / math.sqrt(8))) > 1e-3
+
+
+# ---------------------------------------------------------------- projections
+
+def test_project_identity_and_permutation():
+    """W = identity gives H back exactly; a permutation matrix permutes
+    columns; a scaled identity scales them (powers of two: exact)."""
+    rng = _rng(20)
+    H = _rand(rng, 7, 16)
+    np.testing.assert_array_equal(oracle.project(H, np.eye(16, dtype=np.float32)), H.astype(np.float64))
+    perm = rng.permutation(16)
+    P = np.eye(16, dtype=np.float32)[perm]
+    np.testing.assert_array_equal(oracle.project(H, P), H[:, perm].astype(np.float64))
+    np.testing.assert_array_equal(oracle.project(H, 4 * np.eye(16, dtype=np.float32)), 4.0 * H.astype(np.float64))
+
+
+def test_project_matches_numpy_and_is_linear():
+    rng = _rng(21)
+    H, W, W2 = _rand(rng, 9, 64), _rand(rng, 12, 64), _rand(rng, 12, 64)
+    np.testing.assert_allclose(oracle.project(H, W), H.astype(np.float64) @ W.astype(np.float64).T, rtol=1e-12,
+                               atol=1e-12)
+    # additive in W (the float32 sum W + W2 is exact when it is computed in
+    # float64 and compared in float64)
+    lhs = oracle.project(H, W) + oracle.project(H, W2)
+    rhs = H.astype(np.float64) @ (W.astype(np.float64) + W2.astype(np.float64)).T
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+    assert oracle.project(H, W).shape == (9, 12)
+
+
+def test_project_score_with_identity_heads_is_plain_score():
+    """Identity heads (D = Din) leave the readout unchanged."""
+    rng = _rng(22)
+    Hq, Hc = _rand(rng, 3, 32), _rand(rng, 3, 20, 32)
+    I = np.eye(32, dtype=np.float32)
+    for normalize in (0, 1):
+        np.testing.assert_array_equal(oracle.project_score_batch(Hq, I, Hc, I, normalize, 2.0, 1.0),
+                                      oracle.score_batch(Hq, Hc, normalize, 2.0, 1.0))
+
+
+def test_project_score_cosine_ignores_head_scale():
+    """Cosine scoring is unchanged when a head is multiplied by a positive
+    power of two."""
+    rng = _rng(23)
+    Hq, Hc = _rand(rng, 2, 32), _rand(rng, 2, 9, 32)
+    Wq, Wc = _rand(rng, 16, 32), _rand(rng, 16, 32)
+    a = oracle.project_score_batch(Hq, Wq, Hc, Wc, 1, 14.2857, 1.0)
+    b = oracle.project_score_batch(Hq, 2 * Wq, Hc, 8 * Wc, 1, 14.2857, 1.0)
+    np.testing.assert_allclose(a, b, rtol=1e-15)
