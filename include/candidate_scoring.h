@@ -150,6 +150,32 @@ int cs_score_candidates_ragged_bf16(const float *Q, const uint16_t *C,
                                     float scale, float temperature, float *out,
                                     cs_stream_t stream);
 
+/*
+ * Caller-side projections on the tensor cores (the page leaves them to the
+ * caller: CLM scores state_head(s) against action_head(c), Kev k(h_opts)
+ * against q(h_decide)). Features and weights are bfloat16 bit patterns,
+ * row-major; accumulation is float32.
+ *
+ * cs_project_rows: P[r][n] = sum_i H[r][i] * W[n][i] for H [rows][Din],
+ *   W [D][Din], P [rows][D] float32.
+ * cs_project_score_batch: q_b = Wq hq_b (written to qproj [B][D] float32,
+ *   a caller-owned buffer), then for each question the projected candidates
+ *   c_bk = Wc hc_bk (Hc [B][K][Din]) are scored against q_b exactly as
+ *   cs_score_candidates_batch scores C -- without the projected candidates
+ *   ever being written to memory: they exist only in tensor memory.
+ *   Two kernels are enqueued on `stream`.
+ * Shapes: D = 256 or 512, Din a multiple of 64, 1 <= K <= 255; all pointers
+ * 16-byte aligned (CS_ERR_BAD_PLAN otherwise). Other errors and conventions
+ * as cs_score_candidates_batch. This is our extension of the page's kernel.
+ */
+int cs_project_rows(const uint16_t *H, const uint16_t *W, long long rows,
+                    int Din, int D, float *P, cs_stream_t stream);
+int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,
+                           const uint16_t *Hc, const uint16_t *Wc, int B,
+                           int K, int Din, int D, int normalize, float scale,
+                           float temperature, float *qproj, float *out,
+                           cs_stream_t stream);
+
 /* Execution plans (kernel choices) the library picks between. */
 #define CS_PLAN_AUTO 0
 #define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions */

@@ -19,6 +19,8 @@ from .binding import (  # noqa: F401
     CSError,
     cs_abi_version,
     cs_device_status,
+    cs_project_rows,
+    cs_project_score_batch,
     cs_query_plan,
     cs_score_candidates,
     cs_score_candidates_bf16,

@@ -80,6 +80,11 @@ def library() -> ctypes.CDLL:
         lib.cs_score_candidates_ragged_bf16.restype = I
         lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
         lib.cs_query_plan.restype = I
+        LL2 = ctypes.c_longlong
+        lib.cs_project_rows.argtypes = [P, P, LL2, I, I, P, P]
+        lib.cs_project_rows.restype = I
+        lib.cs_project_score_batch.argtypes = [P, P, P, P, I, I, I, I, I, F, F, P, P, P]
+        lib.cs_project_score_batch.restype = I
         lib.cs_selftest_bounded_wait.argtypes = [I, P]
         lib.cs_selftest_bounded_wait.restype = I
         lib.cs_device_status.argtypes = [U, I]
@@ -285,6 +290,56 @@ def cs_score_candidates_ragged(Q, C, offsets, normalize: int, scale: float, temp
     s = _call(fn, C.device, (qp, cp, op_, B, total, D, int(normalize), float(scale), float(temperature), op), stream)
     if s != 0:
         raise CSError(s, "cs_score_candidates_ragged")
+    return out
+
+
+def cs_project_rows(H, W, out=None, stream=None):
+    """P = H W^T on the tensor cores: H [rows, Din] and W [D, Din] bfloat16
+    (CUDA) -> P [rows, D] float32. D in {256, 512}, Din a multiple of 64."""
+    import torch
+    hp = _check(H, "H", 2, torch.bfloat16)
+    wp = _check(W, "W", 2, torch.bfloat16)
+    rows, Din = (int(x) for x in H.shape)
+    D = int(W.shape[0])
+    if int(W.shape[1]) != Din or W.device != H.device:
+        raise ValueError(f"W {tuple(W.shape)} does not match H {tuple(H.shape)}")
+    if out is None:
+        out = torch.empty((rows, D), device=H.device, dtype=torch.float32)
+    op = _check(out, "out", 2)
+    if tuple(out.shape) != (rows, D):
+        raise ValueError(f"out must be [{rows}, {D}]")
+    s = _call(library().cs_project_rows, H.device, (hp, wp, rows, Din, D, op), stream)
+    if s != 0:
+        raise CSError(s, "cs_project_rows")
+    return out
+
+
+def cs_project_score_batch(Hq, Wq, Hc, Wc, normalize: int, scale: float, temperature: float, qproj=None, out=None,
+                           stream=None):
+    """Projected readout: q_b = Wq hq_b, c_bk = Wc hc_bk (bfloat16 features
+    and weights, float32 accumulation on the tensor cores), scored as
+    cs_score_candidates_batch; the projected candidates stay on chip.
+    Hq [B, Din], Hc [B, K, Din], Wq and Wc [D, Din] -> out [B, K]; qproj
+    [B, D] float32 receives the projected queries."""
+    import torch
+    bf = torch.bfloat16
+    hq, wq, hc, wc = (_check(Hq, "Hq", 2, bf), _check(Wq, "Wq", 2, bf), _check(Hc, "Hc", 3, bf),
+                      _check(Wc, "Wc", 2, bf))
+    B, K, Din = (int(x) for x in Hc.shape)
+    D = int(Wc.shape[0])
+    if tuple(Hq.shape) != (B, Din) or tuple(Wq.shape) != (D, Din) or tuple(Wc.shape) != (D, Din):
+        raise ValueError("shapes do not match: Hq [B, Din], Hc [B, K, Din], Wq and Wc [D, Din]")
+    if qproj is None:
+        qproj = torch.empty((B, D), device=Hc.device, dtype=torch.float32)
+    if out is None:
+        out = torch.empty((B, K), device=Hc.device, dtype=torch.float32)
+    qp = _check(qproj, "qproj", 2)
+    op = _check(out, "out", 2)
+    lib = library()
+    s = _call(lambda *a: lib.cs_project_score_batch(*a[:11], qp, op, a[11]), Hc.device,
+              (hq, wq, hc, wc, B, K, Din, D, int(normalize), float(scale), float(temperature)), stream)
+    if s != 0:
+        raise CSError(s, "cs_project_score_batch")
     return out
 
 

@@ -35,6 +35,8 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     int smem_optin = 0;
+    bool proj_ready = false;      // tensor-core projection kernels configured
+    unsigned* status = nullptr;   // device address of the status word
     std::map<std::pair<int, long long>, int> clusters;  // (cluster, smem|nq4|cos) -> max active
 };
 
@@ -84,6 +86,10 @@ cudaError_t device_state(DeviceState** st) {
         if (e != cudaSuccess) return e;
         e = cs::configure_device_kernels(d.smem_optin);
         if (e != cudaSuccess) return e;
+        e = cs::status_word_address(&d.status);
+        if (e != cudaSuccess) return e;
+        d.proj_ready = cs::configure_proj_kernels(d.smem_optin) == cudaSuccess;
+        (void)cudaGetLastError();
         d.ready = true;
     }
     *st = &d;
@@ -441,6 +447,67 @@ int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int norma
     if (ctas) *ctas = pl.ctas;
     if (smem_bytes) *smem_bytes = static_cast<int>(pl.smem);
     return CS_OK;
+}
+
+// Shapes the tensor-core projection kernels take.
+int validate_projection(long long rows, int Din, int D) {
+    if (rows <= 0) return CS_ERR_BAD_BATCH;
+    if (Din <= 0 || D <= 0) return CS_ERR_D_ZERO;
+    if (Din % 64 != 0 || (D != 256 && D != 512)) return CS_ERR_BAD_PLAN;
+    return CS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cs_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
+                    cs_stream_t stream) {
+    if (!H || !W || !P) return CS_ERR_NULL_POINTER;
+    const int v = validate_projection(rows, Din, D);
+    if (v != CS_OK) return v;
+    if (!aligned16(H) || !aligned16(W) || !aligned16(P)) return CS_ERR_BAD_PLAN;
+    const unsigned long long rb = static_cast<unsigned long long>(rows);
+    if (overlaps(P, rb * D * 4ull, H, rb * Din * 2ull) || overlaps(P, rb * D * 4ull, W, 2ull * D * Din))
+        return CS_ERR_ALIAS;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
+    if (!d->proj_ready) return CS_ERR_BAD_PLAN;
+    return cs::launch_project_rows(H, W, rows, Din, D, P, d->sms, d->status, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? CS_OK
+               : CS_ERR_LAUNCH;
+}
+
+int cs_project_score_batch(const uint16_t* Hq, const uint16_t* Wq, const uint16_t* Hc, const uint16_t* Wc, int B,
+                           int K, int Din, int D, int normalize, float scale, float temperature, float* qproj,
+                           float* out, cs_stream_t stream) {
+    if (!Hq || !Wq || !Hc || !Wc || !qproj || !out) return CS_ERR_NULL_POINTER;
+    if (B <= 0) return CS_ERR_BAD_BATCH;
+    if (K <= 0) return CS_ERR_K_ZERO;
+    if (K > CS_MAX_K) return CS_ERR_K_TOO_LARGE;
+    const int v = validate_projection(static_cast<long long>(B) * K, Din, D);
+    if (v != CS_OK) return v;
+    if (normalize != 0 && normalize != 1) return CS_ERR_BAD_SIMILARITY;
+    if (!std::isfinite(scale) || scale == 0.0f) return CS_ERR_BAD_SCALE;
+    if (!std::isfinite(temperature) || !(temperature > 0.0f)) return CS_ERR_BAD_TEMPERATURE;
+    if (!aligned16(Hq) || !aligned16(Wq) || !aligned16(Hc) || !aligned16(Wc) || !aligned16(qproj))
+        return CS_ERR_BAD_PLAN;
+    const unsigned long long bk = static_cast<unsigned long long>(B) * K;
+    const unsigned long long ob = bk * 4ull, qb = static_cast<unsigned long long>(B) * D * 4ull;
+    const void* ins[4] = {Hq, Wq, Hc, Wc};
+    const unsigned long long insb[4] = {static_cast<unsigned long long>(B) * Din * 2ull, 2ull * D * Din,
+                                        bk * Din * 2ull, 2ull * D * Din};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(out, ob, ins[i], insb[i]) || overlaps(qproj, qb, ins[i], insb[i])) return CS_ERR_ALIAS;
+    if (overlaps(out, ob, qproj, qb)) return CS_ERR_ALIAS;
+    DeviceState* d = nullptr;
+    if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
+    if (!d->proj_ready) return CS_ERR_BAD_PLAN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cs::launch_project_rows(Hq, Wq, B, Din, D, qproj, d->sms, d->status, st);
+    if (e == cudaSuccess)
+        e = cs::launch_project_score(Hc, Wc, qproj, B, K, Din, D, normalize, scale, temperature, out, d->sms,
+                                     d->status, st);
+    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
 }
 
 int cs_selftest_bounded_wait(int limit_us, cs_stream_t stream) {

@@ -121,6 +121,20 @@ int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_
 // Bounded-wait self-test: one wait that nothing completes, limit_ns long.
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
+// Projections on the tensor cores (project.cu). H, W: bfloat16 bit
+// patterns, row-major [rows][Din] and [D][Din]; D in {256, 512}, Din a
+// multiple of 64; 16-byte aligned pointers.
+size_t proj_smem_bytes(int D);
+cudaError_t configure_proj_kernels(int smem_optin);
+cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
+                                int sms, unsigned* status, cudaStream_t stream);
+cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
+                                 int D, int normalize, float scale, float temperature, float* out, int sms,
+                                 unsigned* status, cudaStream_t stream);
+// Device address of the status word on the current device (for kernels in
+// other translation units).
+cudaError_t status_word_address(unsigned** ptr);
+
 // Device status word (bounded-wait give-ups).
 cudaError_t read_device_status(unsigned* flags, bool clear);
 

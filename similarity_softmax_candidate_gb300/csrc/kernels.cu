@@ -1010,6 +1010,13 @@ cudaError_t noalloc_staged_address(int device, float** ptr) {
     return cudaSuccess;
 }
 
+cudaError_t status_word_address(unsigned** ptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_status);
+    if (e == cudaSuccess) *ptr = static_cast<unsigned*>(p);
+    return e;
+}
+
 cudaError_t read_device_status(unsigned* flags, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(flags, g_status, sizeof(unsigned));
     if (e != cudaSuccess || !clear) return e;

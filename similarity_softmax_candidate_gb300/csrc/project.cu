@@ -1,0 +1,497 @@
+// Caller-side projections on the tensor cores, fused with the scoring.
+//
+// PR #69 "cuda: add a fused candidate-scoring kernel for CLM and Kev" (its
+// opening table) scores projected vectors: CLM compares state_head(s) with
+// action_head(c), Kev k(h_opts) with q(h_decide); the page leaves those
+// projections to the caller. Here they run on the 5th-generation tensor
+// cores and the candidate projection feeds the scoring directly from the
+// accumulators, so the projected candidates never reach global memory:
+//
+//   proj_kernel<PLAIN>: P = H W^T, float32 rows written out (the queries).
+//   proj_kernel<SCORE>: per question b, the K projected candidate rows
+//     c_k = W h_k live only in tensor memory; each becomes its dot with q_b
+//     and its squared norm, then a logit, and the question's softmax is
+//     written as in the plain scoring path.
+//
+// H and W are bfloat16, K-major (a row of H and a row of W are both Din
+// contiguous elements); accumulation is float32.
+//
+// GB300 structure: one CTA per SM, 6 warps. Warp 0 (one lane) streams A =
+// 128-row tiles of H and B = all D rows of W, 64 columns of Din at a time,
+// with 2-D TMA copies (128-byte swizzle) into a 2-stage ring tracked by
+// mbarriers. Warp 1 allocates D columns of tensor memory and (one lane)
+// issues tcgen05.mma (M=128, N=256 per instruction, K=16) into that
+// accumulator; tcgen05.commit frees a ring stage when its MMAs finish and
+// signals the epilogue when a tile is complete. Warps 2-5 (128 threads, one
+// accumulator row each) read the rows back with tcgen05.ld and either store
+// them or fold them into dot, norm and softmax. Every wait is bounded.
+#include "internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+namespace cs {
+namespace {
+
+constexpr int kTileM = 128;        // accumulator rows (TMEM lanes)
+constexpr int kTileK = 64;         // Din columns per ring stage: 128 bytes of bf16, one swizzle row
+constexpr int kMmaN = 256;         // N of one tcgen05.mma
+constexpr int kMmaK = 16;          // K of one tcgen05.mma (bf16)
+constexpr int kProjStages = 2;
+constexpr int kProjThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiThreads = 128;
+constexpr unsigned long long kProjWaitNs = 1000000000ull;
+constexpr float kPEps = 1e-8f, kPEps2 = 1e-16f;
+
+enum ProjMode { kProjPlain = 0, kProjScore = 1 };
+
+struct ProjArgs {
+    long long rows;     // rows of A (PLAIN: rows to project; SCORE: B*K)
+    int B, K, Din, D;   // SCORE: B questions of K rows
+    int normalize;
+    float scale, temperature;
+    const float* qproj; // SCORE: projected queries [B][D]
+    float* out;         // PLAIN: [rows][D]; SCORE: [B][K]
+    unsigned* status;   // device status word
+};
+
+// ---------------------------------------------------------------- PTX
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void bar_init(uint32_t b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint32_t b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait; false once this CTA has given up.
+__device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* give_up, unsigned* status) {
+    if (bar_try(b, parity)) return true;
+    if (*give_up) return false;
+    const unsigned long long t0 = gtimer();
+    for (uint32_t it = 1;; ++it) {
+        if (bar_try(b, parity)) return true;
+        if (*give_up) return false;
+        if ((it & 31u) == 0 && gtimer() - t0 > kProjWaitNs) {
+            *give_up = 1;
+            atomicOr(status, 1u);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void wait_bar_until(uint32_t b, uint32_t parity, unsigned long long deadline) {
+    while (!bar_try(b, parity))
+        if (gtimer() > deadline) return;
+}
+
+// 2-D tiled TMA load: box at (x = column, y = row) of the tensor map.
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// Fields: start address >> 4 (bits 0-13), leading byte offset >> 4 (16-29,
+// unused for this layout), stride byte offset >> 4 (32-45), version 1
+// (46-47), swizzle mode 2 = 128-byte (61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D float32 (bits 4-5 = 1), A and B
+// bfloat16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");  // the wait is in the same statement: no use of r can move above it
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory"); }
+
+__device__ __forceinline__ float wsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float wmax(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Shared memory, from a 1024-byte aligned base: ring stages (A tile, then
+// the D rows of W), q (D floats), 2 x 256 logits, barriers, TMEM address.
+struct ProjLayout {
+    uint32_t stage_bytes, a_bytes, ring, q, logits, bars, tmem, flag, total;
+};
+__host__ __device__ inline ProjLayout proj_layout(int D) {
+    ProjLayout L;
+    L.a_bytes = kTileM * kTileK * 2;
+    L.stage_bytes = L.a_bytes + static_cast<uint32_t>(D) * kTileK * 2;
+    L.ring = 0;
+    L.q = L.ring + kProjStages * L.stage_bytes;
+    L.logits = L.q + static_cast<uint32_t>(D) * 4;
+    L.bars = L.logits + 2 * 256 * 4;
+    L.tmem = L.bars + (2 * kProjStages + 2) * 8;
+    L.flag = L.tmem + 8;
+    L.total = L.flag + 8 + 1024;  // + alignment slack for the base
+    return L;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kProjThreads, 1)
+    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const ProjArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    const int D = a.D, nk = a.Din / kTileK, nhalf = D / kMmaN;
+    const ProjLayout L = proj_layout(D);
+    const uint32_t raw = su32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* sm = smem_raw + (base - raw);
+    float* qs = reinterpret_cast<float*>(sm + L.q);
+    float* logits = reinterpret_cast<float*>(sm + L.logits);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + L.tmem);
+    volatile int* give_up = reinterpret_cast<volatile int*>(sm + L.flag);
+    const uint32_t full0 = base + L.bars, empty0 = full0 + 8u * kProjStages;
+    const uint32_t accf = empty0 + 8u * kProjStages, acce = accf + 8u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // work items: PLAIN = 128-row tiles; SCORE = questions of ceil(K/128) tiles
+    const int tiles_per_item = MODE == kProjScore ? (a.K + kTileM - 1) / kTileM : 1;
+    const long long items = MODE == kProjScore ? a.B : (a.rows + kTileM - 1) / kTileM;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kProjStages; ++s) {
+            bar_init(full0 + 8u * s, 1);
+            bar_init(empty0 + 8u * s, 1);
+        }
+        bar_init(accf, 1);
+        bar_init(acce, kEpiThreads);
+        *give_up = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {  // the whole warp allocates D columns of tensor memory
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + L.tmem),
+                     "r"(static_cast<uint32_t>(D)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool stop = false;
+            for (long long item = blockIdx.x; item < items && !stop; item += gridDim.x) {
+                for (int h = 0; h < tiles_per_item && !stop; ++h) {
+                    const long long row0 = MODE == kProjScore ? item * a.K + static_cast<long long>(h) * kTileM
+                                                              : item * kTileM;
+                    for (int kk = 0; kk < nk; ++kk, ++it) {
+                        const uint32_t s = it % kProjStages, ph = (it / kProjStages) & 1u;
+                        if (it >= kProjStages && !wait_bar(empty0 + 8u * s, ph ^ 1u, give_up, a.status)) {
+                            stop = true;
+                            break;
+                        }
+                        const uint32_t st = base + L.ring + s * L.stage_bytes;
+                        bar_expect(full0 + 8u * s, L.stage_bytes);
+                        tma_2d(st, &tmA, kk * kTileK, static_cast<int>(row0), full0 + 8u * s);
+                        for (int n = 0; n < nhalf; ++n)
+                            tma_2d(st + L.a_bytes + static_cast<uint32_t>(n) * kMmaN * kTileK * 2, &tmW, kk * kTileK,
+                                   n * kMmaN, full0 + 8u * s);
+                    }
+                }
+            }
+            if (*give_up) {  // let issued copies land before the CTA leaves
+                const unsigned long long dl = gtimer() + kProjWaitNs;
+                const uint32_t first = it > kProjStages ? it - kProjStages : 0;
+                for (uint32_t u = first; u < it; ++u)
+                    wait_bar_until(full0 + 8u * (u % kProjStages), (u / kProjStages) & 1u, dl);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = mma_idesc(kTileM, kMmaN);
+            uint32_t it = 0, tile = 0;
+            bool stop = false;
+            for (long long item = blockIdx.x; item < items && !stop; item += gridDim.x) {
+                for (int h = 0; h < tiles_per_item && !stop; ++h, ++tile) {
+                    // the epilogue has read the previous tile's accumulator
+                    if (tile > 0 && !wait_bar(acce, (tile & 1u) ^ 1u, give_up, a.status)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int kk = 0; kk < nk; ++kk, ++it) {
+                        const uint32_t s = it % kProjStages, ph = (it / kProjStages) & 1u;
+                        if (!wait_bar(full0 + 8u * s, ph, give_up, a.status)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = base + L.ring + s * L.stage_bytes;
+                        const uint64_t ad = sw128_desc(st);
+#pragma unroll
+                        for (int k = 0; k < kTileK / kMmaK; ++k) {
+                            // +32 bytes per K step inside the 128-byte swizzled row
+                            for (int n = 0; n < nhalf; ++n) {
+                                const uint64_t bd = sw128_desc(st + L.a_bytes + static_cast<uint32_t>(n) * kMmaN * 128u);
+                                mma_bf16(tmem + static_cast<uint32_t>(n) * kMmaN, ad + 2u * k, bd + 2u * k, idesc,
+                                         (kk | k) != 0);
+                            }
+                        }
+                        mma_commit(empty0 + 8u * s);  // stage free once these MMAs are done
+                    }
+                    if (stop) break;
+                    mma_commit(accf);  // the tile's accumulator is complete
+                }
+            }
+            {  // every issued MMA has finished before TMEM is released
+                const unsigned long long dl = gtimer() + kProjWaitNs;
+                const uint32_t first = it > kProjStages ? it - kProjStages : 0;
+                for (uint32_t u = first; u < it; ++u)
+                    wait_bar_until(empty0 + 8u * (u % kProjStages), (u / kProjStages) & 1u, dl);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: thread = accumulator row (TMEM lane)
+        const int et = threadIdx.x - 64;                  // 0..127
+        const int row = 32 * (warp & 3) + lane;           // TMEM lane this warp may read
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        uint32_t tile = 0;
+        long long nq = 0;
+        for (long long item = blockIdx.x; item < items; item += gridDim.x, ++nq) {
+            float fac = 1.f;  // SCORE: scale / (T * max(|q|, eps)), or scale / T
+            float* lg = logits + (nq & 1) * 256;
+            if (MODE == kProjScore) {
+                const float* q = a.qproj + static_cast<size_t>(item) * D;
+                for (int i = et; i < D; i += kEpiThreads) qs[i] = q[i];
+                epi_bar_sync();
+                float sq = 0.f;
+                if (a.normalize)
+                    for (int i = lane; i < D; i += 32) sq = fmaf(qs[i], qs[i], sq);
+                sq = wsum(sq);
+                fac = a.normalize ? a.scale / (a.temperature * fmaxf(sqrtf(sq), kPEps)) : a.scale / a.temperature;
+            }
+            for (int h = 0; h < tiles_per_item; ++h, ++tile) {
+                const bool ok = wait_bar(accf, tile & 1u, give_up, a.status);
+                tc_fence_after();
+                if (MODE == kProjScore) {
+                    float dot = 0.f, nrm = 0.f;
+                    for (int c = 0; c < D; c += 32) {
+                        float v[32];
+                        tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            dot = fmaf(v[j], qs[c + j], dot);
+                            nrm = fmaf(v[j], v[j], nrm);
+                        }
+                    }
+                    const int k = h * kTileM + row;
+                    if (k < a.K) {
+                        const float z = a.normalize ? fac * dot * rsqrtf(fmaxf(nrm, kPEps2)) : fac * dot;
+                        lg[k] = ok ? z : __int_as_float(0x7fc00000);
+                    }
+                } else {
+                    const long long r = item * kTileM + row;
+                    for (int c = 0; c < D; c += 32) {
+                        float v[32];
+                        tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+                        if (r < a.rows) {
+                            float4* dst = reinterpret_cast<float4*>(a.out + static_cast<size_t>(r) * D + c);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = ok ? make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3])
+                                            : make_float4(NAN, NAN, NAN, NAN);
+                        }
+                    }
+                }
+                tc_fence_before();
+                bar_arrive(acce);  // this thread is done with the accumulator
+            }
+            if (MODE == kProjScore) {
+                epi_bar_sync();  // every logit of the question is in lg
+                if (warp == 2) {
+                    float z[8];
+                    float m = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int k = lane + 32 * j;
+                        z[j] = k < a.K ? lg[k] : -INFINITY;
+                        m = fmaxf(m, z[j]);
+                    }
+                    m = wmax(m);
+                    float s = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        z[j] = lane + 32 * j < a.K ? __expf(z[j] - m) : 0.f;
+                        s += z[j];
+                    }
+                    const float inv = 1.0f / wsum(s);
+                    float* dst = a.out + static_cast<size_t>(item) * a.K;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (lane + 32 * j < a.K) dst[lane + 32 * j] = z[j] * inv;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(static_cast<uint32_t>(D)));
+}
+
+// ---------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows][cols], boxes of box_rows x 64
+// columns, 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* map, const void* ptr, unsigned long long rows, unsigned long long cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t proj_smem_bytes(int D) { return proj_layout(D).total; }
+
+cudaError_t configure_proj_kernels(int smem_optin) {
+    const int need = static_cast<int>(proj_layout(512).total);
+    if (need > smem_optin) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(proj_kernel<kProjPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(proj_kernel<kProjScore>, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+}
+
+cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
+                                int sms, unsigned* status, cudaStream_t stream) {
+    CUtensorMap ma, mw;
+    if (!make_map(&ma, H, rows, Din, kTileM) || !make_map(&mw, W, D, Din, kMmaN)) return cudaErrorInvalidValue;
+    ProjArgs a{};
+    a.rows = rows;
+    a.Din = Din;
+    a.D = D;
+    a.out = P;
+    a.status = status;
+    const long long tiles = (rows + kTileM - 1) / kTileM;
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
+    proj_kernel<kProjPlain><<<grid, kProjThreads, proj_layout(D).total, stream>>>(ma, mw, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
+                                 int D, int normalize, float scale, float temperature, float* out, int sms,
+                                 unsigned* status, cudaStream_t stream) {
+    CUtensorMap ma, mw;
+    const unsigned long long rows = static_cast<unsigned long long>(B) * K;
+    if (!make_map(&ma, Hc, rows, Din, kTileM) || !make_map(&mw, Wc, D, Din, kMmaN)) return cudaErrorInvalidValue;
+    ProjArgs a{};
+    a.rows = static_cast<long long>(rows);
+    a.B = B;
+    a.K = K;
+    a.Din = Din;
+    a.D = D;
+    a.normalize = normalize;
+    a.scale = scale;
+    a.temperature = temperature;
+    a.qproj = qproj;
+    a.out = out;
+    a.status = status;
+    const unsigned grid = static_cast<unsigned>(B < sms ? B : sms);
+    proj_kernel<kProjScore><<<grid, kProjThreads, proj_layout(D).total, stream>>>(ma, mw, a);
+    return cudaGetLastError();
+}
+
+}  // namespace cs

@@ -221,3 +221,36 @@ def test_ragged_rejects(host_lib):
     assert _ragged(host_lib, out=C_ADDR + 4 * 512 * 39) == E.CS_ERR_ALIAS
     assert host_lib.cs_score_candidates_ragged_bf16(Q_ADDR, C_ADDR, OFF_ADDR, 4, 40, 512, 1, 2.0, 1.0,
                                                     C_ADDR + 2 * 512 * 39, None) == E.CS_ERR_ALIAS
+
+
+W_ADDR, P_ADDR = 0x7F5000000000, 0x7F6000000000
+
+
+def test_project_rejects(host_lib):
+    E = binding
+    f = host_lib.cs_project_rows
+    assert f(None, W_ADDR, 10, 64, 256, P_ADDR, None) == E.CS_ERR_NULL_POINTER
+    assert f(Q_ADDR, W_ADDR, 0, 64, 256, P_ADDR, None) == E.CS_ERR_BAD_BATCH
+    assert f(Q_ADDR, W_ADDR, 10, 0, 256, P_ADDR, None) == E.CS_ERR_D_ZERO
+    assert f(Q_ADDR, W_ADDR, 10, 96, 256, P_ADDR, None) == E.CS_ERR_BAD_PLAN     # Din not a multiple of 64
+    assert f(Q_ADDR, W_ADDR, 10, 64, 384, P_ADDR, None) == E.CS_ERR_BAD_PLAN     # D not 256 or 512
+    assert f(Q_ADDR + 8, W_ADDR, 10, 64, 256, P_ADDR, None) == E.CS_ERR_BAD_PLAN  # unaligned
+    assert f(Q_ADDR, W_ADDR, 10, 64, 256, Q_ADDR + 64, None) == E.CS_ERR_ALIAS
+    g = host_lib.cs_project_score_batch
+    args = dict(Hq=Q_ADDR, Wq=W_ADDR, Hc=C_ADDR, Wc=W_ADDR + (1 << 24), B=2, K=5, Din=64, D=256, n=1, s=2.0, t=1.0,
+                qp=P_ADDR, out=OUT_ADDR)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return g(a["Hq"], a["Wq"], a["Hc"], a["Wc"], a["B"], a["K"], a["Din"], a["D"], a["n"], a["s"], a["t"],
+                 a["qp"], a["out"], None)
+    assert call(Hc=None) == E.CS_ERR_NULL_POINTER
+    assert call(K=256) == E.CS_ERR_K_TOO_LARGE
+    assert call(K=0) == E.CS_ERR_K_ZERO
+    assert call(B=0) == E.CS_ERR_BAD_BATCH
+    assert call(s=0.0) == E.CS_ERR_BAD_SCALE
+    assert call(t=-1.0) == E.CS_ERR_BAD_TEMPERATURE
+    assert call(n=5) == E.CS_ERR_BAD_SIMILARITY
+    assert call(D=128) == E.CS_ERR_BAD_PLAN
+    assert call(out=C_ADDR) == E.CS_ERR_ALIAS
+    assert call(qp=OUT_ADDR) == E.CS_ERR_ALIAS

@@ -1,0 +1,99 @@
+"""GPU parity of the tensor-core projections (tcgen05) and the fused
+projected readout.
+
+The page (PR #69 "cuda: add a fused candidate-scoring kernel for CLM and
+Kev", opening table) scores projected vectors -- CLM's state_head(s) against
+action_head(c), Kev's k(h_opts) against q(h_decide) -- and leaves the
+projections to the caller; here they run on the tensor cores. Features and
+weights are bfloat16; the oracle widens them exactly and projects in fp64.
+
+Projection bound: a float32 accumulation of Din products is within
+Din * 2^-24 * sum_i |h_i w_i| of the exact sum; the tests use 1e-4 * that
+sum per element (well above the bound, far below any layout mistake, which
+permutes or garbles whole columns). Probabilities: the usual 1e-4 / 1e-5.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from similarity_softmax_candidate_gb300 import binding
+from tests._util import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _bf16(shape, seed, std=1.0):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * std).to(torch.bfloat16)
+
+
+def test_project_identity_weights_exact(cuda_lib):
+    """W = [I; 0] (D=256 >= Din) returns H exactly in its first Din columns:
+    any swizzle, descriptor or lane mistake would move or garble values."""
+    for rows, Din in ((128, 64), (300, 128), (129, 256)):
+        H = _bf16((rows, Din), rows + Din)
+        W = torch.zeros((256, Din), dtype=torch.bfloat16)
+        W[:Din] = torch.eye(Din, dtype=torch.bfloat16)
+        P = binding.cs_project_rows(H.to(DEV), W.to(DEV))
+        torch.cuda.synchronize()
+        P = P.cpu()
+        assert torch.equal(P[:, :Din], H.float()), f"rows={rows} Din={Din}"
+        assert torch.all(P[:, Din:] == 0)
+
+
+@pytest.mark.parametrize("D", [256, 512])
+def test_project_rows_random(cuda_lib, D):
+    for rows, Din in ((1, 64), (127, 512), (128, 512), (129, 512), (1000, 1024), (4096, 512)):
+        H = _bf16((rows, Din), 10 + rows)
+        W = _bf16((D, Din), 20 + Din, std=Din ** -0.5)
+        P = binding.cs_project_rows(H.to(DEV), W.to(DEV))
+        torch.cuda.synchronize()
+        ref = oracle.project(H.float().numpy(), W.float().numpy())
+        bound = 1e-4 * (np.abs(H.float().numpy()).astype(np.float64) @ np.abs(W.float().numpy()).astype(np.float64).T)
+        err = np.abs(P.cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= bound + 1e-30), f"rows={rows} Din={Din} D={D}: max err {err.max():.3e}"
+
+
+CASES = [(1, 5, 64, 256), (3, 128, 512, 256), (2, 129, 512, 512), (5, 255, 512, 512), (20, 255, 512, 512),
+         (7, 1, 128, 256), (40, 64, 1024, 512)]
+
+
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_project_score_parity(cuda_lib, normalize):
+    for B, K, Din, D in CASES:
+        Hq = _bf16((B, Din), 100 + B)
+        Hc = _bf16((B, K, Din), 200 + K)
+        Wq = _bf16((D, Din), 300 + D, std=Din ** -0.5)
+        Wc = _bf16((D, Din), 400 + D, std=Din ** -0.5)
+        scale = 14.2857 if normalize else 0.0625
+        qproj = torch.empty((B, D), device=DEV)
+        p = binding.cs_project_score_batch(Hq.to(DEV), Wq.to(DEV), Hc.to(DEV), Wc.to(DEV), normalize, scale, 1.0,
+                                           qproj=qproj)
+        torch.cuda.synchronize()
+        ref = oracle.project_score_batch(Hq.float().numpy(), Wq.float().numpy(), Hc.float().numpy(),
+                                         Wc.float().numpy(), normalize, scale, 1.0)
+        assert_parity(p, ref, f"projected B={B} K={K} Din={Din} D={D}")
+        qref = oracle.project(Hq.float().numpy(), Wq.float().numpy())
+        np.testing.assert_allclose(qproj.cpu().numpy(), qref, rtol=1e-3, atol=1e-3)
+    assert binding.cs_device_status() == 0
+
+
+def test_project_score_matches_scoring_of_projected_rows(cuda_lib):
+    """Fused projection + scoring equals projecting with cs_project_rows and
+    scoring with cs_score_candidates_batch (two paths through different
+    kernels; agreement within float32 rounding)."""
+    B, K, Din, D = 16, 255, 512, 512
+    Hq, Hc = _bf16((B, Din), 1).to(DEV), _bf16((B, K, Din), 2).to(DEV)
+    Wq, Wc = _bf16((D, Din), 3, Din ** -0.5).to(DEV), _bf16((D, Din), 4, Din ** -0.5).to(DEV)
+    fused = binding.cs_project_score_batch(Hq, Wq, Hc, Wc, 1, 14.2857, 1.0)
+    q = binding.cs_project_rows(Hq, Wq)
+    c = binding.cs_project_rows(Hc.view(B * K, Din), Wc).view(B, K, D)
+    composed = binding.cs_score_candidates_batch(q, c, 1, 14.2857, 1.0)
+    torch.cuda.synchronize()
+    assert torch.max(torch.abs(fused - composed)).item() <= 1e-5
