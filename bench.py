@@ -94,6 +94,17 @@ def _peak_hbm():
         return 6800.0, "fallback"
 
 
+def _peak_bf16():
+    """Dense bf16 tensor peak in TFLOP/s: the measured cuBLAS burst figure
+    (the projections are timed alone), else the recipe's fallback."""
+    path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def _traffic_from_profile(kernel_src_sha):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
@@ -258,6 +269,8 @@ def main():
     ap.add_argument("--questions", type=int, default=B_TOTAL,
                     help="questions per step (default 16384; smaller only for profiling captures)")
     ap.add_argument("--chunk", type=int, default=CHUNK, help="questions per launch (default 4096)")
+    ap.add_argument("--only-projected", type=int, default=0, metavar="B",
+                    help="profiling aid: time only the projected readout on B questions and print its record")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -278,6 +291,10 @@ def main():
     import similarity_softmax_candidate_gb300 as cs
     from similarity_softmax_candidate_gb300 import _build, workloads
     _build.build_library()
+    if args.only_projected:
+        if rank == 0:
+            print(json.dumps(projected_readout(cs, dev, args.steps, args.warmup, B=args.only_projected)), flush=True)
+        return 0
 
     def barrier():
         if world > 1:
@@ -378,6 +395,7 @@ def main():
     }
 
     if not args.skip_extra:
+        line["extra"]["projected_readout"] = projected_readout(cs, dev, 20, args.warmup)
         line["extra"]["latency_b1"] = latency_table(cs, workloads, dev, args.latency_calls)
         line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
     del wls, wl_cos, wl_dot
@@ -478,6 +496,54 @@ def extras(cs, workloads, wl_cos, wl_dot, out, dev, stream, args, world, barrier
     del staged
 
     return bf16, ragged_info, unfused
+
+
+def projected_readout(cs, dev, steps, warmup, B=4096):
+    """The readout with caller-side projections on the tensor cores
+    (cs_project_score_batch), B questions (4096 by default), K=255,
+    Din=D=512, bfloat16 features and heads; against projecting with cuBLAS
+    (torch.matmul, bf16 out) and scoring the bfloat16 result with the
+    streaming kernel."""
+    import torch
+    Kq, Din, Dp = K, 512, 512
+    g = torch.Generator(device=dev)
+    g.manual_seed(21)
+    Hq = torch.randn(B, Din, device=dev, generator=g).to(torch.bfloat16)
+    Hc = torch.randn(B, Kq, Din, device=dev, generator=g).to(torch.bfloat16)
+    Wq = (torch.randn(Dp, Din, device=dev, generator=g) * Din ** -0.5).to(torch.bfloat16)
+    Wc = (torch.randn(Dp, Din, device=dev, generator=g) * Din ** -0.5).to(torch.bfloat16)
+    qproj = torch.empty(B, Dp, device=dev)
+    outp = torch.empty(B, Kq, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(steps):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    fused_ms = timed(lambda: cs.cs_project_score_batch(Hq, Wq, Hc, Wc, 1, 14.285714, 1.0, qproj=qproj, out=outp,
+                                                       stream=s))
+
+    def composed():
+        c = torch.matmul(Hc.view(B * Kq, Din), Wc.t()).view(B, Kq, Dp)
+        q = torch.matmul(Hq, Wq.t()).float()
+        cs.cs_score_candidates_batch_bf16(q, c, 1, 14.285714, 1.0, out=outp, stream=s)
+    composed_ms = timed(composed)
+    flop = 2.0 * B * Kq * Din * Dp + 2.0 * B * Din * Dp
+    peak, peak_src = _peak_bf16()
+    return {"workload": f"{B} questions x K=255, Din=512 -> D=512, bf16 features and heads, cosine",
+            "questions_per_s": B / (fused_ms / 1e3), "ms_per_call": fused_ms,
+            "tflops": flop / (fused_ms / 1e3) / 1e12, "peak_tflops": peak,
+            "frac": flop / (fused_ms / 1e3) / 1e12 / peak,
+            "peak_source": peak_src,
+            "composed_cublas_bf16_ms": composed_ms, "fused_over_composed": composed_ms / fused_ms}
 
 
 def latency_table(cs, workloads, dev, calls):

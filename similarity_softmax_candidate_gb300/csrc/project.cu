@@ -16,15 +16,18 @@
 // H and W are bfloat16, K-major (a row of H and a row of W are both Din
 // contiguous elements); accumulation is float32.
 //
-// GB300 structure: one CTA per SM, 6 warps. Warp 0 (one lane) streams A =
-// 128-row tiles of H and B = all D rows of W, 64 columns of Din at a time,
-// with 2-D TMA copies (128-byte swizzle) into a 2-stage ring tracked by
-// mbarriers. Warp 1 allocates D columns of tensor memory and (one lane)
-// issues tcgen05.mma (M=128, N=256 per instruction, K=16) into that
-// accumulator; tcgen05.commit frees a ring stage when its MMAs finish and
-// signals the epilogue when a tile is complete. Warps 2-5 (128 threads, one
-// accumulator row each) read the rows back with tcgen05.ld and either store
-// them or fold them into dot, norm and softmax. Every wait is bounded.
+// GB300 structure: one CTA per SM, 6 warps. The work is cut into units of
+// 128 rows x 256 output features (one N half of a 128-row tile). Warp 0 (one
+// lane) streams, per unit, the 128-row tile of H and the unit's 256 rows of
+// W, 64 columns of Din at a time, with 2-D TMA copies (128-byte swizzle) into
+// a 4-stage ring tracked by mbarriers. Warp 1 allocates all 512 columns of
+// tensor memory as two 256-column accumulators and (one lane) issues
+// tcgen05.mma (M=128, N=256, K=16) into them in turn; tcgen05.commit frees a
+// ring stage when its MMAs finish and hands a finished accumulator to the
+// epilogue. Warps 2-5 (128 threads, one accumulator row each) read a unit
+// back with tcgen05.ld while the tensor cores fill the other accumulator,
+// and either store it or fold it into dot, norm and softmax. Every wait is
+// bounded.
 #include "internal.h"
 
 #include <cuda.h>
@@ -40,7 +43,8 @@ constexpr int kTileM = 128;        // accumulator rows (TMEM lanes)
 constexpr int kTileK = 64;         // Din columns per ring stage: 128 bytes of bf16, one swizzle row
 constexpr int kMmaN = 256;         // N of one tcgen05.mma
 constexpr int kMmaK = 16;          // K of one tcgen05.mma (bf16)
-constexpr int kProjStages = 2;
+constexpr int kProjStages = 4;
+constexpr int kAccCols = 2 * kMmaN;  // two accumulators of kMmaN columns: all of tensor memory
 constexpr int kProjThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiThreads = 128;
 constexpr unsigned long long kProjWaitNs = 1000000000ull;
@@ -153,21 +157,41 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 32 consecutive accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// 128 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+    uint32_t r[128];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, "
+        "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
+        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
+        "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
+        "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127"
+        "}, [%128];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+          "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+          "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+          "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+          "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+          "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+          "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+          "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+          "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
         : "r"(taddr)
         : "memory");  // the wait is in the same statement: no use of r can move above it
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory"); }
@@ -184,19 +208,20 @@ __device__ __forceinline__ float wmax(float v) {
 }
 
 // Shared memory, from a 1024-byte aligned base: ring stages (A tile, then
-// the D rows of W), q (D floats), 2 x 256 logits, barriers, TMEM address.
+// the unit's kMmaN rows of W), q (D floats), 2 x 256 logits, barriers, TMEM
+// address.
 struct ProjLayout {
     uint32_t stage_bytes, a_bytes, ring, q, logits, bars, tmem, flag, total;
 };
 __host__ __device__ inline ProjLayout proj_layout(int D) {
     ProjLayout L;
     L.a_bytes = kTileM * kTileK * 2;
-    L.stage_bytes = L.a_bytes + static_cast<uint32_t>(D) * kTileK * 2;
+    L.stage_bytes = L.a_bytes + kMmaN * kTileK * 2;
     L.ring = 0;
     L.q = L.ring + kProjStages * L.stage_bytes;
     L.logits = L.q + static_cast<uint32_t>(D) * 4;
     L.bars = L.logits + 2 * 256 * 4;
-    L.tmem = L.bars + (2 * kProjStages + 2) * 8;
+    L.tmem = L.bars + (2 * kProjStages + 4) * 8;
     L.flag = L.tmem + 8;
     L.total = L.flag + 8 + 1024;  // + alignment slack for the base
     return L;
@@ -215,11 +240,14 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     float* logits = reinterpret_cast<float*>(sm + L.logits);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(sm + L.tmem);
     volatile int* give_up = reinterpret_cast<volatile int*>(sm + L.flag);
+    // full/empty per ring stage; accf/acce per accumulator (0: columns
+    // 0..255, 1: columns 256..511)
     const uint32_t full0 = base + L.bars, empty0 = full0 + 8u * kProjStages;
-    const uint32_t accf = empty0 + 8u * kProjStages, acce = accf + 8u;
+    const uint32_t accf0 = empty0 + 8u * kProjStages, acce0 = accf0 + 16u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // work items: PLAIN = 128-row tiles; SCORE = questions of ceil(K/128) tiles
+    // work items: PLAIN = 128-row tiles; SCORE = questions of ceil(K/128)
+    // tiles; each tile is nhalf units of kMmaN output features
     const int tiles_per_item = MODE == kProjScore ? (a.K + kTileM - 1) / kTileM : 1;
     const long long items = MODE == kProjScore ? a.B : (a.rows + kTileM - 1) / kTileM;
 
@@ -228,14 +256,16 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             bar_init(full0 + 8u * s, 1);
             bar_init(empty0 + 8u * s, 1);
         }
-        bar_init(accf, 1);
-        bar_init(acce, kEpiThreads);
+        for (int b = 0; b < 2; ++b) {
+            bar_init(accf0 + 8u * b, 1);
+            bar_init(acce0 + 8u * b, kEpiThreads);
+        }
         *give_up = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {  // the whole warp allocates D columns of tensor memory
+    if (warp == 1) {  // the whole warp allocates both accumulators
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(base + L.tmem),
-                     "r"(static_cast<uint32_t>(D)));
+                     "r"(static_cast<uint32_t>(kAccCols)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
@@ -252,18 +282,18 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 for (int h = 0; h < tiles_per_item && !stop; ++h) {
                     const long long row0 = MODE == kProjScore ? item * a.K + static_cast<long long>(h) * kTileM
                                                               : item * kTileM;
-                    for (int kk = 0; kk < nk; ++kk, ++it) {
-                        const uint32_t s = it % kProjStages, ph = (it / kProjStages) & 1u;
-                        if (it >= kProjStages && !wait_bar(empty0 + 8u * s, ph ^ 1u, give_up, a.status)) {
-                            stop = true;
-                            break;
+                    for (int n = 0; n < nhalf && !stop; ++n) {
+                        for (int kk = 0; kk < nk; ++kk, ++it) {
+                            const uint32_t s = it % kProjStages, ph = (it / kProjStages) & 1u;
+                            if (it >= kProjStages && !wait_bar(empty0 + 8u * s, ph ^ 1u, give_up, a.status)) {
+                                stop = true;
+                                break;
+                            }
+                            const uint32_t st = base + L.ring + s * L.stage_bytes;
+                            bar_expect(full0 + 8u * s, L.stage_bytes);
+                            tma_2d(st, &tmA, kk * kTileK, static_cast<int>(row0), full0 + 8u * s);
+                            tma_2d(st + L.a_bytes, &tmW, kk * kTileK, n * kMmaN, full0 + 8u * s);
                         }
-                        const uint32_t st = base + L.ring + s * L.stage_bytes;
-                        bar_expect(full0 + 8u * s, L.stage_bytes);
-                        tma_2d(st, &tmA, kk * kTileK, static_cast<int>(row0), full0 + 8u * s);
-                        for (int n = 0; n < nhalf; ++n)
-                            tma_2d(st + L.a_bytes + static_cast<uint32_t>(n) * kMmaN * kTileK * 2, &tmW, kk * kTileK,
-                                   n * kMmaN, full0 + 8u * s);
                     }
                 }
             }
@@ -279,12 +309,13 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = mma_idesc(kTileM, kMmaN);
-            uint32_t it = 0, tile = 0;
+            uint32_t it = 0, unit = 0;
             bool stop = false;
             for (long long item = blockIdx.x; item < items && !stop; item += gridDim.x) {
-                for (int h = 0; h < tiles_per_item && !stop; ++h, ++tile) {
-                    // the epilogue has read the previous tile's accumulator
-                    if (tile > 0 && !wait_bar(acce, (tile & 1u) ^ 1u, give_up, a.status)) {
+                for (int h = 0; h < tiles_per_item * nhalf && !stop; ++h, ++unit) {
+                    const uint32_t acc = unit & 1u;
+                    // the epilogue has read this accumulator's previous unit
+                    if (unit >= 2 && !wait_bar(acce0 + 8u * acc, ((unit >> 1) & 1u) ^ 1u, give_up, a.status)) {
                         stop = true;
                         break;
                     }
@@ -297,20 +328,14 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t st = base + L.ring + s * L.stage_bytes;
-                        const uint64_t ad = sw128_desc(st);
+                        const uint64_t ad = sw128_desc(st), bd = sw128_desc(st + L.a_bytes);
 #pragma unroll
-                        for (int k = 0; k < kTileK / kMmaK; ++k) {
-                            // +32 bytes per K step inside the 128-byte swizzled row
-                            for (int n = 0; n < nhalf; ++n) {
-                                const uint64_t bd = sw128_desc(st + L.a_bytes + static_cast<uint32_t>(n) * kMmaN * 128u);
-                                mma_bf16(tmem + static_cast<uint32_t>(n) * kMmaN, ad + 2u * k, bd + 2u * k, idesc,
-                                         (kk | k) != 0);
-                            }
-                        }
+                        for (int k = 0; k < kTileK / kMmaK; ++k)  // +32 bytes per K step inside the swizzled row
+                            mma_bf16(tmem + acc * kMmaN, ad + 2u * k, bd + 2u * k, idesc, (kk | k) != 0);
                         mma_commit(empty0 + 8u * s);  // stage free once these MMAs are done
                     }
                     if (stop) break;
-                    mma_commit(accf);  // the tile's accumulator is complete
+                    mma_commit(accf0 + 8u * acc);  // the unit's accumulator is complete
                 }
             }
             {  // every issued MMA has finished before TMEM is released
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         const int et = threadIdx.x - 64;                  // 0..127
         const int row = 32 * (warp & 3) + lane;           // TMEM lane this warp may read
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        uint32_t tile = 0;
+        uint32_t unit = 0;
         long long nq = 0;
         for (long long item = blockIdx.x; item < items; item += gridDim.x, ++nq) {
             float fac = 1.f;  // SCORE: scale / (T * max(|q|, eps)), or scale / T
@@ -341,41 +366,53 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 sq = wsum(sq);
                 fac = a.normalize ? a.scale / (a.temperature * fmaxf(sqrtf(sq), kPEps)) : a.scale / a.temperature;
             }
-            for (int h = 0; h < tiles_per_item; ++h, ++tile) {
-                const bool ok = wait_bar(accf, tile & 1u, give_up, a.status);
-                tc_fence_after();
-                if (MODE == kProjScore) {
-                    float dot = 0.f, nrm = 0.f;
-                    for (int c = 0; c < D; c += 32) {
-                        float v[32];
-                        tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
+            for (int h = 0; h < tiles_per_item; ++h) {
+                float dot = 0.f, nrm = 0.f;
+                bool ok = true;
+                for (int n = 0; n < nhalf; ++n, ++unit) {
+                    const uint32_t acc = unit & 1u;
+                    ok = wait_bar(accf0 + 8u * acc, (unit >> 1) & 1u, give_up, a.status) && ok;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kMmaN; c += 128) {
+                        float v[128];
+                        tmem_ld128(lane_addr + acc * kMmaN + static_cast<uint32_t>(c), v);
+                        const int col = n * kMmaN + c;  // output feature of v[0]
+                        if (MODE == kProjScore) {
+                            const float4* q4 = reinterpret_cast<const float4*>(qs + col);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            dot = fmaf(v[j], qs[c + j], dot);
-                            nrm = fmaf(v[j], v[j], nrm);
+                            for (int j = 0; j < 32; ++j) {
+                                const float4 w = q4[j];
+                                dot = fmaf(v[4 * j], w.x, dot);
+                                dot = fmaf(v[4 * j + 1], w.y, dot);
+                                dot = fmaf(v[4 * j + 2], w.z, dot);
+                                dot = fmaf(v[4 * j + 3], w.w, dot);
+                                nrm = fmaf(v[4 * j], v[4 * j], nrm);
+                                nrm = fmaf(v[4 * j + 1], v[4 * j + 1], nrm);
+                                nrm = fmaf(v[4 * j + 2], v[4 * j + 2], nrm);
+                                nrm = fmaf(v[4 * j + 3], v[4 * j + 3], nrm);
+                            }
+                        } else {
+                            const long long r = item * kTileM + row;
+                            if (r < a.rows) {
+                                float4* dst = reinterpret_cast<float4*>(a.out + static_cast<size_t>(r) * D + col);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    dst[j] = ok ? make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3])
+                                                : make_float4(NAN, NAN, NAN, NAN);
+                            }
                         }
                     }
+                    tc_fence_before();
+                    bar_arrive(acce0 + 8u * acc);  // this thread is done with the accumulator
+                }
+                if (MODE == kProjScore) {
                     const int k = h * kTileM + row;
                     if (k < a.K) {
                         const float z = a.normalize ? fac * dot * rsqrtf(fmaxf(nrm, kPEps2)) : fac * dot;
                         lg[k] = ok ? z : __int_as_float(0x7fc00000);
                     }
-                } else {
-                    const long long r = item * kTileM + row;
-                    for (int c = 0; c < D; c += 32) {
-                        float v[32];
-                        tmem_ld32(lane_addr + static_cast<uint32_t>(c), v);
-                        if (r < a.rows) {
-                            float4* dst = reinterpret_cast<float4*>(a.out + static_cast<size_t>(r) * D + c);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                dst[j] = ok ? make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3])
-                                            : make_float4(NAN, NAN, NAN, NAN);
-                        }
-                    }
                 }
-                tc_fence_before();
-                bar_arrive(acce);  // this thread is done with the accumulator
             }
             if (MODE == kProjScore) {
                 epi_bar_sync();  // every logit of the question is in lg
@@ -409,7 +446,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(static_cast<uint32_t>(D)));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(static_cast<uint32_t>(kAccCols)));
 }
 
 // ---------------------------------------------------------------- host
