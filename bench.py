@@ -536,6 +536,11 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
         q = torch.matmul(Hq, Wq.t()).float()
         cs.cs_score_candidates_batch_bf16(q, c, 1, 14.285714, 1.0, out=outp, stream=s)
     composed_ms = timed(composed)
+    Hrows = Hc.view(B * Kq, Din)
+    Prows = torch.empty((B * Kq, Dp), device=dev)
+    rows_ms = timed(lambda: cs.cs_project_rows(Hrows, Wc, out=Prows, stream=s))
+    rows_bytes = 2.0 * B * Kq * Din + 2.0 * Dp * Din + 4.0 * B * Kq * Dp
+    hbm, hbm_src = _peak_hbm()
     flop = 2.0 * B * Kq * Din * Dp + 2.0 * B * Din * Dp
     peak, peak_src = _peak_bf16()
     return {"workload": f"{B} questions x K=255, Din=512 -> D=512, bf16 features and heads, cosine",
@@ -543,7 +548,12 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
             "tflops": flop / (fused_ms / 1e3) / 1e12, "peak_tflops": peak,
             "frac": flop / (fused_ms / 1e3) / 1e12 / peak,
             "peak_source": peak_src,
-            "composed_cublas_bf16_ms": composed_ms, "fused_over_composed": composed_ms / fused_ms}
+            "composed_cublas_bf16_ms": composed_ms, "fused_over_composed": composed_ms / fused_ms,
+            "project_rows": {"rows": B * Kq, "ms_per_call": rows_ms,
+                             "tflops": 2.0 * B * Kq * Din * Dp / (rows_ms / 1e3) / 1e12,
+                             "bound": "hbm", "gbs": rows_bytes / (rows_ms / 1e3) / 1e9,
+                             "frac": rows_bytes / (rows_ms / 1e3) / 1e9 / hbm,
+                             "peak_source": f"hbm_gbs ({hbm_src})"}}
 
 
 def latency_table(cs, workloads, dev, calls):

@@ -165,9 +165,12 @@ int cs_score_candidates_ragged_bf16(const float *Q, const uint16_t *C,
  *   ever being written to memory: they exist only in tensor memory.
  *   Two kernels are enqueued on `stream`.
  * Shapes: D = 256 or 512, Din a multiple of 64, 1 <= K <= 255; all pointers
- * 16-byte aligned (CS_ERR_BAD_PLAN otherwise). Other errors and conventions
- * as cs_score_candidates_batch. This is our extension of the page's kernel.
+ * 16-byte aligned (CS_ERR_BAD_PLAN otherwise); at most CS_PROJ_MAX_ROWS rows
+ * (rows, or B*K; tensor-copy coordinates are 32-bit; CS_ERR_BAD_BATCH
+ * otherwise). Other errors and conventions as cs_score_candidates_batch.
+ * This is our extension of the page's kernel.
  */
+#define CS_PROJ_MAX_ROWS 2147483392LL /* 2^31 - 256 */
 int cs_project_rows(const uint16_t *H, const uint16_t *W, long long rows,
                     int Din, int D, float *P, cs_stream_t stream);
 int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,

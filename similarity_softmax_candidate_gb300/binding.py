@@ -28,6 +28,7 @@ STATUS = {
     12: "CS_ERR_BAD_PLAN", 13: "CS_ERR_SCRATCH_TOO_SMALL",
 }
 CS_NOALLOC_MAX_ROWS = 1 << 20
+CS_PROJ_MAX_ROWS = (1 << 31) - 256
 globals().update({name: code for code, name in STATUS.items()})
 
 _lock = threading.Lock()

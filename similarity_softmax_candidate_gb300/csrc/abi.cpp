@@ -451,7 +451,7 @@ int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int norma
 
 // Shapes the tensor-core projection kernels take.
 int validate_projection(long long rows, int Din, int D) {
-    if (rows <= 0) return CS_ERR_BAD_BATCH;
+    if (rows <= 0 || rows > CS_PROJ_MAX_ROWS) return CS_ERR_BAD_BATCH;
     if (Din <= 0 || D <= 0) return CS_ERR_D_ZERO;
     if (Din % 64 != 0 || (D != 256 && D != 512)) return CS_ERR_BAD_PLAN;
     return CS_OK;

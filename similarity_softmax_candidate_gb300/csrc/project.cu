@@ -43,7 +43,12 @@ constexpr int kTileM = 128;        // accumulator rows (TMEM lanes)
 constexpr int kTileK = 64;         // Din columns per ring stage: 128 bytes of bf16, one swizzle row
 constexpr int kMmaN = 256;         // N of one tcgen05.mma
 constexpr int kMmaK = 16;          // K of one tcgen05.mma (bf16)
-constexpr int kProjStages = 4;
+// Ring stages: 4 for the scoring kernel; 3 for the plain kernel, whose
+// shared memory also holds the output staging boxes.
+__host__ __device__ constexpr int proj_stages(int mode) { return mode == 1 ? 4 : 3; }
+constexpr int kMaxProjStages = 4;
+constexpr int kOutBox = 32;                    // output box: 32 rows x 32 float32 columns (128-byte rows)
+constexpr int kOutBoxBytes = kOutBox * kOutBox * 4;
 constexpr int kAccCols = 2 * kMmaN;  // two accumulators of kMmaN columns: all of tensor memory
 constexpr int kProjThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiThreads = 128;
@@ -117,6 +122,21 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+
+// 2-D tiled TMA store of a shared-memory box at (x = column, y = row); rows
+// and columns outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most one committed store group of this thread still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Every committed store group of this thread complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -208,20 +228,21 @@ __device__ __forceinline__ float wmax(float v) {
 }
 
 // Shared memory, from a 1024-byte aligned base: ring stages (A tile, then
-// the unit's kMmaN rows of W), q (D floats), 2 x 256 logits, barriers, TMEM
-// address.
+// the unit's kMmaN rows of W), output staging (plain kernel: two boxes per
+// epilogue warp), q (D floats), 2 x 256 logits, barriers, TMEM address.
 struct ProjLayout {
-    uint32_t stage_bytes, a_bytes, ring, q, logits, bars, tmem, flag, total;
+    uint32_t stage_bytes, a_bytes, ring, out, q, logits, bars, tmem, flag, total;
 };
-__host__ __device__ inline ProjLayout proj_layout(int D) {
+__host__ __device__ inline ProjLayout proj_layout(int D, int mode) {
     ProjLayout L;
     L.a_bytes = kTileM * kTileK * 2;
     L.stage_bytes = L.a_bytes + kMmaN * kTileK * 2;
     L.ring = 0;
-    L.q = L.ring + kProjStages * L.stage_bytes;
+    L.out = L.ring + proj_stages(mode) * L.stage_bytes;
+    L.q = L.out + (mode == 1 ? 0u : (kEpiThreads / 32) * 2u * kOutBoxBytes);
     L.logits = L.q + static_cast<uint32_t>(D) * 4;
     L.bars = L.logits + 2 * 256 * 4;
-    L.tmem = L.bars + (2 * kProjStages + 4) * 8;
+    L.tmem = L.bars + (2 * kMaxProjStages + 4) * 8;
     L.flag = L.tmem + 8;
     L.total = L.flag + 8 + 1024;  // + alignment slack for the base
     return L;
@@ -229,10 +250,12 @@ __host__ __device__ inline ProjLayout proj_layout(int D) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kProjThreads, 1)
-    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const ProjArgs a) {
+    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                const __grid_constant__ CUtensorMap tmP, const ProjArgs a) {
     extern __shared__ unsigned char smem_raw[];
+    constexpr int kProjStages = proj_stages(MODE);
     const int D = a.D, nk = a.Din / kTileK, nhalf = D / kMmaN;
-    const ProjLayout L = proj_layout(D);
+    const ProjLayout L = proj_layout(D, MODE);
     const uint32_t raw = su32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char* sm = smem_raw + (base - raw);
@@ -351,7 +374,9 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         const int et = threadIdx.x - 64;                  // 0..127
         const int row = 32 * (warp & 3) + lane;           // TMEM lane this warp may read
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        uint32_t unit = 0;
+        uint32_t unit = 0, nbox = 0;
+        unsigned char* stage_out = sm + L.out + (warp - 2) * 2 * kOutBoxBytes;  // plain kernel only
+        const uint32_t stage_out_s = base + L.out + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
         long long nq = 0;
         for (long long item = blockIdx.x; item < items; item += gridDim.x, ++nq) {
             float fac = 1.f;  // SCORE: scale / (T * max(|q|, eps)), or scale / T
@@ -393,13 +418,32 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                                 nrm = fmaf(v[4 * j + 3], v[4 * j + 3], nrm);
                             }
                         } else {
-                            const long long r = item * kTileM + row;
-                            if (r < a.rows) {
-                                float4* dst = reinterpret_cast<float4*>(a.out + static_cast<size_t>(r) * D + col);
+                            // 4 boxes of 32 rows x 32 columns through this warp's two
+                            // staging buffers (128-byte swizzle: 16-byte chunk j of row
+                            // r sits at chunk j ^ (r & 7), so the lanes' stores hit
+                            // distinct banks), each written out by one TMA store
 #pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    dst[j] = ok ? make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3])
-                                                : make_float4(NAN, NAN, NAN, NAN);
+                            for (int bx = 0; bx < 4; ++bx, ++nbox) {
+                                const uint32_t buf = nbox & 1u;
+                                if (nbox >= 2) {
+                                    if (lane == 0) bulk_wait_read1();  // this buffer's last store has read it
+                                    __syncwarp();
+                                }
+                                unsigned char* box = stage_out + buf * kOutBoxBytes + lane * 128;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const int e = 32 * bx + 4 * j;
+                                    *reinterpret_cast<float4*>(box + ((j ^ (lane & 7)) << 4)) =
+                                        ok ? make_float4(v[e], v[e + 1], v[e + 2], v[e + 3])
+                                           : make_float4(NAN, NAN, NAN, NAN);
+                                }
+                                fence_proxy_async();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&tmP, stage_out_s + buf * kOutBoxBytes, col + 32 * bx,
+                                                 static_cast<int>(item * kTileM + 32 * (warp & 3)));
+                                    bulk_commit();
+                                }
                             }
                         }
                     }
@@ -440,6 +484,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 }
             }
         }
+        if (MODE == kProjPlain && lane == 0) bulk_wait_all();  // stores done before shared memory goes away
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -467,36 +513,47 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Tensor map of a row-major bf16 matrix [rows][cols], boxes of box_rows x 64
-// columns, 128-byte swizzle; rows past the end read as zero.
-bool make_map(CUtensorMap* map, const void* ptr, unsigned long long rows, unsigned long long cols, int box_rows) {
+// Tensor map of a row-major matrix [rows][cols] with boxes of box_rows x
+// box_cols elements and 128-byte swizzle (box_cols x element size = 128
+// bytes); loads read rows past the end as zero, stores skip them.
+bool make_map(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes, const void* ptr, unsigned long long rows,
+              unsigned long long cols, int box_cols, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t strides[1] = {cols * static_cast<unsigned long long>(elem_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_bf16_map(CUtensorMap* map, const void* ptr, unsigned long long rows, unsigned long long cols, int box_rows) {
+    return make_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, rows, cols, kTileK, box_rows);
 }
 
 }  // namespace
 
-size_t proj_smem_bytes(int D) { return proj_layout(D).total; }
+size_t proj_smem_bytes(int D) {
+    const size_t p = proj_layout(D, kProjPlain).total, s = proj_layout(D, kProjScore).total;
+    return p > s ? p : s;
+}
 
 cudaError_t configure_proj_kernels(int smem_optin) {
-    const int need = static_cast<int>(proj_layout(512).total);
-    if (need > smem_optin) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(proj_kernel<kProjPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+    const int plain = static_cast<int>(proj_layout(512, kProjPlain).total);
+    const int score = static_cast<int>(proj_layout(512, kProjScore).total);
+    if (plain > smem_optin || score > smem_optin) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(proj_kernel<kProjPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, plain);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(proj_kernel<kProjScore>, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+    return cudaFuncSetAttribute(proj_kernel<kProjScore>, cudaFuncAttributeMaxDynamicSharedMemorySize, score);
 }
 
 cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
                                 int sms, unsigned* status, cudaStream_t stream) {
-    CUtensorMap ma, mw;
-    if (!make_map(&ma, H, rows, Din, kTileM) || !make_map(&mw, W, D, Din, kMmaN)) return cudaErrorInvalidValue;
+    CUtensorMap ma, mw, mp;
+    if (!make_bf16_map(&ma, H, rows, Din, kTileM) || !make_bf16_map(&mw, W, D, Din, kMmaN) ||
+        !make_map(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P, rows, D, kOutBox, kOutBox))
+        return cudaErrorInvalidValue;
     ProjArgs a{};
     a.rows = rows;
     a.Din = Din;
@@ -505,7 +562,7 @@ cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long 
     a.status = status;
     const long long tiles = (rows + kTileM - 1) / kTileM;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    proj_kernel<kProjPlain><<<grid, kProjThreads, proj_layout(D).total, stream>>>(ma, mw, a);
+    proj_kernel<kProjPlain><<<grid, kProjThreads, proj_layout(D, kProjPlain).total, stream>>>(ma, mw, mp, a);
     return cudaGetLastError();
 }
 
@@ -514,7 +571,8 @@ cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const f
                                  unsigned* status, cudaStream_t stream) {
     CUtensorMap ma, mw;
     const unsigned long long rows = static_cast<unsigned long long>(B) * K;
-    if (!make_map(&ma, Hc, rows, Din, kTileM) || !make_map(&mw, Wc, D, Din, kMmaN)) return cudaErrorInvalidValue;
+    if (!make_bf16_map(&ma, Hc, rows, Din, kTileM) || !make_bf16_map(&mw, Wc, D, Din, kMmaN))
+        return cudaErrorInvalidValue;
     ProjArgs a{};
     a.rows = static_cast<long long>(rows);
     a.B = B;
@@ -528,7 +586,8 @@ cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const f
     a.out = out;
     a.status = status;
     const unsigned grid = static_cast<unsigned>(B < sms ? B : sms);
-    proj_kernel<kProjScore><<<grid, kProjThreads, proj_layout(D).total, stream>>>(ma, mw, a);
+    // the scoring kernel stores no rows: its output map is never used
+    proj_kernel<kProjScore><<<grid, kProjThreads, proj_layout(D, kProjScore).total, stream>>>(ma, mw, ma, a);
     return cudaGetLastError();
 }
 

@@ -40,6 +40,14 @@ def test_header_declares_the_entry_points():
         assert n in names
 
 
+def test_header_limits_match_binding():
+    text = open(os.path.join(ROOT, "include", "candidate_scoring.h")).read()
+    m = re.search(r"#define CS_PROJ_MAX_ROWS (\d+)LL", text)
+    assert m and int(m.group(1)) == binding.CS_PROJ_MAX_ROWS == (1 << 31) - 256
+    m = re.search(r"#define CS_NOALLOC_MAX_ROWS (\d+)", text)
+    assert m and int(m.group(1)) == binding.CS_NOALLOC_MAX_ROWS
+
+
 @pytest.mark.parametrize("name", _declared_functions())
 def test_library_exports_declared_symbol(host_lib, name):
     assert hasattr(host_lib, name), f"{name} declared in include/*.h but not exported"
@@ -231,6 +239,7 @@ def test_project_rejects(host_lib):
     f = host_lib.cs_project_rows
     assert f(None, W_ADDR, 10, 64, 256, P_ADDR, None) == E.CS_ERR_NULL_POINTER
     assert f(Q_ADDR, W_ADDR, 0, 64, 256, P_ADDR, None) == E.CS_ERR_BAD_BATCH
+    assert f(Q_ADDR, W_ADDR, (1 << 31) - 255, 64, 256, P_ADDR, None) == E.CS_ERR_BAD_BATCH  # > CS_PROJ_MAX_ROWS
     assert f(Q_ADDR, W_ADDR, 10, 0, 256, P_ADDR, None) == E.CS_ERR_D_ZERO
     assert f(Q_ADDR, W_ADDR, 10, 96, 256, P_ADDR, None) == E.CS_ERR_BAD_PLAN     # Din not a multiple of 64
     assert f(Q_ADDR, W_ADDR, 10, 64, 384, P_ADDR, None) == E.CS_ERR_BAD_PLAN     # D not 256 or 512
@@ -248,6 +257,7 @@ def test_project_rejects(host_lib):
     assert call(K=256) == E.CS_ERR_K_TOO_LARGE
     assert call(K=0) == E.CS_ERR_K_ZERO
     assert call(B=0) == E.CS_ERR_BAD_BATCH
+    assert call(B=(1 << 31) // 200, K=255) == E.CS_ERR_BAD_BATCH  # B*K > CS_PROJ_MAX_ROWS
     assert call(s=0.0) == E.CS_ERR_BAD_SCALE
     assert call(t=-1.0) == E.CS_ERR_BAD_TEMPERATURE
     assert call(n=5) == E.CS_ERR_BAD_SIMILARITY

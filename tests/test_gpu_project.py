@@ -97,3 +97,79 @@ def test_project_score_matches_scoring_of_projected_rows(cuda_lib):
     composed = binding.cs_score_candidates_batch(q, c, 1, 14.2857, 1.0)
     torch.cuda.synchronize()
     assert torch.max(torch.abs(fused - composed)).item() <= 1e-5
+
+
+def _sample(n, first, last, rand, seed):
+    rng = np.random.default_rng(seed)
+    idx = set(range(min(first, n))) | set(range(max(0, n - last), n))
+    idx |= set(rng.integers(0, n, size=rand).tolist())
+    return np.array(sorted(idx))
+
+
+@pytest.mark.parametrize("D", [256, 512])
+def test_project_rows_many_tiles_per_cta(cuda_lib, D):
+    """Enough rows that every CTA projects several tiles (each tensor-memory
+    accumulator is reused many times) plus a ragged last tile; every row is
+    written and sampled rows match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, Din = sms * 128 * 3 + 77, 512
+    H = _bf16((rows, Din), 31)
+    W = _bf16((D, Din), 32, std=Din ** -0.5)
+    P = torch.full((rows, D), float("nan"), device=DEV)
+    binding.cs_project_rows(H.to(DEV), W.to(DEV), out=P)
+    torch.cuda.synchronize()
+    P = P.cpu().numpy()
+    assert np.isfinite(P).all(), "some projected rows were not written"
+    idx = _sample(rows, 200, 200, 400, 33)
+    Hs = H.float().numpy()[idx]
+    ref = oracle.project(Hs, W.float().numpy())
+    bound = 1e-4 * (np.abs(Hs).astype(np.float64) @ np.abs(W.float().numpy()).astype(np.float64).T)
+    err = np.abs(P[idx].astype(np.float64) - ref)
+    assert np.all(err <= bound + 1e-30), f"D={D}: max err {err.max():.3e}"
+    assert binding.cs_device_status() == 0
+
+
+@pytest.mark.parametrize("D,K", [(256, 100), (256, 255), (512, 255)])
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_project_score_many_questions_per_cta(cuda_lib, D, K, normalize):
+    """Several questions per CTA: accumulators and logit buffers are reused;
+    sampled questions match the oracle and every row is a distribution."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, Din = 3 * sms + 5, 512
+    Hq, Hc = _bf16((B, Din), 41), _bf16((B, K, Din), 42)
+    Wq, Wc = _bf16((D, Din), 43, std=Din ** -0.5), _bf16((D, Din), 44, std=Din ** -0.5)
+    scale = 14.2857 if normalize else 0.0625
+    p = torch.full((B, K), float("nan"), device=DEV)
+    binding.cs_project_score_batch(Hq.to(DEV), Wq.to(DEV), Hc.to(DEV), Wc.to(DEV), normalize, scale, 1.0, out=p)
+    torch.cuda.synchronize()
+    p = p.cpu().numpy()
+    assert np.isfinite(p).all()
+    np.testing.assert_allclose(p.astype(np.float64).sum(axis=1), 1.0, atol=1e-5)
+    idx = _sample(B, 3, 3, 10, 45)
+    ref = oracle.project_score_batch(Hq.float().numpy()[idx], Wq.float().numpy(), Hc.float().numpy()[idx],
+                                     Wc.float().numpy(), normalize, scale, 1.0)
+    assert_parity(torch.from_numpy(p[idx]), ref, f"projected B={B} K={K} D={D} sampled")
+    assert binding.cs_device_status() == 0
+
+
+def test_project_score_benchmark_size(cuda_lib):
+    """The projected readout at the size the benchmark times (4096 questions,
+    K=255, Din=D=512, inputs drawn on the device), checked on sampled
+    questions."""
+    B, K, Din, D = 4096, 255, 512, 512
+    g = torch.Generator(device=DEV)
+    g.manual_seed(21)
+    Hq = torch.randn(B, Din, device=DEV, generator=g).to(torch.bfloat16)
+    Hc = torch.randn(B, K, Din, device=DEV, generator=g).to(torch.bfloat16)
+    Wq = (torch.randn(D, Din, device=DEV, generator=g) * Din ** -0.5).to(torch.bfloat16)
+    Wc = (torch.randn(D, Din, device=DEV, generator=g) * Din ** -0.5).to(torch.bfloat16)
+    p = binding.cs_project_score_batch(Hq, Wq, Hc, Wc, 1, 14.285714, 1.0)
+    torch.cuda.synchronize()
+    idx = _sample(B, 2, 2, 8, 46)
+    t = torch.from_numpy(idx).to(DEV)
+    ref = oracle.project_score_batch(Hq[t].float().cpu().numpy(), Wq.float().cpu().numpy(),
+                                     Hc[t].float().cpu().numpy(), Wc.float().cpu().numpy(), 1, 14.285714, 1.0)
+    assert_parity(p[t], ref, "projected readout, benchmark size, sampled")
+    sums = p.double().sum(dim=1)
+    assert torch.max(torch.abs(sums - 1.0)).item() <= 1e-5
+    assert binding.cs_device_status() == 0
