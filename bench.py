@@ -205,6 +205,75 @@ def _host_sample(n, seed=4):
     return wl.Q.numpy(), wl.C.numpy()
 
 
+# ---- the oracle on every host core: one spawned worker process per core,
+# each scoring its own host-drawn sample (the oracle itself is single-threaded
+# C; questions are independent, so the workers share nothing).
+_POOL_SAMPLE = None
+
+
+def _pool_init(n, seed):
+    global _POOL_SAMPLE
+    _POOL_SAMPLE = _host_sample(n, seed=seed)
+
+
+def _pool_passes(passes):
+    from similarity_softmax_candidate_gb300 import workloads
+    Qs, Cs = _POOL_SAMPLE
+    t = 0.0
+    for _ in range(passes):
+        t += _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
+    return len(Qs) * passes, t
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OraclePool:
+    """Spawned worker processes (spawn, never fork, after CUDA has been
+    used), each holding n host-drawn questions."""
+
+    def __init__(self, n, seed, workers=None):
+        import multiprocessing as mp
+        self.workers = workers or _host_cores()
+        self.n = n
+        self.pool = mp.get_context("spawn").Pool(self.workers, initializer=_pool_init, initargs=(n, seed))
+        self.run(1)  # every worker initialised and warm
+
+    def run(self, passes):
+        """Each worker scores its sample `passes` times; returns (questions,
+        wall seconds)."""
+        t0 = time.perf_counter()
+        res = self.pool.map(_pool_passes, [passes] * self.workers, chunksize=1)
+        return sum(r[0] for r in res), time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline_all_cores(target_s=10.0):
+    """The oracle as it stands on every host core (one process per core)
+    for about target_s of wall time."""
+    from similarity_softmax_candidate_gb300 import workloads
+    Qp, Cp = _host_sample(8)
+    t_q = _time_oracle(Qp, Cp, 1, workloads.CLM_SCALE) / 8
+    n = 128
+    pool = OraclePool(n, seed=7)
+    try:
+        passes = int(max(1, target_s / max(t_q * n, 1e-6)))
+        done, dt = pool.run(passes)
+    finally:
+        pool.close()
+    return {"value": done / dt, "unit": "questions/s", "cores": pool.workers, "kind": "oracle",
+            "sample": f"{done} question scorings: {pool.workers} processes (one per affine host core), each "
+                      f"{passes} passes over its own {n} host-drawn questions of the K=255, D=512 cosine "
+                      f"workload; fp64 C oracle, {dt:.1f} s wall"}
+
+
 def cpu_baseline(target_s=10.0):
     """The oracle as it stands (single-threaded C, fp64) on a bounded sample:
     passes over up to 2048 host-drawn questions until about target_s of CPU
@@ -224,30 +293,39 @@ def cpu_baseline(target_s=10.0):
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands, one process per affine
+    host core; each step every worker scores its own bounded sample once."""
     rank, world, _ = _dist()
     if rank != 0:
         return 0
     from similarity_softmax_candidate_gb300 import workloads
     Qp, Cp = _host_sample(8)
     t_q = _time_oracle(Qp, Cp, 1, workloads.CLM_SCALE) / 8
-    budget = 60.0
-    n = int(max(1, min(1024, budget / max(t_q, 1e-6) / max(1, args.steps + args.warmup))))
-    Qs, Cs = _host_sample(n, seed=6)
-    for _ in range(args.warmup):
-        _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
-    total = 0.0
-    for _ in range(args.steps):
-        total += _time_oracle(Qs, Cs, 1, workloads.CLM_SCALE)
-    qps = n * args.steps / total
+    budget = 60.0  # seconds of wall time for warm-up + timed steps
+    n = int(max(1, min(256, budget / max(t_q, 1e-6) / max(1, args.steps + args.warmup))))
+    pool = OraclePool(n, seed=6)
+    try:
+        for _ in range(args.warmup):
+            pool.run(1)
+        total, done = 0.0, 0
+        for _ in range(args.steps):
+            q, dt = pool.run(1)
+            total += dt
+            done += q
+    finally:
+        pool.close()
+    qps = done / total
     line = {
         "impl": "reference", "metric": METRIC, "value": qps, "unit": "questions/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"throughput: cosine, K={K}, D={D}; each step a bounded sample of {n} questions",
-                   "B": n, "K": K, "D": D},
-        "cpu_baseline": {"value": qps, "unit": "questions/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{n} questions per step, host-drawn N(0,1), fp64 C oracle, single thread"},
+        "config": {"workload": f"throughput: cosine, K={K}, D={D}; each step a bounded sample of "
+                               f"{n} questions per host core",
+                   "B": n * pool.workers, "K": K, "D": D},
+        "cpu_baseline": {"value": qps, "unit": "questions/s", "cores": pool.workers, "kind": "oracle",
+                         "sample": f"{n} questions per process per step, {pool.workers} processes (one per "
+                                   f"affine host core), host-drawn N(0,1), fp64 C oracle"},
         "e2e": {"value": qps, "unit": "questions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -271,6 +349,9 @@ def main():
     ap.add_argument("--chunk", type=int, default=CHUNK, help="questions per launch (default 4096)")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
                     help="profiling aid: time only the projected readout on B questions and print its record")
+    ap.add_argument("--only-shape", choices=[r[0] for r in PAGE_SHAPES], default=None,
+                    help="profiling aid: W warm-up calls, then K back-to-back calls of one of the page's "
+                         "small shapes; prints us per call and the plan")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -291,6 +372,10 @@ def main():
     import similarity_softmax_candidate_gb300 as cs
     from similarity_softmax_candidate_gb300 import _build, workloads
     _build.build_library()
+    if args.only_shape:
+        if rank == 0:
+            print(json.dumps(single_shape(cs, workloads, dev, args.only_shape, args.steps, args.warmup)), flush=True)
+        return 0
     if args.only_projected:
         if rank == 0:
             print(json.dumps(projected_readout(cs, dev, args.steps, args.warmup, B=args.only_projected)), flush=True)
@@ -403,7 +488,8 @@ def main():
 
     if rank == 0 and not args.no_cpu:
         try:
-            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline_all_cores(args.cpu_seconds)
+            line["extra"]["cpu_baseline_one_core"] = cpu_baseline(args.cpu_seconds / 2)
         except Exception as e:  # the oracle is optional for the GPU numbers
             line["cpu_baseline"] = {"value": None, "unit": "questions/s", "cores": 1, "kind": "oracle",
                                     "sample": f"failed: {e}"}
@@ -554,6 +640,35 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
                              "bound": "hbm", "gbs": rows_bytes / (rows_ms / 1e3) / 1e9,
                              "frac": rows_bytes / (rows_ms / 1e3) / 1e9 / hbm,
                              "peak_source": f"hbm_gbs ({hbm_src})"}}
+
+
+def single_shape(cs, workloads, dev, name, calls, warmup):
+    """One of the page's small shapes alone: warm-up calls, then `calls`
+    back-to-back calls timed with CUDA events."""
+    import torch
+    _, B, k, d, normalize, page_us, _ = next(r for r in PAGE_SHAPES if r[0] == name)
+    wl = workloads.random_case(B, k, d, normalize, workloads.CLM_SCALE if normalize else workloads.KEV_SCALE,
+                               90 + k, dev)
+    out = torch.empty(B, k, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def call():
+        if B == 1:
+            cs.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=out[0], stream=s)
+        else:
+            cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=s)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(calls):
+        call()
+    b.record(s)
+    torch.cuda.synchronize()
+    return {"shape": name, "B": B, "K": k, "D": d, "us_per_call": 1e3 * a.elapsed_time(b) / calls,
+            "calls": calls, "plan": cs.cs_query_plan(wl.Q, wl.C, normalize), "page_rtx4090_us": page_us}
 
 
 def latency_table(cs, workloads, dev, calls):

@@ -407,15 +407,16 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
             }
         }
     } else {
-        for (int i = lane; i < DC; i += 32) {
-            float4 q[QF4];
 #pragma unroll
-            for (int h = 0; h < QF4; ++h) q[h] = q4[i * QF4 + h];
+        for (int r = 0; r < kMaxRowsPerStage; ++r) {
+            if (r < nr) {
+                const uint4* __restrict__ row = st + r * DC;
+                for (int i = lane; i < DC; i += 32) {
+                    float4 q[QF4];
 #pragma unroll
-            for (int r = 0; r < kMaxRowsPerStage; ++r) {
-                if (r < nr) {
+                    for (int h = 0; h < QF4; ++h) q[h] = q4[i * QF4 + h];
                     float4 c[QF4];
-                    Elem<T>::widen(st[r * DC + i], c);
+                    Elem<T>::widen(row[i], c);
 #pragma unroll
                     for (int h = 0; h < QF4; ++h) accumulate(c[h], q[h], r);
                 }

@@ -69,3 +69,18 @@ def test_single_process_needs_no_group():
     import bench
     assert bench.reduce_max(3.0) == 3.0
     assert bench.whole_job_rate(100, 2.0, 1) == pytest.approx(50000.0)
+
+
+def test_oracle_pool_counts_every_worker():
+    """The CPU baseline's process pool (spawned workers, one sample each):
+    every worker scores its own sample the asked number of times."""
+    sys.path.insert(0, ROOT)
+    import bench
+    pool = bench.OraclePool(3, seed=1, workers=2)
+    try:
+        done, wall = pool.run(2)
+    finally:
+        pool.close()
+    assert done == 2 * 3 * 2
+    assert wall > 0.0
+    assert bench._host_cores() >= 1
