@@ -392,14 +392,15 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
     };
     if constexpr (NQC > 0) {
 #pragma unroll
-        for (int j = 0; j < NQC; ++j) {
-            const int i = lane + 32 * j;
-            if (i < DC) {
+        for (int r = 0; r < kMaxRowsPerStage; ++r) {
+            if (r < nr) {
+                const uint4* __restrict__ row = st + r * DC;
 #pragma unroll
-                for (int r = 0; r < kMaxRowsPerStage; ++r) {
-                    if (r < nr) {
+                for (int j = 0; j < NQC; ++j) {
+                    const int i = lane + 32 * j;
+                    if (i < DC) {
                         float4 c[QF4];
-                        Elem<T>::widen(st[r * DC + i], c);
+                        Elem<T>::widen(row[i], c);
 #pragma unroll
                         for (int h = 0; h < QF4; ++h) accumulate(c[h], qv[j * QF4 + h], r);
                     }
