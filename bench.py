@@ -269,6 +269,7 @@ def cpu_baseline_all_cores(target_s=10.0):
     finally:
         pool.close()
     return {"value": done / dt, "unit": "questions/s", "cores": pool.workers, "kind": "oracle",
+            "host_cpu_count": os.cpu_count(), "affine_cores": _host_cores(),
             "sample": f"{done} question scorings: {pool.workers} processes (one per affine host core), each "
                       f"{passes} passes over its own {n} host-drawn questions of the K=255, D=512 cosine "
                       f"workload; fp64 C oracle, {dt:.1f} s wall"}
@@ -324,6 +325,7 @@ def run_reference(args):
                                f"{n} questions per host core",
                    "B": n * pool.workers, "K": K, "D": D},
         "cpu_baseline": {"value": qps, "unit": "questions/s", "cores": pool.workers, "kind": "oracle",
+                         "host_cpu_count": os.cpu_count(), "affine_cores": _host_cores(),
                          "sample": f"{n} questions per process per step, {pool.workers} processes (one per "
                                    f"affine host core), host-drawn N(0,1), fp64 C oracle"},
         "e2e": {"value": qps, "unit": "questions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
