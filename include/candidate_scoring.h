@@ -262,6 +262,7 @@ int cs_score_candidates_batch_unfused_noalloc(const float *Q, const float *C,
 #define CS_DEVERR_WAIT_TIMEOUT 1u  /* an on-chip wait gave up after ~1 s */
 #define CS_DEVERR_BAD_CONFIG 2u    /* a kernel refused an inconsistent launch plan */
 #define CS_DEVERR_BAD_OFFSETS 4u   /* a ragged question had invalid offsets and was skipped */
+#define CS_DEVERR_BOUNDS 8u        /* bounds-checked build: an access outside its buffer was skipped */
 
 /*
  * Reads (and, if clear != 0, resets) the status word the kernels of this
@@ -281,6 +282,29 @@ int cs_device_status(unsigned *flags, int clear);
  * never completes ends in a status, not a hang.
  */
 int cs_selftest_bounded_wait(int limit_us, cs_stream_t stream);
+
+/*
+ * Bounds-checked builds. The library can also be compiled with
+ * -DCS_DEBUG_BOUNDS (libcandidate_scoring_debug.so, built on demand by the
+ * tests; same entry points). There, before every global-memory access a
+ * kernel makes -- rows of C and q copied into shared memory, probabilities,
+ * staged values, ragged offsets, projected queries -- the range is checked
+ * against the extent of its buffer (from the call's arguments); a failing
+ * check skips the access, sets CS_DEVERR_BOUNDS in the device status word
+ * and records its site number (first failure only). It stands in for a
+ * memory checker and has no counterpart on the page. Release builds compile
+ * the checks away.
+ *
+ * cs_debug_bounds_build: 1 in a bounds-checked build, 0 otherwise.
+ * cs_bounds_violation: reads (and, if clear != 0, resets) the recorded site
+ *   number, 0 when no check has failed; synchronizes the device.
+ * cs_selftest_bounds: enqueues one tiny kernel that checks a range one past
+ *   the end of a buffer (arithmetic only, nothing is read or written), so
+ *   that site 99 is recorded; CS_ERR_BAD_PLAN in a release build.
+ */
+int cs_debug_bounds_build(void);
+int cs_bounds_violation(unsigned *site, int clear);
+int cs_selftest_bounds(cs_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     CS_PLAN_STREAM,
     CSError,
     cs_abi_version,
+    cs_bounds_violation,
+    cs_debug_bounds_build,
     cs_device_status,
     cs_project_rows,
     cs_project_score_batch,
@@ -30,6 +32,9 @@ from .binding import (  # noqa: F401
     cs_score_candidates_batch_unfused,
     cs_score_candidates_batch_unfused_noalloc,
     cs_score_candidates_ragged,
+    cs_selftest_bounds,
     cs_status_string,
+    debug_library,
     library,
+    using,
 )

@@ -17,6 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libcandidate_scoring.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
+# Bounds-checked build of the same sources (-DCS_DEBUG_BOUNDS), for tests.
+DEBUG_LIB_NAME = "libcandidate_scoring_debug.so"
+DEBUG_LIB_PATH = os.path.join(PKG, DEBUG_LIB_NAME)
 # Native latency harness (calls the C ABI from C++; see csrc/latency_main.cu).
 LATENCY_NAME = "cs_latency"
 LATENCY_PATH = os.path.join(PKG, LATENCY_NAME)
@@ -42,20 +45,22 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: cannot build the CUDA library")
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the library path. Raises on failure."""
-    if not force and not is_stale():
-        return LIB_PATH
+def build_library(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
+    """Compile (if needed) and return the library path. Raises on failure.
+    debug_bounds: the bounds-checked variant (DEBUG_LIB_PATH)."""
+    path, name = (DEBUG_LIB_PATH, DEBUG_LIB_NAME) if debug_bounds else (LIB_PATH, LIB_NAME)
+    if not force and not is_stale(path):
+        return path
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", "-lineinfo", *ARCH_FLAGS, "-Xcompiler", "-fPIC,-O2",
-              "-I", INCLUDE, "-I", CSRC]
+              "-I", INCLUDE, "-I", CSRC] + (["-DCS_DEBUG_BOUNDS"] if debug_bounds else [])
     with tempfile.TemporaryDirectory(prefix="cs_build_") as tmp:
         objs = []
         procs = []
@@ -72,15 +77,15 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
                 raise RuntimeError(f"nvcc failed ({pr.returncode}): {' '.join(cmd)}\n{out.decode(errors='replace')}")
             if verbose and out:
                 print(out.decode(errors="replace"))
-        tmp_lib = os.path.join(tmp, LIB_NAME)
+        tmp_lib = os.path.join(tmp, name)
         link = [nvcc, *ARCH_FLAGS, "-shared", "-o", tmp_lib, *objs]
         r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(link)}\n{r.stdout.decode(errors='replace')}")
-        staged = LIB_PATH + f".tmp{os.getpid()}"
+        staged = path + f".tmp{os.getpid()}"
         shutil.copyfile(tmp_lib, staged)
-        os.replace(staged, LIB_PATH)
-    return LIB_PATH
+        os.replace(staged, path)
+    return path
 
 
 def build_latency_tool(force: bool = False) -> str:

@@ -33,6 +33,8 @@ globals().update({name: code for code, name in STATUS.items()})
 
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
+CS_DEVERR_BOUNDS = 8
 
 
 class CSError(RuntimeError):
@@ -53,45 +55,87 @@ def library() -> ctypes.CDLL:
         if not os.path.exists(_build.LIB_PATH):
             raise RuntimeError(f"{_build.LIB_NAME} is not built; run __graft_entry__.build() or "
                                "python -m similarity_softmax_candidate_gb300._build")
-        lib = ctypes.CDLL(_build.LIB_PATH)
-        P, I, F, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_uint)
-        IP = ctypes.POINTER(ctypes.c_int)
-        lib.cs_abi_version.argtypes = []
-        lib.cs_abi_version.restype = I
-        lib.cs_status_string.argtypes = [I]
-        lib.cs_status_string.restype = ctypes.c_char_p
-        lib.cs_score_candidates.argtypes = [P, P, I, I, I, F, F, P, P]
-        lib.cs_score_candidates.restype = I
-        lib.cs_score_candidates_batch.argtypes = [P, P, I, I, I, I, F, F, P, P]
-        lib.cs_score_candidates_batch.restype = I
-        lib.cs_score_candidates_batch_plan.argtypes = [P, P, I, I, I, I, F, F, P, P, I, I, I]
-        lib.cs_score_candidates_batch_plan.restype = I
-        lib.cs_score_candidates_batch_unfused.argtypes = [P, P, I, I, I, I, F, F, P, P, P]
-        lib.cs_score_candidates_batch_unfused.restype = I
-        lib.cs_score_candidates_batch_unfused_noalloc.argtypes = [P, P, I, I, I, I, F, F, P, P]
-        lib.cs_score_candidates_batch_unfused_noalloc.restype = I
-        lib.cs_score_candidates_bf16.argtypes = [P, P, I, I, I, F, F, P, P]
-        lib.cs_score_candidates_bf16.restype = I
-        lib.cs_score_candidates_batch_bf16.argtypes = [P, P, I, I, I, I, F, F, P, P]
-        lib.cs_score_candidates_batch_bf16.restype = I
-        LL = ctypes.c_longlong
-        lib.cs_score_candidates_ragged.argtypes = [P, P, P, I, LL, I, I, F, F, P, P]
-        lib.cs_score_candidates_ragged.restype = I
-        lib.cs_score_candidates_ragged_bf16.argtypes = [P, P, P, I, LL, I, I, F, F, P, P]
-        lib.cs_score_candidates_ragged_bf16.restype = I
-        lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
-        lib.cs_query_plan.restype = I
-        LL2 = ctypes.c_longlong
-        lib.cs_project_rows.argtypes = [P, P, LL2, I, I, P, P]
-        lib.cs_project_rows.restype = I
-        lib.cs_project_score_batch.argtypes = [P, P, P, P, I, I, I, I, I, F, F, P, P, P]
-        lib.cs_project_score_batch.restype = I
-        lib.cs_selftest_bounded_wait.argtypes = [I, P]
-        lib.cs_selftest_bounded_wait.restype = I
-        lib.cs_device_status.argtypes = [U, I]
-        lib.cs_device_status.restype = I
-        _lib = lib
-        return lib
+        _lib = _declare(ctypes.CDLL(_build.LIB_PATH))
+        return _lib
+
+
+def debug_library() -> ctypes.CDLL:
+    """The bounds-checked build of the same library (compiled on first use,
+    about half a minute). For tests: ``with using(debug_library()):`` routes
+    this module's calls through it."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _declare(ctypes.CDLL(_build.build_library(debug_bounds=True)))
+        return _debug_lib
+
+
+class using:
+    """Context manager: this module's calls go to `lib` (another build of
+    the same ABI, e.g. debug_library()) until the block ends."""
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def __enter__(self):
+        global _lib
+        library()
+        with _lock:
+            self.saved, _lib = _lib, self.lib
+        return self.lib
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.saved
+        return False
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare argument and result types of every entry point of `lib`."""
+    P, I, F, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.POINTER(ctypes.c_uint)
+    IP = ctypes.POINTER(ctypes.c_int)
+    lib.cs_abi_version.argtypes = []
+    lib.cs_abi_version.restype = I
+    lib.cs_status_string.argtypes = [I]
+    lib.cs_status_string.restype = ctypes.c_char_p
+    lib.cs_score_candidates.argtypes = [P, P, I, I, I, F, F, P, P]
+    lib.cs_score_candidates.restype = I
+    lib.cs_score_candidates_batch.argtypes = [P, P, I, I, I, I, F, F, P, P]
+    lib.cs_score_candidates_batch.restype = I
+    lib.cs_score_candidates_batch_plan.argtypes = [P, P, I, I, I, I, F, F, P, P, I, I, I]
+    lib.cs_score_candidates_batch_plan.restype = I
+    lib.cs_score_candidates_batch_unfused.argtypes = [P, P, I, I, I, I, F, F, P, P, P]
+    lib.cs_score_candidates_batch_unfused.restype = I
+    lib.cs_score_candidates_batch_unfused_noalloc.argtypes = [P, P, I, I, I, I, F, F, P, P]
+    lib.cs_score_candidates_batch_unfused_noalloc.restype = I
+    lib.cs_score_candidates_bf16.argtypes = [P, P, I, I, I, F, F, P, P]
+    lib.cs_score_candidates_bf16.restype = I
+    lib.cs_score_candidates_batch_bf16.argtypes = [P, P, I, I, I, I, F, F, P, P]
+    lib.cs_score_candidates_batch_bf16.restype = I
+    LL = ctypes.c_longlong
+    lib.cs_score_candidates_ragged.argtypes = [P, P, P, I, LL, I, I, F, F, P, P]
+    lib.cs_score_candidates_ragged.restype = I
+    lib.cs_score_candidates_ragged_bf16.argtypes = [P, P, P, I, LL, I, I, F, F, P, P]
+    lib.cs_score_candidates_ragged_bf16.restype = I
+    lib.cs_query_plan.argtypes = [P, P, I, I, I, I, IP, IP, IP, IP]
+    lib.cs_query_plan.restype = I
+    LL2 = ctypes.c_longlong
+    lib.cs_project_rows.argtypes = [P, P, LL2, I, I, P, P]
+    lib.cs_project_rows.restype = I
+    lib.cs_project_score_batch.argtypes = [P, P, P, P, I, I, I, I, I, F, F, P, P, P]
+    lib.cs_project_score_batch.restype = I
+    lib.cs_selftest_bounded_wait.argtypes = [I, P]
+    lib.cs_selftest_bounded_wait.restype = I
+    lib.cs_device_status.argtypes = [U, I]
+    lib.cs_device_status.restype = I
+    lib.cs_debug_bounds_build.argtypes = []
+    lib.cs_debug_bounds_build.restype = I
+    lib.cs_bounds_violation.argtypes = [U, I]
+    lib.cs_bounds_violation.restype = I
+    lib.cs_selftest_bounds.argtypes = [P]
+    lib.cs_selftest_bounds.restype = I
+    return lib
 
 
 def cs_abi_version() -> int:
@@ -367,3 +411,27 @@ def cs_device_status(clear: bool = False) -> int:
     if s != 0:
         raise CSError(s, "cs_device_status")
     return int(v.value)
+
+
+def cs_debug_bounds_build() -> bool:
+    """True when the library in use is the bounds-checked build."""
+    return bool(library().cs_debug_bounds_build())
+
+
+def cs_bounds_violation(clear: bool = False) -> int:
+    """Site number of the first failed bounds check (0: none; bounds-checked
+    builds only record any). Synchronizes."""
+    v = ctypes.c_uint(0)
+    s = library().cs_bounds_violation(ctypes.byref(v), int(bool(clear)))
+    if s != 0:
+        raise CSError(s, "cs_bounds_violation")
+    return int(v.value)
+
+
+def cs_selftest_bounds(stream=None) -> None:
+    """Bounds-checked builds: record site 99 from a check of a range one
+    past a buffer's end (nothing is accessed)."""
+    import torch
+    s = _call(library().cs_selftest_bounds, torch.device("cuda", torch.cuda.current_device()), (), stream)
+    if s != 0:
+        raise CSError(s, "cs_selftest_bounds")

@@ -37,6 +37,7 @@ struct DeviceState {
     int smem_optin = 0;
     bool proj_ready = false;      // tensor-core projection kernels configured
     unsigned* status = nullptr;   // device address of the status word
+    unsigned* bounds = nullptr;   // device address of the bounds word
     std::map<std::pair<int, long long>, int> clusters;  // (cluster, smem|nq4|cos) -> max active
 };
 
@@ -87,6 +88,8 @@ cudaError_t device_state(DeviceState** st) {
         e = cs::configure_device_kernels(d.smem_optin);
         if (e != cudaSuccess) return e;
         e = cs::status_word_address(&d.status);
+        if (e != cudaSuccess) return e;
+        e = cs::bounds_site_address(&d.bounds);
         if (e != cudaSuccess) return e;
         d.proj_ready = cs::configure_proj_kernels(d.smem_optin) == cudaSuccess;
         (void)cudaGetLastError();
@@ -471,7 +474,8 @@ int cs_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Di
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
     if (!d->proj_ready) return CS_ERR_BAD_PLAN;
-    return cs::launch_project_rows(H, W, rows, Din, D, P, d->sms, d->status, reinterpret_cast<cudaStream_t>(stream)) ==
+    return cs::launch_project_rows(H, W, rows, Din, D, P, d->sms, d->status, d->bounds,
+                                   reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? CS_OK
                : CS_ERR_LAUNCH;
@@ -503,10 +507,10 @@ int cs_project_score_batch(const uint16_t* Hq, const uint16_t* Wq, const uint16_
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
     if (!d->proj_ready) return CS_ERR_BAD_PLAN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cs::launch_project_rows(Hq, Wq, B, Din, D, qproj, d->sms, d->status, st);
+    cudaError_t e = cs::launch_project_rows(Hq, Wq, B, Din, D, qproj, d->sms, d->status, d->bounds, st);
     if (e == cudaSuccess)
         e = cs::launch_project_score(Hc, Wc, qproj, B, K, Din, D, normalize, scale, temperature, out, d->sms,
-                                     d->status, st);
+                                     d->status, d->bounds, st);
     return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
 }
 
@@ -520,6 +524,19 @@ int cs_selftest_bounded_wait(int limit_us, cs_stream_t stream) {
 int cs_device_status(unsigned* flags, int clear) {
     if (!flags) return CS_ERR_NULL_POINTER;
     return cs::read_device_status(flags, clear != 0) == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
+int cs_debug_bounds_build(void) { return cs::debug_bounds_build() ? 1 : 0; }
+
+int cs_bounds_violation(unsigned* site, int clear) {
+    if (!site) return CS_ERR_NULL_POINTER;
+    return cs::read_bounds_site(site, clear != 0) == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+}
+
+int cs_selftest_bounds(cs_stream_t stream) {
+    if (!cs::debug_bounds_build()) return CS_ERR_BAD_PLAN;
+    return cs::launch_selftest_bounds(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? CS_OK
+                                                                                             : CS_ERR_LAUNCH;
 }
 
 }  // extern "C"

@@ -127,13 +127,48 @@ cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t strea
 size_t proj_smem_bytes(int D);
 cudaError_t configure_proj_kernels(int smem_optin);
 cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
-                                int sms, unsigned* status, cudaStream_t stream);
+                                int sms, unsigned* status, unsigned* bounds, cudaStream_t stream);
 cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
                                  int D, int normalize, float scale, float temperature, float* out, int sms,
-                                 unsigned* status, cudaStream_t stream);
+                                 unsigned* status, unsigned* bounds, cudaStream_t stream);
 // Device address of the status word on the current device (for kernels in
 // other translation units).
 cudaError_t status_word_address(unsigned** ptr);
+
+// Bounds-checked builds (compiled with -DCS_DEBUG_BOUNDS; the tests use one
+// in place of a memory checker): before every global-memory access of the
+// kernels, the range is checked against the extent of its buffer; a failing
+// check records its site number (BoundsSite) in the bounds word if that is
+// still 0, sets kDevErrBounds in the status word and skips the access.
+// Release builds compile the checks away.
+constexpr unsigned kDevErrBounds = 8u;
+enum BoundsSite : unsigned {
+    kSiteCopyC = 1,        // stream producer: rows of C
+    kSiteRing = 2,         // stream producer: the ring slot they land in
+    kSiteCopyQ = 3,        // query producer: q
+    kSiteQbuf = 4,         // query producer: the q slot
+    kSiteOut = 5,          // softmax of a question (STREAM plan)
+    kSiteOutCluster = 6,   // softmax rows of a CTA (CLUSTER plan)
+    kSiteStagedWrite = 7,  // unfused pass 1
+    kSiteStagedRead = 8,   // unfused pass 2 (cosine)
+    kSiteOffsets = 9,      // ragged: a question's offsets
+    kSiteOffsetsSearch = 10,  // ragged: the CTA's first and last question
+    kSiteGenericC = 11,
+    kSiteGenericQ = 12,
+    kSiteGenericOut = 13,
+    kSiteStagedSoftmax = 14,     // unfused pass 2 (dot): staged similarities
+    kSiteStagedSoftmaxOut = 15,
+    kSitePeer = 16,        // cluster exchange slot in a peer CTA
+    kSiteProjQ = 20,       // projected readout: projected query
+    kSiteProjOut = 21,     // projected readout: probabilities
+    kSiteSelftest = 99,
+};
+bool debug_bounds_build();
+cudaError_t bounds_site_address(unsigned** ptr);
+cudaError_t read_bounds_site(unsigned* site, bool clear);
+// Bounds-checked builds: one thread checks an address one past a buffer's
+// end (arithmetic only, nothing is accessed); cudaErrorNotSupported otherwise.
+cudaError_t launch_selftest_bounds(cudaStream_t stream);
 
 // Device status word (bounded-wait give-ups).
 cudaError_t read_device_status(unsigned* flags, bool clear);

@@ -46,8 +46,32 @@
 namespace cs {
 
 __device__ unsigned int g_status;
+__device__ unsigned int g_bounds_site;  // bounds-checked builds: first failing site (0 = none)
 
 namespace {
+
+#ifdef CS_DEBUG_BOUNDS
+// [ptr, ptr + bytes) inside [base, base + extent)? Otherwise record the site
+// (first one only) and the status bit, and tell the caller to skip.
+__device__ __noinline__ bool check_range(const void* ptr, unsigned long long bytes, const void* base,
+                                         unsigned long long extent, unsigned site) {
+    const unsigned long long a = reinterpret_cast<unsigned long long>(ptr);
+    const unsigned long long b = reinterpret_cast<unsigned long long>(base);
+    if (a >= b && bytes <= extent && a - b <= extent - bytes) return true;
+    atomicCAS(&g_bounds_site, 0u, site);
+    atomicOr(&g_status, kDevErrBounds);
+    return false;
+}
+#define CS_IN_BOUNDS(ptr, bytes, base, extent, site) \
+    check_range((ptr), static_cast<unsigned long long>(bytes), (base), static_cast<unsigned long long>(extent), (site))
+#else
+#define CS_IN_BOUNDS(ptr, bytes, base, extent, site) true
+#endif
+
+// Rows of C (and of out, and of staged) of a launch.
+[[maybe_unused]] __host__ __device__ inline long long rows_total(const Problem& p) {
+    return p.offsets ? p.total_rows : p.B * static_cast<long long>(p.K);
+}
 
 constexpr float kEps = 1e-8f;        // norm clamp of the cosine
 constexpr float kEps2 = 1e-16f;      // kEps squared: max(|c|, eps) = sqrt(max(|c|^2, eps^2))
@@ -309,6 +333,7 @@ __device__ __forceinline__ QRows question_rows(const Problem& p, long long b, in
     long long o0 = b * p.K, kb = p.K;
     bool bad = false;
     if (p.offsets) {
+        if (!CS_IN_BOUNDS(p.offsets + b, 16, p.offsets, (p.B + 1) * 8, kSiteOffsets)) return QRows{0, 0, true};
         o0 = p.offsets[b];
         const long long o1 = p.offsets[b + 1];
         kb = o1 - o0;
@@ -334,7 +359,8 @@ __device__ long long lower_bound_warp(const long long* off, long long n, long lo
         const long long step = span <= 31 ? 1 : (span + 30) / 31;  // lo + 31 step >= hi
         long long pos = lo + step * lane;
         if (pos > hi) pos = hi;
-        const bool ge = pos == n || off[pos] >= target;
+        const bool ge = pos == n || !CS_IN_BOUNDS(off + pos, 8, off, (n + 1) * 8, kSiteOffsetsSearch) ||
+                        off[pos] >= target;
         const unsigned m = __ballot_sync(0xffffffffu, ge);
         const int f = __ffs(m) - 1;  // m != 0: the lanes at hi satisfy
         long long pf = lo + step * f;
@@ -544,9 +570,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     break;
                 const int k0 = s * R;
                 const uint32_t bytes = static_cast<uint32_t>(min(R, qr.n - k0)) * row_bytes;
-                mbar_arrive_expect_tx(bar_f, bytes);
-                bulk_g2s(smem_u32(ring + static_cast<size_t>(slot) * stage_bytes),
-                         Cg + static_cast<size_t>(qr.row0 + k0) * D, bytes, bar_f);
+                const T* src = Cg + static_cast<size_t>(qr.row0 + k0) * D;
+                unsigned char* dst = ring + static_cast<size_t>(slot) * stage_bytes;
+                const bool inb = CS_IN_BOUNDS(src, bytes, p.C, rows_total(p) * row_bytes, kSiteCopyC) &&
+                                 CS_IN_BOUNDS(dst, bytes, ring, static_cast<size_t>(NS) * stage_bytes, kSiteRing);
+                mbar_arrive_expect_tx(bar_f, inb ? bytes : 0u);
+                if (inb) bulk_g2s(smem_u32(dst), src, bytes, bar_f);
                 slot += kConsumerWarps;
                 if (slot >= static_cast<uint32_t>(NS)) {
                     slot -= NS;
@@ -580,8 +609,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             for (long long b = qb; b < qe; ++b, ++nq) {
                 const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
                 if (nq >= 2 && !wait_phase(qempty0 + 8u * qs, qpar ^ 1u, give_up)) break;
-                mbar_arrive_expect_tx(qfull0 + 8u * qs, q_bytes);
-                bulk_g2s(smem_u32(qbuf + qs * D), p.Q + static_cast<size_t>(b) * D, q_bytes, qfull0 + 8u * qs);
+                const float* src = p.Q + static_cast<size_t>(b) * D;
+                const bool inb = CS_IN_BOUNDS(src, q_bytes, p.Q, p.B * q_bytes, kSiteCopyQ) &&
+                                 CS_IN_BOUNDS(qbuf + qs * D, q_bytes, qbuf, 2 * q_bytes, kSiteQbuf);
+                mbar_arrive_expect_tx(qfull0 + 8u * qs, inb ? q_bytes : 0u);
+                if (inb) bulk_g2s(smem_u32(qbuf + qs * D), src, q_bytes, qfull0 + 8u * qs);
             }
             if (*give_up) {
                 const unsigned long long deadline = globaltimer() + kWaitLimitNs;
@@ -657,7 +689,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     if (r < nr) {
                         if constexpr (does_softmax(MODE))
                             (VPR == 2 && (idx & 1) ? nb : tb)[k0 + r] = val;
-                        else
+                        else if (CS_IN_BOUNDS(p.staged + qr.row0 + k0 + r, 4, p.staged, rows_total(p) * 4,
+                                              kSiteStagedWrite))
                             p.staged[qr.row0 + k0 + r] = MODE == kRowNorm ? sqrtf(val) : val;
                     }
                 }
@@ -676,8 +709,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             consumer_bar_sync();  // every row of question b has its dot (and norm)
             if (does_softmax(MODE) && G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
                 float z[kSlotsPerLane];
-                load_logits<MODE>(tb, nb, MODE == kStagedCos ? p.staged + qr.row0 : nullptr, nrows, a, lane, z);
-                softmax_store(z, nrows, p.out + qr.row0, lane);
+                const bool inb =
+                    CS_IN_BOUNDS(p.out + qr.row0, nrows * 4, p.out, rows_total(p) * 4, kSiteOut) &&
+                    (MODE != kStagedCos ||
+                     CS_IN_BOUNDS(p.staged + qr.row0, nrows * 4, p.staged, rows_total(p) * 4, kSiteStagedRead));
+                if (inb) {
+                    load_logits<MODE>(tb, nb, MODE == kStagedCos ? p.staged + qr.row0 : nullptr, nrows, a, lane, z);
+                    softmax_store(z, nrows, p.out + qr.row0, lane);
+                }
             }
             gst0 += nst;
             last = qr;
@@ -696,8 +735,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const uint32_t rank = cluster_ctarank();
             float z[kSlotsPerLane];
             const int nrows = last.n;
-            load_logits<MODE>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr, nrows, a,
-                              lane, z);
+            const bool rd = MODE != kStagedCos || CS_IN_BOUNDS(p.staged + last.row0, nrows * 4, p.staged,
+                                                                rows_total(p) * 4, kSiteStagedRead);
+            load_logits<MODE>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr,
+                              rd ? nrows : 0, a, lane, z);
             float m = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
@@ -707,7 +748,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             for (int j = 0; j < kSlotsPerLane; ++j)
                 if (lane + 32 * j < nrows) s += __expf(z[j] - m);
             s = warp_sum(s);
-            if (lane < G)
+            if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
                 st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
                               peer_addr(xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(xbar), 0, give_up);
@@ -720,10 +761,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const float M = warp_max(mj);
             const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
             float* dst = p.out + last.row0;
+            if (CS_IN_BOUNDS(dst, nrows * 4, p.out, rows_total(p) * 4, kSiteOutCluster)) {
 #pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j) {
-                const int k = lane + 32 * j;
-                if (k < nrows) dst[k] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
+                for (int j = 0; j < kSlotsPerLane; ++j) {
+                    const int k = lane + 32 * j;
+                    if (k < nrows) dst[k] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
+                }
             }
         }
         __syncwarp();
@@ -751,6 +794,9 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     }
     const int K = qr.n, D = p.D;
     const float* __restrict__ q = p.Q + static_cast<size_t>(b) * D;
+    if (!CS_IN_BOUNDS(q, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ) ||
+        !CS_IN_BOUNDS(p.out + qr.row0, K * 4ll, p.out, rows_total(p) * 4, kSiteGenericOut))
+        return;
     float qn = 1.f;
     if (COS) {
         float sq = 0.f;
@@ -763,6 +809,11 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     const float a = logit_factor(qn, p.scale, p.temperature, COS);
     for (int k = warp; k < K; k += nwarps) {
         const T* __restrict__ c = static_cast<const T*>(p.C) + static_cast<size_t>(qr.row0 + k) * D;
+        if (!CS_IN_BOUNDS(c, D * static_cast<long long>(sizeof(T)), p.C, rows_total(p) * D * static_cast<long long>(sizeof(T)),
+                          kSiteGenericC)) {
+            if (lane == 0) lg[k] = -INFINITY;
+            continue;
+        }
         float t0 = 0.f, t1 = 0.f, n0 = 0.f, n1 = 0.f;
         int d = lane;
         for (; d + 32 < D; d += 64) {
@@ -800,6 +851,9 @@ __global__ void __launch_bounds__(256) staged_softmax_kernel(const Problem p) {
     if (b >= p.B) return;
     const float a = p.scale / p.temperature;
     const float* t = p.staged + static_cast<size_t>(b) * p.K;
+    if (!CS_IN_BOUNDS(t, p.K * 4ll, p.staged, p.B * p.K * 4ll, kSiteStagedSoftmax) ||
+        !CS_IN_BOUNDS(p.out + static_cast<size_t>(b) * p.K, p.K * 4ll, p.out, p.B * p.K * 4ll, kSiteStagedSoftmaxOut))
+        return;
     float z[kSlotsPerLane];
 #pragma unroll
     for (int j = 0; j < kSlotsPerLane; ++j) {
@@ -823,6 +877,15 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns) {
         (void)wait_phase(smem_u32(&bar), 0, reinterpret_cast<volatile int*>(&flag), limit_ns);
     }
 }
+
+#ifdef CS_DEBUG_BOUNDS
+// Self-test of the bounds checks: one thread checks the range one past the
+// end of a 64-byte buffer (arithmetic only: nothing is read or written).
+__global__ void selftest_bounds_kernel() {
+    __shared__ float buf[16];
+    if (threadIdx.x == 0) (void)CS_IN_BOUNDS(buf + 16, 4, buf, sizeof(buf), kSiteSelftest);
+}
+#endif
 
 // ------------------------------------------------------------------ dispatch
 
@@ -1017,6 +1080,38 @@ cudaError_t status_word_address(unsigned** ptr) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_status);
     if (e == cudaSuccess) *ptr = static_cast<unsigned*>(p);
     return e;
+}
+
+bool debug_bounds_build() {
+#ifdef CS_DEBUG_BOUNDS
+    return true;
+#else
+    return false;
+#endif
+}
+
+cudaError_t bounds_site_address(unsigned** ptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_bounds_site);
+    if (e == cudaSuccess) *ptr = static_cast<unsigned*>(p);
+    return e;
+}
+
+cudaError_t read_bounds_site(unsigned* site, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(site, g_bounds_site, sizeof(unsigned));
+    if (e != cudaSuccess || !clear) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_bounds_site, &zero, sizeof(unsigned));
+}
+
+cudaError_t launch_selftest_bounds(cudaStream_t stream) {
+#ifdef CS_DEBUG_BOUNDS
+    selftest_bounds_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+#else
+    (void)stream;
+    return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t read_device_status(unsigned* flags, bool clear) {

@@ -65,7 +65,28 @@ struct ProjArgs {
     const float* qproj; // SCORE: projected queries [B][D]
     float* out;         // PLAIN: [rows][D]; SCORE: [B][K]
     unsigned* status;   // device status word
+    unsigned* bounds;   // bounds word (first failing check of a bounds-checked build)
 };
+
+#ifdef CS_DEBUG_BOUNDS
+// [ptr, ptr + bytes) inside [base, base + extent)? Otherwise record the site
+// (first one only) and the status bit, and tell the caller to skip.
+__device__ __noinline__ bool check_range(const void* ptr, unsigned long long bytes, const void* base,
+                                         unsigned long long extent, unsigned site, unsigned* bounds,
+                                         unsigned* status) {
+    const unsigned long long x = reinterpret_cast<unsigned long long>(ptr);
+    const unsigned long long b = reinterpret_cast<unsigned long long>(base);
+    if (x >= b && bytes <= extent && x - b <= extent - bytes) return true;
+    atomicCAS(bounds, 0u, site);
+    atomicOr(status, kDevErrBounds);
+    return false;
+}
+#define CS_IN_BOUNDS(ptr, bytes, base, extent, site)                                                        \
+    check_range((ptr), static_cast<unsigned long long>(bytes), (base), static_cast<unsigned long long>(extent), \
+                (site), a.bounds, a.status)
+#else
+#define CS_IN_BOUNDS(ptr, bytes, base, extent, site) true
+#endif
 
 // ---------------------------------------------------------------- PTX
 
@@ -383,7 +404,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             float* lg = logits + (nq & 1) * 256;
             if (MODE == kProjScore) {
                 const float* q = a.qproj + static_cast<size_t>(item) * D;
-                for (int i = et; i < D; i += kEpiThreads) qs[i] = q[i];
+                if (CS_IN_BOUNDS(q, D * 4ll, a.qproj, a.B * D * 4ll, kSiteProjQ))
+                    for (int i = et; i < D; i += kEpiThreads) qs[i] = q[i];
                 epi_bar_sync();
                 float sq = 0.f;
                 if (a.normalize)
@@ -478,9 +500,11 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                     }
                     const float inv = 1.0f / wsum(s);
                     float* dst = a.out + static_cast<size_t>(item) * a.K;
+                    if (CS_IN_BOUNDS(dst, a.K * 4ll, a.out, a.B * a.K * 4ll, kSiteProjOut)) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (lane + 32 * j < a.K) dst[lane + 32 * j] = z[j] * inv;
+                        for (int j = 0; j < 8; ++j)
+                            if (lane + 32 * j < a.K) dst[lane + 32 * j] = z[j] * inv;
+                    }
                 }
             }
         }
@@ -549,7 +573,7 @@ cudaError_t configure_proj_kernels(int smem_optin) {
 }
 
 cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
-                                int sms, unsigned* status, cudaStream_t stream) {
+                                int sms, unsigned* status, unsigned* bounds, cudaStream_t stream) {
     CUtensorMap ma, mw, mp;
     if (!make_bf16_map(&ma, H, rows, Din, kTileM) || !make_bf16_map(&mw, W, D, Din, kMmaN) ||
         !make_map(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P, rows, D, kOutBox, kOutBox))
@@ -560,6 +584,7 @@ cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long 
     a.D = D;
     a.out = P;
     a.status = status;
+    a.bounds = bounds;
     const long long tiles = (rows + kTileM - 1) / kTileM;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
     proj_kernel<kProjPlain><<<grid, kProjThreads, proj_layout(D, kProjPlain).total, stream>>>(ma, mw, mp, a);
@@ -568,7 +593,7 @@ cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long 
 
 cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
                                  int D, int normalize, float scale, float temperature, float* out, int sms,
-                                 unsigned* status, cudaStream_t stream) {
+                                 unsigned* status, unsigned* bounds, cudaStream_t stream) {
     CUtensorMap ma, mw;
     const unsigned long long rows = static_cast<unsigned long long>(B) * K;
     if (!make_bf16_map(&ma, Hc, rows, Din, kTileM) || !make_bf16_map(&mw, Wc, D, Din, kMmaN))
@@ -585,6 +610,7 @@ cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const f
     a.qproj = qproj;
     a.out = out;
     a.status = status;
+    a.bounds = bounds;
     const unsigned grid = static_cast<unsigned>(B < sms ? B : sms);
     // the scoring kernel stores no rows: its output map is never used
     proj_kernel<kProjScore><<<grid, kProjThreads, proj_layout(D, kProjScore).total, stream>>>(ma, mw, ma, a);

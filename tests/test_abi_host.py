@@ -264,3 +264,16 @@ def test_project_rejects(host_lib):
     assert call(D=128) == E.CS_ERR_BAD_PLAN
     assert call(out=C_ADDR) == E.CS_ERR_ALIAS
     assert call(qp=OUT_ADDR) == E.CS_ERR_ALIAS
+
+
+def test_bounds_checked_build_compiles_and_reports_itself(host_lib):
+    """The -DCS_DEBUG_BOUNDS variant builds from the same sources and says
+    so; the release library does not (neither call touches a GPU)."""
+    import ctypes
+
+    from similarity_softmax_candidate_gb300 import _build
+    dbg = ctypes.CDLL(_build.build_library(debug_bounds=True))
+    assert dbg.cs_debug_bounds_build() == 1
+    assert host_lib.cs_debug_bounds_build() == 0
+    for name in _declared_functions():
+        assert hasattr(dbg, name), f"{name} missing from the bounds-checked build"
