@@ -200,6 +200,29 @@ __device__ __forceinline__ void consumer_bar_sync() {
 
 // ------------------------------------------------------------------ helpers
 
+// Packed float32 pairs (low = first element): d = a * b + c element-wise,
+// one instruction for two fused multiply-adds.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float unpack_lo(unsigned long long x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return lo;
+}
+__device__ __forceinline__ float unpack_hi(unsigned long long x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return hi;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -395,25 +418,22 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
                                            float (&v)[values_per_row(MODE) * kMaxRowsPerStage]) {
     constexpr int VPR = values_per_row(MODE);
     constexpr int QF4 = Elem<T>::kQF4;
+    // Each value accumulates as two partial sums (even and odd elements of
+    // the row) with packed float32 FMAs, added together at the end.
+    unsigned long long acc[VPR * kMaxRowsPerStage];
 #pragma unroll
-    for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = 0.f;
+    for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) acc[i] = 0ull;
     auto accumulate = [&](const float4& c, const float4& q, int r) {
+        const unsigned long long c01 = pack2(c.x, c.y), c23 = pack2(c.z, c.w);
         if (acc_dot(MODE)) {
-            float t = v[VPR * r];
-            t = fmaf(c.x, q.x, t);
-            t = fmaf(c.y, q.y, t);
-            t = fmaf(c.z, q.z, t);
-            t = fmaf(c.w, q.w, t);
-            v[VPR * r] = t;
+            unsigned long long& t = acc[VPR * r];
+            t = fma2(c01, pack2(q.x, q.y), t);
+            t = fma2(c23, pack2(q.z, q.w), t);
         }
         if (acc_norm(MODE)) {
-            const int i = VPR * r + VPR - 1;
-            float n = v[i];
-            n = fmaf(c.x, c.x, n);
-            n = fmaf(c.y, c.y, n);
-            n = fmaf(c.z, c.z, n);
-            n = fmaf(c.w, c.w, n);
-            v[i] = n;
+            unsigned long long& n = acc[VPR * r + VPR - 1];
+            n = fma2(c01, c01, n);
+            n = fma2(c23, c23, n);
         }
     };
     if constexpr (NQC > 0) {
@@ -450,6 +470,8 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = unpack_lo(acc[i]) + unpack_hi(acc[i]);
 }
 
 template <int NQC, int MODE, typename T>
