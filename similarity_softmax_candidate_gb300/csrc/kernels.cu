@@ -42,6 +42,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 namespace cs {
 
@@ -271,11 +272,11 @@ __device__ __forceinline__ float logit_factor(float qn, float scale, float tempe
 // Logits of rows lane, lane+32, ... (< n) from their dots t and, for the
 // fused cosine, squared norms n_sq, or, for the staged cosine, norms read
 // from the staged array; -inf beyond n.
-template <int MODE>
+template <int MODE, int S = kSlotsPerLane>
 __device__ __forceinline__ void load_logits(const float* t, const float* n_sq, const float* staged_norm, int n,
-                                            float a, int lane, float (&z)[kSlotsPerLane]) {
+                                            float a, int lane, float (&z)[S]) {
 #pragma unroll
-    for (int j = 0; j < kSlotsPerLane; ++j) {
+    for (int j = 0; j < S; ++j) {
         const int k = lane + 32 * j;
         z[j] = -INFINITY;
         if (k < n) {
@@ -290,20 +291,21 @@ __device__ __forceinline__ void load_logits(const float* t, const float* n_sq, c
 }
 
 // Softmax of z over one warp (rows lane + 32 j < n), written to dst[0..n).
-__device__ __forceinline__ void softmax_store(float (&z)[kSlotsPerLane], int n, float* __restrict__ dst, int lane) {
+template <int S = kSlotsPerLane>
+__device__ __forceinline__ void softmax_store(float (&z)[S], int n, float* __restrict__ dst, int lane) {
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
+    for (int j = 0; j < S; ++j) m = fmaxf(m, z[j]);
     m = warp_max(m);
     float s = 0.f;
 #pragma unroll
-    for (int j = 0; j < kSlotsPerLane; ++j) {
+    for (int j = 0; j < S; ++j) {
         z[j] = lane + 32 * j < n ? __expf(z[j] - m) : 0.f;
         s += z[j];
     }
     const float inv = 1.0f / warp_sum(s);
 #pragma unroll
-    for (int j = 0; j < kSlotsPerLane; ++j) {
+    for (int j = 0; j < S; ++j) {
         const int k = lane + 32 * j;
         if (k < n) dst[k] = z[j] * inv;
     }
@@ -730,13 +732,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             }
             consumer_bar_sync();  // every row of question b has its dot (and norm)
             if (does_softmax(MODE) && G == 1 && warp == static_cast<int>(nq % kConsumerWarps)) {
-                float z[kSlotsPerLane];
                 const bool inb =
                     CS_IN_BOUNDS(p.out + qr.row0, nrows * 4, p.out, rows_total(p) * 4, kSiteOut) &&
                     (MODE != kStagedCos ||
                      CS_IN_BOUNDS(p.staged + qr.row0, nrows * 4, p.staged, rows_total(p) * 4, kSiteStagedRead));
-                if (inb) {
-                    load_logits<MODE>(tb, nb, MODE == kStagedCos ? p.staged + qr.row0 : nullptr, nrows, a, lane, z);
+                const float* sn = MODE == kStagedCos ? p.staged + qr.row0 : nullptr;
+                if (inb && nrows <= 32) {  // one row per lane: the short code path
+                    float z[1];
+                    load_logits<MODE, 1>(tb, nb, sn, nrows, a, lane, z);
+                    softmax_store<1>(z, nrows, p.out + qr.row0, lane);
+                } else if (inb) {
+                    float z[kSlotsPerLane];
+                    load_logits<MODE>(tb, nb, sn, nrows, a, lane, z);
                     softmax_store(z, nrows, p.out + qr.row0, lane);
                 }
             }
@@ -753,21 +760,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         // for all G pairs to arrive here, and writes p = exp(z - M) / S with
         // M = max m_g and S = sum s_g exp(m_g - M).
         cluster_wait();  // every CTA of the cluster has initialised its barriers
-        if (warp == 0) {
+        // Warp 0; S slots of 32 rows per lane (S = 1 whenever this CTA holds
+        // at most 32 rows: the short code path).
+        auto finish = [&](auto slots) {
+            constexpr int S = decltype(slots)::value;
             const uint32_t rank = cluster_ctarank();
-            float z[kSlotsPerLane];
+            float z[S];
             const int nrows = last.n;
             const bool rd = MODE != kStagedCos || CS_IN_BOUNDS(p.staged + last.row0, nrows * 4, p.staged,
                                                                 rows_total(p) * 4, kSiteStagedRead);
-            load_logits<MODE>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr,
-                              rd ? nrows : 0, a, lane, z);
+            load_logits<MODE, S>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr,
+                                 rd ? nrows : 0, a, lane, z);
             float m = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
+            for (int j = 0; j < S; ++j) m = fmaxf(m, z[j]);
             m = warp_max(m);
             float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j)
+            for (int j = 0; j < S; ++j)
                 if (lane + 32 * j < nrows) s += __expf(z[j] - m);
             s = warp_sum(s);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
@@ -785,11 +795,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             float* dst = p.out + last.row0;
             if (CS_IN_BOUNDS(dst, nrows * 4, p.out, rows_total(p) * 4, kSiteOutCluster)) {
 #pragma unroll
-                for (int j = 0; j < kSlotsPerLane; ++j) {
+                for (int j = 0; j < S; ++j) {
                     const int k = lane + 32 * j;
                     if (k < nrows) dst[k] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
                 }
             }
+        };
+        if (warp == 0) {
+            if (last.n <= 32)
+                finish(std::integral_constant<int, 1>{});
+            else
+                finish(std::integral_constant<int, kSlotsPerLane>{});
         }
         __syncwarp();
         // Leave only when every CTA has received every pair: no push into a
