@@ -99,12 +99,13 @@ cudaError_t device_state(DeviceState** st) {
     return cudaSuccess;
 }
 
-int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16) {
-    const long long key2 = (static_cast<long long>(smem) << 8) | (nq4 << 2) | (c_bf16 << 1) | normalize;
+int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows) {
+    const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) | (nq4 << 2) |
+                           (c_bf16 << 1) | normalize;
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = d.clusters.find({cluster, key2});
     if (it != d.clusters.end()) return it->second;
-    const int n = cs::max_active_clusters(cluster, smem, nq4, normalize, c_bf16);
+    const int n = cs::max_active_clusters(cluster, smem, nq4, normalize, c_bf16, rows);
     d.clusters[{cluster, key2}] = n;
     return n;
 }
@@ -247,7 +248,8 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         if (cluster == 1)  // one CTA per question: the STREAM kernel with B CTAs
             return stream_plan(d, p, static_cast<int>(p.B), plan) ? CS_OK : CS_ERR_BAD_PLAN;
         if (!cluster_plan(d, p, cluster, plan)) return CS_ERR_BAD_PLAN;
-        if (cached_max_clusters(d, cluster, plan->smem, plan->nq4, p.normalize, p.c_bf16) < 1) return CS_ERR_BAD_PLAN;
+        if (cached_max_clusters(d, cluster, plan->smem, plan->nq4, p.normalize, p.c_bf16, plan->rows_per_stage) < 1)
+            return CS_ERR_BAD_PLAN;
         return CS_OK;
     }
     // automatic choice
@@ -262,7 +264,7 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
             G *= 2;
         for (; G > 1; G /= 2) {
             if (cluster_plan(d, p, G, plan) &&
-                cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize, p.c_bf16) >= p.B)
+                cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize, p.c_bf16, plan->rows_per_stage) >= p.B)
                 return CS_OK;
         }
     }

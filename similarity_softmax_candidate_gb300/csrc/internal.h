@@ -20,6 +20,9 @@ constexpr int kStreamThreads = (kConsumerWarps + 2) * 32;
 constexpr int kLogitSlots = 256;
 // Most candidate rows in one ring stage; one warp reduces a whole stage.
 constexpr int kMaxRowsPerStage = 8;
+// Plans whose stages hold at most this many rows run a short-stage build of
+// the fused kernels (less code to fetch on a batch-1 launch).
+constexpr int kSmallStageRows = 2;
 // Largest cluster the split plan uses (non-portable size on sm_100-class parts).
 constexpr int kMaxCluster = 16;
 // Threads of the scalar fallback kernel.
@@ -116,7 +119,7 @@ cudaError_t configure_device_kernels(int smem_optin);
 
 // Clusters of `cluster` CTAs with `smem` bytes each that fit on the device
 // at once (0 if none).
-int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16);
+int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows_per_stage);
 
 // Bounded-wait self-test: one wait that nothing completes, limit_ns long.
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);

@@ -400,31 +400,31 @@ __device__ long long lower_bound_warp(const long long* off, long long n, long lo
 
 struct StreamArgs {
     Problem p;
-    int rows_per_stage;  // R <= kMaxRowsPerStage
+    int rows_per_stage;  // R <= the instantiation's MR
     int stages;          // NS, a multiple of kConsumerWarps
     int cluster;         // G: CTAs per question (1 = STREAM plan)
     int q_per_cta;       // STREAM plan: CTA c takes q_per_cta (+1 if c < q_rem) questions
     int q_rem;
 };
 
-// Per-row sums of the nr <= kMaxRowsPerStage rows of one stage (rows of DC
+// Per-row sums of the nr <= MR rows of one stage (rows of DC
 // 16-byte chunks each). Lane handles chunks lane, lane+32, ...; q comes from
 // registers (NQC > 0: qv holds the q float4s of those chunks) or from shared
 // memory (NQC == 0, large D). With two values per row (fused cosine)
 // v[2r] = c_r . q and v[2r + 1] = c_r . c_r; with one, v[r] = c_r . q, or
 // c_r . c_r for the norm pass.
-template <int NQC, int MODE, typename T>
+template <int NQC, int MODE, typename T, int MR>
 __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr, int DC,
                                            const float4 (&qv)[(NQC > 0 ? NQC : 1) * Elem<T>::kQF4],
                                            const float4* __restrict__ q4, int lane,
-                                           float (&v)[values_per_row(MODE) * kMaxRowsPerStage]) {
+                                           float (&v)[values_per_row(MODE) * MR]) {
     constexpr int VPR = values_per_row(MODE);
     constexpr int QF4 = Elem<T>::kQF4;
     // Each value accumulates as two partial sums (even and odd elements of
     // the row) with packed float32 FMAs, added together at the end.
-    unsigned long long acc[VPR * kMaxRowsPerStage];
+    unsigned long long acc[VPR * MR];
 #pragma unroll
-    for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) acc[i] = 0ull;
+    for (int i = 0; i < VPR * MR; ++i) acc[i] = 0ull;
     auto accumulate = [&](const float4& c, const float4& q, int r) {
         const unsigned long long c01 = pack2(c.x, c.y), c23 = pack2(c.z, c.w);
         if (acc_dot(MODE)) {
@@ -440,7 +440,7 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
     };
     if constexpr (NQC > 0) {
 #pragma unroll
-        for (int r = 0; r < kMaxRowsPerStage; ++r) {
+        for (int r = 0; r < MR; ++r) {
             if (r < nr) {
                 const uint4* __restrict__ row = st + r * DC;
 #pragma unroll
@@ -457,7 +457,7 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
         }
     } else {
 #pragma unroll
-        for (int r = 0; r < kMaxRowsPerStage; ++r) {
+        for (int r = 0; r < MR; ++r) {
             if (r < nr) {
                 const uint4* __restrict__ row = st + r * DC;
                 for (int i = lane; i < DC; i += 32) {
@@ -473,14 +473,17 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
         }
     }
 #pragma unroll
-    for (int i = 0; i < VPR * kMaxRowsPerStage; ++i) v[i] = unpack_lo(acc[i]) + unpack_hi(acc[i]);
+    for (int i = 0; i < VPR * MR; ++i) v[i] = unpack_lo(acc[i]) + unpack_hi(acc[i]);
 }
 
-template <int NQC, int MODE, typename T>
+// MR: most rows per stage this instantiation handles (kMaxRowsPerStage, or
+// kSmallStageRows for the fused modes when the plan's stages are that short:
+// the per-stage code a batch-1 launch fetches is then a quarter as long).
+template <int NQC, int MODE, typename T, int MR>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamArgs args) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int VPR = values_per_row(MODE);
-    constexpr int V = VPR * kMaxRowsPerStage;
+    constexpr int V = VPR * MR;
     constexpr bool COS = cos_logits(MODE);
     constexpr int QF4 = Elem<T>::kQF4;
     const Problem& p = args.p;
@@ -491,10 +494,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // The ring must hold whole rounds of consumer warps (slot s is always
-    // owned by warp s % kConsumerWarps) and a stage at most kMaxRowsPerStage
+    // owned by warp s % kConsumerWarps) and a stage at most MR
     // rows; the host plans it so. Every CTA sees the same arguments, so a bad
     // plan makes every CTA of every cluster leave here, before any barrier.
-    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || R < 1 || R > kMaxRowsPerStage || G < 1 ||
+    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || R < 1 || R > MR || G < 1 ||
         G > kMaxCluster) {
         if (threadIdx.x == 0) atomicOr(&g_status, 2u);
         return;
@@ -703,7 +706,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
                 float v[V];
-                stage_dots<NQC, MODE, T>(reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes),
+                stage_dots<NQC, MODE, T, MR>(reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes),
                                          nr, DC, qv, q4, lane, v);
                 int idx;
                 const float sum = transpose_reduce<V>(v, lane, &idx);
@@ -927,7 +930,7 @@ __global__ void selftest_bounds_kernel() {
 
 // ------------------------------------------------------------------ dispatch
 
-template <int NQC, int MODE, typename T>
+template <int NQC, int MODE, typename T, int MR>
 cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -947,50 +950,66 @@ cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t 
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    return cudaLaunchKernelEx(&cfg, stream_kernel<NQC, MODE, T>, a);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<NQC, MODE, T, MR>, a);
 }
 
-template <int MODE, typename T>
+template <int MODE, typename T, int MR>
 cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     switch (plan.nq4) {
-        case 1: return launch_stream_t<1, MODE, T>(a, plan, stream);
-        case 2: return launch_stream_t<2, MODE, T>(a, plan, stream);
-        case 4: return launch_stream_t<4, MODE, T>(a, plan, stream);
-        case 8: return launch_stream_t<8, MODE, T>(a, plan, stream);
-        case 0: return launch_stream_t<0, MODE, T>(a, plan, stream);
+        case 1: return launch_stream_t<1, MODE, T, MR>(a, plan, stream);
+        case 2: return launch_stream_t<2, MODE, T, MR>(a, plan, stream);
+        case 4: return launch_stream_t<4, MODE, T, MR>(a, plan, stream);
+        case 8: return launch_stream_t<8, MODE, T, MR>(a, plan, stream);
+        case 0: return launch_stream_t<0, MODE, T, MR>(a, plan, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <int MODE, typename T>
+template <int MODE, typename T, int MR>
 const void* stream_fn_m(int nqc) {
     switch (nqc) {
-        case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE, T>);
-        case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE, T>);
-        case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE, T>);
-        case 8: return reinterpret_cast<const void*>(stream_kernel<8, MODE, T>);
-        case 0: return reinterpret_cast<const void*>(stream_kernel<0, MODE, T>);
+        case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE, T, MR>);
+        case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE, T, MR>);
+        case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE, T, MR>);
+        case 8: return reinterpret_cast<const void*>(stream_kernel<8, MODE, T, MR>);
+        case 0: return reinterpret_cast<const void*>(stream_kernel<0, MODE, T, MR>);
     }
     return nullptr;
 }
 
+// The row limit of the instantiation that runs stages of R rows in `mode`.
+constexpr int rows_limit(int mode, int R) {
+    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows ? kSmallStageRows : kMaxRowsPerStage;
+}
+
 // Kernels exist for every mode over float32 C, and for the fused modes over
-// bfloat16 C (nqc 8 is never planned for bfloat16: q would take 64 registers).
-const void* stream_fn_for(int nqc, int mode, int c_bf16) {
+// bfloat16 C (nqc 8 is never planned for bfloat16: q would take 64 registers);
+// the fused modes also in a short-stage form (mr = kSmallStageRows).
+const void* stream_fn_for(int nqc, int mode, int c_bf16, int mr) {
+    const bool fused = mode == kFusedCos || mode == kFusedDot;
+    if (mr == kSmallStageRows) {
+        if (!fused || (c_bf16 && nqc == 8)) return nullptr;
+        if (c_bf16)
+            return mode == kFusedCos ? stream_fn_m<kFusedCos, uint16_t, kSmallStageRows>(nqc)
+                                     : stream_fn_m<kFusedDot, uint16_t, kSmallStageRows>(nqc);
+        return mode == kFusedCos ? stream_fn_m<kFusedCos, float, kSmallStageRows>(nqc)
+                                 : stream_fn_m<kFusedDot, float, kSmallStageRows>(nqc);
+    }
+    if (mr != kMaxRowsPerStage) return nullptr;
     if (c_bf16) {
         if (nqc == 8) return nullptr;
         switch (mode) {
-            case kFusedCos: return stream_fn_m<kFusedCos, uint16_t>(nqc);
-            case kFusedDot: return stream_fn_m<kFusedDot, uint16_t>(nqc);
+            case kFusedCos: return stream_fn_m<kFusedCos, uint16_t, kMaxRowsPerStage>(nqc);
+            case kFusedDot: return stream_fn_m<kFusedDot, uint16_t, kMaxRowsPerStage>(nqc);
         }
         return nullptr;
     }
     switch (mode) {
-        case kFusedCos: return stream_fn_m<kFusedCos, float>(nqc);
-        case kFusedDot: return stream_fn_m<kFusedDot, float>(nqc);
-        case kRowNorm: return stream_fn_m<kRowNorm, float>(nqc);
-        case kRowDot: return stream_fn_m<kRowDot, float>(nqc);
-        case kStagedCos: return stream_fn_m<kStagedCos, float>(nqc);
+        case kFusedCos: return stream_fn_m<kFusedCos, float, kMaxRowsPerStage>(nqc);
+        case kFusedDot: return stream_fn_m<kFusedDot, float, kMaxRowsPerStage>(nqc);
+        case kRowNorm: return stream_fn_m<kRowNorm, float, kMaxRowsPerStage>(nqc);
+        case kRowDot: return stream_fn_m<kRowDot, float, kMaxRowsPerStage>(nqc);
+        case kStagedCos: return stream_fn_m<kStagedCos, float, kMaxRowsPerStage>(nqc);
     }
     return nullptr;
 }
@@ -1006,20 +1025,29 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
     const long long ctas = plan.kind == kPlanCluster ? 1 : plan.ctas;
     a.q_per_cta = static_cast<int>(p.B / ctas);
     a.q_rem = static_cast<int>(p.B % ctas);
+    const bool small = rows_limit(mode, plan.rows_per_stage) == kSmallStageRows;
     if (p.c_bf16) {
         if (plan.nq4 == 8) return cudaErrorInvalidValue;
         switch (mode) {
-            case kFusedCos: return launch_stream_m<kFusedCos, uint16_t>(a, plan, stream);
-            case kFusedDot: return launch_stream_m<kFusedDot, uint16_t>(a, plan, stream);
+            case kFusedCos:
+                return small ? launch_stream_m<kFusedCos, uint16_t, kSmallStageRows>(a, plan, stream)
+                             : launch_stream_m<kFusedCos, uint16_t, kMaxRowsPerStage>(a, plan, stream);
+            case kFusedDot:
+                return small ? launch_stream_m<kFusedDot, uint16_t, kSmallStageRows>(a, plan, stream)
+                             : launch_stream_m<kFusedDot, uint16_t, kMaxRowsPerStage>(a, plan, stream);
         }
         return cudaErrorInvalidValue;
     }
     switch (mode) {
-        case kFusedCos: return launch_stream_m<kFusedCos, float>(a, plan, stream);
-        case kFusedDot: return launch_stream_m<kFusedDot, float>(a, plan, stream);
-        case kRowNorm: return launch_stream_m<kRowNorm, float>(a, plan, stream);
-        case kRowDot: return launch_stream_m<kRowDot, float>(a, plan, stream);
-        case kStagedCos: return launch_stream_m<kStagedCos, float>(a, plan, stream);
+        case kFusedCos:
+            return small ? launch_stream_m<kFusedCos, float, kSmallStageRows>(a, plan, stream)
+                         : launch_stream_m<kFusedCos, float, kMaxRowsPerStage>(a, plan, stream);
+        case kFusedDot:
+            return small ? launch_stream_m<kFusedDot, float, kSmallStageRows>(a, plan, stream)
+                         : launch_stream_m<kFusedDot, float, kMaxRowsPerStage>(a, plan, stream);
+        case kRowNorm: return launch_stream_m<kRowNorm, float, kMaxRowsPerStage>(a, plan, stream);
+        case kRowDot: return launch_stream_m<kRowDot, float, kMaxRowsPerStage>(a, plan, stream);
+        case kStagedCos: return launch_stream_m<kStagedCos, float, kMaxRowsPerStage>(a, plan, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -1056,20 +1084,23 @@ cudaError_t configure_device_kernels(int smem_optin) {
     for (int bf = 0; bf < 2; ++bf) {
         for (int m = kFusedCos; m <= kStagedCos; ++m) {
             for (int i = 0; i < 5; ++i) {
-                const void* f = stream_fn_for(nq4s[i], m, bf);
-                if (!f) continue;
-                cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
-                if (e != cudaSuccess) return e;
-                e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-                if (e != cudaSuccess) return e;
+                for (int mr : {kSmallStageRows, kMaxRowsPerStage}) {
+                    const void* f = stream_fn_for(nq4s[i], m, bf, mr);
+                    if (!f) continue;
+                    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+                    if (e != cudaSuccess) return e;
+                    e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (e != cudaSuccess) return e;
+                }
             }
         }
     }
     return cudaSuccess;
 }
 
-int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16) {
-    const void* f = stream_fn_for(nq4, normalize ? kFusedCos : kFusedDot, c_bf16);
+int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows_per_stage) {
+    const int mode = normalize ? kFusedCos : kFusedDot;
+    const void* f = stream_fn_for(nq4, mode, c_bf16, rows_limit(mode, rows_per_stage));
     if (!f) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
