@@ -184,6 +184,16 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     if (ctas > p.B) ctas = static_cast<int>(p.B);
     // Stages one CTA ever needs: no point reserving more ring than that.
     const long long qpc = (p.B + ctas - 1) / ctas;
+    // Few rows per CTA (one short question): fewer rows per stage, so that
+    // every consumer warp gets a stage instead of one warp doing them all.
+    if (!p.offsets && qpc * p.K < static_cast<long long>(cs::kConsumerWarps) * R) {
+        const int r = static_cast<int>((qpc * p.K + cs::kConsumerWarps - 1) / cs::kConsumerWarps);
+        const int ns = max_stages(d, r, p.D, cb);
+        if (ns > 0) {
+            R = r;
+            max_ns = ns;
+        }
+    }
     const int ns = ring_stages(qpc * ((p.K + R - 1) / R), max_ns);
     plan->kind = cs::kPlanStream;
     plan->cluster = 1;
