@@ -184,6 +184,9 @@ int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,
 #define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions */
 #define CS_PLAN_CLUSTER 2  /* one thread-block cluster per question, rows split */
 #define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment */
+#define CS_PLAN_DIRECT 4   /* one CTA (or cluster) per short question: at most 32
+                              rows per CTA, q and rows loaded straight into
+                              registers, no shared-memory ring */
 
 /*
  * The plan cs_score_candidates_batch would use for these arguments.
@@ -198,8 +201,11 @@ int cs_query_plan(const float *Q, const float *C, int B, int K, int D,
 
 /*
  * cs_score_candidates_batch with the plan chosen by the caller, for tests
- * and tuning. plan is CS_PLAN_*; cluster (CS_PLAN_CLUSTER: 1..16, at most
- * K) and ctas (CS_PLAN_STREAM: 1..B) may be 0 for the automatic choice.
+ * and tuning. plan is CS_PLAN_*; cluster (CS_PLAN_CLUSTER and
+ * CS_PLAN_DIRECT: 1..16, at most K; CS_PLAN_DIRECT also needs
+ * ceil(K / cluster) <= 32, D <= 512 for float32 and D <= 1024 for bfloat16
+ * candidates) and ctas (CS_PLAN_STREAM: 1..B) may be 0 for the automatic
+ * choice.
  * Returns CS_ERR_BAD_PLAN when the plan cannot run these arguments (e.g.
  * CS_PLAN_STREAM or CS_PLAN_CLUSTER with D % 4 != 0 or unaligned pointers).
  * The result equals the automatic plan's within float32 rounding.

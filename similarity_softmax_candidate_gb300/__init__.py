@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     CS_MAX_K,
     CS_PLAN_AUTO,
     CS_PLAN_CLUSTER,
+    CS_PLAN_DIRECT,
     CS_PLAN_GENERIC,
     CS_PLAN_STREAM,
     CSError,

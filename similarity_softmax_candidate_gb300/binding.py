@@ -18,8 +18,9 @@ import threading
 from . import _build
 
 CS_MAX_K = 255
-CS_PLAN_AUTO, CS_PLAN_STREAM, CS_PLAN_CLUSTER, CS_PLAN_GENERIC = 0, 1, 2, 3
-PLAN_NAMES = {CS_PLAN_STREAM: "stream", CS_PLAN_CLUSTER: "cluster", CS_PLAN_GENERIC: "generic"}
+CS_PLAN_AUTO, CS_PLAN_STREAM, CS_PLAN_CLUSTER, CS_PLAN_GENERIC, CS_PLAN_DIRECT = 0, 1, 2, 3, 4
+PLAN_NAMES = {CS_PLAN_STREAM: "stream", CS_PLAN_CLUSTER: "cluster", CS_PLAN_GENERIC: "generic",
+              CS_PLAN_DIRECT: "direct"}
 
 STATUS = {
     0: "CS_OK", 1: "CS_ERR_NULL_POINTER", 2: "CS_ERR_K_ZERO", 3: "CS_ERR_K_TOO_LARGE",

@@ -99,6 +99,16 @@ cudaError_t device_state(DeviceState** st) {
     return cudaSuccess;
 }
 
+int cached_direct_clusters(DeviceState& d, int cluster, int nq4, int normalize, int c_bf16) {
+    const long long key2 = (1ll << 62) | (nq4 << 2) | (c_bf16 << 1) | normalize;  // apart from the stream keys
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = d.clusters.find({cluster, key2});
+    if (it != d.clusters.end()) return it->second;
+    const int n = cs::max_active_direct_clusters(cluster, nq4, normalize, c_bf16);
+    d.clusters[{cluster, key2}] = n;
+    return n;
+}
+
 int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows) {
     const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) | (nq4 << 2) |
                            (c_bf16 << 1) | normalize;
@@ -227,6 +237,25 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     return true;
 }
 
+// DIRECT plan: G CTAs per question (one CTA if G == 1), each with at most
+// kDirectMaxRows rows of it, q and rows in registers (nq4 in 1, 2, 4; a
+// question's longest share for ragged batches is ceil(255 / G)).
+bool direct_plan(const Problem& p, int G, Plan* plan) {
+    const int nq4 = nq4_for(p);
+    if (!tma_eligible(p) || p.B > 65535 || G < 1 || G > cs::kMaxCluster || G > p.K) return false;
+    if (nq4 != 1 && nq4 != 2 && nq4 != 4) return false;
+    const int kmax = p.offsets ? CS_MAX_K : p.K;
+    if ((kmax + G - 1) / G > cs::kDirectMaxRows) return false;
+    plan->kind = cs::kPlanDirect;
+    plan->cluster = G;
+    plan->ctas = G * static_cast<int>(p.B);
+    plan->rows_per_stage = 0;
+    plan->stages = 0;
+    plan->nq4 = nq4;
+    plan->smem = 0;
+    return true;
+}
+
 void generic_plan(const Problem& p, Plan* plan) {
     plan->kind = cs::kPlanGeneric;
     plan->cluster = 1;
@@ -237,9 +266,22 @@ void generic_plan(const Problem& p, Plan* plan) {
     plan->smem = 0;
 }
 
-// Chooses (or checks a forced) plan. Returns a cs_status.
-int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas, Plan* plan) {
+// Chooses (or checks a forced) plan. Returns a cs_status. direct: the fused
+// readout may take the DIRECT plan (the unfused baseline's passes may not).
+int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas, Plan* plan, bool direct = true) {
     const bool aligned = tma_eligible(p);
+    if (kind == cs::kPlanDirect) {
+        if (!direct) return CS_ERR_BAD_PLAN;
+        if (cluster == 0) {  // fewest CTAs per question that keep each at most kDirectMaxRows rows
+            const int kmax = p.offsets ? CS_MAX_K : p.K;
+            cluster = 1;
+            while ((kmax + cluster - 1) / cluster > cs::kDirectMaxRows && cluster < cs::kMaxCluster) cluster *= 2;
+        }
+        if (!direct_plan(p, cluster, plan)) return CS_ERR_BAD_PLAN;
+        if (cluster > 1 && cached_direct_clusters(d, cluster, plan->nq4, p.normalize, p.c_bf16) < 1)
+            return CS_ERR_BAD_PLAN;
+        return CS_OK;
+    }
     if (kind == cs::kPlanGeneric) {
         generic_plan(p, plan);
         return CS_OK;
@@ -272,6 +314,18 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         while (G * 2 <= cs::kMaxCluster && G * 2 <= avg_k && (G * 2) * p.B <= d.sms &&
                q_bytes / (G * 2) >= kSplitMinBytes)
             G *= 2;
+        // Short questions (at most kDirectMaxRows rows per CTA): the DIRECT
+        // plan, one trip to memory and no ring.
+        if (direct) {
+            int g = G;
+            const int kmax = p.offsets ? CS_MAX_K : p.K;
+            while ((kmax + g - 1) / g > cs::kDirectMaxRows && g * 2 <= cs::kMaxCluster && g * 2 <= p.K &&
+                   (g * 2) * p.B <= d.sms)
+                g *= 2;
+            if (direct_plan(p, g, plan) &&
+                (g == 1 || cached_direct_clusters(d, g, plan->nq4, p.normalize, p.c_bf16) >= p.B))
+                return CS_OK;
+        }
         for (; G > 1; G /= 2) {
             if (cluster_plan(d, p, G, plan) &&
                 cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize, p.c_bf16, plan->rows_per_stage) >= p.B)
@@ -281,6 +335,19 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
     if (aligned && stream_plan(d, p, 0, plan)) return CS_OK;
     generic_plan(p, plan);
     return CS_OK;
+}
+
+// The fused readout under `plan`.
+int launch_fused(const Problem& p, const Plan& plan, cs_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (plan.kind == cs::kPlanGeneric)
+        e = cs::launch_generic(p, st);
+    else if (plan.kind == cs::kPlanDirect)
+        e = cs::launch_direct(p, plan, st);
+    else
+        e = cs::launch_stream(p, plan, p.normalize ? cs::kFusedCos : cs::kFusedDot, st);
+    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
 }
 
 int run(const float* Q, const void* C, long long B, int K, int D, int normalize, float scale, float temperature,
@@ -293,11 +360,7 @@ int run(const float* Q, const void* C, long long B, int K, int D, int normalize,
     Plan plan{};
     const int s = make_plan(*d, p, kind, cluster, ctas, &plan);
     if (s != CS_OK) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = plan.kind == cs::kPlanGeneric
-                              ? cs::launch_generic(p, st)
-                              : cs::launch_stream(p, plan, normalize ? cs::kFusedCos : cs::kFusedDot, st);
-    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+    return launch_fused(p, plan, stream);
 }
 
 bool overlaps(const void* a, unsigned long long abytes, const void* b, unsigned long long bbytes) {
@@ -331,11 +394,7 @@ int run_ragged(const float* Q, const void* C, const long long* offsets, long lon
     Plan plan{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
     if (s != CS_OK) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = plan.kind == cs::kPlanGeneric
-                              ? cs::launch_generic(p, st)
-                              : cs::launch_stream(p, plan, normalize ? cs::kFusedCos : cs::kFusedDot, st);
-    return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
+    return launch_fused(p, plan, stream);
 }
 
 // The unfused baseline: pass 1 stages one value per row in `staged`, pass 2
@@ -353,7 +412,7 @@ int run_unfused(const float* Q, const float* C, long long B, int K, int D, int n
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
     Problem p{Q, C, out, B, K, D, normalize, scale, temperature, staged, 0, nullptr, 0};
     Plan plan{};
-    const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
+    const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan, false);
     if (s != CS_OK) return s;
     if (plan.kind == cs::kPlanGeneric) return CS_ERR_BAD_PLAN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -403,7 +462,7 @@ int cs_score_candidates_batch(const float* Q, const float* C, int B, int K, int 
 int cs_score_candidates_batch_plan(const float* Q, const float* C, int B, int K, int D, int normalize, float scale,
                                    float temperature, float* out, cs_stream_t stream, int plan, int cluster,
                                    int ctas) {
-    if (plan < CS_PLAN_AUTO || plan > CS_PLAN_GENERIC) return CS_ERR_BAD_PLAN;
+    if (plan < CS_PLAN_AUTO || plan > CS_PLAN_DIRECT) return CS_ERR_BAD_PLAN;
     return run(Q, C, B, K, D, normalize, scale, temperature, out, stream, plan, cluster, ctas);
 }
 

@@ -51,7 +51,10 @@ struct Problem {
 // Bytes of one element of C.
 inline int c_elem_bytes(const Problem& p) { return p.c_bf16 ? 2 : 4; }
 
-enum PlanKind { kPlanAuto = 0, kPlanStream = 1, kPlanCluster = 2, kPlanGeneric = 3 };
+enum PlanKind { kPlanAuto = 0, kPlanStream = 1, kPlanCluster = 2, kPlanGeneric = 3, kPlanDirect = 4 };
+// DIRECT plan: at most this many rows of a question per CTA, q and rows
+// loaded into registers (chunks per lane nq4 in {1, 2, 4}).
+constexpr int kDirectMaxRows = 32;
 
 struct Plan {
     int kind;          // PlanKind
@@ -120,6 +123,10 @@ cudaError_t configure_device_kernels(int smem_optin);
 // Clusters of `cluster` CTAs with `smem` bytes each that fit on the device
 // at once (0 if none).
 int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows_per_stage);
+// DIRECT plan (fused modes only): grid (cluster, B), clusters of `cluster`
+// CTAs when cluster > 1; B <= 65535.
+cudaError_t launch_direct(const Problem& p, const Plan& plan, cudaStream_t stream);
+int max_active_direct_clusters(int cluster, int nq4, int normalize, int c_bf16);
 
 // Bounded-wait self-test: one wait that nothing completes, limit_ns long.
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);

@@ -818,6 +818,159 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     }
 }
 
+// ------------------------------------------------------------------ direct kernel
+
+// Short path for one or a few questions whose rows come to at most 32 per CTA
+// (DIRECT plan): no ring and no producer warps. CTA `rank` of a cluster of G
+// takes its share of question blockIdx.y; warp w owns rows w, w+8, w+16, w+24
+// of that share and loads them, and q, straight into registers with 16-byte
+// loads, all issued before any arithmetic, so the whole question costs one
+// trip to L2/HBM. Dots and squared norms are reduced as in the stream kernel
+// (packed FMAs, transposed butterfly), one warp takes the softmax of the
+// CTA's rows, and a cluster combines (max, sum) through distributed shared
+// memory exactly like the CLUSTER plan.
+constexpr int kDirectThreads = 256;
+constexpr int kDirectRowsPerWarp = 4;
+constexpr int kDirectRows = kDirectRowsPerWarp * (kDirectThreads / 32);  // 32
+
+template <int NQC, int MODE, typename T>
+__global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p, int G) {
+    constexpr int VPR = values_per_row(MODE);
+    constexpr int V = VPR * kDirectRowsPerWarp;
+    constexpr bool COS = cos_logits(MODE);
+    constexpr int QF4 = Elem<T>::kQF4;
+    __shared__ float tn[2 * kDirectRows];  // dots, then squared norms
+    __shared__ float2 xch[kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar;
+    __shared__ int give_up_flag;
+    volatile int* give_up = &give_up_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int D = p.D, DC = D / Elem<T>::kPerChunk;
+    const long long b = blockIdx.y;
+    const int rank = G > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&xbar), 1);
+        give_up_flag = 0;
+        fence_mbar_init();
+        if (G > 1) mbar_arrive_expect_tx(smem_u32(&xbar), 8u * G);
+    }
+    __syncthreads();
+    if (G > 1) cluster_arrive_release();  // "my barrier exists"; waited on before the first push
+
+    const QRows qr = question_rows(p, b, rank, G);
+    const int n = qr.n;
+    const bool skip = qr.bad || n > kDirectRows;  // the host never plans n > 32
+    if (threadIdx.x == 0 && qr.bad) atomicOr(&g_status, 4u);
+    if (threadIdx.x == 0 && n > kDirectRows) atomicOr(&g_status, 2u);
+
+    // q and this warp's rows, every load issued up front
+    const float4* q4 = reinterpret_cast<const float4*>(p.Q + b * D);
+    const bool q_ok = !skip && CS_IN_BOUNDS(q4, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ);
+    float4 qv[NQC * QF4];
+#pragma unroll
+    for (int j = 0; j < NQC; ++j) {
+        const int i = lane + 32 * j;
+#pragma unroll
+        for (int h = 0; h < QF4; ++h)
+            qv[j * QF4 + h] = q_ok && i < DC ? __ldg(q4 + i * QF4 + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint4 cv[kDirectRowsPerWarp][NQC];
+#pragma unroll
+    for (int m = 0; m < kDirectRowsPerWarp; ++m) {
+        const int r = warp + 8 * m;
+        const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(p.C) +
+                                                          static_cast<size_t>(qr.row0 + (r < n ? r : 0)) * D);
+        const bool ok = !skip && r < n &&
+                        CS_IN_BOUNDS(row, static_cast<long long>(D) * sizeof(T), p.C,
+                                     rows_total(p) * D * static_cast<long long>(sizeof(T)), kSiteGenericC);
+#pragma unroll
+        for (int j = 0; j < NQC; ++j) {
+            const int i = lane + 32 * j;
+            cv[m][j] = ok && i < DC ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    float qn = 1.f;
+    if (COS) {
+        float sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < NQC * QF4; ++j)
+            sq += qv[j].x * qv[j].x + qv[j].y * qv[j].y + qv[j].z * qv[j].z + qv[j].w * qv[j].w;
+        qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // each warp holds all of q: never summed across warps
+    }
+    const float a = logit_factor(qn, p.scale, p.temperature, COS);
+
+    // dot (and squared norm) of each row: two packed partial sums each
+    unsigned long long acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0ull;
+#pragma unroll
+    for (int m = 0; m < kDirectRowsPerWarp; ++m) {
+#pragma unroll
+        for (int j = 0; j < NQC; ++j) {
+            float4 c[QF4];
+            Elem<T>::widen(cv[m][j], c);
+#pragma unroll
+            for (int h = 0; h < QF4; ++h) {
+                const float4& q = qv[j * QF4 + h];
+                const unsigned long long c01 = pack2(c[h].x, c[h].y), c23 = pack2(c[h].z, c[h].w);
+                if (acc_dot(MODE)) {
+                    acc[VPR * m] = fma2(c01, pack2(q.x, q.y), acc[VPR * m]);
+                    acc[VPR * m] = fma2(c23, pack2(q.z, q.w), acc[VPR * m]);
+                }
+                if (acc_norm(MODE)) {
+                    acc[VPR * m + VPR - 1] = fma2(c01, c01, acc[VPR * m + VPR - 1]);
+                    acc[VPR * m + VPR - 1] = fma2(c23, c23, acc[VPR * m + VPR - 1]);
+                }
+            }
+        }
+    }
+    float v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) v[i] = unpack_lo(acc[i]) + unpack_hi(acc[i]);
+    int idx;
+    const float sum = transpose_reduce<V>(v, lane, &idx);
+    if ((lane & (32 / V - 1)) == 0) {
+        const int r = warp + 8 * (idx / VPR);
+        if (r < n && !skip) tn[(VPR == 2 && (idx & 1) ? kDirectRows : 0) + r] = sum;
+    }
+    __syncthreads();
+
+    if (G > 1) cluster_wait();  // every CTA of the cluster has initialised its barrier
+    if (warp == 0 && !skip) {
+        float z = -INFINITY;
+        if (lane < n) z = COS ? a * tn[lane] * rsqrtf(fmaxf(tn[kDirectRows + lane], kEps2)) : a * tn[lane];
+        float* dst = p.out + qr.row0;
+        const bool out_ok = CS_IN_BOUNDS(dst, n * 4ll, p.out, rows_total(p) * 4, kSiteOutCluster);
+        if (G == 1) {
+            float zz[1] = {z};
+            if (out_ok) softmax_store<1>(zz, n, dst, lane);
+        } else {
+            const float m = warp_max(z);
+            const float s = warp_sum(lane < n ? __expf(z - m) : 0.f);
+            if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
+                              peer_addr(&xbar, static_cast<uint32_t>(lane)));
+            const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
+            float mj = -INFINITY, sj = 0.f;
+            if (lane < G) {
+                const float2 x = xch[lane];
+                mj = x.x;
+                sj = x.y;
+            }
+            const float M = warp_max(mj);
+            const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
+            if (out_ok && lane < n) dst[lane] = ok ? __expf(z - M) * inv : __int_as_float(0x7fc00000);
+        }
+    }
+    if (G > 1) {
+        // Leave only when every CTA has received every pair (none in flight
+        // into a CTA that has exited).
+        __syncwarp();
+        cluster_arrive_release();
+        cluster_wait();
+    }
+}
+
 // ------------------------------------------------------------------ generic kernel
 
 // One CTA per question, one warp per candidate row, scalar coalesced loads:
@@ -1052,6 +1205,64 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
     return cudaErrorInvalidValue;
 }
 
+template <int MODE, typename T>
+const void* direct_fn_m(int nqc) {
+    switch (nqc) {
+        case 1: return reinterpret_cast<const void*>(direct_kernel<1, MODE, T>);
+        case 2: return reinterpret_cast<const void*>(direct_kernel<2, MODE, T>);
+        case 4: return reinterpret_cast<const void*>(direct_kernel<4, MODE, T>);
+    }
+    return nullptr;
+}
+
+const void* direct_fn_for(int nqc, int normalize, int c_bf16) {
+    if (c_bf16) return normalize ? direct_fn_m<kFusedCos, uint16_t>(nqc) : direct_fn_m<kFusedDot, uint16_t>(nqc);
+    return normalize ? direct_fn_m<kFusedCos, float>(nqc) : direct_fn_m<kFusedDot, float>(nqc);
+}
+
+cudaError_t launch_direct(const Problem& p, const Plan& plan, cudaStream_t stream) {
+    const void* f = direct_fn_for(plan.nq4, p.normalize, p.c_bf16);
+    if (!f || p.B > 65535 || plan.cluster < 1 || plan.cluster > kMaxCluster) return cudaErrorInvalidValue;
+    int G = plan.cluster;
+    void* args[] = {const_cast<Problem*>(&p), &G};
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(G), static_cast<unsigned>(p.B), 1);
+    cfg.blockDim = dim3(kDirectThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    if (G > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(G);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, f, args);
+}
+
+int max_active_direct_clusters(int cluster, int nq4, int normalize, int c_bf16) {
+    const void* f = direct_fn_for(nq4, normalize, c_bf16);
+    if (!f) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+    cfg.blockDim = dim3(kDirectThreads, 1, 1);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
     selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);
     return cudaGetLastError();
@@ -1080,6 +1291,13 @@ cudaError_t launch_generic(const Problem& p, cudaStream_t stream) {
 }
 
 cudaError_t configure_device_kernels(int smem_optin) {
+    for (int nqc : {1, 2, 4})
+        for (int cos = 0; cos < 2; ++cos)
+            for (int bf = 0; bf < 2; ++bf) {
+                const cudaError_t e =
+                    cudaFuncSetAttribute(direct_fn_for(nqc, cos, bf), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
     const int nq4s[5] = {1, 2, 4, 8, 0};
     for (int bf = 0; bf < 2; ++bf) {
         for (int m = kFusedCos; m <= kStagedCos; ++m) {

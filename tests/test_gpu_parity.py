@@ -126,7 +126,15 @@ PLANS = [
     ("cluster_8", binding.CS_PLAN_CLUSTER, 8, 0),
     ("cluster_16", binding.CS_PLAN_CLUSTER, 16, 0),
     ("generic", binding.CS_PLAN_GENERIC, 0, 0),
+    ("direct_auto", binding.CS_PLAN_DIRECT, 0, 0),
+    ("direct_1", binding.CS_PLAN_DIRECT, 1, 0),
+    ("direct_3", binding.CS_PLAN_DIRECT, 3, 0),
+    ("direct_8", binding.CS_PLAN_DIRECT, 8, 0),
+    ("direct_16", binding.CS_PLAN_DIRECT, 16, 0),
 ]
+# shapes a DIRECT plan cannot take (rows per CTA above 32, or q too long for
+# registers) must be refused, not run
+DIRECT_ELIGIBLE_D = 512
 
 
 @pytest.mark.parametrize("plan", PLANS, ids=[p[0] for p in PLANS])
@@ -138,6 +146,13 @@ def test_every_plan(cuda_lib, plan, normalize):
             continue
         wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 1000 + B * K + D)
         Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+        if kind == binding.CS_PLAN_DIRECT:
+            g = cluster or next((x for x in (1, 2, 4, 8, 16) if -(-K // x) <= 32), 16)
+            eligible = D % 4 == 0 and D <= DIRECT_ELIGIBLE_D and -(-K // g) <= 32 and g <= K
+            if not eligible:
+                with pytest.raises(binding.CSError):
+                    binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, kind, cluster, ctas)
+                continue
         p = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, kind, cluster, ctas)
         torch.cuda.synchronize()
         assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0), f"{plan[0]} B={B} K={K} D={D}")
@@ -181,8 +196,11 @@ def test_automatic_plans(cuda_lib):
         C = torch.empty(B, K, D, device=DEV)
         return binding.cs_query_plan(Q, C, 1)
     one = plan(1, 255, 512)
-    assert one["plan"] == "cluster" and one["cluster"] >= 2, one
-    assert plan(1, 255, 2560)["plan"] == "cluster"
+    assert one["plan"] == "direct" and one["cluster"] >= 8, one  # at most 32 rows per CTA
+    assert plan(1, 5, 512)["plan"] == "direct" and plan(1, 5, 512)["cluster"] == 1
+    assert plan(8, 255, 512)["plan"] == "direct"
+    assert plan(1, 255, 2560)["plan"] == "cluster"  # q too long for registers: the ring
+    assert plan(1, 255, 1024)["plan"] == "cluster"
     big = plan(4096, 255, 512)
     assert big["plan"] == "stream" and big["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
     assert plan(2, 255, 511)["plan"] == "generic"
