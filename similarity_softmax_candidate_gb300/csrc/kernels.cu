@@ -171,8 +171,13 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// Arrive without ordering this thread's memory operations: the cluster
+// barrier phases here publish nothing but the mbarrier initialisation
+// (already ordered by fence.mbarrier_init.release.cluster) or only keep CTAs
+// alive until every push into them has landed (which their own mbarrier
+// wait has seen).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait() {
@@ -208,15 +213,11 @@ __device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
-__device__ __forceinline__ float unpack_lo(unsigned long long x) {
+// The two halves of a packed pair, added: the value its partial sums make.
+__device__ __forceinline__ float sum2(unsigned long long x) {
     float lo, hi;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-    return lo;
-}
-__device__ __forceinline__ float unpack_hi(unsigned long long x) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-    return hi;
+    return lo + hi;
 }
 __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
     unsigned long long d;
@@ -473,7 +474,7 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
         }
     }
 #pragma unroll
-    for (int i = 0; i < VPR * MR; ++i) v[i] = unpack_lo(acc[i]) + unpack_hi(acc[i]);
+    for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
 }
 
 // MR: most rows per stage this instantiation handles (kMaxRowsPerStage, or
@@ -549,7 +550,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     }
     __syncthreads();
     // Cluster: announce "my barriers exist"; waited on before the first push.
-    if (G > 1 && does_softmax(MODE)) cluster_arrive_release();
+    if (G > 1 && does_softmax(MODE)) cluster_arrive_relaxed();
 
     // Questions [qb, qe) of this CTA, and its rank among the CTAs of a question.
     long long qb, qe;
@@ -813,7 +814,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         __syncwarp();
         // Leave only when every CTA has received every pair: no push into a
         // CTA that has exited, none left in flight.
-        cluster_arrive_release();
+        cluster_arrive_relaxed();
         cluster_wait();
     }
 }
@@ -855,7 +856,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p,
         if (G > 1) mbar_arrive_expect_tx(smem_u32(&xbar), 8u * G);
     }
     __syncthreads();
-    if (G > 1) cluster_arrive_release();  // "my barrier exists"; waited on before the first push
+    if (G > 1) cluster_arrive_relaxed();  // "my barrier exists"; waited on before the first push
 
     const QRows qr = question_rows(p, b, rank, G);
     const int n = qr.n;
@@ -926,7 +927,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p,
     }
     float v[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) v[i] = unpack_lo(acc[i]) + unpack_hi(acc[i]);
+    for (int i = 0; i < V; ++i) v[i] = sum2(acc[i]);
     int idx;
     const float sum = transpose_reduce<V>(v, lane, &idx);
     if ((lane & (32 / V - 1)) == 0) {
@@ -966,7 +967,7 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p,
         // Leave only when every CTA has received every pair (none in flight
         // into a CTA that has exited).
         __syncwarp();
-        cluster_arrive_release();
+        cluster_arrive_relaxed();
         cluster_wait();
     }
 }
