@@ -237,15 +237,35 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     return true;
 }
 
-// DIRECT plan: G CTAs per question (one CTA if G == 1), each with at most
-// kDirectMaxRows rows of it, q and rows in registers (nq4 in 1, 2, 4; a
-// question's longest share for ragged batches is ceil(255 / G)).
-bool direct_plan(const Problem& p, int G, Plan* plan) {
+// The DIRECT kernel form these rows take: narrow (q in registers, nq4 in
+// 1, 2, 4, at most kDirectMaxRows rows per CTA) or wide (q in shared memory,
+// at most kDirectWideChunks 16-byte chunks of a row per lane, at most
+// kDirectWideMaxRows rows per CTA). Returns the chunks per lane the kernel is
+// built for (0: no DIRECT form) and the row limit.
+int direct_form(const Problem& p, int* max_rows) {
     const int nq4 = nq4_for(p);
-    if (!tma_eligible(p) || p.B > 65535 || G < 1 || G > cs::kMaxCluster || G > p.K) return false;
-    if (nq4 != 1 && nq4 != 2 && nq4 != 4) return false;
+    if (nq4 == 1 || nq4 == 2 || nq4 == 4) {
+        *max_rows = cs::kDirectMaxRows;
+        return nq4;
+    }
+    const long long dc = p.D / (16 / cs::c_elem_bytes(p));
+    if (dc <= 32ll * cs::kDirectWideChunks && p.D <= cs::kDirectWideMaxD) {
+        *max_rows = cs::kDirectWideMaxRows;
+        return cs::kDirectWideChunks;
+    }
+    *max_rows = 0;
+    return 0;
+}
+
+// DIRECT plan: G CTAs per question (one CTA if G == 1), each with at most
+// the form's row limit of it (a question's longest share for ragged batches
+// is ceil(255 / G)).
+bool direct_plan(const Problem& p, int G, Plan* plan) {
+    int max_rows = 0;
+    const int nq4 = direct_form(p, &max_rows);
+    if (!tma_eligible(p) || p.B > 65535 || G < 1 || G > cs::kMaxCluster || G > p.K || nq4 == 0) return false;
     const int kmax = p.offsets ? CS_MAX_K : p.K;
-    if ((kmax + G - 1) / G > cs::kDirectMaxRows) return false;
+    if ((kmax + G - 1) / G > max_rows) return false;
     plan->kind = cs::kPlanDirect;
     plan->cluster = G;
     plan->ctas = G * static_cast<int>(p.B);
@@ -272,10 +292,13 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
     const bool aligned = tma_eligible(p);
     if (kind == cs::kPlanDirect) {
         if (!direct) return CS_ERR_BAD_PLAN;
-        if (cluster == 0) {  // fewest CTAs per question that keep each at most kDirectMaxRows rows
+        if (cluster == 0) {  // fewest CTAs per question that keep each within the row limit
+            int max_rows = 0;
+            direct_form(p, &max_rows);
             const int kmax = p.offsets ? CS_MAX_K : p.K;
             cluster = 1;
-            while ((kmax + cluster - 1) / cluster > cs::kDirectMaxRows && cluster < cs::kMaxCluster) cluster *= 2;
+            while (max_rows > 0 && (kmax + cluster - 1) / cluster > max_rows && cluster < cs::kMaxCluster)
+                cluster *= 2;
         }
         if (!direct_plan(p, cluster, plan)) return CS_ERR_BAD_PLAN;
         if (cluster > 1 && cached_direct_clusters(d, cluster, plan->nq4, p.normalize, p.c_bf16) < 1)
@@ -316,10 +339,11 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
             G *= 2;
         // Short questions (at most kDirectMaxRows rows per CTA): the DIRECT
         // plan, one trip to memory and no ring.
-        if (direct) {
+        int max_rows = 0;
+        if (direct && direct_form(p, &max_rows) != 0) {
             int g = G;
             const int kmax = p.offsets ? CS_MAX_K : p.K;
-            while ((kmax + g - 1) / g > cs::kDirectMaxRows && g * 2 <= cs::kMaxCluster && g * 2 <= p.K &&
+            while ((kmax + g - 1) / g > max_rows && g * 2 <= cs::kMaxCluster && g * 2 <= p.K &&
                    (g * 2) * p.B <= d.sms)
                 g *= 2;
             if (direct_plan(p, g, plan) &&

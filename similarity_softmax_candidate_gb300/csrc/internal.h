@@ -53,8 +53,14 @@ inline int c_elem_bytes(const Problem& p) { return p.c_bf16 ? 2 : 4; }
 
 enum PlanKind { kPlanAuto = 0, kPlanStream = 1, kPlanCluster = 2, kPlanGeneric = 3, kPlanDirect = 4 };
 // DIRECT plan: at most this many rows of a question per CTA, q and rows
-// loaded into registers (chunks per lane nq4 in {1, 2, 4}).
+// loaded into registers (chunks per lane nq4 in {1, 2, 4}); the wide form
+// (long rows: q in shared memory) takes kDirectWideChunks 16-byte chunks of
+// a row per lane, at most kDirectWideMaxRows rows per CTA and D up to
+// kDirectWideMaxD.
 constexpr int kDirectMaxRows = 32;
+constexpr int kDirectWideChunks = 20;
+constexpr int kDirectWideMaxRows = 16;
+constexpr int kDirectWideMaxD = 5120;
 
 struct Plan {
     int kind;          // PlanKind

@@ -823,27 +823,33 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
 
 // Short path for one or a few questions whose rows come to at most 32 per CTA
 // (DIRECT plan): no ring and no producer warps. CTA `rank` of a cluster of G
-// takes its share of question blockIdx.y; warp w owns rows w, w+8, w+16, w+24
-// of that share and loads them, and q, straight into registers with 16-byte
-// loads, all issued before any arithmetic, so the whole question costs one
-// trip to L2/HBM. Dots and squared norms are reduced as in the stream kernel
-// (packed FMAs, transposed butterfly), one warp takes the softmax of the
-// CTA's rows, and a cluster combines (max, sum) through distributed shared
-// memory exactly like the CLUSTER plan.
+// takes its share of question blockIdx.y; warp w owns rows w, w+8, ... of
+// that share and loads them straight into registers with 16-byte loads, all
+// issued before any arithmetic, so the whole question costs one trip to
+// L2/HBM. q sits in registers (narrow form: RPW = 4 rows per warp, D up to
+// 32 * NQC chunks) or, for long rows, once per CTA in shared memory (wide
+// form: RPW = 2, QSH). Dots and squared norms are reduced as in the stream
+// kernel (packed FMAs, transposed butterfly), one warp takes the softmax of
+// the CTA's rows, and a cluster combines (max, sum) through distributed
+// shared memory exactly like the CLUSTER plan.
 constexpr int kDirectThreads = 256;
-constexpr int kDirectRowsPerWarp = 4;
-constexpr int kDirectRows = kDirectRowsPerWarp * (kDirectThreads / 32);  // 32
+constexpr int kDirectRows = kDirectMaxRows;     // rows per CTA, narrow form (4 per warp)
+constexpr int kDirectWideNqc = kDirectWideChunks;  // wide form: chunks per lane (D <= 2560 float32, 5120 bfloat16)
+constexpr int kDirectMaxQ4 = kDirectWideMaxD / 4;  // wide form: q in shared memory, float4s
+static_assert(kDirectWideMaxRows == 2 * (kDirectThreads / 32), "wide form: 2 rows per warp");
 
-template <int NQC, int MODE, typename T>
-__global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p, int G) {
+template <int NQC, int MODE, typename T, int RPW, bool QSH>
+__global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem p, int G) {
     constexpr int VPR = values_per_row(MODE);
-    constexpr int V = VPR * kDirectRowsPerWarp;
+    constexpr int V = VPR * RPW;
+    constexpr int ROWS = RPW * (kDirectThreads / 32);
     constexpr bool COS = cos_logits(MODE);
     constexpr int QF4 = Elem<T>::kQF4;
     __shared__ float tn[2 * kDirectRows];  // dots, then squared norms
     __shared__ float2 xch[kMaxCluster];
     __shared__ __align__(8) uint64_t xbar;
     __shared__ int give_up_flag;
+    __shared__ float4 qsh[QSH ? kDirectMaxQ4 : 1];
     volatile int* give_up = &give_up_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int D = p.D, DC = D / Elem<T>::kPerChunk;
@@ -855,29 +861,17 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p,
         fence_mbar_init();
         if (G > 1) mbar_arrive_expect_tx(smem_u32(&xbar), 8u * G);
     }
-    __syncthreads();
-    if (G > 1) cluster_arrive_relaxed();  // "my barrier exists"; waited on before the first push
 
     const QRows qr = question_rows(p, b, rank, G);
     const int n = qr.n;
-    const bool skip = qr.bad || n > kDirectRows;  // the host never plans n > 32
+    const bool skip = qr.bad || n > ROWS || (QSH && D > 4 * kDirectMaxQ4);  // the host plans neither
     if (threadIdx.x == 0 && qr.bad) atomicOr(&g_status, 4u);
-    if (threadIdx.x == 0 && n > kDirectRows) atomicOr(&g_status, 2u);
+    if (threadIdx.x == 0 && !qr.bad && skip) atomicOr(&g_status, 2u);
 
-    // q and this warp's rows, every load issued up front
-    const float4* q4 = reinterpret_cast<const float4*>(p.Q + b * D);
-    const bool q_ok = !skip && CS_IN_BOUNDS(q4, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ);
-    float4 qv[NQC * QF4];
+    // this warp's rows, then q: every load issued before any arithmetic
+    uint4 cv[RPW][NQC];
 #pragma unroll
-    for (int j = 0; j < NQC; ++j) {
-        const int i = lane + 32 * j;
-#pragma unroll
-        for (int h = 0; h < QF4; ++h)
-            qv[j * QF4 + h] = q_ok && i < DC ? __ldg(q4 + i * QF4 + h) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    uint4 cv[kDirectRowsPerWarp][NQC];
-#pragma unroll
-    for (int m = 0; m < kDirectRowsPerWarp; ++m) {
+    for (int m = 0; m < RPW; ++m) {
         const int r = warp + 8 * m;
         const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(p.C) +
                                                           static_cast<size_t>(qr.row0 + (r < n ? r : 0)) * D);
@@ -890,13 +884,44 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p,
             cv[m][j] = ok && i < DC ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
+    const float4* q4 = reinterpret_cast<const float4*>(p.Q + b * D);
+    const bool q_ok = !skip && CS_IN_BOUNDS(q4, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ);
+    float4 qv[QSH ? 1 : NQC * QF4];
+    if constexpr (QSH) {
+        for (int i = threadIdx.x; i < D / 4; i += kDirectThreads)
+            qsh[i] = q_ok ? __ldg(q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NQC; ++j) {
+            const int i = lane + 32 * j;
+#pragma unroll
+            for (int h = 0; h < QF4; ++h)
+                qv[j * QF4 + h] = q_ok && i < DC ? __ldg(q4 + i * QF4 + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    __syncthreads();  // the mbarrier is initialised; q is in shared memory (wide form)
+    if (G > 1) cluster_arrive_relaxed();  // "my barrier exists"; waited on before the first push
+
+    // q's chunk (j, h) of this lane
+    auto qchunk = [&](int j, int h) -> float4 {
+        if constexpr (QSH) {
+            const int i = lane + 32 * j;
+            return i < DC ? qsh[i * QF4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            return qv[j * QF4 + h];
+        }
+    };
     float qn = 1.f;
     if (COS) {
         float sq = 0.f;
 #pragma unroll
-        for (int j = 0; j < NQC * QF4; ++j)
-            sq += qv[j].x * qv[j].x + qv[j].y * qv[j].y + qv[j].z * qv[j].z + qv[j].w * qv[j].w;
-        qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // each warp holds all of q: never summed across warps
+        for (int j = 0; j < NQC; ++j)
+#pragma unroll
+            for (int h = 0; h < QF4; ++h) {
+                const float4 x = qchunk(j, h);
+                sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+            }
+        qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // each warp covers all of q: never summed across warps
     }
     const float a = logit_factor(qn, p.scale, p.temperature, COS);
 
@@ -905,18 +930,21 @@ __global__ void __launch_bounds__(kDirectThreads) direct_kernel(const Problem p,
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0ull;
 #pragma unroll
-    for (int m = 0; m < kDirectRowsPerWarp; ++m) {
+    for (int j = 0; j < NQC; ++j) {
+        float4 q[QF4];
 #pragma unroll
-        for (int j = 0; j < NQC; ++j) {
+        for (int h = 0; h < QF4; ++h) q[h] = qchunk(j, h);
+#pragma unroll
+        for (int m = 0; m < RPW; ++m) {
             float4 c[QF4];
             Elem<T>::widen(cv[m][j], c);
 #pragma unroll
             for (int h = 0; h < QF4; ++h) {
-                const float4& q = qv[j * QF4 + h];
+                const unsigned long long q01 = pack2(q[h].x, q[h].y), q23 = pack2(q[h].z, q[h].w);
                 const unsigned long long c01 = pack2(c[h].x, c[h].y), c23 = pack2(c[h].z, c[h].w);
                 if (acc_dot(MODE)) {
-                    acc[VPR * m] = fma2(c01, pack2(q.x, q.y), acc[VPR * m]);
-                    acc[VPR * m] = fma2(c23, pack2(q.z, q.w), acc[VPR * m]);
+                    acc[VPR * m] = fma2(c01, q01, acc[VPR * m]);
+                    acc[VPR * m] = fma2(c23, q23, acc[VPR * m]);
                 }
                 if (acc_norm(MODE)) {
                     acc[VPR * m + VPR - 1] = fma2(c01, c01, acc[VPR * m + VPR - 1]);
@@ -1209,9 +1237,11 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
 template <int MODE, typename T>
 const void* direct_fn_m(int nqc) {
     switch (nqc) {
-        case 1: return reinterpret_cast<const void*>(direct_kernel<1, MODE, T>);
-        case 2: return reinterpret_cast<const void*>(direct_kernel<2, MODE, T>);
-        case 4: return reinterpret_cast<const void*>(direct_kernel<4, MODE, T>);
+        case 1: return reinterpret_cast<const void*>(direct_kernel<1, MODE, T, 4, false>);
+        case 2: return reinterpret_cast<const void*>(direct_kernel<2, MODE, T, 4, false>);
+        case 4: return reinterpret_cast<const void*>(direct_kernel<4, MODE, T, 4, false>);
+        case kDirectWideNqc:
+            return reinterpret_cast<const void*>(direct_kernel<kDirectWideNqc, MODE, T, 2, true>);
     }
     return nullptr;
 }
@@ -1292,7 +1322,7 @@ cudaError_t launch_generic(const Problem& p, cudaStream_t stream) {
 }
 
 cudaError_t configure_device_kernels(int smem_optin) {
-    for (int nqc : {1, 2, 4})
+    for (int nqc : {1, 2, 4, kDirectWideNqc})
         for (int cos = 0; cos < 2; ++cos)
             for (int bf = 0; bf < 2; ++bf) {
                 const cudaError_t e =

@@ -132,9 +132,15 @@ PLANS = [
     ("direct_8", binding.CS_PLAN_DIRECT, 8, 0),
     ("direct_16", binding.CS_PLAN_DIRECT, 16, 0),
 ]
-# shapes a DIRECT plan cannot take (rows per CTA above 32, or q too long for
-# registers) must be refused, not run
-DIRECT_ELIGIBLE_D = 512
+# shapes a DIRECT plan cannot take must be refused, not run: at most 32 rows
+# per CTA with q in registers (D <= 512), 16 with q in shared memory
+# (D <= 2560), float32 rows of whole 16-byte chunks
+
+
+def _direct_row_limit(D):
+    if D % 4:
+        return 0
+    return 32 if D <= 512 else 16 if D <= 2560 else 0
 
 
 @pytest.mark.parametrize("plan", PLANS, ids=[p[0] for p in PLANS])
@@ -147,8 +153,9 @@ def test_every_plan(cuda_lib, plan, normalize):
         wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 1000 + B * K + D)
         Q, C = wl.Q.to(DEV), wl.C.to(DEV)
         if kind == binding.CS_PLAN_DIRECT:
-            g = cluster or next((x for x in (1, 2, 4, 8, 16) if -(-K // x) <= 32), 16)
-            eligible = D % 4 == 0 and D <= DIRECT_ELIGIBLE_D and -(-K // g) <= 32 and g <= K
+            lim = _direct_row_limit(D)
+            g = cluster or next((x for x in (1, 2, 4, 8, 16) if lim and -(-K // x) <= lim), 16)
+            eligible = lim > 0 and -(-K // g) <= lim and g <= K
             if not eligible:
                 with pytest.raises(binding.CSError):
                     binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, kind, cluster, ctas)
@@ -199,8 +206,10 @@ def test_automatic_plans(cuda_lib):
     assert one["plan"] == "direct" and one["cluster"] >= 8, one  # at most 32 rows per CTA
     assert plan(1, 5, 512)["plan"] == "direct" and plan(1, 5, 512)["cluster"] == 1
     assert plan(8, 255, 512)["plan"] == "direct"
-    assert plan(1, 255, 2560)["plan"] == "cluster"  # q too long for registers: the ring
-    assert plan(1, 255, 1024)["plan"] == "cluster"
+    kev = plan(1, 255, 2560)  # q in shared memory: at most 16 rows per CTA
+    assert kev["plan"] == "direct" and kev["cluster"] == 16, kev
+    assert plan(1, 255, 1024)["plan"] == "direct"
+    assert plan(1, 255, 4096)["plan"] == "cluster"  # rows too long for registers: the ring
     big = plan(4096, 255, 512)
     assert big["plan"] == "stream" and big["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
     assert plan(2, 255, 511)["plan"] == "generic"
