@@ -171,6 +171,14 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     return r;
 }
 
+// Programmatic dependent launch. The kernels are launched so that they may
+// start while the previous kernel in the stream is still running; before
+// its first global-memory access each thread waits until that kernel has
+// completed and its writes are visible (so inputs it produced are read
+// intact), and each CTA at once lets the next launch be scheduled.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Arrive without ordering this thread's memory operations: the cluster
 // barrier phases here publish nothing but the mbarrier initialisation
 // (already ordered by fence.mbarrier_init.release.cluster) or only keep CTAs
@@ -533,6 +541,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         fence_mbar_init();
         __syncwarp();
         if (lane == 0 && G > 1 && does_softmax(MODE)) mbar_arrive_expect_tx(smem_u32(xbar), 8u * G);
+    }
+    wait_prior_grid();  // no global access before this point
+    allow_next_grid();
+    if (warp == 0) {
         if (G == 1 && p.offsets) {
             // Ragged STREAM plan: CTA c takes the questions whose first row
             // falls in [c T / grid, (c+1) T / grid), T = total rows. CTA 0
@@ -861,6 +873,8 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
         fence_mbar_init();
         if (G > 1) mbar_arrive_expect_tx(smem_u32(&xbar), 8u * G);
     }
+    wait_prior_grid();  // no global access before this point
+    allow_next_grid();
 
     const QRows qr = question_rows(p, b, rank, G);
     const int n = qr.n;
@@ -1115,22 +1129,23 @@ __global__ void selftest_bounds_kernel() {
 template <int NQC, int MODE, typename T, int MR>
 cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kStreamThreads, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (plan.kind == kPlanCluster) {
         cfg.gridDim = dim3(static_cast<unsigned>(plan.cluster), static_cast<unsigned>(a.p.B), 1);
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(plan.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     } else {
         cfg.gridDim = dim3(static_cast<unsigned>(plan.ctas), 1, 1);
-        cfg.attrs = nullptr;
-        cfg.numAttrs = 0;
     }
     return cudaLaunchKernelEx(&cfg, stream_kernel<NQC, MODE, T, MR>, a);
 }
@@ -1257,18 +1272,21 @@ cudaError_t launch_direct(const Problem& p, const Plan& plan, cudaStream_t strea
     int G = plan.cluster;
     void* args[] = {const_cast<Problem*>(&p), &G};
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(static_cast<unsigned>(G), static_cast<unsigned>(p.B), 1);
     cfg.blockDim = dim3(kDirectThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (G > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(G);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(G);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelExC(&cfg, f, args);
 }

@@ -292,3 +292,34 @@ def test_nondefault_stream(cuda_lib):
 def test_no_wait_gave_up(cuda_lib):
     torch.cuda.synchronize()
     assert binding.cs_device_status() == 0
+
+
+@pytest.mark.parametrize("B", [1, 200], ids=["direct", "stream"])
+def test_back_to_back_calls_see_the_previous_kernels_writes(cuda_lib, B):
+    """The kernels may start while the previous kernel in the stream is still
+    running (programmatic dependent launch) and wait for it before touching
+    memory: a call whose query is the previous call's output, and a call
+    right after an in-stream overwrite of C, must see the new values."""
+    K, D = 4, 4
+    g = torch.Generator(device="cpu")
+    g.manual_seed(77 + B)
+    Q1 = torch.randn(B, D, generator=g).to(DEV)
+    C1 = torch.randn(B, K, D, generator=g).to(DEV)
+    C2 = torch.randn(B, K, D, generator=g).to(DEV)
+    p1 = torch.empty(B, K, device=DEV)
+    p2 = torch.empty(B, K, device=DEV)
+    for _ in range(3):  # repeated, so later rounds overlap earlier launches
+        binding.cs_score_candidates_batch(Q1, C1, 1, 3.0, 1.0, out=p1)
+        binding.cs_score_candidates_batch(p1, C2, 0, 2.0, 1.0, out=p2)  # q = the previous output
+    torch.cuda.synchronize()
+    ref1 = oracle_probs(Q1.cpu(), C1.cpu(), 1, 3.0, 1.0)
+    assert_parity(p1, ref1, "first call")
+    ref2 = oracle_probs(p1.cpu(), C2.cpu(), 0, 2.0, 1.0)
+    assert_parity(p2, ref2, "second call reads the first call's output")
+    Cnew = torch.randn(B, K, D, generator=g).to(DEV)
+    C1.copy_(Cnew)  # an in-stream kernel writes C just before the call
+    binding.cs_score_candidates_batch(Q1, C1, 1, 3.0, 1.0, out=p1)
+    torch.cuda.synchronize()
+    assert_parity(p1, oracle_probs(Q1.cpu(), Cnew.cpu(), 1, 3.0, 1.0), "call after an in-stream overwrite")
+    plan = binding.cs_query_plan(Q1, C1, 1)["plan"]
+    assert plan == ("direct" if B == 1 else "stream"), plan
