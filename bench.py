@@ -654,9 +654,11 @@ def single_shape(cs, workloads, dev, name, calls, warmup):
     out = torch.empty(B, k, device=dev)
     s = torch.cuda.current_stream(dev)
 
+    q0, c0, o0 = wl.Q[0], wl.C[0], out[0]  # views made once, outside the timed calls
+
     def call():
         if B == 1:
-            cs.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=out[0], stream=s)
+            cs.cs_score_candidates(q0, c0, normalize, wl.scale, 1.0, out=o0, stream=s)
         else:
             cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=s)
 
@@ -685,9 +687,11 @@ def latency_table(cs, workloads, dev, calls):
         out = torch.empty(B, k, device=dev)
         s = torch.cuda.current_stream(dev)
 
+        q0, c0, o0 = wl.Q[0], wl.C[0], out[0]  # views made once, outside the timed calls
+
         def call():
             if B == 1:
-                cs.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=out[0], stream=s)
+                cs.cs_score_candidates(q0, c0, normalize, wl.scale, 1.0, out=o0, stream=s)
             else:
                 cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=s)
 

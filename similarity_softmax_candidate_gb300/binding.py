@@ -50,6 +50,9 @@ def library() -> ctypes.CDLL:
     """The loaded library with argument types declared. Raises RuntimeError
     if it has not been built (call ``_build.build_library()``)."""
     global _lib
+    lib = _lib
+    if lib is not None:  # loaded: no lock on the per-call path
+        return lib
     with _lock:
         if _lib is not None:
             return _lib
