@@ -68,7 +68,8 @@ def test_ragged_bad_offsets_are_skipped_and_flagged(cuda_lib):
     out keep their old contents, the other questions are scored, and the
     device status word says so. The kernel checks each question's range
     before touching it, so no access leaves the buffers."""
-    for B, D in ((6, 512), (200, 512), (4, 20)):  # cluster, stream and scalar plans
+    # DIRECT, CLUSTER (rows too long for the DIRECT kernel), STREAM and scalar plans
+    for B, D in ((6, 512), (3, 4100), (200, 512), (5, 513)):
         wl = workloads.ragged(B, D, 1, 14.2857, 77 + B, "cpu", kmin=1, kmax=40)
         off = wl.offsets.clone()
         bad = B // 2
