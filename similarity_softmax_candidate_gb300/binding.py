@@ -168,10 +168,20 @@ def _check(t, name, ndim, dtype=None):
     return t.data_ptr()
 
 
-def _stream_handle(stream, device):
+def _current_raw_stream(device):
+    """cudaStream_t of torch's current stream on `device`. torch's raw-stream
+    accessor (the one Triton launches on) skips building a Stream object,
+    ~2 us per call; the public API is the fallback."""
     import torch
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device.index if device.index is not None else torch.cuda.current_device())
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _stream_handle(stream, device):
     if stream is None:
-        return torch.cuda.current_stream(device).cuda_stream
+        return _current_raw_stream(device)
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream

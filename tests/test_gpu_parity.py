@@ -323,3 +323,17 @@ def test_back_to_back_calls_see_the_previous_kernels_writes(cuda_lib, B):
     assert_parity(p1, oracle_probs(Q1.cpu(), Cnew.cpu(), 1, 3.0, 1.0), "call after an in-stream overwrite")
     plan = binding.cs_query_plan(Q1, C1, 1)["plan"]
     assert plan == ("direct" if B == 1 else "stream"), plan
+
+
+def test_calls_without_a_stream_use_torchs_current_stream(cuda_lib):
+    """stream=None means torch's current stream on the tensors' device, also
+    inside `with torch.cuda.stream(...)`."""
+    dev = torch.device(DEV)
+    side = torch.cuda.Stream(dev)
+    assert binding._stream_handle(None, dev) == torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.stream(side):
+        assert binding._stream_handle(None, dev) == side.cuda_stream
+        wl = workloads.random_case(2, 9, 64, 1, 3.0, 88, DEV)
+        p = binding.cs_score_candidates_batch(wl.Q, wl.C, 1, 3.0, 1.0)
+    side.synchronize()
+    assert_parity(p, oracle_probs(wl.Q, wl.C, 1, 3.0, 1.0), "call on a side stream")
