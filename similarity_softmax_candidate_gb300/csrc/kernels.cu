@@ -27,7 +27,16 @@
 //         to (local max, local sum of exp) and pushes the pair into every
 //         peer's shared memory with st.async, completing on the peer's
 //         mbarrier, so one question uses up to 16 SMs.
+//     Dots and norms accumulate as packed float32 pairs (fma.rn.f32x2);
+//     plans of at most 2 rows per stage run a short-stage build.
+//   * direct_kernel -- DIRECT plan, one or a few short questions: one CTA or
+//     cluster per question, at most 32 rows per CTA (16 for long rows), q
+//     and the rows loaded straight into registers (q in shared memory for
+//     long rows), one trip to memory, the same cluster exchange.
 //   * generic_kernel -- scalar loads, any D and any alignment.
+// The stream and direct kernels are launched with programmatic dependent
+// launch: they may start while the previous kernel runs and wait for it
+// (griddepcontrol.wait) before their first global access.
 //   * the unfused baseline (PR #69, "What it is worth": a separate norm pass
 //     and a scoring block that loads the norm from a staged array) reuses
 //     stream_kernel: pass 1 writes one value per row (the norm, or for the dot
