@@ -122,12 +122,40 @@ def _traffic_from_profile(kernel_src_sha):
         return None
 
 
+def _strip_comments(src):
+    """C/C++ source without its comments (string and character literals
+    kept), blank lines and trailing blanks: a comment-only edit leaves the
+    code, and so its fingerprint, alone."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = ("".join(out)).splitlines()
+    return "\n".join(line.rstrip() for line in lines if line.strip())
+
+
 def _kernel_sha():
+    """Fingerprint of the streaming kernel's code (kernels.cu, internal.h,
+    abi.cpp without comments), matched against the committed ncu summary."""
     import hashlib
     h = hashlib.sha256()
     for name in ("kernels.cu", "internal.h", "abi.cpp"):
-        with open(os.path.join(_ROOT, "similarity_softmax_candidate_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(_ROOT, "similarity_softmax_candidate_gb300", "csrc", name)) as f:
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()
 
 
