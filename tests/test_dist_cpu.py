@@ -84,3 +84,16 @@ def test_oracle_pool_counts_every_worker():
     assert done == 2 * 3 * 2
     assert wall > 0.0
     assert bench._host_cores() >= 1
+
+
+def test_kernel_fingerprint_ignores_comments_only():
+    """The bench matches its ncu summary by a fingerprint of the kernel code:
+    comments and blank lines do not change it, code does."""
+    sys.path.insert(0, ROOT)
+    import bench
+    a = 'int x = 1; // note\n/* block\n comment */\n\nchar* s = "a // b";\n'
+    b = 'int x = 1;\n\nchar* s = "a // b"; /* other note */\n'
+    c = 'int x = 2;\nchar* s = "a // b";\n'
+    assert bench._strip_comments(a) == bench._strip_comments(b) == 'int x = 1;\nchar* s = "a // b";'
+    assert bench._strip_comments(c) != bench._strip_comments(a)
+    assert len(bench._kernel_sha()) == 64
