@@ -430,12 +430,19 @@ struct StreamArgs {
 // registers (NQC > 0: qv holds the q float4s of those chunks) or from shared
 // memory (NQC == 0, large D). With two values per row (fused cosine)
 // v[2r] = c_r . q and v[2r + 1] = c_r . c_r; with one, v[r] = c_r . q, or
-// c_r . c_r for the norm pass.
-template <int NQC, int MODE, typename T, int MR>
+// c_r . c_r for the norm pass. release() is called once, as soon as the
+// stage's shared memory is no longer needed: for the modes that accumulate
+// norms (twice the arithmetic of a dot), when the stage fits in registers
+// (q in registers and at most kEarlyReleaseChunks 16-byte chunks per lane),
+// every row is loaded first, so the slot goes back to the producer before
+// the arithmetic; otherwise after the last row.
+constexpr int kEarlyReleaseChunks = 16;  // 64 registers of staged rows at most
+
+template <int NQC, int MODE, typename T, int MR, typename Release>
 __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr, int DC,
                                            const float4 (&qv)[(NQC > 0 ? NQC : 1) * Elem<T>::kQF4],
                                            const float4* __restrict__ q4, int lane,
-                                           float (&v)[values_per_row(MODE) * MR]) {
+                                           float (&v)[values_per_row(MODE) * MR], Release&& release) {
     constexpr int VPR = values_per_row(MODE);
     constexpr int QF4 = Elem<T>::kQF4;
     // Each value accumulates as two partial sums (even and odd elements of
@@ -456,7 +463,32 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
             n = fma2(c23, c23, n);
         }
     };
-    if constexpr (NQC > 0) {
+    if constexpr (NQC > 0 && MR * NQC <= kEarlyReleaseChunks && acc_norm(MODE)) {
+        uint4 cr[MR][NQC];
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+#pragma unroll
+            for (int j = 0; j < NQC; ++j) {
+                const int i = lane + 32 * j;
+                cr[r][j] = r < nr && i < DC ? st[r * DC + i] : make_uint4(0u, 0u, 0u, 0u);
+            }
+        release();
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+            if (r < nr) {
+#pragma unroll
+                for (int j = 0; j < NQC; ++j) {
+                    const int i = lane + 32 * j;
+                    if (i < DC) {
+                        float4 c[QF4];
+                        Elem<T>::widen(cr[r][j], c);
+#pragma unroll
+                        for (int h = 0; h < QF4; ++h) accumulate(c[h], qv[j * QF4 + h], r);
+                    }
+                }
+            }
+        }
+    } else if constexpr (NQC > 0) {
 #pragma unroll
         for (int r = 0; r < MR; ++r) {
             if (r < nr) {
@@ -473,6 +505,7 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
                 }
             }
         }
+        release();
     } else {
 #pragma unroll
         for (int r = 0; r < MR; ++r) {
@@ -489,6 +522,7 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
                 }
             }
         }
+        release();
     }
 #pragma unroll
     for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
@@ -728,8 +762,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
                 float v[V];
-                stage_dots<NQC, MODE, T, MR>(reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes),
-                                         nr, DC, qv, q4, lane, v);
+                stage_dots<NQC, MODE, T, MR>(
+                    reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes), nr, DC, qv, q4,
+                    lane, v, [&] {
+                        __syncwarp();  // every lane's reads of the slot are done
+                        if (lane == 0) mbar_arrive(bar_e);
+                    });
                 int idx;
                 const float sum = transpose_reduce<V>(v, lane, &idx);
                 if ((lane & (32 / V - 1)) == 0) {
@@ -743,8 +781,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                             p.staged[qr.row0 + k0 + r] = MODE == kRowNorm ? sqrtf(val) : val;
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_e);
                 slot += kConsumerWarps;
                 if (slot >= static_cast<uint32_t>(NS)) {
                     slot -= NS;
