@@ -43,10 +43,9 @@ constexpr int kTileM = 128;        // accumulator rows (TMEM lanes)
 constexpr int kTileK = 64;         // Din columns per ring stage: 128 bytes of bf16, one swizzle row
 constexpr int kMmaN = 256;         // N of one tcgen05.mma
 constexpr int kMmaK = 16;          // K of one tcgen05.mma (bf16)
-// Ring stages: 4 for the scoring kernel; 3 for the plain kernel, whose
-// shared memory also holds the output staging boxes.
-__host__ __device__ constexpr int proj_stages(int mode) { return mode == 1 ? 4 : 3; }
-constexpr int kMaxProjStages = 4;
+// Ring stages of 48 KB; the plain kernel's output boxes (32 KB) take the
+// room of the scoring kernel's query and logits.
+constexpr int kProjStages = 4;
 constexpr int kOutBox = 32;                    // output box: 32 rows x 32 float32 columns (128-byte rows)
 constexpr int kOutBoxBytes = kOutBox * kOutBox * 4;
 constexpr int kAccCols = 2 * kMmaN;  // two accumulators of kMmaN columns: all of tensor memory
@@ -259,11 +258,11 @@ __host__ __device__ inline ProjLayout proj_layout(int D, int mode) {
     L.a_bytes = kTileM * kTileK * 2;
     L.stage_bytes = L.a_bytes + kMmaN * kTileK * 2;
     L.ring = 0;
-    L.out = L.ring + proj_stages(mode) * L.stage_bytes;
+    L.out = L.ring + kProjStages * L.stage_bytes;
     L.q = L.out + (mode == 1 ? 0u : (kEpiThreads / 32) * 2u * kOutBoxBytes);
-    L.logits = L.q + static_cast<uint32_t>(D) * 4;
-    L.bars = L.logits + 2 * 256 * 4;
-    L.tmem = L.bars + (2 * kMaxProjStages + 4) * 8;
+    L.logits = L.q + (mode == 1 ? static_cast<uint32_t>(D) * 4 : 0u);  // q and logits: scoring kernel only
+    L.bars = L.logits + (mode == 1 ? 2u * 256u * 4u : 0u);
+    L.tmem = L.bars + (2 * kProjStages + 4) * 8;
     L.flag = L.tmem + 8;
     L.total = L.flag + 8 + 1024;  // + alignment slack for the base
     return L;
@@ -274,7 +273,6 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmP, const ProjArgs a) {
     extern __shared__ unsigned char smem_raw[];
-    constexpr int kProjStages = proj_stages(MODE);
     const int D = a.D, nk = a.Din / kTileK, nhalf = D / kMmaN;
     const ProjLayout L = proj_layout(D, MODE);
     const uint32_t raw = su32(smem_raw);
