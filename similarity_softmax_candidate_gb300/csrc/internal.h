@@ -175,6 +175,7 @@ enum BoundsSite : unsigned {
     kSiteStagedSoftmax = 14,     // unfused pass 2 (dot): staged similarities
     kSiteStagedSoftmaxOut = 15,
     kSitePeer = 16,        // cluster exchange slot in a peer CTA
+    kSitePrefetchC = 17,   // stream prologue: L2 prefetch of the first rows
     kSiteProjQ = 20,       // projected readout: projected query
     kSiteProjOut = 21,     // projected readout: probabilities
     kSiteSelftest = 99,

@@ -168,6 +168,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// Hint: fetch `bytes` (a multiple of 16, src 16-byte aligned) of global
+// memory into L2. It changes no value anyone reads (L2 is where global
+// memory is coherent), so it may be issued before the previous kernel's
+// writes are visible.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -585,7 +593,33 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         __syncwarp();
         if (lane == 0 && G > 1 && does_softmax(MODE)) mbar_arrive_expect_tx(smem_u32(xbar), 8u * G);
     }
-    wait_prior_grid();  // no global access before this point
+    // While the previous kernel in the stream may still be running: the
+    // stage-producer lanes ask L2 for the first ring's worth of this CTA's
+    // rows, so that its first copies after the wait are served from L2.
+    // (Ragged plans skip it: their rows depend on offsets, which may not be
+    // read before the wait.)
+    if (warp == kConsumerWarps && lane < kConsumerWarps && !p.offsets) {
+        long long row0, nrows;
+        if (G > 1) {
+            const QRows qr = question_rows(p, blockIdx.y, static_cast<int>(cluster_ctarank()), G);
+            row0 = qr.row0;
+            nrows = qr.n;
+        } else {
+            const int c = blockIdx.x;
+            row0 = (static_cast<long long>(c) * args.q_per_cta + min(c, args.q_rem)) * p.K;
+            nrows = static_cast<long long>(args.q_per_cta + (c < args.q_rem ? 1 : 0)) * p.K;
+        }
+        const long long rb = static_cast<long long>(D) * sizeof(T);  // a multiple of 16 (aligned plans)
+        const long long total = min(nrows, static_cast<long long>(NS) * R) * rb;
+        const long long piece = ((total + kConsumerWarps * 16 - 1) / (kConsumerWarps * 16)) * 16;
+        const long long off = lane * piece;
+        if (off < total) {
+            const uint32_t bytes = static_cast<uint32_t>(min(piece, total - off));
+            const unsigned char* src = reinterpret_cast<const unsigned char*>(Cg) + row0 * rb + off;
+            if (CS_IN_BOUNDS(src, bytes, p.C, rows_total(p) * rb, kSitePrefetchC)) bulk_prefetch_l2(src, bytes);
+        }
+    }
+    wait_prior_grid();  // no global access before this point (prefetch hints aside)
     allow_next_grid();
     if (warp == 0) {
         if (G == 1 && p.offsets) {
