@@ -515,6 +515,8 @@ def main():
         line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
     del wls, wl_cos, wl_dot
     torch.cuda.empty_cache()
+    if rank == 0 and not args.skip_extra:
+        line["extra"]["copy_ceiling"] = copy_ceiling(line["extra"]["hbm_gbs_step"] / world, achieved)
 
     if rank == 0 and not args.no_cpu:
         try:
@@ -828,6 +830,29 @@ def native_latency(B, K, D, normalize, calls):
         res["fused_over_unfused_direct"] = res["unfused_direct_us"] / res["direct_us"]
         return res
     except Exception as e:  # the Python-side numbers stand without it
+        return {"error": str(e)[:200]}
+
+
+def copy_ceiling(step_gbs, launch_gbs):
+    """The read ceiling of the streaming kernel's access pattern on this GPU
+    (cs_copy_ceiling: the same 152-CTA geometry, 12 KB stages, a 16-stage
+    ring, 8 issuing lanes, no arithmetic) over the workload's 8.6 GB, as one
+    launch and as the step's 4 launches; and the kernel's fraction of it."""
+    from similarity_softmax_candidate_gb300 import _build
+    try:
+        tool = _build.build_copy_ceiling_tool()
+        res = {"what": "bulk-copy stream, same geometry as the stream plan, no arithmetic (cs_copy_ceiling)"}
+        for launches in (1, B_TOTAL // CHUNK):
+            r = subprocess.run([tool, str(B_TOTAL * K * D * 4), "12288", "16", "8", str(launches)],
+                               capture_output=True, text=True, timeout=120)
+            if r.returncode != 0:
+                return {"error": (r.stderr.strip() or f"exit {r.returncode}")[-200:]}
+            res[f"gbs_{launches}_launch" + ("es" if launches > 1 else "")] = json.loads(r.stdout.strip())["gbs"]
+        four = res[f"gbs_{B_TOTAL // CHUNK}_launches"]
+        res["step_over_ceiling"] = step_gbs / four
+        res["launch_over_ceiling_one_launch"] = launch_gbs / res["gbs_1_launch"]
+        return res
+    except Exception as e:  # the kernel's own numbers stand without it
         return {"error": str(e)[:200]}
 
 

@@ -24,6 +24,11 @@ DEBUG_LIB_PATH = os.path.join(PKG, DEBUG_LIB_NAME)
 LATENCY_NAME = "cs_latency"
 LATENCY_PATH = os.path.join(PKG, LATENCY_NAME)
 LATENCY_SRC = os.path.join(CSRC, "latency_main.cu")
+# Read ceiling of the streaming access pattern (bulk copies, no arithmetic;
+# see csrc/copy_ceiling_main.cu). Standalone: it does not link the library.
+CEILING_NAME = "cs_copy_ceiling"
+CEILING_PATH = os.path.join(PKG, CEILING_NAME)
+CEILING_SRC = os.path.join(CSRC, "copy_ceiling_main.cu")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -88,23 +93,53 @@ def build_library(force: bool = False, verbose: bool = False, debug_bounds: bool
     return path
 
 
-def build_latency_tool(force: bool = False) -> str:
-    """Compile the native latency harness next to the library (linked to
-    it, found at run time through an $ORIGIN rpath)."""
+def _tool_jobs(force: bool):
+    """(path, staged output, nvcc command) of each native tool that needs
+    compiling: the latency harness (linked to the library, found at run time
+    through an $ORIGIN rpath) and the copy-ceiling program."""
+    jobs = []
+    if force or not os.path.exists(LATENCY_PATH) or \
+            os.path.getmtime(LATENCY_PATH) < max(os.path.getmtime(LATENCY_SRC), os.path.getmtime(LIB_PATH)):
+        staged = LATENCY_PATH + f".tmp{os.getpid()}"
+        jobs.append((LATENCY_PATH, staged,
+                     [_nvcc(), "-O2", "-std=c++17", *ARCH_FLAGS, "-I", INCLUDE, LATENCY_SRC, "-o", staged, "-L",
+                      PKG, "-lcandidate_scoring", "-Xlinker", "-rpath,$ORIGIN"]))
+    if force or not os.path.exists(CEILING_PATH) or os.path.getmtime(CEILING_PATH) < os.path.getmtime(CEILING_SRC):
+        staged = CEILING_PATH + f".tmp{os.getpid()}"
+        jobs.append((CEILING_PATH, staged, [_nvcc(), "-O2", "-std=c++17", *ARCH_FLAGS, CEILING_SRC, "-o", staged]))
+    return jobs
+
+
+def build_tools(force: bool = False) -> None:
+    """Compile the native tools next to the library, in parallel."""
     build_library()
-    if not force and os.path.exists(LATENCY_PATH) and \
-            os.path.getmtime(LATENCY_PATH) >= max(os.path.getmtime(LATENCY_SRC), os.path.getmtime(LIB_PATH)):
-        return LATENCY_PATH
-    staged = LATENCY_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), "-O2", "-std=c++17", *ARCH_FLAGS, "-I", INCLUDE, LATENCY_SRC, "-o", staged, "-L", PKG,
-           "-lcandidate_scoring", "-Xlinker", "-rpath,$ORIGIN"]
-    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout.decode(errors='replace')}")
-    os.replace(staged, LATENCY_PATH)
+    procs = [(path, staged, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT))
+             for path, staged, cmd in _tool_jobs(force)]
+    failed = []
+    for path, staged, cmd, pr in procs:
+        out, _ = pr.communicate()
+        if pr.returncode != 0:
+            failed.append(f"nvcc failed: {' '.join(cmd)}\n{out.decode(errors='replace')}")
+        else:
+            os.replace(staged, path)
+    if failed:
+        raise RuntimeError("\n".join(failed))
+
+
+def build_latency_tool(force: bool = False) -> str:
+    """The native latency harness (built with the other tools)."""
+    build_tools(force)
     return LATENCY_PATH
+
+
+def build_copy_ceiling_tool(force: bool = False) -> str:
+    """The copy-ceiling program (built with the other tools)."""
+    build_tools(force)
+    return CEILING_PATH
 
 
 if __name__ == "__main__":
     print(build_library(force=True, verbose=True))
-    print(build_latency_tool(force=True))
+    build_tools(force=True)
+    print(LATENCY_PATH)
+    print(CEILING_PATH)
