@@ -1058,6 +1058,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
     __syncthreads();
 
     if (G > 1) cluster_wait();  // every CTA of the cluster has initialised its barrier
+    bool arrived = false;  // warp-uniform: this warp has arrived at the closing cluster barrier
     if (warp == 0 && !skip) {
         float z = -INFINITY;
         if (lane < n) z = COS ? a * tn[lane] * rsqrtf(fmaxf(tn[kDirectRows + lane], kEps2)) : a * tn[lane];
@@ -1073,6 +1074,13 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
                 st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
                               peer_addr(&xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
+            // Every pair bound for this CTA has landed (or the wait gave up,
+            // after which the closing barrier still holds the CTA until all
+            // peers have arrived): arrive now, so that the barrier's round
+            // trip overlaps the rest of the softmax and the stores.
+            __syncwarp();
+            cluster_arrive_relaxed();
+            arrived = true;
             float mj = -INFINITY, sj = 0.f;
             if (lane < G) {
                 const float2 x = xch[lane];
@@ -1088,7 +1096,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
         // Leave only when every CTA has received every pair (none in flight
         // into a CTA that has exited).
         __syncwarp();
-        cluster_arrive_relaxed();
+        if (!arrived) cluster_arrive_relaxed();
         cluster_wait();
     }
 }
