@@ -94,6 +94,15 @@ def _peak_hbm():
         return 6800.0, "fallback"
 
 
+def _sm_max_mhz():
+    """Maximum SM clock in MHz (measured file, else the GB300's 2070)."""
+    try:
+        with open(os.path.join(_ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        return 2070.0
+
+
 def _peak_bf16():
     """Dense bf16 tensor peak in TFLOP/s: the measured cuBLAS burst figure
     (the projections are timed alone), else the recipe's fallback."""
@@ -661,11 +670,21 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
     hbm, hbm_src = _peak_hbm()
     flop = 2.0 * B * Kq * Din * Dp + 2.0 * B * Din * Dp
     peak, peak_src = _peak_bf16()
+    # Shared-memory bound of a one-SM tcgen05 kernel: each 128-row x 256-
+    # feature unit (Din deep) writes its A and W tiles into shared memory by
+    # TMA and the MMAs read them back once, 2 x (128 + 256) x Din x 2 bytes
+    # through a port of 32 banks x 4 bytes per clock.
+    smem_bytes_unit = 2 * (128 + 256) * Din * 2
+    flop_unit = 2.0 * 128 * 256 * Din
+    sm_mhz, sms = _sm_max_mhz(), torch.cuda.get_device_properties(dev).multi_processor_count
+    smem_bound = flop_unit / (smem_bytes_unit / 128.0) * sms * sm_mhz * 1e6 / 1e12
     return {"workload": f"{B} questions x K=255, Din=512 -> D=512, bf16 features and heads, cosine",
             "questions_per_s": B / (fused_ms / 1e3), "ms_per_call": fused_ms,
             "tflops": flop / (fused_ms / 1e3) / 1e12, "peak_tflops": peak,
             "frac": flop / (fused_ms / 1e3) / 1e12 / peak,
             "peak_source": peak_src,
+            "smem_bound": {"bytes_per_unit": smem_bytes_unit, "bytes_per_clock": 128, "sm_mhz": sm_mhz,
+                           "tflops": smem_bound, "frac": flop / (fused_ms / 1e3) / 1e12 / smem_bound},
             "composed_cublas_bf16_ms": composed_ms, "fused_over_composed": composed_ms / fused_ms,
             "project_rows": {"rows": B * Kq, "ms_per_call": rows_ms,
                              "tflops": 2.0 * B * Kq * Din * Dp / (rows_ms / 1e3) / 1e12,
