@@ -25,8 +25,11 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+# A test may point this wrapper at another build of an altered copy of the
+# source (tests/test_oracle_mutants.py plants mistakes that way, to show the
+# pins catch them); everything else uses the files next to this module.
+_SRC = os.environ.get("CS_ORACLE_SRC") or os.path.join(_HERE, "oracle.c")
+_LIB = os.environ.get("CS_ORACLE_LIB") or os.path.join(_HERE, "liboracle.so")
 
 #: The norm clamp of the cosine similarity. The page gives no value; each
 #: norm is clamped on its own at this floor (plainest cosine convention).
