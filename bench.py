@@ -388,6 +388,9 @@ def main():
     ap.add_argument("--chunk", type=int, default=CHUNK, help="questions per launch (default 4096)")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
                     help="profiling aid: time only the projected readout on B questions and print its record")
+    ap.add_argument("--plan-sweep", action="store_true",
+                    help="profiling aid: us per call of every plan the library offers, against the automatic "
+                         "choice, for B = 1 .. 152 questions of K=255, D=512 (CUDA-graph replays)")
     ap.add_argument("--only-shape", choices=[r[0] for r in PAGE_SHAPES], default=None,
                     help="profiling aid: W warm-up calls, then K back-to-back calls of one of the page's "
                          "small shapes; prints us per call and the plan")
@@ -414,6 +417,10 @@ def main():
     if args.only_shape:
         if rank == 0:
             print(json.dumps(single_shape(cs, workloads, dev, args.only_shape, args.steps, args.warmup)), flush=True)
+        return 0
+    if args.plan_sweep:
+        if rank == 0:
+            print(json.dumps(plan_sweep(cs, dev)), flush=True)
         return 0
     if args.only_projected:
         if rank == 0:
@@ -691,6 +698,68 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
                              "bound": "hbm", "gbs": rows_bytes / (rows_ms / 1e3) / 1e9,
                              "frac": rows_bytes / (rows_ms / 1e3) / 1e9 / hbm,
                              "peak_source": f"hbm_gbs ({hbm_src})"}}
+
+
+def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32):
+    """us per call, cosine K=255 D=512, of the automatic plan and of every
+    forced plan (STREAM; CLUSTER with 2..16 CTAs per question; DIRECT over 16
+    CTAs where it fits), each as n calls on consecutive slices of a
+    4096-question buffer (2.1 GB, so every call reads from HBM) captured in
+    one CUDA graph and replayed: device time per call, no host work."""
+    import torch
+    Bmax = 4096
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    C = torch.randn(Bmax, K, D, device=dev, generator=g)
+    Q = torch.randn(Bmax, D, device=dev, generator=g)
+    out = torch.empty(Bmax, K, device=dev)
+    plans = [("stream", cs.CS_PLAN_STREAM, 0)] + [(f"cluster{G}", cs.CS_PLAN_CLUSTER, G) for G in (2, 4, 8, 16)] + \
+        [("direct16", cs.CS_PLAN_DIRECT, 16)]
+
+    def timed(B, plan, G):
+        nsl = Bmax // B
+
+        def call(i):
+            s0 = (i % nsl) * B
+            if plan is None:
+                cs.cs_score_candidates_batch(Q[s0:s0 + B], C[s0:s0 + B], 1, 14.285714, 1.0, out=out[s0:s0 + B])
+            else:
+                cs.cs_score_candidates_batch_plan(Q[s0:s0 + B], C[s0:s0 + B], 1, 14.285714, 1.0, plan, G, 0,
+                                                  out=out[s0:s0 + B])
+        for i in range(4):
+            call(i)
+        torch.cuda.synchronize()
+        graph, st = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(graph, stream=st):
+                for i in range(n):
+                    call(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, 1e3 * a.elapsed_time(b) / n)
+        return best
+
+    rows = []
+    for B in Bs:
+        auto = cs.cs_query_plan(Q[:B], C[:B], 1)
+        row = {"B": B, "auto": f"{auto['plan']}{auto['cluster'] if auto['cluster'] > 1 else ''}",
+               "auto_us": timed(B, None, 0)}
+        for name, plan, G in plans:
+            try:
+                row[name + "_us"] = timed(B, plan, G)
+            except cs.CSError:
+                row[name + "_us"] = None
+        best = min(v for k, v in row.items() if k.endswith("_us") and k != "auto_us" and v is not None)
+        row["auto_over_best"] = row["auto_us"] / best
+        rows.append(row)
+    return {"plan_sweep": rows, "workload": "cosine, K=255, D=512, inputs in HBM (larger than L2 across the graph)"}
 
 
 def single_shape(cs, workloads, dev, name, calls, warmup):
