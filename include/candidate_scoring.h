@@ -183,7 +183,9 @@ int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,
 #define CS_PLAN_AUTO 0
 #define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions */
 #define CS_PLAN_CLUSTER 2  /* one thread-block cluster per question, rows split */
-#define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment */
+#define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment (one CTA per
+                              question, or a cluster of CTAs per question
+                              when there are few questions) */
 #define CS_PLAN_DIRECT 4   /* one CTA (or cluster) per short question: at most 32
                               rows per CTA, q and rows loaded straight into
                               registers, no shared-memory ring */
@@ -205,7 +207,9 @@ int cs_query_plan(const float *Q, const float *C, int B, int K, int D,
  * CS_PLAN_DIRECT: 1..16, at most K; CS_PLAN_DIRECT also needs
  * ceil(K / cluster) <= 32, D <= 512 for float32 and D <= 1024 for bfloat16
  * candidates) and ctas (CS_PLAN_STREAM: 1..B) may be 0 for the automatic
- * choice.
+ * choice. For CS_PLAN_GENERIC, cluster 0 or 1 means one CTA per question and
+ * 2..16 (at most K) spreads each question's rows over a cluster of that many
+ * CTAs.
  * Returns CS_ERR_BAD_PLAN when the plan cannot run these arguments (e.g.
  * CS_PLAN_STREAM or CS_PLAN_CLUSTER with D % 4 != 0 or unaligned pointers).
  * The result equals the automatic plan's within float32 rounding.

@@ -109,6 +109,16 @@ int cached_direct_clusters(DeviceState& d, int cluster, int nq4, int normalize, 
     return n;
 }
 
+int cached_generic_clusters(DeviceState& d, int cluster, int normalize, int c_bf16) {
+    const long long key2 = (3ll << 61) | (c_bf16 << 1) | normalize;  // apart from the DIRECT and stream keys
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = d.clusters.find({cluster, key2});
+    if (it != d.clusters.end()) return it->second;
+    const int n = cs::max_active_generic_clusters(cluster, normalize, c_bf16);
+    d.clusters[{cluster, key2}] = n;
+    return n;
+}
+
 int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows) {
     const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) | (nq4 << 2) |
                            (c_bf16 << 1) | normalize;
@@ -276,10 +286,26 @@ bool direct_plan(const Problem& p, int G, Plan* plan) {
     return true;
 }
 
-void generic_plan(const Problem& p, Plan* plan) {
+// Questions per cluster of the scalar plan for few questions: the largest
+// power of two that gives every warp at least one row, every CTA at least
+// kSplitMinBytes of rows and keeps all clusters on the GPU at once (1: a CTA
+// per question; always 1 for ragged batches).
+int generic_cluster_size(DeviceState& d, const Problem& p) {
+    if (p.offsets || p.B * 2 > d.sms || p.B > 65535) return 1;
+    const long long q_bytes = static_cast<long long>(cs::c_elem_bytes(p)) * p.K * p.D;
+    const int warps = cs::kGenericThreads / 32;
+    int G = 1;
+    while (G * 2 <= cs::kMaxCluster && G * 2 * warps <= p.K && (G * 2) * p.B <= d.sms &&
+           q_bytes / (G * 2) >= kSplitMinBytes)
+        G *= 2;
+    while (G > 1 && cached_generic_clusters(d, G, p.normalize, p.c_bf16) < p.B) G /= 2;
+    return G;
+}
+
+void generic_plan(const Problem& p, Plan* plan, int G = 1) {
     plan->kind = cs::kPlanGeneric;
-    plan->cluster = 1;
-    plan->ctas = static_cast<int>(p.B);
+    plan->cluster = G;
+    plan->ctas = G * static_cast<int>(p.B);
     plan->rows_per_stage = 0;
     plan->stages = 0;
     plan->nq4 = 0;
@@ -306,7 +332,11 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         return CS_OK;
     }
     if (kind == cs::kPlanGeneric) {
-        generic_plan(p, plan);
+        if (cluster < 0 || cluster > cs::kMaxCluster) return CS_ERR_BAD_PLAN;
+        if (cluster > 1 && (p.offsets || cluster > p.K || p.B > 65535 ||
+                            cached_generic_clusters(d, cluster, p.normalize, p.c_bf16) < 1))
+            return CS_ERR_BAD_PLAN;
+        generic_plan(p, plan, cluster > 1 ? cluster : 1);
         return CS_OK;
     }
     if (kind == cs::kPlanStream) {
@@ -357,7 +387,9 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         }
     }
     if (aligned && stream_plan(d, p, 0, plan)) return CS_OK;
-    generic_plan(p, plan);
+    // Rows the bulk copies cannot take: the scalar plan, each of few
+    // questions spread over a cluster.
+    generic_plan(p, plan, generic_cluster_size(d, p));
     return CS_OK;
 }
 
@@ -366,7 +398,7 @@ int launch_fused(const Problem& p, const Plan& plan, cs_stream_t stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (plan.kind == cs::kPlanGeneric)
-        e = cs::launch_generic(p, st);
+        e = cs::launch_generic(p, plan.cluster, st);
     else if (plan.kind == cs::kPlanDirect)
         e = cs::launch_direct(p, plan, st);
     else

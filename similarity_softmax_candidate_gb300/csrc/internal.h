@@ -112,7 +112,10 @@ enum StreamMode {
 // Launchers (kernels.cu). Each enqueues exactly one kernel on `stream` and
 // returns the launch status; none synchronizes or allocates.
 cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStream_t stream);
-cudaError_t launch_generic(const Problem& p, cudaStream_t stream);
+// G = 1: one CTA per question; G > 1: each question over a cluster of G CTAs
+// (uniform K, B <= 65535).
+cudaError_t launch_generic(const Problem& p, int G, cudaStream_t stream);
+int max_active_generic_clusters(int cluster, int normalize, int c_bf16);
 // Unfused baseline pass 2 (dot): softmax of scale * staged / temperature.
 cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream);
 

@@ -1103,26 +1103,43 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
 
 // ------------------------------------------------------------------ generic kernel
 
-// One CTA per question, one warp per candidate row, scalar coalesced loads:
-// any D, any alignment.
-template <bool COS, typename T>
-__global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem p) {
+// One CTA per question (G = 1), or each question's rows split over the G
+// CTAs of a thread-block cluster (G > 1, uniform K; the rows of CTA r are
+// r K / G .. (r + 1) K / G - 1) with the softmax combined through
+// distributed shared memory as in the DIRECT plan. One warp per candidate
+// row, scalar coalesced loads: any D, any alignment. CL: built for G > 1
+// (the one-CTA form carries none of the exchange, so it keeps its
+// registers, and its occupancy, low).
+template <bool COS, typename T, bool CL>
+__global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem p, int G) {
+    if constexpr (!CL) G = 1;
     __shared__ float lg[kLogitSlots];
+    __shared__ float2 xch[kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar;
+    __shared__ int give_up_flag;
+    volatile int* give_up = &give_up_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = kGenericThreads / 32;
-    const long long b = blockIdx.x;
-    const QRows qr = question_rows(p, b, 0, 1);
-    if (qr.bad) {
-        if (threadIdx.x == 0) atomicOr(&g_status, 4u);
-        return;
+    const long long b = G > 1 ? static_cast<long long>(blockIdx.y) : static_cast<long long>(blockIdx.x);
+    const int rank = G > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    if (G > 1) {
+        if (threadIdx.x == 0) {
+            mbar_init(smem_u32(&xbar), 1);
+            give_up_flag = 0;
+            fence_mbar_init();
+            mbar_arrive_expect_tx(smem_u32(&xbar), 8u * G);
+        }
+        cluster_arrive_relaxed();  // "my barrier exists"; waited on before the first push
     }
+    const QRows qr = question_rows(p, b, rank, G);
     const int K = qr.n, D = p.D;
     const float* __restrict__ q = p.Q + static_cast<size_t>(b) * D;
-    if (!CS_IN_BOUNDS(q, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ) ||
-        !CS_IN_BOUNDS(p.out + qr.row0, K * 4ll, p.out, rows_total(p) * 4, kSiteGenericOut))
-        return;
+    if (qr.bad && threadIdx.x == 0) atomicOr(&g_status, 4u);
+    const bool skip = qr.bad || !CS_IN_BOUNDS(q, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ) ||
+                      !CS_IN_BOUNDS(p.out + qr.row0, K * 4ll, p.out, rows_total(p) * 4, kSiteGenericOut);
+    if (!CL && skip) return;  // nothing waits on a CTA of its own; a cluster's CTAs all reach its barriers
     float qn = 1.f;
-    if (COS) {
+    if (COS && !skip) {
         float sq = 0.f;
         for (int d = lane; d < D; d += 32) {
             const float v = __ldg(q + d);
@@ -1131,7 +1148,7 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // whole norm per warp, never summed across warps
     }
     const float a = logit_factor(qn, p.scale, p.temperature, COS);
-    for (int k = warp; k < K; k += nwarps) {
+    for (int k = warp; k < K && !skip; k += nwarps) {
         const T* __restrict__ c = static_cast<const T*>(p.C) + static_cast<size_t>(qr.row0 + k) * D;
         if (!CS_IN_BOUNDS(c, D * static_cast<long long>(sizeof(T)), p.C, rows_total(p) * D * static_cast<long long>(sizeof(T)),
                           kSiteGenericC)) {
@@ -1159,11 +1176,51 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         if (lane == 0) lg[k] = COS ? a * t * rsqrtf(fmaxf(n, kEps2)) : a * t;
     }
     __syncthreads();
-    if (warp == 0) {
+    if (G > 1) cluster_wait();  // every CTA of the cluster has initialised its barrier
+    bool arrived = false;       // warp-uniform: this warp has arrived at the closing cluster barrier
+    if (warp == 0 && !skip) {
         float z[kSlotsPerLane];
 #pragma unroll
         for (int j = 0; j < kSlotsPerLane; ++j) z[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
-        softmax_store(z, K, p.out + qr.row0, lane);
+        float* dst = p.out + qr.row0;
+        if constexpr (!CL) {
+            softmax_store(z, K, dst, lane);
+        } else {
+            // this CTA's (max, sum of exp) to every CTA of the cluster
+            float m = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
+            m = warp_max(m);
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < kSlotsPerLane; ++j) s += lane + 32 * j < K ? __expf(z[j] - m) : 0.f;
+            s = warp_sum(s);
+            if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
+                              peer_addr(&xbar, static_cast<uint32_t>(lane)));
+            const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
+            // every pair bound for this CTA has landed (or the wait gave up)
+            __syncwarp();
+            cluster_arrive_relaxed();
+            arrived = true;
+            float mj = -INFINITY, sj = 0.f;
+            if (lane < G) {
+                const float2 x = xch[lane];
+                mj = x.x;
+                sj = x.y;
+            }
+            const float M = warp_max(mj);
+            const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
+#pragma unroll
+            for (int j = 0; j < kSlotsPerLane; ++j)
+                if (lane + 32 * j < K) dst[lane + 32 * j] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
+        }
+    }
+    if (G > 1) {
+        // Leave only when every CTA has received every pair.
+        __syncwarp();
+        if (!arrived) cluster_arrive_relaxed();
+        cluster_wait();
     }
 }
 
@@ -1410,23 +1467,59 @@ cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_generic(const Problem& p, cudaStream_t stream) {
-    const dim3 grid(static_cast<unsigned>(p.B)), block(kGenericThreads);
-    if (p.c_bf16) {
-        if (p.normalize)
-            generic_kernel<true, uint16_t><<<grid, block, 0, stream>>>(p);
-        else
-            generic_kernel<false, uint16_t><<<grid, block, 0, stream>>>(p);
-    } else {
-        if (p.normalize)
-            generic_kernel<true, float><<<grid, block, 0, stream>>>(p);
-        else
-            generic_kernel<false, float><<<grid, block, 0, stream>>>(p);
+void (*generic_fn_for(int normalize, int c_bf16, bool clustered))(Problem, int) {
+    if (clustered) {
+        if (c_bf16) return normalize ? generic_kernel<true, uint16_t, true> : generic_kernel<false, uint16_t, true>;
+        return normalize ? generic_kernel<true, float, true> : generic_kernel<false, float, true>;
     }
-    return cudaGetLastError();
+    if (c_bf16) return normalize ? generic_kernel<true, uint16_t, false> : generic_kernel<false, uint16_t, false>;
+    return normalize ? generic_kernel<true, float, false> : generic_kernel<false, float, false>;
+}
+
+cudaLaunchConfig_t generic_cluster_config(unsigned G, unsigned B, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, B, 1);
+    cfg.blockDim = dim3(kGenericThreads, 1, 1);
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+cudaError_t launch_generic(const Problem& p, int G, cudaStream_t stream) {
+    void (*f)(Problem, int) = generic_fn_for(p.normalize, p.c_bf16, G > 1);
+    if (G <= 1) {
+        f<<<dim3(static_cast<unsigned>(p.B)), dim3(kGenericThreads), 0, stream>>>(p, 1);
+        return cudaGetLastError();
+    }
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg =
+        generic_cluster_config(static_cast<unsigned>(G), static_cast<unsigned>(p.B), stream, attr);
+    return cudaLaunchKernelEx(&cfg, f, p, G);
+}
+
+int max_active_generic_clusters(int cluster, int normalize, int c_bf16) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = generic_cluster_config(static_cast<unsigned>(cluster), 1, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, generic_fn_for(normalize, c_bf16, true), &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 cudaError_t configure_device_kernels(int smem_optin) {
+    for (int cos = 0; cos < 2; ++cos)
+        for (int bf = 0; bf < 2; ++bf) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(generic_fn_for(cos, bf, true), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
     for (int nqc : {1, 2, 4, kDirectWideNqc})
         for (int cos = 0; cos < 2; ++cos)
             for (int bf = 0; bf < 2; ++bf) {

@@ -126,6 +126,9 @@ PLANS = [
     ("cluster_8", binding.CS_PLAN_CLUSTER, 8, 0),
     ("cluster_16", binding.CS_PLAN_CLUSTER, 16, 0),
     ("generic", binding.CS_PLAN_GENERIC, 0, 0),
+    ("generic_2", binding.CS_PLAN_GENERIC, 2, 0),
+    ("generic_5", binding.CS_PLAN_GENERIC, 5, 0),
+    ("generic_16", binding.CS_PLAN_GENERIC, 16, 0),
     ("direct_auto", binding.CS_PLAN_DIRECT, 0, 0),
     ("direct_1", binding.CS_PLAN_DIRECT, 1, 0),
     ("direct_3", binding.CS_PLAN_DIRECT, 3, 0),
@@ -188,6 +191,44 @@ def test_unaligned_and_odd_shapes_use_scalar_path(cuda_lib):
             binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_STREAM)
 
 
+@pytest.mark.parametrize("misaligned", [False, True], ids=["odd_d", "misaligned"])
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_scalar_plan_over_a_cluster(cuda_lib, misaligned, normalize):
+    """One or a few questions whose rows the bulk copies cannot take (odd D,
+    or pointers off a 16-byte boundary): the scalar plan spreads each
+    question over a cluster and combines the softmax across its CTAs. Its
+    result matches the oracle, and the one-CTA scalar plan's within float32
+    rounding, for every cluster size the planner or a caller may pick."""
+    for B, K, D in ((1, 255, 510 if not misaligned else 512), (3, 64, 511 if not misaligned else 256), (1, 16, 1001)):
+        wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 700 + B + K + D)
+        if misaligned:
+            Qb = torch.empty(B * D + 1, device=DEV)
+            Cb = torch.empty(B * K * D + 1, device=DEV)
+            Q, C = Qb[1:].view(B, D), Cb[1:].view(B, K, D)
+            Q.copy_(wl.Q)
+            C.copy_(wl.C)
+        else:
+            Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+        auto = binding.cs_query_plan(Q, C, normalize)
+        assert auto["plan"] == "generic", auto
+        ref = oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0)
+        one = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, binding.CS_PLAN_GENERIC, 1)
+        p = (binding.cs_score_candidates(Q[0], C[0], normalize, wl.scale, 1.0)[None]
+             if B == 1 else binding.cs_score_candidates_batch(Q, C, normalize, wl.scale, 1.0))
+        torch.cuda.synchronize()
+        assert_parity(p, ref, f"auto G={auto['cluster']} B={B} K={K} D={D}")
+        assert torch.allclose(p, one, rtol=0, atol=1e-6)
+        for G in (2, 4, 7, 16):
+            if G > K:
+                continue
+            q = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, binding.CS_PLAN_GENERIC, G)
+            torch.cuda.synchronize()
+            assert_parity(q, ref, f"G={G} B={B} K={K} D={D}")
+        with pytest.raises(binding.CSError):  # more CTAs than rows
+            binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, binding.CS_PLAN_GENERIC, 17)
+    assert binding.cs_device_status() == 0
+
+
 def test_large_d(cuda_lib):
     """D large enough that q sits in shared memory, and beyond what the
     shared-memory ring holds (scalar path)."""
@@ -212,7 +253,15 @@ def test_automatic_plans(cuda_lib):
     assert plan(1, 255, 4096)["plan"] == "cluster"  # rows too long for registers: the ring
     big = plan(4096, 255, 512)
     assert big["plan"] == "stream" and big["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
-    assert plan(2, 255, 511)["plan"] == "generic"
+    # rows the bulk copies cannot take: the scalar plan, a few questions each
+    # spread over a cluster (at least one row per warp, 16 KB per CTA)
+    odd = plan(2, 255, 511)
+    assert odd["plan"] == "generic" and odd["cluster"] == 16 and odd["ctas"] == 32, odd
+    assert plan(1, 64, 1001)["cluster"] == 8     # limited by rows: one per warp
+    assert plan(1, 12, 511)["cluster"] == 1      # fewer rows than two CTAs' warps
+    assert plan(1, 255, 3)["cluster"] == 1       # 3 KB of rows: not worth splitting
+    many = plan(100, 255, 511)                   # too many questions for clusters
+    assert many["plan"] == "generic" and many["cluster"] == 1 and many["ctas"] == 100, many
 
 
 def test_throughput_workload_full_size(cuda_lib):
