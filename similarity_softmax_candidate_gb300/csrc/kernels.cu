@@ -33,10 +33,14 @@
 //     cluster per question, at most 32 rows per CTA (16 for long rows), q
 //     and the rows loaded straight into registers (q in shared memory for
 //     long rows), one trip to memory, the same cluster exchange.
-//   * generic_kernel -- scalar loads, any D and any alignment.
+//   * generic_kernel -- scalar loads, any D and any alignment: one CTA per
+//     question, or, for a few questions of a uniform batch, one cluster per
+//     question with the same exchange as the DIRECT plan.
 // The stream and direct kernels are launched with programmatic dependent
 // launch: they may start while the previous kernel runs and wait for it
-// (griddepcontrol.wait) before their first global access.
+// (griddepcontrol.wait) before their first global access. Before that wait
+// a stream-kernel CTA only asks L2 for its first ring's worth of rows (a
+// prefetch changes no value anyone reads).
 //   * the unfused baseline (PR #69, "What it is worth": a separate norm pass
 //     and a scoring block that loads the norm from a staged array) reuses
 //     stream_kernel: pass 1 writes one value per row (the norm, or for the dot
