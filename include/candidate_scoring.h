@@ -74,15 +74,23 @@ typedef enum {
     CS_ERR_SCRATCH_TOO_SMALL = 13 /* B*K above CS_NOALLOC_MAX_ROWS (no-allocation entry) */
 } cs_status;
 
-/* ABI version of this header and library: 1. */
+/* ABI version of this header and library: 1. The page's manifest records
+ * the kernel's ABI as version 1 (PR #69, "The manifest, and CI":
+ * abi_version 1); a caller can check it before binding the entry points.
+ * Takes no arguments, touches no device, cannot fail. */
 int cs_abi_version(void);
 
-/* Static English text for a status code (never NULL). */
+/* Static English text for a status code (never NULL; "unknown status" for
+ * a code this library does not return). An addition of this library: the
+ * page names the rejected arguments but no way to print them. Touches no
+ * device, cannot fail. */
 const char *cs_status_string(int status);
 
 /*
- * One question: q[D], C[K][D] -> out[K]. Identical to
- * cs_score_candidates_batch with B = 1.
+ * One question: q[D], C[K][D] -> out[K]. The page's single-question call
+ * (PR #69, "Verified on hardware": its batch group scores one question
+ * through this call and more through cs_score_candidates_batch, so the two
+ * entry points must agree); here it is cs_score_candidates_batch with B = 1.
  *   normalize   1 = cosine (CLM), 0 = dot (Kev)
  *   scale       multiplies the similarity; for CLM pass exp(logit_scale),
  *               for Kev 1/sqrt(256). Any finite nonzero value.

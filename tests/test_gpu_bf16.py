@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from similarity_softmax_candidate_gb300 import binding, workloads
-from tests._util import ATOL, assert_parity, oracle_probs
+from tests._util import ATOL, assert_parity, oracle_probs, pairs_in_rotation, tempered_case
 
 pytestmark = pytest.mark.gpu
 
@@ -25,12 +25,16 @@ SHAPES = [(1, 5, 512), (1, 64, 512), (1, 255, 512), (8, 255, 512), (1, 255, 2560
 
 @pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
 def test_bf16_parity(cuda_lib, normalize):
-    for B, K, D in SHAPES:
-        wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 700 + B + K + D)
+    """Shape i takes (scale, temperature) pair i % 5 (temperature 1, then
+    0.7, 3 and 0.05 with positive and negative scales)."""
+    pairs = pairs_in_rotation(normalize)
+    for i, (B, K, D) in enumerate(SHAPES):
+        wl = tempered_case(B, K, D, normalize, pairs[i % len(pairs)], 700 + B + K + D)
+        sc, T = wl.scale, wl.temperature
         Cb = wl.C.to(torch.bfloat16)
-        p = binding.cs_score_candidates_batch_bf16(wl.Q.to(DEV), Cb.to(DEV), normalize, wl.scale, 1.0)
+        p = binding.cs_score_candidates_batch_bf16(wl.Q.to(DEV), Cb.to(DEV), normalize, sc, T)
         torch.cuda.synchronize()
-        assert_parity(p, oracle_probs(wl.Q, Cb.float(), normalize, wl.scale, 1.0), f"bf16 B={B} K={K} D={D}")
+        assert_parity(p, oracle_probs(wl.Q, Cb.float(), normalize, sc, T), f"bf16 B={B} K={K} D={D} scale={sc} T={T}")
 
 
 def test_bf16_single_matches_batch(cuda_lib):

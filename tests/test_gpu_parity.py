@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from similarity_softmax_candidate_gb300 import binding, workloads
-from tests._util import ATOL, assert_parity, oracle_probs
+from tests._util import ATOL, TEMPERED, assert_parity, oracle_probs, pairs_in_rotation, tempered_case
 
 pytestmark = pytest.mark.gpu
 
@@ -101,13 +101,17 @@ def test_golden_hand_cases(cuda_lib):
 @pytest.mark.parametrize("B", [1, 8, 4, 3])
 def test_page_batch_group(cuda_lib, B):
     """The page's batch group: K up to 255 and D up to 256; B = 1 goes
-    through the single-question entry point, the rest through the batch one."""
+    through the single-question entry point, the rest through the batch one.
+    Each shape runs at the page's scale and temperature 1 and at every
+    tempered pair (temperatures 0.05, 0.7 and 3, negative scales)."""
     rng = np.random.default_rng(B)
     for normalize in (0, 1):
         for K, D in ((255, 256), (int(rng.integers(1, 256)), int(rng.integers(1, 257))), (7, 3)):
-            wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 100 + K + D)
-            p = _run(wl)
-            assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0), f"B={B} K={K} D={D}")
+            for pair in pairs_in_rotation(normalize):
+                wl = tempered_case(B, K, D, normalize, pair, 100 + K + D)
+                p = _run(wl)
+                assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, wl.temperature),
+                              f"B={B} K={K} D={D} scale={wl.scale} T={wl.temperature}")
 
 
 PLAN_SHAPES = [
@@ -146,26 +150,61 @@ def _direct_row_limit(D):
     return 32 if D <= 512 else 16 if D <= 2560 else 0
 
 
+def _plan_eligible(kind, cluster, K, D):
+    """False where a forced DIRECT plan must be refused rather than run."""
+    if kind != binding.CS_PLAN_DIRECT:
+        return True
+    lim = _direct_row_limit(D)
+    g = cluster or next((x for x in (1, 2, 4, 8, 16) if lim and -(-K // x) <= lim), 16)
+    return lim > 0 and -(-K // g) <= lim and g <= K
+
+
 @pytest.mark.parametrize("plan", PLANS, ids=[p[0] for p in PLANS])
 @pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
 def test_every_plan(cuda_lib, plan, normalize):
+    """Every forced plan on shapes with ragged tails. Shape i takes the
+    (scale, temperature) pair i % 5 -- the page's scale at temperature 1,
+    then temperatures 0.7, 3 and 0.05 with positive and negative scales --
+    so each plan meets every pair."""
     _, kind, cluster, ctas = plan
-    for B, K, D in PLAN_SHAPES:
+    pairs = pairs_in_rotation(normalize)
+    for i, (B, K, D) in enumerate(PLAN_SHAPES):
         if cluster > K or ctas > B:
             continue
-        wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 1000 + B * K + D)
+        wl = tempered_case(B, K, D, normalize, pairs[i % len(pairs)], 1000 + B * K + D)
         Q, C = wl.Q.to(DEV), wl.C.to(DEV)
-        if kind == binding.CS_PLAN_DIRECT:
-            lim = _direct_row_limit(D)
-            g = cluster or next((x for x in (1, 2, 4, 8, 16) if lim and -(-K // x) <= lim), 16)
-            eligible = lim > 0 and -(-K // g) <= lim and g <= K
-            if not eligible:
-                with pytest.raises(binding.CSError):
-                    binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, kind, cluster, ctas)
-                continue
-        p = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, kind, cluster, ctas)
+        if not _plan_eligible(kind, cluster, K, D):
+            with pytest.raises(binding.CSError):
+                binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, wl.temperature, kind, cluster,
+                                                       ctas)
+            continue
+        p = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, wl.temperature, kind, cluster, ctas)
         torch.cuda.synchronize()
-        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0), f"{plan[0]} B={B} K={K} D={D}")
+        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, wl.temperature),
+                      f"{plan[0]} B={B} K={K} D={D} scale={wl.scale} T={wl.temperature}")
+
+
+TEMPERED_PLAN_SHAPES = [(3, 255, 512), (2, 200, 1028), (9, 100, 16)]
+
+
+@pytest.mark.parametrize("plan", PLANS, ids=[p[0] for p in PLANS])
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_every_plan_every_tempered_pair(cuda_lib, plan, normalize):
+    """Every forced plan with every tempered pair on the same shapes: the
+    factor scale / temperature is formed in each kernel's own code, so each
+    is checked with temperatures 0.05, 0.7 and 3 and with negative scales."""
+    _, kind, cluster, ctas = plan
+    for B, K, D in TEMPERED_PLAN_SHAPES:
+        if cluster > K or ctas > B or not _plan_eligible(kind, cluster, K, D):
+            continue
+        for pair in TEMPERED[normalize]:
+            wl = tempered_case(B, K, D, normalize, pair, 2000 + B * K + D)
+            Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+            p = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, wl.temperature, kind, cluster,
+                                                       ctas)
+            torch.cuda.synchronize()
+            assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, wl.temperature),
+                          f"{plan[0]} B={B} K={K} D={D} scale={wl.scale} T={wl.temperature}")
 
 
 def test_unaligned_and_odd_shapes_use_scalar_path(cuda_lib):
@@ -200,42 +239,46 @@ def test_scalar_plan_over_a_cluster(cuda_lib, misaligned, normalize):
     result matches the oracle, and the one-CTA scalar plan's within float32
     rounding, for every cluster size the planner or a caller may pick."""
     for B, K, D in ((1, 255, 510 if not misaligned else 512), (3, 64, 511 if not misaligned else 256), (1, 16, 1001)):
-        wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 700 + B + K + D)
-        if misaligned:
-            Qb = torch.empty(B * D + 1, device=DEV)
-            Cb = torch.empty(B * K * D + 1, device=DEV)
-            Q, C = Qb[1:].view(B, D), Cb[1:].view(B, K, D)
-            Q.copy_(wl.Q)
-            C.copy_(wl.C)
-        else:
-            Q, C = wl.Q.to(DEV), wl.C.to(DEV)
-        auto = binding.cs_query_plan(Q, C, normalize)
-        assert auto["plan"] == "generic", auto
-        ref = oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0)
-        one = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, binding.CS_PLAN_GENERIC, 1)
-        p = (binding.cs_score_candidates(Q[0], C[0], normalize, wl.scale, 1.0)[None]
-             if B == 1 else binding.cs_score_candidates_batch(Q, C, normalize, wl.scale, 1.0))
-        torch.cuda.synchronize()
-        assert_parity(p, ref, f"auto G={auto['cluster']} B={B} K={K} D={D}")
-        assert torch.allclose(p, one, rtol=0, atol=1e-6)
-        for G in (2, 4, 7, 16):
-            if G > K:
-                continue
-            q = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, binding.CS_PLAN_GENERIC, G)
+        for pair in pairs_in_rotation(normalize):
+            wl = tempered_case(B, K, D, normalize, pair, 700 + B + K + D)
+            sc, T = wl.scale, wl.temperature
+            if misaligned:
+                Qb = torch.empty(B * D + 1, device=DEV)
+                Cb = torch.empty(B * K * D + 1, device=DEV)
+                Q, C = Qb[1:].view(B, D), Cb[1:].view(B, K, D)
+                Q.copy_(wl.Q)
+                C.copy_(wl.C)
+            else:
+                Q, C = wl.Q.to(DEV), wl.C.to(DEV)
+            ref = oracle_probs(wl.Q, wl.C, normalize, sc, T)
+            what = f"B={B} K={K} D={D} scale={sc} T={T}"
+            one = binding.cs_score_candidates_batch_plan(Q, C, normalize, sc, T, binding.CS_PLAN_GENERIC, 1)
+            p = (binding.cs_score_candidates(Q[0], C[0], normalize, sc, T)[None]
+                 if B == 1 else binding.cs_score_candidates_batch(Q, C, normalize, sc, T))
             torch.cuda.synchronize()
-            assert_parity(q, ref, f"G={G} B={B} K={K} D={D}")
+            assert_parity(p, ref, "auto " + what)
+            assert_parity(one, ref, "one CTA " + what)
+            for G in (2, 4, 7, 16):
+                if G > K:
+                    continue
+                q = binding.cs_score_candidates_batch_plan(Q, C, normalize, sc, T, binding.CS_PLAN_GENERIC, G)
+                torch.cuda.synchronize()
+                assert_parity(q, ref, f"G={G} " + what)
+                assert torch.allclose(q, one, rtol=0, atol=5e-6)
         with pytest.raises(binding.CSError):  # more CTAs than rows
-            binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, 1.0, binding.CS_PLAN_GENERIC, 17)
+            binding.cs_score_candidates_batch_plan(Q, C, normalize, sc, T, binding.CS_PLAN_GENERIC, 17)
     assert binding.cs_device_status() == 0
 
 
 def test_large_d(cuda_lib):
     """D large enough that q sits in shared memory, and beyond what the
     shared-memory ring holds (scalar path)."""
-    for D in (12288, 20000):
+    for i, D in enumerate((12288, 20000)):
         for normalize in (0, 1):
-            wl = workloads.random_case(2, 9, D, normalize, 3.0, 31)
-            assert_parity(_run(wl), oracle_probs(wl.Q, wl.C, normalize, 3.0, 1.0), f"D={D}")
+            for pair in ((3.0, 1.0), TEMPERED[normalize][i], TEMPERED[normalize][i + 2]):
+                wl = tempered_case(2, 9, D, normalize, pair, 31)
+                assert_parity(_run(wl), oracle_probs(wl.Q, wl.C, normalize, wl.scale, wl.temperature),
+                              f"D={D} scale={wl.scale} T={wl.temperature}")
 
 
 def test_automatic_plans(cuda_lib):

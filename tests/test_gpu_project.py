@@ -20,7 +20,7 @@ import torch
 
 import oracle
 from similarity_softmax_candidate_gb300 import binding
-from tests._util import assert_parity
+from tests._util import TEMPERED, assert_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -81,6 +81,28 @@ def test_project_score_parity(cuda_lib, normalize):
         assert_parity(p, ref, f"projected B={B} K={K} Din={Din} D={D}")
         qref = oracle.project(Hq.float().numpy(), Wq.float().numpy())
         np.testing.assert_allclose(qproj.cpu().numpy(), qref, rtol=1e-3, atol=1e-3)
+    assert binding.cs_device_status() == 0
+
+
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_project_score_tempered(cuda_lib, normalize):
+    """The projected readout forms its logit factor in its own epilogue, so
+    it is checked with temperatures 0.05, 0.7 and 3 and negative scales. For
+    the dot, the candidate head is scaled down so that the logits stay of a
+    few units (projected features are about N(0,1), so a dot has spread
+    sqrt(D))."""
+    for B, K, Din, D in ((5, 255, 512, 512), (3, 128, 512, 256), (2, 7, 64, 256)):
+        for scale, T in TEMPERED[normalize]:
+            f = 1.0 if normalize else min(1.0, 3.0 * T / (abs(scale) * D ** 0.5))
+            Hq = _bf16((B, Din), 110 + B)
+            Hc = _bf16((B, K, Din), 210 + K)
+            Wq = _bf16((D, Din), 310 + D, std=Din ** -0.5)
+            Wc = _bf16((D, Din), 410 + D, std=f * Din ** -0.5)
+            p = binding.cs_project_score_batch(Hq.to(DEV), Wq.to(DEV), Hc.to(DEV), Wc.to(DEV), normalize, scale, T)
+            torch.cuda.synchronize()
+            ref = oracle.project_score_batch(Hq.float().numpy(), Wq.float().numpy(), Hc.float().numpy(),
+                                             Wc.float().numpy(), normalize, scale, T)
+            assert_parity(p, ref, f"projected B={B} K={K} D={D} scale={scale} T={T}")
     assert binding.cs_device_status() == 0
 
 

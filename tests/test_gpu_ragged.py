@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from similarity_softmax_candidate_gb300 import binding, workloads
-from tests._util import assert_parity, oracle_probs
+from tests._util import TEMPERED, assert_parity, oracle_probs, pairs_in_rotation
 
 pytestmark = pytest.mark.gpu
 
@@ -34,20 +34,28 @@ CASES = [(1, 512, 1, 255), (3, 512, 1, 255), (8, 512, 200, 255), (40, 512, 1, 64
 
 @pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
 def test_ragged_parity(cuda_lib, normalize):
-    for B, D, kmin, kmax in CASES:
-        wl = workloads.ragged(B, D, normalize, 14.2857 if normalize else 0.0625, 300 + B + D + kmin, "cpu",
-                              kmin=kmin, kmax=kmax)
-        p = binding.cs_score_candidates_ragged(wl.Q.to(DEV), wl.C.to(DEV), wl.offsets.to(DEV), normalize, wl.scale,
-                                               1.0)
+    """Case i takes (scale, temperature) pair i % 5 (temperature 1, then 0.7,
+    3 and 0.05 with positive and negative scales); dot candidates of a
+    tempered pair are rescaled to keep the logits of a few units."""
+    pairs = pairs_in_rotation(normalize)
+    for i, (B, D, kmin, kmax) in enumerate(CASES):
+        scale, T = pairs[i % len(pairs)]
+        wl = workloads.ragged(B, D, normalize, scale, 300 + B + D + kmin, "cpu", kmin=kmin, kmax=kmax)
+        wl.temperature = T
+        if not normalize and T != 1.0:
+            wl.C.mul_(min(1.0, 3.0 * T / (abs(scale) * D ** 0.5)))
+        p = binding.cs_score_candidates_ragged(wl.Q.to(DEV), wl.C.to(DEV), wl.offsets.to(DEV), normalize, scale, T)
         torch.cuda.synchronize()
         _check_all(wl, p.cpu())
 
 
 def test_ragged_bf16(cuda_lib):
-    for B, D in ((3, 512), (300, 512), (9, 1032)):
-        wl = workloads.ragged(B, D, 1, 14.2857, 40 + B, "cpu")
+    for i, (B, D) in enumerate(((3, 512), (300, 512), (9, 1032))):
+        scale, T = TEMPERED[1][i]
+        wl = workloads.ragged(B, D, 1, scale, 40 + B, "cpu")
+        wl.temperature = T
         Cb = wl.C.to(torch.bfloat16)
-        p = binding.cs_score_candidates_ragged(wl.Q.to(DEV), Cb.to(DEV), wl.offsets.to(DEV), 1, wl.scale, 1.0)
+        p = binding.cs_score_candidates_ragged(wl.Q.to(DEV), Cb.to(DEV), wl.offsets.to(DEV), 1, scale, T)
         torch.cuda.synchronize()
         _check_all(wl, p.cpu(), Cref=Cb.float())
 

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from similarity_softmax_candidate_gb300 import binding, workloads
-from tests._util import ATOL, assert_parity, oracle_probs
+from tests._util import ATOL, assert_parity, oracle_probs, pairs_in_rotation, tempered_case
 
 pytestmark = pytest.mark.gpu
 
@@ -26,20 +26,37 @@ SHAPES = [(1, 5, 512), (1, 64, 512), (1, 255, 512), (8, 255, 512), (1, 255, 2560
 
 @pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
 def test_unfused_parity_and_staged(cuda_lib, normalize):
-    for B, K, D in SHAPES:
-        wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 500 + B + K + D)
+    """Shape i takes (scale, temperature) pair i % 5: the page's scale at
+    temperature 1, then temperatures 0.7, 3 and 0.05 with positive and
+    negative scales (pass 2 forms the factor in its own code)."""
+    pairs = pairs_in_rotation(normalize)
+    for i, (B, K, D) in enumerate(SHAPES):
+        wl = tempered_case(B, K, D, normalize, pairs[i % len(pairs)], 500 + B + K + D)
+        sc, T = wl.scale, wl.temperature
         Q, C = wl.Q.to(DEV), wl.C.to(DEV)
         staged = torch.full((B, K), -7.0, device=DEV)
-        p = binding.cs_score_candidates_batch_unfused(Q, C, normalize, wl.scale, 1.0, staged=staged)
-        pf = binding.cs_score_candidates_batch(Q, C, normalize, wl.scale, 1.0)
+        p = binding.cs_score_candidates_batch_unfused(Q, C, normalize, sc, T, staged=staged)
+        pf = binding.cs_score_candidates_batch(Q, C, normalize, sc, T)
         torch.cuda.synchronize()
-        ref = oracle_probs(wl.Q, wl.C, normalize, wl.scale, 1.0)
-        assert_parity(p, ref, f"unfused B={B} K={K} D={D}")
+        ref = oracle_probs(wl.Q, wl.C, normalize, sc, T)
+        assert_parity(p, ref, f"unfused B={B} K={K} D={D} scale={sc} T={T}")
         assert torch.max(torch.abs(p - pf)).item() <= ATOL
         C64 = wl.C.double().numpy()
         want = np.linalg.norm(C64, axis=2) if normalize else np.einsum("bkd,bd->bk", C64, wl.Q.double().numpy())
         got = staged.cpu().double().numpy()
         np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-4 * max(1.0, float(np.abs(want).max())))
+
+
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_unfused_every_tempered_pair(cuda_lib, normalize):
+    """Both passes with every tempered pair, a few questions and many."""
+    for B, K, D in ((3, 37, 132), (300, 255, 512)):
+        for pair in pairs_in_rotation(normalize)[1:]:
+            wl = tempered_case(B, K, D, normalize, pair, 600 + B + K + D, DEV)
+            p = binding.cs_score_candidates_batch_unfused(wl.Q, wl.C, normalize, wl.scale, wl.temperature)
+            torch.cuda.synchronize()
+            assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, wl.scale, wl.temperature),
+                          f"unfused B={B} K={K} D={D} scale={wl.scale} T={wl.temperature}")
 
 
 def test_unfused_workloads(cuda_lib):

@@ -18,6 +18,7 @@ import pytest
 import torch
 
 from similarity_softmax_candidate_gb300 import binding, workloads
+from tests._util import assert_parity, oracle_probs
 
 pytestmark = pytest.mark.gpu
 
@@ -59,26 +60,32 @@ def _capture(rt, stream, fn):
     return graph
 
 
-CASES = [(1, 5, 512, 1), (1, 255, 512, 1), (8, 255, 512, 1), (1, 255, 2560, 0), (700, 255, 512, 0), (3, 33, 513, 1)]
+# (B, K, D, normalize, scale, temperature): the page's shapes, a large batch,
+# odd D, and two calls with a temperature other than 1 and a negative scale.
+CASES = [(1, 5, 512, 1, 14.2857, 1.0), (1, 255, 512, 1, 14.2857, 1.0), (8, 255, 512, 1, 14.2857, 1.0),
+         (1, 255, 2560, 0, 0.0625, 1.0), (700, 255, 512, 0, 0.0625, 1.0), (3, 33, 513, 1, 14.2857, 1.0),
+         (4, 255, 512, 1, -14.2857, 0.7), (300, 64, 256, 0, -0.0625, 3.0)]
 
 
-@pytest.mark.parametrize("B,K,D,normalize", CASES)
-def test_one_node_and_bitwise_replay(cuda_lib, B, K, D, normalize):
+@pytest.mark.parametrize("B,K,D,normalize,scale,temperature", CASES)
+def test_one_node_and_bitwise_replay(cuda_lib, B, K, D, normalize, scale, temperature):
     rt = _cudart()
-    wl = workloads.random_case(B, K, D, normalize, 14.2857 if normalize else 0.0625, 71, "cuda:0")
+    wl = workloads.random_case(B, K, D, normalize, scale, 71, "cuda:0", temperature=temperature)
     s = torch.cuda.Stream()
     direct = torch.empty(B, K, device="cuda:0")
     replay = torch.full((B, K), -1.0, device="cuda:0")
     torch.cuda.synchronize()
     # an ordinary call first: one-time per-device set-up happens here
-    binding.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=direct, stream=s)
+    binding.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, wl.temperature, out=direct, stream=s)
     torch.cuda.synchronize()
+    ref = oracle_probs(wl.Q, wl.C, normalize, wl.scale, wl.temperature)
 
     def call():
         if B == 1:
-            binding.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=replay[0], stream=s)
+            binding.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, wl.temperature, out=replay[0],
+                                        stream=s)
         else:
-            binding.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=replay, stream=s)
+            binding.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, wl.temperature, out=replay, stream=s)
 
     graph = _capture(rt, s, call)
     try:
@@ -98,6 +105,7 @@ def test_one_node_and_bitwise_replay(cuda_lib, B, K, D, normalize):
                 assert rt.cudaGraphLaunch(exe, s.cuda_stream) == 0
                 torch.cuda.synchronize()
                 assert torch.equal(replay, direct), "graph replay differs from the direct call"
+                assert_parity(replay, ref, f"replay B={B} K={K} D={D} scale={scale} T={temperature}")
                 replay.fill_(-1.0)
                 torch.cuda.synchronize()
         finally:

@@ -66,6 +66,25 @@ def test_no_alloc_rejects_more_rows_than_its_buffer(cuda_lib):
                                                       0x7F2000000000, None)
     assert s == binding.CS_ERR_SCRATCH_TOO_SMALL
     assert "no-allocation" in binding.cs_status_string(s)
-    # exactly at the limit is accepted by validation (checked by the size
-    # rule alone: K=1 rows of one question each would launch, so not called)
-    assert (binding.CS_NOALLOC_MAX_ROWS // 255) * 255 <= binding.CS_NOALLOC_MAX_ROWS
+
+
+def test_no_alloc_at_exactly_its_row_limit(cuda_lib):
+    """B*K equal to the built-in buffer's size (8192 questions of K=128, D=4:
+    1,048,576 rows, every float of the buffer used) is accepted and scored
+    like the caller-buffer form and the oracle, on two calls in a row."""
+    lib = cuda_lib
+    stream = torch.cuda.current_stream().cuda_stream
+    B, K = 8192, 128
+    assert B * K == binding.CS_NOALLOC_MAX_ROWS
+    wl = workloads.random_case(B, K, 4, 1, workloads.CLM_SCALE, 903, DEV)
+    outs = [torch.full((B, K), -1.0, device=DEV) for _ in range(2)]
+    for out in outs:
+        assert _call_noalloc(lib, wl, out, stream) == binding.CS_OK
+    staged = torch.empty((B, K), device=DEV)
+    ref = torch.empty((B, K), device=DEV)
+    assert _call_unfused(lib, wl, staged, ref, stream) == binding.CS_OK
+    torch.cuda.synchronize()
+    expected = oracle_probs(wl.Q, wl.C, wl.normalize, wl.scale, wl.temperature)
+    for out in outs:
+        assert torch.max(torch.abs(out - ref)).item() <= ATOL
+        assert_parity(out, expected, "no-alloc at the row limit")
