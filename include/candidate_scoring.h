@@ -37,6 +37,24 @@
  *     next synchronizing call.
  *   - Results are deterministic: the same call on the same device gives
  *     bit-identical output, directly or replayed from a graph.
+ *   - Range. Every finite input within the range below gets a probability
+ *     distribution, never NaN. The logit factor scale / temperature is
+ *     formed in double precision and rounded once to float32; a factor
+ *     beyond float32's range (|scale / temperature| > FLT_MAX, e.g. scale
+ *     14.3 at temperature 1e-38) is refused with CS_ERR_RANGE before any
+ *     CUDA call. The logits enter the softmax only as differences from
+ *     their maximum, formed so that a huge factor drives them to -inf
+ *     (probability exactly 0) and never to NaN; the largest logit's
+ *     candidates share the probability. Dots, squared norms and |q|^2
+ *     accumulate in float32, so they must stay within FLT_MAX: for the dot
+ *     |c| |q| <= FLT_MAX is enough, for the cosine |c| and |q| below about
+ *     1.8e19 (every element below 1.8e19 / sqrt(D) is enough); tiny rows
+ *     need nothing, since their norms are clamped at 1e-8 before float32
+ *     loses them. A question outside that range, or with a NaN or
+ *     infinite element, is skipped: its rows of out are left unwritten and
+ *     CS_DEVERR_RANGE is set in the device status word (cs_device_status).
+ *     The page's rule is the same: an error rather than a scored answer
+ *     (PR #69, "Verified on hardware", rejected arguments).
  */
 #ifndef CANDIDATE_SCORING_H
 #define CANDIDATE_SCORING_H
@@ -71,7 +89,8 @@ typedef enum {
     CS_ERR_ALIAS = 10,         /* out overlaps Q or C */
     CS_ERR_TOO_LARGE = 11,     /* B*K*D elements do not fit the 64-bit index space */
     CS_ERR_BAD_PLAN = 12,      /* cs_score_candidates_batch_plan: plan not feasible */
-    CS_ERR_SCRATCH_TOO_SMALL = 13 /* B*K above CS_NOALLOC_MAX_ROWS (no-allocation entry) */
+    CS_ERR_SCRATCH_TOO_SMALL = 13,/* B*K above CS_NOALLOC_MAX_ROWS (no-allocation entry) */
+    CS_ERR_RANGE = 14          /* |scale / temperature| exceeds FLT_MAX */
 } cs_status;
 
 /* ABI version of this header and library: 1. The page's manifest records
@@ -281,12 +300,15 @@ int cs_score_candidates_batch_unfused_noalloc(const float *Q, const float *C,
 #define CS_DEVERR_BAD_CONFIG 2u    /* a kernel refused an inconsistent launch plan */
 #define CS_DEVERR_BAD_OFFSETS 4u   /* a ragged question had invalid offsets and was skipped */
 #define CS_DEVERR_BOUNDS 8u        /* bounds-checked build: an access outside its buffer was skipped */
+#define CS_DEVERR_RANGE 16u        /* a question's dots or norms left float32's range (or an input was
+                                      NaN or infinite): it was skipped, its rows of out unwritten */
 
 /*
  * Reads (and, if clear != 0, resets) the status word the kernels of this
  * library set on the current device when one of their bounded waits gives
- * up. A kernel that gives up stops early and leaves NaN in the results it
- * could not finish. Synchronizes the device; not for the hot path.
+ * up, skips a question it cannot score (CS_DEVERR_*). A kernel that gives
+ * up stops early; the results it could not finish are left NaN or
+ * unwritten. Synchronizes the device; not for the hot path.
  */
 int cs_device_status(unsigned *flags, int clear);
 

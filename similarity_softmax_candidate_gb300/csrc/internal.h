@@ -37,8 +37,11 @@ struct Problem {
     int K;
     int D;
     int normalize;     // 1 cosine, 0 dot
-    float scale;       // multiplies the similarity
-    float temperature; // divides the scaled similarity
+    // The logit factor scale / temperature, formed in double precision and
+    // rounded once to float32 by the host, which refuses a factor beyond
+    // float32's range: finite, possibly 0 (a factor below float32's
+    // smallest denormal) or negative. Logits are factor * similarity.
+    float factor;
     float* staged;     // unfused baseline only: one float per row [B][K]
     int c_bf16;        // 1: C holds bfloat16 bit patterns (2 bytes each)
     // Ragged batches: question b owns rows offsets[b] .. offsets[b+1]-1 of C
@@ -116,7 +119,7 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
 // (uniform K, B <= 65535).
 cudaError_t launch_generic(const Problem& p, int G, cudaStream_t stream);
 int max_active_generic_clusters(int cluster, int normalize, int c_bf16);
-// Unfused baseline pass 2 (dot): softmax of scale * staged / temperature.
+// Unfused baseline pass 2 (dot): softmax of factor * staged.
 cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream);
 
 // Size, in floats, of the built-in staged array of the no-allocation
@@ -148,8 +151,8 @@ cudaError_t configure_proj_kernels(int smem_optin);
 cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
                                 int sms, unsigned* status, unsigned* bounds, cudaStream_t stream);
 cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
-                                 int D, int normalize, float scale, float temperature, float* out, int sms,
-                                 unsigned* status, unsigned* bounds, cudaStream_t stream);
+                                 int D, int normalize, float factor, float* out, int sms, unsigned* status,
+                                 unsigned* bounds, cudaStream_t stream);
 // Device address of the status word on the current device (for kernels in
 // other translation units).
 cudaError_t status_word_address(unsigned** ptr);
@@ -161,6 +164,9 @@ cudaError_t status_word_address(unsigned** ptr);
 // still 0, sets kDevErrBounds in the status word and skips the access.
 // Release builds compile the checks away.
 constexpr unsigned kDevErrBounds = 8u;
+// Device status bit: a question's dot products or squared norms left
+// float32's range (or an input was not finite), so it was skipped unscored.
+constexpr unsigned kDevErrRange = 16u;
 enum BoundsSite : unsigned {
     kSiteCopyC = 1,        // stream producer: rows of C
     kSiteRing = 2,         // stream producer: the ring slot they land in

@@ -47,10 +47,14 @@
 //     the similarity) to a staged array in global memory; pass 2 is the
 //     scoring block reading the staged norms (cosine) or staged_softmax_kernel
 //     (dot).
+// Logits enter the softmax in a range-safe form (softmax_form.cuh): no
+// finite input gives NaN, and a question whose sums leave float32's range
+// is skipped with a device status bit instead of being scored.
 // Every on-chip wait is bounded (about 1 s); a CTA that gives up sets a
-// device status bit, writes NaN where it could not finish, waits (bounded)
-// for its own copies in flight, and exits.
+// device status bit, leaves what it could not finish NaN or unwritten,
+// waits (bounded) for its own copies in flight, and exits.
 #include "internal.h"
+#include "softmax_form.cuh"
 
 #include <math.h>
 
@@ -87,8 +91,9 @@ __device__ __noinline__ bool check_range(const void* ptr, unsigned long long byt
     return p.offsets ? p.total_rows : p.B * static_cast<long long>(p.K);
 }
 
-constexpr float kEps = 1e-8f;        // norm clamp of the cosine
-constexpr float kEps2 = 1e-16f;      // kEps squared: max(|c|, eps) = sqrt(max(|c|^2, eps^2))
+using form::qnan;
+using form::softmax_term;
+using form::value_scale;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
 constexpr int kSlotsPerLane = kLogitSlots / 32;
 
@@ -293,52 +298,97 @@ __device__ __forceinline__ void wait_phase_until(uint32_t bar, uint32_t parity, 
     }
 }
 
-// Logit factor of a question: z = a * t (dot) or a * t / max(|c|, eps)
-// (cosine, with a already divided by max(|q|, eps)).
-__device__ __forceinline__ float logit_factor(float qn, float scale, float temperature, bool cos) {
-    return cos ? scale / (temperature * qn) : scale / temperature;
+// ------------------------------------------------------------------ range-safe softmax
+//
+// Rows become values v_k (softmax_form.cuh: the softmax of the logits is
+// exp(2|a| (v_k - max v)) normalised, which no finite input turns into NaN);
+// a row float32 could not hold is NaN, and its question is skipped.
+
+// v of one row from its dot t and, for the fused cosine, its squared norm
+// nsq (the staged cosine passes the staged norm instead).
+template <int MODE>
+__device__ __forceinline__ float row_value(float t, float nsq, float w) {
+    if (MODE == kFusedCos) return form::cos_value(t, nsq, w);
+    if (MODE == kStagedCos) return form::staged_cos_value(t, nsq, w);
+    return form::dot_value(t, w);
 }
 
-// Logits of rows lane, lane+32, ... (< n) from their dots t and, for the
+// Values of rows lane, lane+32, ... (< n) from their dots t and, for the
 // fused cosine, squared norms n_sq, or, for the staged cosine, norms read
 // from the staged array; -inf beyond n.
 template <int MODE, int S = kSlotsPerLane>
-__device__ __forceinline__ void load_logits(const float* t, const float* n_sq, const float* staged_norm, int n,
-                                            float a, int lane, float (&z)[S]) {
+__device__ __forceinline__ void load_values(const float* t, const float* n_sq, const float* staged_norm, int n,
+                                            float w, int lane, float (&v)[S]) {
 #pragma unroll
     for (int j = 0; j < S; ++j) {
         const int k = lane + 32 * j;
-        z[j] = -INFINITY;
-        if (k < n) {
-            if (MODE == kFusedCos)
-                z[j] = a * t[k] * rsqrtf(fmaxf(n_sq[k], kEps2));
-            else if (MODE == kStagedCos)
-                z[j] = a * t[k] / fmaxf(staged_norm[k], kEps);
-            else
-                z[j] = a * t[k];
-        }
+        v[j] = -INFINITY;
+        if (k < n)
+            v[j] = row_value<MODE>(t[k], MODE == kFusedCos ? n_sq[k] : MODE == kStagedCos ? staged_norm[k] : 0.f, w);
     }
 }
 
-// Softmax of z over one warp (rows lane + 32 j < n), written to dst[0..n).
+// True on every lane when some row lane + 32 j < n of the warp is flagged.
+template <int S>
+__device__ __forceinline__ bool any_flagged(const float (&v)[S], int n, int lane) {
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < S; ++j) bad |= lane + 32 * j < n && !isfinite(v[j]);
+    return __any_sync(0xffffffffu, bad);
+}
+
+// Softmax over one warp (rows lane + 32 j < n) of the values v, written to
+// dst[0..n). Returns false, writing nothing, when a row is flagged; the
+// caller then records the range bit (unless its CTA gave up waiting, which
+// is what flagged the rows).
 template <int S = kSlotsPerLane>
-__device__ __forceinline__ void softmax_store(float (&z)[S], int n, float* __restrict__ dst, int lane) {
+__device__ __forceinline__ bool softmax_store(float (&v)[S], int n, float afac, float* __restrict__ dst, int lane) {
+    if (any_flagged(v, n, lane)) return false;
     float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < S; ++j) m = fmaxf(m, z[j]);
+    for (int j = 0; j < S; ++j) m = fmaxf(m, v[j]);
     m = warp_max(m);
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < S; ++j) {
-        z[j] = lane + 32 * j < n ? __expf(z[j] - m) : 0.f;
-        s += z[j];
+        v[j] = lane + 32 * j < n ? softmax_term(afac, v[j] - m) : 0.f;
+        s += v[j];
     }
     const float inv = 1.0f / warp_sum(s);
 #pragma unroll
     for (int j = 0; j < S; ++j) {
         const int k = lane + 32 * j;
-        if (k < n) dst[k] = z[j] * inv;
+        if (k < n) dst[k] = v[j] * inv;
     }
+    return true;
+}
+
+// A question's rows were flagged: record it, unless this CTA gave up
+// waiting (the status word already says so, and that is what flagged them).
+__device__ __forceinline__ void record_range(volatile int* give_up) {
+    if (!*give_up) atomicOr(&g_status, kDevErrRange);
+}
+
+// Cluster exchange: each CTA reduces its rows to (m, s) = (max v, sum of
+// exp(2|a| (v - m))); a CTA with a flagged row sends m = NaN, so that every
+// CTA of the cluster skips the question. combine_pairs reads the G pairs in
+// xch (lanes < G one each) and returns the normaliser
+// 1 / sum_g s_g exp(2|a| (m_g - M)) with M = max m_g (M_out); flagged: some
+// CTA sent NaN. A CTA without rows sends (-inf, 0) and adds nothing.
+__device__ __forceinline__ float combine_pairs(const float2* xch, int G, float afac, int lane, float* M_out,
+                                               bool* flagged) {
+    float mj = -INFINITY, sj = 0.f;
+    bool bad = false;
+    if (lane < G) {
+        const float2 x = xch[lane];
+        mj = x.x;
+        sj = x.y;
+        bad = isnan(mj);
+    }
+    *flagged = __any_sync(0xffffffffu, bad);
+    const float M = warp_max(bad ? -INFINITY : mj);
+    *M_out = M;
+    return 1.0f / warp_sum(lane < G && sj > 0.f ? sj * softmax_term(afac, mj - M) : 0.f);
 }
 
 // Sums each of the V values v[0..V) over the 32 lanes of a warp with V - 1
@@ -662,7 +712,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     }
     const uint32_t row_bytes = static_cast<uint32_t>(D) * sizeof(T);  // a row of C
     const uint32_t q_bytes = static_cast<uint32_t>(D) * 4u;
-    float a = 1.f;  // logit factor of the current question
+    float w = 1.f;  // value scale of the current question (value_scale)
+    const float afac = fabsf(p.factor);
     QRows last{0, 0, false};  // rows of the last question (the cluster plan's only one)
 
     if (warp == kConsumerWarps) {
@@ -761,7 +812,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
             const float4* q4 = reinterpret_cast<const float4*>(qbuf + qs * D);
             float4 qv[(NQC > 0 ? NQC : 1) * QF4];
-            float qn = 1.f;
+            float qsq = 0.f;  // |q|^2 (cosine)
             if constexpr (NQC > 0) {
                 float sq = 0.f;
 #pragma unroll
@@ -778,16 +829,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
                 // Every warp holds all of q, so this warp-wide sum is the whole
                 // norm; it is never added across warps.
-                if (COS) qn = fmaxf(sqrtf(warp_sum(sq)), kEps);
+                if (COS) qsq = warp_sum(sq);
             } else if (COS) {
                 float sq = 0.f;
                 for (int i = lane; i < D / 4; i += 32) {
                     const float4 x = q4[i];
                     sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
                 }
-                qn = fmaxf(sqrtf(warp_sum(sq)), kEps);
+                qsq = warp_sum(sq);
             }
-            a = logit_factor(qn, p.scale, p.temperature, COS);
+            w = value_scale(p.factor, qsq, COS);
 
             float* tb = tn + (nq & 1) * 2 * kLogitSlots;  // dots
             float* nb = tb + kLogitSlots;                 // squared norms
@@ -836,15 +887,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     (MODE != kStagedCos ||
                      CS_IN_BOUNDS(p.staged + qr.row0, nrows * 4, p.staged, rows_total(p) * 4, kSiteStagedRead));
                 const float* sn = MODE == kStagedCos ? p.staged + qr.row0 : nullptr;
+                bool done = true;
                 if (inb && nrows <= 32) {  // one row per lane: the short code path
-                    float z[1];
-                    load_logits<MODE, 1>(tb, nb, sn, nrows, a, lane, z);
-                    softmax_store<1>(z, nrows, p.out + qr.row0, lane);
+                    float v[1];
+                    load_values<MODE, 1>(tb, nb, sn, nrows, w, lane, v);
+                    done = softmax_store<1>(v, nrows, afac, p.out + qr.row0, lane);
                 } else if (inb) {
-                    float z[kSlotsPerLane];
-                    load_logits<MODE>(tb, nb, sn, nrows, a, lane, z);
-                    softmax_store(z, nrows, p.out + qr.row0, lane);
+                    float v[kSlotsPerLane];
+                    load_values<MODE>(tb, nb, sn, nrows, w, lane, v);
+                    done = softmax_store(v, nrows, afac, p.out + qr.row0, lane);
                 }
+                if (!done && lane == 0) record_range(give_up);
             }
             gst0 += nst;
             last = qr;
@@ -854,49 +907,50 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
 
     if (G > 1 && does_softmax(MODE)) {
         // Cluster plan (one question per cluster): warp 0 reduces this CTA's
-        // rows to (m, s) = (max z, sum exp(z - m)), pushes the pair into slot
-        // `rank` of every peer's xch (completing on the peer's xbar), waits
-        // for all G pairs to arrive here, and writes p = exp(z - M) / S with
-        // M = max m_g and S = sum s_g exp(m_g - M).
+        // rows to (m, s) = (max v, sum exp(2|a| (v - m))), pushes the pair into
+        // slot `rank` of every peer's xch (completing on the peer's xbar),
+        // waits for all G pairs to arrive here, and writes
+        // p = exp(2|a| (v - M)) / S with M = max m_g and
+        // S = sum s_g exp(2|a| (m_g - M)). A CTA with a flagged row sends NaN
+        // for m, and then no CTA writes the question.
         cluster_wait();  // every CTA of the cluster has initialised its barriers
         // Warp 0; S slots of 32 rows per lane (S = 1 whenever this CTA holds
         // at most 32 rows: the short code path).
         auto finish = [&](auto slots) {
             constexpr int S = decltype(slots)::value;
             const uint32_t rank = cluster_ctarank();
-            float z[S];
+            float v[S];
             const int nrows = last.n;
             const bool rd = MODE != kStagedCos || CS_IN_BOUNDS(p.staged + last.row0, nrows * 4, p.staged,
                                                                 rows_total(p) * 4, kSiteStagedRead);
-            load_logits<MODE, S>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr,
-                                 rd ? nrows : 0, a, lane, z);
+            const int nread = rd ? nrows : 0;
+            load_values<MODE, S>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr, nread, w,
+                                 lane, v);
+            const bool bad = any_flagged(v, nread, lane);
             float m = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < S; ++j) m = fmaxf(m, z[j]);
+            for (int j = 0; j < S; ++j) m = fmaxf(m, v[j]);
             m = warp_max(m);
             float s = 0.f;
 #pragma unroll
             for (int j = 0; j < S; ++j)
-                if (lane + 32 * j < nrows) s += __expf(z[j] - m);
+                if (lane + 32 * j < nread) s += softmax_term(afac, v[j] - m);
             s = warp_sum(s);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
-                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(bad ? qnan() : m, s),
                               peer_addr(xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(xbar), 0, give_up);
-            float mj = -INFINITY, sj = 0.f;
-            if (lane < G) {
-                const float2 x = xch[lane];
-                mj = x.x;
-                sj = x.y;
-            }
-            const float M = warp_max(mj);
-            const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
+            float M;
+            bool flagged;
+            const float inv = combine_pairs(xch, G, afac, lane, &M, &flagged);
             float* dst = p.out + last.row0;
-            if (CS_IN_BOUNDS(dst, nrows * 4, p.out, rows_total(p) * 4, kSiteOutCluster)) {
+            if (ok && flagged) {
+                if (lane == 0) record_range(give_up);
+            } else if (CS_IN_BOUNDS(dst, nrows * 4, p.out, rows_total(p) * 4, kSiteOutCluster)) {
 #pragma unroll
                 for (int j = 0; j < S; ++j) {
                     const int k = lane + 32 * j;
-                    if (k < nrows) dst[k] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
+                    if (k < nrows) dst[k] = ok ? softmax_term(afac, v[j] - M) * inv : qnan();
                 }
             }
         };
@@ -1008,7 +1062,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
             return qv[j * QF4 + h];
         }
     };
-    float qn = 1.f;
+    float qsq = 0.f;
     if (COS) {
         float sq = 0.f;
 #pragma unroll
@@ -1018,9 +1072,10 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
                 const float4 x = qchunk(j, h);
                 sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
             }
-        qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // each warp covers all of q: never summed across warps
+        qsq = warp_sum(sq);  // each warp covers all of q: never summed across warps
     }
-    const float a = logit_factor(qn, p.scale, p.temperature, COS);
+    const float w = value_scale(p.factor, qsq, COS);
+    const float afac = fabsf(p.factor);
 
     // dot (and squared norm) of each row: two packed partial sums each
     unsigned long long acc[V];
@@ -1064,18 +1119,18 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
     if (G > 1) cluster_wait();  // every CTA of the cluster has initialised its barrier
     bool arrived = false;  // warp-uniform: this warp has arrived at the closing cluster barrier
     if (warp == 0 && !skip) {
-        float z = -INFINITY;
-        if (lane < n) z = COS ? a * tn[lane] * rsqrtf(fmaxf(tn[kDirectRows + lane], kEps2)) : a * tn[lane];
+        float v[1] = {-INFINITY};
+        if (lane < n) v[0] = row_value<COS ? kFusedCos : kFusedDot>(tn[lane], tn[kDirectRows + lane], w);
         float* dst = p.out + qr.row0;
         const bool out_ok = CS_IN_BOUNDS(dst, n * 4ll, p.out, rows_total(p) * 4, kSiteOutCluster);
         if (G == 1) {
-            float zz[1] = {z};
-            if (out_ok) softmax_store<1>(zz, n, dst, lane);
+            if (out_ok && !softmax_store<1>(v, n, afac, dst, lane) && lane == 0) record_range(give_up);
         } else {
-            const float m = warp_max(z);
-            const float s = warp_sum(lane < n ? __expf(z - m) : 0.f);
+            const bool bad = any_flagged(v, n, lane);
+            const float m = warp_max(v[0]);
+            const float s = warp_sum(lane < n ? softmax_term(afac, v[0] - m) : 0.f);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
-                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(bad ? qnan() : m, s),
                               peer_addr(&xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
             // Every pair bound for this CTA has landed (or the wait gave up,
@@ -1085,15 +1140,14 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
             __syncwarp();
             cluster_arrive_relaxed();
             arrived = true;
-            float mj = -INFINITY, sj = 0.f;
-            if (lane < G) {
-                const float2 x = xch[lane];
-                mj = x.x;
-                sj = x.y;
+            float M;
+            bool flagged;
+            const float inv = combine_pairs(xch, G, afac, lane, &M, &flagged);
+            if (ok && flagged) {
+                if (lane == 0) record_range(give_up);
+            } else if (out_ok && lane < n) {
+                dst[lane] = ok ? softmax_term(afac, v[0] - M) * inv : qnan();
             }
-            const float M = warp_max(mj);
-            const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
-            if (out_ok && lane < n) dst[lane] = ok ? __expf(z - M) * inv : __int_as_float(0x7fc00000);
         }
     }
     if (G > 1) {
@@ -1142,16 +1196,17 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
     const bool skip = qr.bad || !CS_IN_BOUNDS(q, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ) ||
                       !CS_IN_BOUNDS(p.out + qr.row0, K * 4ll, p.out, rows_total(p) * 4, kSiteGenericOut);
     if (!CL && skip) return;  // nothing waits on a CTA of its own; a cluster's CTAs all reach its barriers
-    float qn = 1.f;
+    float qsq = 0.f;
     if (COS && !skip) {
         float sq = 0.f;
         for (int d = lane; d < D; d += 32) {
             const float v = __ldg(q + d);
             sq = fmaf(v, v, sq);
         }
-        qn = fmaxf(sqrtf(warp_sum(sq)), kEps);  // whole norm per warp, never summed across warps
+        qsq = warp_sum(sq);  // whole norm per warp, never summed across warps
     }
-    const float a = logit_factor(qn, p.scale, p.temperature, COS);
+    const float w = value_scale(p.factor, qsq, COS);
+    const float afac = fabsf(p.factor);
     for (int k = warp; k < K && !skip; k += nwarps) {
         const T* __restrict__ c = static_cast<const T*>(p.C) + static_cast<size_t>(qr.row0 + k) * D;
         if (!CS_IN_BOUNDS(c, D * static_cast<long long>(sizeof(T)), p.C, rows_total(p) * D * static_cast<long long>(sizeof(T)),
@@ -1177,47 +1232,48 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         }
         const float t = warp_sum(t0 + t1);
         const float n = COS ? warp_sum(n0 + n1) : 0.f;
-        if (lane == 0) lg[k] = COS ? a * t * rsqrtf(fmaxf(n, kEps2)) : a * t;
+        if (lane == 0) lg[k] = row_value<COS ? kFusedCos : kFusedDot>(t, n, w);
     }
     __syncthreads();
     if (G > 1) cluster_wait();  // every CTA of the cluster has initialised its barrier
     bool arrived = false;       // warp-uniform: this warp has arrived at the closing cluster barrier
     if (warp == 0 && !skip) {
-        float z[kSlotsPerLane];
+        float v[kSlotsPerLane];
 #pragma unroll
-        for (int j = 0; j < kSlotsPerLane; ++j) z[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
+        for (int j = 0; j < kSlotsPerLane; ++j) v[j] = lane + 32 * j < K ? lg[lane + 32 * j] : -INFINITY;
         float* dst = p.out + qr.row0;
         if constexpr (!CL) {
-            softmax_store(z, K, dst, lane);
+            // no waits in this form, so a flagged row is a range failure
+            if (!softmax_store(v, K, afac, dst, lane) && lane == 0) atomicOr(&g_status, kDevErrRange);
         } else {
             // this CTA's (max, sum of exp) to every CTA of the cluster
+            const bool bad = any_flagged(v, K, lane);
             float m = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, z[j]);
+            for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, v[j]);
             m = warp_max(m);
             float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j) s += lane + 32 * j < K ? __expf(z[j] - m) : 0.f;
+            for (int j = 0; j < kSlotsPerLane; ++j) s += lane + 32 * j < K ? softmax_term(afac, v[j] - m) : 0.f;
             s = warp_sum(s);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
-                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(bad ? qnan() : m, s),
                               peer_addr(&xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
             // every pair bound for this CTA has landed (or the wait gave up)
             __syncwarp();
             cluster_arrive_relaxed();
             arrived = true;
-            float mj = -INFINITY, sj = 0.f;
-            if (lane < G) {
-                const float2 x = xch[lane];
-                mj = x.x;
-                sj = x.y;
-            }
-            const float M = warp_max(mj);
-            const float inv = 1.0f / warp_sum(lane < G ? sj * __expf(mj - M) : 0.f);
+            float M;
+            bool flagged;
+            const float inv = combine_pairs(xch, G, afac, lane, &M, &flagged);
+            if (ok && flagged) {
+                if (lane == 0) record_range(give_up);
+            } else {
 #pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j)
-                if (lane + 32 * j < K) dst[lane + 32 * j] = ok ? __expf(z[j] - M) * inv : __int_as_float(0x7fc00000);
+                for (int j = 0; j < kSlotsPerLane; ++j)
+                    if (lane + 32 * j < K) dst[lane + 32 * j] = ok ? softmax_term(afac, v[j] - M) * inv : qnan();
+            }
         }
     }
     if (G > 1) {
@@ -1229,23 +1285,20 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
 }
 
 // Unfused baseline pass 2 (dot): one warp per question, softmax of
-// scale * staged / temperature over the question's K staged similarities.
+// factor * staged over the question's K staged similarities.
 __global__ void __launch_bounds__(256) staged_softmax_kernel(const Problem p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long b = static_cast<long long>(blockIdx.x) * 8 + warp;
     if (b >= p.B) return;
-    const float a = p.scale / p.temperature;
+    const float w = value_scale(p.factor, 0.f, false), afac = fabsf(p.factor);
     const float* t = p.staged + static_cast<size_t>(b) * p.K;
     if (!CS_IN_BOUNDS(t, p.K * 4ll, p.staged, p.B * p.K * 4ll, kSiteStagedSoftmax) ||
         !CS_IN_BOUNDS(p.out + static_cast<size_t>(b) * p.K, p.K * 4ll, p.out, p.B * p.K * 4ll, kSiteStagedSoftmaxOut))
         return;
-    float z[kSlotsPerLane];
-#pragma unroll
-    for (int j = 0; j < kSlotsPerLane; ++j) {
-        const int k = lane + 32 * j;
-        z[j] = k < p.K ? a * t[k] : -INFINITY;
-    }
-    softmax_store(z, p.K, p.out + static_cast<size_t>(b) * p.K, lane);
+    float v[kSlotsPerLane];
+    load_values<kFusedDot>(t, nullptr, nullptr, p.K, w, lane, v);
+    if (!softmax_store(v, p.K, afac, p.out + static_cast<size_t>(b) * p.K, lane) && lane == 0)
+        atomicOr(&g_status, kDevErrRange);  // no waits here: a flagged row is a range failure
 }
 
 // Self-test of the bounded wait: one thread waits, with the kernels' own

@@ -29,6 +29,7 @@
 // and either store it or fold it into dot, norm and softmax. Every wait is
 // bounded.
 #include "internal.h"
+#include "softmax_form.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -52,7 +53,6 @@ constexpr int kAccCols = 2 * kMmaN;  // two accumulators of kMmaN columns: all o
 constexpr int kProjThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiThreads = 128;
 constexpr unsigned long long kProjWaitNs = 1000000000ull;
-constexpr float kPEps = 1e-8f, kPEps2 = 1e-16f;
 
 enum ProjMode { kProjPlain = 0, kProjScore = 1 };
 
@@ -60,7 +60,7 @@ struct ProjArgs {
     long long rows;     // rows of A (PLAIN: rows to project; SCORE: B*K)
     int B, K, Din, D;   // SCORE: B questions of K rows
     int normalize;
-    float scale, temperature;
+    float factor;       // SCORE: scale / temperature (finite, rounded once on the host)
     const float* qproj; // SCORE: projected queries [B][D]
     float* out;         // PLAIN: [rows][D]; SCORE: [B][K]
     unsigned* status;   // device status word
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         const uint32_t stage_out_s = base + L.out + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
         long long nq = 0;
         for (long long item = blockIdx.x; item < items; item += gridDim.x, ++nq) {
-            float fac = 1.f;  // SCORE: scale / (T * max(|q|, eps)), or scale / T
+            float w = 1.f;  // SCORE: the question's value scale (softmax_form.cuh)
             float* lg = logits + (nq & 1) * 256;
             if (MODE == kProjScore) {
                 const float* q = a.qproj + static_cast<size_t>(item) * D;
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 if (a.normalize)
                     for (int i = lane; i < D; i += 32) sq = fmaf(qs[i], qs[i], sq);
                 sq = wsum(sq);
-                fac = a.normalize ? a.scale / (a.temperature * fmaxf(sqrtf(sq), kPEps)) : a.scale / a.temperature;
+                w = form::value_scale(a.factor, sq, a.normalize != 0);
             }
             for (int h = 0; h < tiles_per_item; ++h) {
                 float dot = 0.f, nrm = 0.f;
@@ -473,32 +473,40 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 if (MODE == kProjScore) {
                     const int k = h * kTileM + row;
                     if (k < a.K) {
-                        const float z = a.normalize ? fac * dot * rsqrtf(fmaxf(nrm, kPEps2)) : fac * dot;
-                        lg[k] = ok ? z : __int_as_float(0x7fc00000);
+                        const float v = a.normalize ? form::cos_value(dot, nrm, w) : form::dot_value(dot, w);
+                        lg[k] = ok ? v : form::qnan();
                     }
                 }
             }
             if (MODE == kProjScore) {
                 epi_bar_sync();  // every logit of the question is in lg
                 if (warp == 2) {
+                    // softmax of the values (softmax_form.cuh); a question with
+                    // a flagged row is skipped unscored
+                    const float afac = fabsf(a.factor);
                     float z[8];
                     float m = -INFINITY;
+                    bool bad = false;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int k = lane + 32 * j;
                         z[j] = k < a.K ? lg[k] : -INFINITY;
+                        bad |= k < a.K && !isfinite(z[j]);
                         m = fmaxf(m, z[j]);
                     }
+                    bad = __any_sync(0xffffffffu, bad);
                     m = wmax(m);
                     float s = 0.f;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        z[j] = lane + 32 * j < a.K ? __expf(z[j] - m) : 0.f;
+                        z[j] = lane + 32 * j < a.K ? form::softmax_term(afac, z[j] - m) : 0.f;
                         s += z[j];
                     }
                     const float inv = 1.0f / wsum(s);
                     float* dst = a.out + static_cast<size_t>(item) * a.K;
-                    if (CS_IN_BOUNDS(dst, a.K * 4ll, a.out, a.B * a.K * 4ll, kSiteProjOut)) {
+                    if (bad) {
+                        if (lane == 0 && !*give_up) atomicOr(a.status, kDevErrRange);
+                    } else if (CS_IN_BOUNDS(dst, a.K * 4ll, a.out, a.B * a.K * 4ll, kSiteProjOut)) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             if (lane + 32 * j < a.K) dst[lane + 32 * j] = z[j] * inv;
@@ -590,7 +598,7 @@ cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long 
 }
 
 cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
-                                 int D, int normalize, float scale, float temperature, float* out, int sms,
+                                 int D, int normalize, float factor, float* out, int sms,
                                  unsigned* status, unsigned* bounds, cudaStream_t stream) {
     CUtensorMap ma, mw;
     const unsigned long long rows = static_cast<unsigned long long>(B) * K;
@@ -603,8 +611,7 @@ cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const f
     a.Din = Din;
     a.D = D;
     a.normalize = normalize;
-    a.scale = scale;
-    a.temperature = temperature;
+    a.factor = factor;
     a.qproj = qproj;
     a.out = out;
     a.status = status;
