@@ -15,8 +15,11 @@ Printed on one JSON line (rank 0):
              launch time (CUDA events on its stream), against the measured
              HBM copy bandwidth
   cpu_baseline  the fp64 oracle timed on a bounded sample on the host cores
-  extra      dot scoring, and single-question latency (us/call, direct and
-             CUDA-graph replay) for the page's five shapes
+  extra      dot scoring, bfloat16 candidates, a ragged batch, the unfused
+             baseline, the projected readout, the copy ceiling of the
+             access pattern, and single-question latency for the page's
+             five shapes (us/call: warm and HBM-cold, direct and in a
+             CUDA graph, and isolated calls)
 
 --impl reference times the fp64 oracle (the only reference there is) on
 bounded samples of the same workload, on the host cores.
@@ -704,8 +707,10 @@ def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32)
     """us per call, cosine K=255 D=512, of the automatic plan and of every
     forced plan (STREAM; CLUSTER with 2..16 CTAs per question; DIRECT over 16
     CTAs where it fits), each as n calls on consecutive slices of a
-    4096-question buffer (2.1 GB, so every call reads from HBM) captured in
-    one CUDA graph and replayed: device time per call, no host work."""
+    4096-question buffer captured in one CUDA graph after a read of a
+    256 MiB buffer (which leaves L2 holding none of the slices), minus the
+    same graph without the calls: device time per call, every call reading
+    from HBM, no host work."""
     import torch
     Bmax = 4096
     g = torch.Generator(device=dev)
@@ -713,6 +718,7 @@ def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32)
     C = torch.randn(Bmax, K, D, device=dev, generator=g)
     Q = torch.randn(Bmax, D, device=dev, generator=g)
     out = torch.empty(Bmax, K, device=dev)
+    flush = torch.ones(64 << 20, device=dev)  # 256 MiB, read only
     plans = [("stream", cs.CS_PLAN_STREAM, 0)] + [(f"cluster{G}", cs.CS_PLAN_CLUSTER, G) for G in (2, 4, 8, 16)] + \
         [("direct16", cs.CS_PLAN_DIRECT, 16)]
 
@@ -729,22 +735,27 @@ def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32)
         for i in range(4):
             call(i)
         torch.cuda.synchronize()
-        graph, st = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
-        with torch.cuda.stream(st):
-            with torch.cuda.graph(graph, stream=st):
-                for i in range(n):
-                    call(i)
-        graph.replay()
-        torch.cuda.synchronize()
-        best = float("inf")
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
+
+        def graph_ms(calls):
+            graph, st = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(graph, stream=st):
+                    flush.sum()
+                    for i in range(calls):
+                        call(i)
             graph.replay()
-            b.record()
             torch.cuda.synchronize()
-            best = min(best, 1e3 * a.elapsed_time(b) / n)
-        return best
+            best = float("inf")
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(10):
+                    graph.replay()
+                b.record()
+                torch.cuda.synchronize()
+                best = min(best, a.elapsed_time(b) / 10)
+            return best
+        return 1e3 * (graph_ms(n) - graph_ms(0)) / n
 
     rows = []
     for B in Bs:
@@ -794,11 +805,16 @@ def single_shape(cs, workloads, dev, name, calls, warmup):
 
 
 def latency_table(cs, workloads, dev, calls):
-    """us per call for the page's shapes: back-to-back direct calls, graph
-    replay of a one-call graph, and single calls with L2 flushed before each."""
+    """us per call for the page's shapes. From native code (cs_latency, the
+    C ABI called from C++): back-to-back calls on the same inputs (warm L2)
+    and on rotating slices of a 512 MiB pool (every call reads from HBM),
+    directly and inside a 50-call CUDA graph, and an isolated call (each
+    preceded by an empty kernel, so it overlaps nothing) reading from HBM;
+    the unfused baseline in the same graphs. From Python: back-to-back
+    calls through the binding on the same inputs (the binding's own cost is
+    the difference from the native direct figure)."""
     import torch
     rows = []
-    flush = torch.empty(64 * 1024 * 1024, device=dev)  # 256 MB > L2
     for name, B, k, d, normalize, page_us, page_ratio in PAGE_SHAPES:
         wl = workloads.random_case(B, k, d, normalize, workloads.CLM_SCALE if normalize else workloads.KEV_SCALE,
                                    90 + k, dev)
@@ -825,97 +841,42 @@ def latency_table(cs, workloads, dev, calls):
             b.record(s)
             torch.cuda.synchronize()
             reps.append(1e3 * a.elapsed_time(b) / calls)
-        direct = statistics.median(reps)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            call_in = torch.cuda.current_stream(dev)
-            if B == 1:
-                cs.cs_score_candidates(wl.Q[0], wl.C[0], normalize, wl.scale, 1.0, out=out[0], stream=call_in)
-            else:
-                cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=call_in)
-        for _ in range(20):
-            g.replay()
-        torch.cuda.synchronize()
-        reps = []
-        for _ in range(5):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            for _ in range(calls):
-                g.replay()
-            b.record(s)
-            torch.cuda.synchronize()
-            reps.append(1e3 * a.elapsed_time(b) / calls)
-        graph = statistics.median(reps)
-
-        def graph_loop_us(fn, n=50):
-            gl = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gl):
-                for _ in range(n):
-                    fn(torch.cuda.current_stream(dev))
-            for _ in range(3):
-                gl.replay()
-            torch.cuda.synchronize()
-            vals = []
-            for _ in range(5):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(s)
-                for _ in range(20):
-                    gl.replay()
-                b.record(s)
-                torch.cuda.synchronize()
-                vals.append(1e3 * a.elapsed_time(b) / (20 * n))
-            del gl
-            return statistics.median(vals)
-
-        staged = torch.empty(B, k, device=dev)
-
-        def fused_on(st):
-            cs.cs_score_candidates_batch(wl.Q, wl.C, normalize, wl.scale, 1.0, out=out, stream=st)
-
-        def unfused_on(st):
-            cs.cs_score_candidates_batch_unfused(wl.Q, wl.C, normalize, wl.scale, 1.0, staged=staged, out=out,
-                                                 stream=st)
-        fused_loop = graph_loop_us(fused_on)
-        unfused_loop = graph_loop_us(unfused_on)
-        cold = []
-        for _ in range(200):
-            flush.fill_(1.0)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            call()
-            b.record(s)
-            torch.cuda.synchronize()
-            cold.append(1e3 * a.elapsed_time(b))
+        python_direct = statistics.median(reps)
         plan = cs.cs_query_plan(wl.Q, wl.C, normalize)
         native = native_latency(B, k, d, normalize, calls)
-        rows.append({"shape": name, "B": B, "K": k, "D": d, "c_abi": native, "direct_us": direct, "graph_us": graph,
-                     "graph_loop_us": fused_loop, "cold_l2_us": statistics.median(cold),
-                     "unfused_graph_loop_us": unfused_loop, "fused_over_unfused": unfused_loop / fused_loop,
-                     "plan": plan["plan"], "cluster": plan["cluster"], "ctas": plan["ctas"],
-                     "rtx4090_fused_us_context": page_us, "rtx4090_ratio_context": page_ratio})
-        del g
+        row = {"shape": name, "B": B, "K": k, "D": d, "c_abi": native, "python_direct_warm_us": python_direct,
+               "plan": plan["plan"], "cluster": plan["cluster"], "ctas": plan["ctas"],
+               "rtx4090_fused_us_context": page_us, "rtx4090_ratio_context": page_ratio}
+        if "direct_warm_us" in native:
+            row["python_over_c_abi_direct_us"] = python_direct - native["direct_warm_us"]
+        rows.append(row)
     return rows
 
 
 def native_latency(B, K, D, normalize, calls):
     """us per call from native code (cs_latency: the C ABI called from C++,
-    no Python between calls): direct back-to-back calls, a one-call graph
-    replayed, and 50 calls in one graph; fused and unfused."""
+    no Python between calls): warm and HBM-cold back-to-back calls, direct
+    and in a 50-call graph, and isolated HBM-cold calls; the unfused
+    baseline's graph figures beside them."""
     from similarity_softmax_candidate_gb300 import _build
     try:
         tool = _build.build_latency_tool()
         res = {}
         for unfused in (0, 1):
             r = subprocess.run([tool, str(B), str(K), str(D), str(normalize), str(calls), str(unfused)],
-                               capture_output=True, text=True, timeout=120)
+                               capture_output=True, text=True, timeout=300)
             if r.returncode != 0:
                 return {"error": r.stderr.strip()[-200:]}
             d = json.loads(r.stdout.strip().splitlines()[-1])
-            tag = "unfused_" if unfused else ""
-            for key in ("direct_us", "graph1_us", "graph50_us"):
-                res[tag + key] = d[key]
-        res["fused_over_unfused_graph50"] = res["unfused_graph50_us"] / res["graph50_us"]
-        res["fused_over_unfused_direct"] = res["unfused_direct_us"] / res["direct_us"]
+            if unfused:
+                for key in ("graph_warm_us", "graph_cold_us"):
+                    res["unfused_" + key] = d[key]
+            else:
+                for key in ("direct_warm_us", "direct_cold_us", "graph_warm_us", "graph_cold_us", "isolated_cold_us",
+                            "calls", "pool_mib", "flush_us", "empty_kernel_us"):
+                    res[key] = d[key]
+        res["fused_over_unfused_graph_warm"] = res["unfused_graph_warm_us"] / res["graph_warm_us"]
+        res["fused_over_unfused_graph_cold"] = res["unfused_graph_cold_us"] / res["graph_cold_us"]
         return res
     except Exception as e:  # the Python-side numbers stand without it
         return {"error": str(e)[:200]}
