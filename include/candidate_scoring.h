@@ -39,13 +39,15 @@
  *     bit-identical output, directly or replayed from a graph.
  *   - Range. Every finite input within the range below gets a probability
  *     distribution, never NaN. The logit factor scale / temperature is
- *     formed in double precision and rounded once to float32; a factor
- *     beyond float32's range (|scale / temperature| > FLT_MAX, e.g. scale
- *     14.3 at temperature 1e-38) is refused with CS_ERR_RANGE before any
- *     CUDA call. The logits enter the softmax only as differences from
- *     their maximum, formed so that a huge factor drives them to -inf
- *     (probability exactly 0) and never to NaN; the largest logit's
- *     candidates share the probability. Dots, squared norms and |q|^2
+ *     formed in double precision; a factor with |scale / temperature| >
+ *     2^126 (about 8.5e37; e.g. scale 14.3 at temperature 1e-37) is refused
+ *     with CS_ERR_RANGE before any CUDA call -- the exact softmax of such
+ *     logits is an argmax that float32 similarities cannot settle. The
+ *     logits enter the softmax only as differences from their maximum,
+ *     formed so that a huge factor drives them to -inf (probability exactly
+ *     0) and never to NaN, and a factor below float32's range scores every
+ *     candidate alike, as the exact softmax does to within far less than
+ *     1e-4. Dots, squared norms and |q|^2
  *     accumulate in float32, so they must stay within FLT_MAX: for the dot
  *     |c| |q| <= FLT_MAX is enough, for the cosine |c| and |q| below about
  *     1.8e19 (every element below 1.8e19 / sqrt(D) is enough); tiny rows
@@ -90,7 +92,7 @@ typedef enum {
     CS_ERR_TOO_LARGE = 11,     /* B*K*D elements do not fit the 64-bit index space */
     CS_ERR_BAD_PLAN = 12,      /* cs_score_candidates_batch_plan: plan not feasible */
     CS_ERR_SCRATCH_TOO_SMALL = 13,/* B*K above CS_NOALLOC_MAX_ROWS (no-allocation entry) */
-    CS_ERR_RANGE = 14          /* |scale / temperature| exceeds FLT_MAX */
+    CS_ERR_RANGE = 14          /* |scale / temperature| exceeds 2^126 (about 8.5e37) */
 } cs_status;
 
 /* ABI version of this header and library: 1. The page's manifest records

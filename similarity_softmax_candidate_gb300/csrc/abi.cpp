@@ -46,15 +46,26 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// The logit factor scale / temperature, formed in double precision and
-// rounded once to float32. Returns CS_ERR_RANGE when it is beyond float32's
-// range (the kernels need it finite: softmax_form.cuh); a factor below
-// float32's smallest value rounds to a signed 0, which scores every
-// candidate alike, as the exact softmax does to within far less than 1e-4.
-int logit_factor(float scale, float temperature, float* factor) {
-    const double f = static_cast<double>(scale) / static_cast<double>(temperature);
-    if (!(std::fabs(f) <= static_cast<double>(FLT_MAX))) return CS_ERR_RANGE;
-    *factor = static_cast<float>(f);
+// The logit factor a = scale / temperature, formed in double precision and
+// split into the value scale w0 and exponent scale kexp of softmax_form.cuh
+// (both rounded once to float32). Returns CS_ERR_RANGE for |a| > 2^126:
+// the form needs kexp finite, and the exact softmax of such logits is an
+// argmax that float32 similarities cannot settle anyway. A factor too small
+// for float32 gives kexp = 0, which scores every candidate alike, as the
+// exact softmax does to within far less than 1e-4.
+constexpr double kLog2e = 1.44269504088896340736;  // log2(e)
+constexpr double kMaxFactor = 85070591730234615865843651857942052864.0;  // 2^126
+constexpr double kHalveBelow = 7.88860905221011805411728565283e-31;    // 2^-100
+
+int logit_form(float scale, float temperature, int normalize, float* w0, float* kexp) {
+    const double a = static_cast<double>(scale) / static_cast<double>(temperature);
+    const double mag = std::fabs(a);
+    if (!(mag <= kMaxFactor)) return CS_ERR_RANGE;
+    // the dot halves its values under a tiny factor, so that the difference
+    // of two dots stays finite where the factor would not shrink it to 0
+    const double w = (!normalize && mag < kHalveBelow) ? 0.5 : 1.0;
+    if (w0) *w0 = static_cast<float>(a < 0 ? -w : w);
+    if (kexp) *kexp = static_cast<float>(mag * kLog2e / w);
     return CS_OK;
 }
 
@@ -70,8 +81,7 @@ int validate(const float* Q, const void* C, long long B, int K, int D, int norma
     if (check_scalars) {
         if (!std::isfinite(scale) || scale == 0.0f) return CS_ERR_BAD_SCALE;
         if (!std::isfinite(temperature) || !(temperature > 0.0f)) return CS_ERR_BAD_TEMPERATURE;
-        float f;
-        const int r = logit_factor(scale, temperature, &f);
+        const int r = logit_form(scale, temperature, normalize, nullptr, nullptr);
         if (r != CS_OK) return r;
     }
     // B*K*D elements, as bytes, must fit comfortably in 64 bits.
@@ -428,8 +438,8 @@ int run(const float* Q, const void* C, long long B, int K, int D, int normalize,
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, 0.f, nullptr, c_bf16, nullptr, 0};
-    (void)logit_factor(scale, temperature, &p.factor);  // validated above
+    Problem p{Q, C, out, B, K, D, normalize, 0.f, 0.f, nullptr, c_bf16, nullptr, 0};
+    (void)logit_form(scale, temperature, normalize, &p.w0, &p.kexp);  // validated above
     Plan plan{};
     const int s = make_plan(*d, p, kind, cluster, ctas, &plan);
     if (s != CS_OK) return s;
@@ -455,8 +465,8 @@ int run_ragged(const float* Q, const void* C, const long long* offsets, long lon
     if (normalize != 0 && normalize != 1) return CS_ERR_BAD_SIMILARITY;
     if (!std::isfinite(scale) || scale == 0.0f) return CS_ERR_BAD_SCALE;
     if (!std::isfinite(temperature) || !(temperature > 0.0f)) return CS_ERR_BAD_TEMPERATURE;
-    float factor;
-    if (logit_factor(scale, temperature, &factor) != CS_OK) return CS_ERR_RANGE;
+    float w0, kexp;
+    if (logit_form(scale, temperature, normalize, &w0, &kexp) != CS_OK) return CS_ERR_RANGE;
     const unsigned long long cb = c_bf16 ? 2ull : 4ull, rows = static_cast<unsigned long long>(total_rows);
     if (rows > (1ull << 60) / static_cast<unsigned long long>(D)) return CS_ERR_TOO_LARGE;
     const unsigned long long out_b = rows * 4ull, q_b = static_cast<unsigned long long>(B) * D * 4ull,
@@ -465,7 +475,7 @@ int run_ragged(const float* Q, const void* C, const long long* offsets, long lon
         return CS_ERR_ALIAS;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, CS_MAX_K, D, normalize, factor, nullptr, c_bf16, offsets, total_rows};
+    Problem p{Q, C, out, B, CS_MAX_K, D, normalize, w0, kexp, nullptr, c_bf16, offsets, total_rows};
     Plan plan{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan);
     if (s != CS_OK) return s;
@@ -485,8 +495,8 @@ int run_unfused(const float* Q, const float* C, long long B, int K, int D, int n
         return CS_ERR_ALIAS;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, out, B, K, D, normalize, 0.f, staged, 0, nullptr, 0};
-    (void)logit_factor(scale, temperature, &p.factor);  // validated above
+    Problem p{Q, C, out, B, K, D, normalize, 0.f, 0.f, staged, 0, nullptr, 0};
+    (void)logit_form(scale, temperature, normalize, &p.w0, &p.kexp);  // validated above
     Plan plan{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &plan, false);
     if (s != CS_OK) return s;
@@ -519,7 +529,7 @@ const char* cs_status_string(int status) {
         case CS_ERR_ALIAS: return "out overlaps Q or C";
         case CS_ERR_TOO_LARGE: return "B*K*D is too large";
         case CS_ERR_BAD_PLAN: return "requested plan cannot run these arguments";
-        case CS_ERR_RANGE: return "scale / temperature is beyond float32's range";
+        case CS_ERR_RANGE: return "|scale / temperature| exceeds 2^126";
         case CS_ERR_SCRATCH_TOO_SMALL:
             return "B*K exceeds the built-in scratch of the no-allocation entry point (1048576 rows)";
         default: return "unknown status";
@@ -589,7 +599,7 @@ int cs_query_plan(const float* Q, const float* C, int B, int K, int D, int norma
     if (v != CS_OK) return v;
     DeviceState* d = nullptr;
     if (device_state(&d) != cudaSuccess) return CS_ERR_LAUNCH;
-    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, nullptr, 0, nullptr, 0};
+    Problem p{Q, C, nullptr, B, K, D, normalize, 1.f, 1.f, nullptr, 0, nullptr, 0};
     Plan pl{};
     const int s = make_plan(*d, p, cs::kPlanAuto, 0, 0, &pl);
     if (s != CS_OK) return s;
@@ -641,8 +651,8 @@ int cs_project_score_batch(const uint16_t* Hq, const uint16_t* Wq, const uint16_
     if (normalize != 0 && normalize != 1) return CS_ERR_BAD_SIMILARITY;
     if (!std::isfinite(scale) || scale == 0.0f) return CS_ERR_BAD_SCALE;
     if (!std::isfinite(temperature) || !(temperature > 0.0f)) return CS_ERR_BAD_TEMPERATURE;
-    float factor;
-    if (logit_factor(scale, temperature, &factor) != CS_OK) return CS_ERR_RANGE;
+    float w0, kexp;
+    if (logit_form(scale, temperature, normalize, &w0, &kexp) != CS_OK) return CS_ERR_RANGE;
     if (!aligned16(Hq) || !aligned16(Wq) || !aligned16(Hc) || !aligned16(Wc) || !aligned16(qproj))
         return CS_ERR_BAD_PLAN;
     const unsigned long long bk = static_cast<unsigned long long>(B) * K;
@@ -659,7 +669,7 @@ int cs_project_score_batch(const uint16_t* Hq, const uint16_t* Wq, const uint16_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cs::launch_project_rows(Hq, Wq, B, Din, D, qproj, d->sms, d->status, d->bounds, st);
     if (e == cudaSuccess)
-        e = cs::launch_project_score(Hc, Wc, qproj, B, K, Din, D, normalize, factor, out, d->sms, d->status,
+        e = cs::launch_project_score(Hc, Wc, qproj, B, K, Din, D, normalize, w0, kexp, out, d->sms, d->status,
                                      d->bounds, st);
     return e == cudaSuccess ? CS_OK : CS_ERR_LAUNCH;
 }

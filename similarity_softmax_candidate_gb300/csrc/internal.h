@@ -37,11 +37,13 @@ struct Problem {
     int K;
     int D;
     int normalize;     // 1 cosine, 0 dot
-    // The logit factor scale / temperature, formed in double precision and
-    // rounded once to float32 by the host, which refuses a factor beyond
-    // float32's range: finite, possibly 0 (a factor below float32's
-    // smallest denormal) or negative. Logits are factor * similarity.
-    float factor;
+    // The logit factor a = scale / temperature, split by the host (which
+    // forms it in double precision and refuses |a| > 2^126) into the signed
+    // value scale w0 and the exponent scale kexp = |a| log2(e) / |w0| of
+    // softmax_form.cuh: w0 = sign(a) for the cosine, and for the dot sign(a)
+    // or, when |a| < 2^-100, sign(a) / 2.
+    float w0;
+    float kexp;
     float* staged;     // unfused baseline only: one float per row [B][K]
     int c_bf16;        // 1: C holds bfloat16 bit patterns (2 bytes each)
     // Ragged batches: question b owns rows offsets[b] .. offsets[b+1]-1 of C
@@ -119,7 +121,7 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
 // (uniform K, B <= 65535).
 cudaError_t launch_generic(const Problem& p, int G, cudaStream_t stream);
 int max_active_generic_clusters(int cluster, int normalize, int c_bf16);
-// Unfused baseline pass 2 (dot): softmax of factor * staged.
+// Unfused baseline pass 2 (dot): softmax of a * staged (a the logit factor).
 cudaError_t launch_staged_softmax(const Problem& p, cudaStream_t stream);
 
 // Size, in floats, of the built-in staged array of the no-allocation
@@ -151,7 +153,7 @@ cudaError_t configure_proj_kernels(int smem_optin);
 cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
                                 int sms, unsigned* status, unsigned* bounds, cudaStream_t stream);
 cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
-                                 int D, int normalize, float factor, float* out, int sms, unsigned* status,
+                                 int D, int normalize, float w0, float kexp, float* out, int sms, unsigned* status,
                                  unsigned* bounds, cudaStream_t stream);
 // Device address of the status word on the current device (for kernels in
 // other translation units).

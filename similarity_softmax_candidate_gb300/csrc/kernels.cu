@@ -300,9 +300,11 @@ __device__ __forceinline__ void wait_phase_until(uint32_t bar, uint32_t parity, 
 
 // ------------------------------------------------------------------ range-safe softmax
 //
-// Rows become values v_k (softmax_form.cuh: the softmax of the logits is
-// exp(2|a| (v_k - max v)) normalised, which no finite input turns into NaN);
-// a row float32 could not hold is NaN, and its question is skipped.
+// Rows become values v_k (softmax_form.cuh): the probabilities are
+// 2^(kexp (v_k - max v)) normalised, which no finite input turns into NaN,
+// and a row float32 could not hold has the value NaN. NaN carries into the
+// question's sum of exponentials (the max ignores it), and a question whose
+// sum is NaN is skipped unscored.
 
 // v of one row from its dot t and, for the fused cosine, its squared norm
 // nsq (the staged cosine passes the staged norm instead).
@@ -328,22 +330,11 @@ __device__ __forceinline__ void load_values(const float* t, const float* n_sq, c
     }
 }
 
-// True on every lane when some row lane + 32 j < n of the warp is flagged.
+// One warp's rows (lane + 32 j < n) reduced to the max of their values
+// (flagged rows ignored) and, in v, their exponentials relative to it;
+// returns the warp's sum of those, NaN when a row is flagged.
 template <int S>
-__device__ __forceinline__ bool any_flagged(const float (&v)[S], int n, int lane) {
-    bool bad = false;
-#pragma unroll
-    for (int j = 0; j < S; ++j) bad |= lane + 32 * j < n && !isfinite(v[j]);
-    return __any_sync(0xffffffffu, bad);
-}
-
-// Softmax over one warp (rows lane + 32 j < n) of the values v, written to
-// dst[0..n). Returns false, writing nothing, when a row is flagged; the
-// caller then records the range bit (unless its CTA gave up waiting, which
-// is what flagged the rows).
-template <int S = kSlotsPerLane>
-__device__ __forceinline__ bool softmax_store(float (&v)[S], int n, float afac, float* __restrict__ dst, int lane) {
-    if (any_flagged(v, n, lane)) return false;
+__device__ __forceinline__ float exp_rows(float (&v)[S], int n, float kexp, int lane, float* m_out) {
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < S; ++j) m = fmaxf(m, v[j]);
@@ -351,10 +342,23 @@ __device__ __forceinline__ bool softmax_store(float (&v)[S], int n, float afac, 
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < S; ++j) {
-        v[j] = lane + 32 * j < n ? softmax_term(afac, v[j] - m) : 0.f;
+        v[j] = lane + 32 * j < n ? softmax_term(kexp, v[j] - m) : 0.f;
         s += v[j];
     }
-    const float inv = 1.0f / warp_sum(s);
+    *m_out = m;
+    return warp_sum(s);
+}
+
+// Softmax over one warp (rows lane + 32 j < n) of the values v, written to
+// dst[0..n). Returns false, writing nothing, when a row is flagged; the
+// caller then records the range bit (unless its CTA gave up waiting, which
+// is what flagged the rows).
+template <int S = kSlotsPerLane>
+__device__ __forceinline__ bool softmax_store(float (&v)[S], int n, float kexp, float* __restrict__ dst, int lane) {
+    float m;
+    const float s = exp_rows(v, n, kexp, lane, &m);
+    if (isnan(s)) return false;
+    const float inv = 1.0f / s;
 #pragma unroll
     for (int j = 0; j < S; ++j) {
         const int k = lane + 32 * j;
@@ -370,25 +374,23 @@ __device__ __forceinline__ void record_range(volatile int* give_up) {
 }
 
 // Cluster exchange: each CTA reduces its rows to (m, s) = (max v, sum of
-// exp(2|a| (v - m))); a CTA with a flagged row sends m = NaN, so that every
-// CTA of the cluster skips the question. combine_pairs reads the G pairs in
+// 2^(kexp (v - m))), s NaN when it holds a flagged row, and every CTA of
+// the cluster then skips the question. combine_pairs reads the G pairs in
 // xch (lanes < G one each) and returns the normaliser
-// 1 / sum_g s_g exp(2|a| (m_g - M)) with M = max m_g (M_out); flagged: some
+// 1 / sum_g s_g 2^(kexp (m_g - M)) with M = max m_g (M_out); flagged: some
 // CTA sent NaN. A CTA without rows sends (-inf, 0) and adds nothing.
-__device__ __forceinline__ float combine_pairs(const float2* xch, int G, float afac, int lane, float* M_out,
+__device__ __forceinline__ float combine_pairs(const float2* xch, int G, float kexp, int lane, float* M_out,
                                                bool* flagged) {
     float mj = -INFINITY, sj = 0.f;
-    bool bad = false;
     if (lane < G) {
         const float2 x = xch[lane];
         mj = x.x;
         sj = x.y;
-        bad = isnan(mj);
     }
-    *flagged = __any_sync(0xffffffffu, bad);
-    const float M = warp_max(bad ? -INFINITY : mj);
+    *flagged = __any_sync(0xffffffffu, isnan(sj));
+    const float M = warp_max(mj);
     *M_out = M;
-    return 1.0f / warp_sum(lane < G && sj > 0.f ? sj * softmax_term(afac, mj - M) : 0.f);
+    return 1.0f / warp_sum(sj > 0.f ? sj * softmax_term(kexp, mj - M) : 0.f);
 }
 
 // Sums each of the V values v[0..V) over the 32 lanes of a warp with V - 1
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     const uint32_t row_bytes = static_cast<uint32_t>(D) * sizeof(T);  // a row of C
     const uint32_t q_bytes = static_cast<uint32_t>(D) * 4u;
     float w = 1.f;  // value scale of the current question (value_scale)
-    const float afac = fabsf(p.factor);
+    const float kexp = p.kexp;
     QRows last{0, 0, false};  // rows of the last question (the cluster plan's only one)
 
     if (warp == kConsumerWarps) {
@@ -838,7 +840,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 }
                 qsq = warp_sum(sq);
             }
-            w = value_scale(p.factor, qsq, COS);
+            w = value_scale(p.w0, qsq, COS);
 
             float* tb = tn + (nq & 1) * 2 * kLogitSlots;  // dots
             float* nb = tb + kLogitSlots;                 // squared norms
@@ -891,11 +893,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 if (inb && nrows <= 32) {  // one row per lane: the short code path
                     float v[1];
                     load_values<MODE, 1>(tb, nb, sn, nrows, w, lane, v);
-                    done = softmax_store<1>(v, nrows, afac, p.out + qr.row0, lane);
+                    done = softmax_store<1>(v, nrows, kexp, p.out + qr.row0, lane);
                 } else if (inb) {
                     float v[kSlotsPerLane];
                     load_values<MODE>(tb, nb, sn, nrows, w, lane, v);
-                    done = softmax_store(v, nrows, afac, p.out + qr.row0, lane);
+                    done = softmax_store(v, nrows, kexp, p.out + qr.row0, lane);
                 }
                 if (!done && lane == 0) record_range(give_up);
             }
@@ -926,23 +928,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const int nread = rd ? nrows : 0;
             load_values<MODE, S>(tn, tn + kLogitSlots, MODE == kStagedCos ? p.staged + last.row0 : nullptr, nread, w,
                                  lane, v);
-            const bool bad = any_flagged(v, nread, lane);
-            float m = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < S; ++j) m = fmaxf(m, v[j]);
-            m = warp_max(m);
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < S; ++j)
-                if (lane + 32 * j < nread) s += softmax_term(afac, v[j] - m);
-            s = warp_sum(s);
+            float m;
+            const float s = exp_rows<S>(v, nread, kexp, lane, &m);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
-                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(bad ? qnan() : m, s),
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
                               peer_addr(xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(xbar), 0, give_up);
             float M;
             bool flagged;
-            const float inv = combine_pairs(xch, G, afac, lane, &M, &flagged);
+            const float inv = combine_pairs(xch, G, kexp, lane, &M, &flagged);
+            const float rescale = softmax_term(kexp, m - M) * inv;  // 2^(kexp (m - M)) / S
             float* dst = p.out + last.row0;
             if (ok && flagged) {
                 if (lane == 0) record_range(give_up);
@@ -950,7 +945,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
 #pragma unroll
                 for (int j = 0; j < S; ++j) {
                     const int k = lane + 32 * j;
-                    if (k < nrows) dst[k] = ok ? softmax_term(afac, v[j] - M) * inv : qnan();
+                    if (k < nrows) dst[k] = ok ? v[j] * rescale : qnan();
                 }
             }
         };
@@ -1074,8 +1069,8 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
             }
         qsq = warp_sum(sq);  // each warp covers all of q: never summed across warps
     }
-    const float w = value_scale(p.factor, qsq, COS);
-    const float afac = fabsf(p.factor);
+    const float w = value_scale(p.w0, qsq, COS);
+    const float kexp = p.kexp;
 
     // dot (and squared norm) of each row: two packed partial sums each
     unsigned long long acc[V];
@@ -1124,13 +1119,12 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
         float* dst = p.out + qr.row0;
         const bool out_ok = CS_IN_BOUNDS(dst, n * 4ll, p.out, rows_total(p) * 4, kSiteOutCluster);
         if (G == 1) {
-            if (out_ok && !softmax_store<1>(v, n, afac, dst, lane) && lane == 0) record_range(give_up);
+            if (out_ok && !softmax_store<1>(v, n, kexp, dst, lane) && lane == 0) record_range(give_up);
         } else {
-            const bool bad = any_flagged(v, n, lane);
-            const float m = warp_max(v[0]);
-            const float s = warp_sum(lane < n ? softmax_term(afac, v[0] - m) : 0.f);
+            float m;
+            const float s = exp_rows<1>(v, n, kexp, lane, &m);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
-                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(bad ? qnan() : m, s),
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
                               peer_addr(&xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
             // Every pair bound for this CTA has landed (or the wait gave up,
@@ -1142,11 +1136,11 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
             arrived = true;
             float M;
             bool flagged;
-            const float inv = combine_pairs(xch, G, afac, lane, &M, &flagged);
+            const float inv = combine_pairs(xch, G, kexp, lane, &M, &flagged);
             if (ok && flagged) {
                 if (lane == 0) record_range(give_up);
             } else if (out_ok && lane < n) {
-                dst[lane] = ok ? softmax_term(afac, v[0] - M) * inv : qnan();
+                dst[lane] = ok ? v[0] * (softmax_term(kexp, m - M) * inv) : qnan();
             }
         }
     }
@@ -1205,8 +1199,8 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         }
         qsq = warp_sum(sq);  // whole norm per warp, never summed across warps
     }
-    const float w = value_scale(p.factor, qsq, COS);
-    const float afac = fabsf(p.factor);
+    const float w = value_scale(p.w0, qsq, COS);
+    const float kexp = p.kexp;
     for (int k = warp; k < K && !skip; k += nwarps) {
         const T* __restrict__ c = static_cast<const T*>(p.C) + static_cast<size_t>(qr.row0 + k) * D;
         if (!CS_IN_BOUNDS(c, D * static_cast<long long>(sizeof(T)), p.C, rows_total(p) * D * static_cast<long long>(sizeof(T)),
@@ -1244,20 +1238,13 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
         float* dst = p.out + qr.row0;
         if constexpr (!CL) {
             // no waits in this form, so a flagged row is a range failure
-            if (!softmax_store(v, K, afac, dst, lane) && lane == 0) atomicOr(&g_status, kDevErrRange);
+            if (!softmax_store(v, K, kexp, dst, lane) && lane == 0) atomicOr(&g_status, kDevErrRange);
         } else {
             // this CTA's (max, sum of exp) to every CTA of the cluster
-            const bool bad = any_flagged(v, K, lane);
-            float m = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j) m = fmaxf(m, v[j]);
-            m = warp_max(m);
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < kSlotsPerLane; ++j) s += lane + 32 * j < K ? softmax_term(afac, v[j] - m) : 0.f;
-            s = warp_sum(s);
+            float m;
+            const float s = exp_rows<kSlotsPerLane>(v, K, kexp, lane, &m);
             if (lane < G && CS_IN_BOUNDS(xch + rank, 8, xch, kMaxCluster * 8, kSitePeer))
-                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(bad ? qnan() : m, s),
+                st_async_peer(peer_addr(xch + rank, static_cast<uint32_t>(lane)), make_float2(m, s),
                               peer_addr(&xbar, static_cast<uint32_t>(lane)));
             const bool ok = wait_phase(smem_u32(&xbar), 0, give_up);
             // every pair bound for this CTA has landed (or the wait gave up)
@@ -1266,13 +1253,14 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Problem 
             arrived = true;
             float M;
             bool flagged;
-            const float inv = combine_pairs(xch, G, afac, lane, &M, &flagged);
+            const float inv = combine_pairs(xch, G, kexp, lane, &M, &flagged);
+            const float rescale = softmax_term(kexp, m - M) * inv;
             if (ok && flagged) {
                 if (lane == 0) record_range(give_up);
             } else {
 #pragma unroll
                 for (int j = 0; j < kSlotsPerLane; ++j)
-                    if (lane + 32 * j < K) dst[lane + 32 * j] = ok ? softmax_term(afac, v[j] - M) * inv : qnan();
+                    if (lane + 32 * j < K) dst[lane + 32 * j] = ok ? v[j] * rescale : qnan();
             }
         }
     }
@@ -1290,14 +1278,14 @@ __global__ void __launch_bounds__(256) staged_softmax_kernel(const Problem p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long b = static_cast<long long>(blockIdx.x) * 8 + warp;
     if (b >= p.B) return;
-    const float w = value_scale(p.factor, 0.f, false), afac = fabsf(p.factor);
+    const float w = p.w0;
     const float* t = p.staged + static_cast<size_t>(b) * p.K;
     if (!CS_IN_BOUNDS(t, p.K * 4ll, p.staged, p.B * p.K * 4ll, kSiteStagedSoftmax) ||
         !CS_IN_BOUNDS(p.out + static_cast<size_t>(b) * p.K, p.K * 4ll, p.out, p.B * p.K * 4ll, kSiteStagedSoftmaxOut))
         return;
     float v[kSlotsPerLane];
     load_values<kFusedDot>(t, nullptr, nullptr, p.K, w, lane, v);
-    if (!softmax_store(v, p.K, afac, p.out + static_cast<size_t>(b) * p.K, lane) && lane == 0)
+    if (!softmax_store(v, p.K, p.kexp, p.out + static_cast<size_t>(b) * p.K, lane) && lane == 0)
         atomicOr(&g_status, kDevErrRange);  // no waits here: a flagged row is a range failure
 }
 

@@ -60,7 +60,7 @@ struct ProjArgs {
     long long rows;     // rows of A (PLAIN: rows to project; SCORE: B*K)
     int B, K, Din, D;   // SCORE: B questions of K rows
     int normalize;
-    float factor;       // SCORE: scale / temperature (finite, rounded once on the host)
+    float w0, kexp;     // SCORE: value and exponent scales of the logit factor (softmax_form.cuh)
     const float* qproj; // SCORE: projected queries [B][D]
     float* out;         // PLAIN: [rows][D]; SCORE: [B][K]
     unsigned* status;   // device status word
@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 if (a.normalize)
                     for (int i = lane; i < D; i += 32) sq = fmaf(qs[i], qs[i], sq);
                 sq = wsum(sq);
-                w = form::value_scale(a.factor, sq, a.normalize != 0);
+                w = form::value_scale(a.w0, sq, a.normalize != 0);
             }
             for (int h = 0; h < tiles_per_item; ++h) {
                 float dot = 0.f, nrm = 0.f;
@@ -481,30 +481,27 @@ __global__ void __launch_bounds__(kProjThreads, 1)
             if (MODE == kProjScore) {
                 epi_bar_sync();  // every logit of the question is in lg
                 if (warp == 2) {
-                    // softmax of the values (softmax_form.cuh); a question with
-                    // a flagged row is skipped unscored
-                    const float afac = fabsf(a.factor);
+                    // softmax of the values (softmax_form.cuh); a flagged row
+                    // makes the sum NaN, and the question is skipped unscored
                     float z[8];
                     float m = -INFINITY;
-                    bool bad = false;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int k = lane + 32 * j;
                         z[j] = k < a.K ? lg[k] : -INFINITY;
-                        bad |= k < a.K && !isfinite(z[j]);
                         m = fmaxf(m, z[j]);
                     }
-                    bad = __any_sync(0xffffffffu, bad);
                     m = wmax(m);
                     float s = 0.f;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        z[j] = lane + 32 * j < a.K ? form::softmax_term(afac, z[j] - m) : 0.f;
+                        z[j] = lane + 32 * j < a.K ? form::softmax_term(a.kexp, z[j] - m) : 0.f;
                         s += z[j];
                     }
-                    const float inv = 1.0f / wsum(s);
+                    s = wsum(s);
+                    const float inv = 1.0f / s;
                     float* dst = a.out + static_cast<size_t>(item) * a.K;
-                    if (bad) {
+                    if (isnan(s)) {
                         if (lane == 0 && !*give_up) atomicOr(a.status, kDevErrRange);
                     } else if (CS_IN_BOUNDS(dst, a.K * 4ll, a.out, a.B * a.K * 4ll, kSiteProjOut)) {
 #pragma unroll
@@ -598,7 +595,7 @@ cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long 
 }
 
 cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const float* qproj, int B, int K, int Din,
-                                 int D, int normalize, float factor, float* out, int sms,
+                                 int D, int normalize, float w0, float kexp, float* out, int sms,
                                  unsigned* status, unsigned* bounds, cudaStream_t stream) {
     CUtensorMap ma, mw;
     const unsigned long long rows = static_cast<unsigned long long>(B) * K;
@@ -611,7 +608,8 @@ cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const f
     a.Din = Din;
     a.D = D;
     a.normalize = normalize;
-    a.factor = factor;
+    a.w0 = w0;
+    a.kexp = kexp;
     a.qproj = qproj;
     a.out = out;
     a.status = status;

@@ -87,10 +87,10 @@ REJECTS = [
     ("temperature_zero", dict(temperature=0.0), binding.CS_ERR_BAD_TEMPERATURE),
     ("temperature_nan", dict(temperature=math.nan), binding.CS_ERR_BAD_TEMPERATURE),
     ("temperature_inf", dict(temperature=math.inf), binding.CS_ERR_BAD_TEMPERATURE),
-    # scale / temperature beyond float32's range: the kernels need the logit
-    # factor finite, and the exact softmax of such logits is an argmax that
-    # float32 similarities cannot settle reliably
-    ("factor_tiny_temperature", dict(scale=14.2857, temperature=1e-38), binding.CS_ERR_RANGE),
+    # |scale / temperature| above 2^126: the kernels need the logit factor
+    # times log2(e) finite, and the exact softmax of such logits is an
+    # argmax that float32 similarities cannot settle reliably
+    ("factor_tiny_temperature", dict(scale=14.2857, temperature=1e-37), binding.CS_ERR_RANGE),
     ("factor_huge_scale", dict(scale=3e38, temperature=0.5), binding.CS_ERR_RANGE),
     ("factor_negative", dict(scale=-1e30, temperature=1e-10), binding.CS_ERR_RANGE),
     ("null_query", dict(Q=None), binding.CS_ERR_NULL_POINTER),
@@ -131,15 +131,17 @@ def test_rejects_oversized_problem(host_lib):
 
 def test_largest_factor_is_checked_in_double_precision(host_lib):
     """The factor is scale / temperature formed in double precision and
-    refused beyond FLT_MAX. A factor of exactly FLT_MAX passes the scalar
+    refused above 2^126. A factor of exactly 2^126 passes the scalar
     checks: with an overlapping out, the call then stops at the overlap
-    check, which validation makes after the scalars."""
-    f32max = float(np.finfo(np.float32).max)
-    assert _batch(host_lib, scale=f32max, temperature=0.99999) == binding.CS_ERR_RANGE
-    assert _batch(host_lib, scale=-f32max, temperature=0.5) == binding.CS_ERR_RANGE
+    check, which validation makes after the scalars; so does a factor too
+    small for float32."""
+    top = 2.0 ** 126
+    assert _batch(host_lib, scale=top, temperature=0.999) == binding.CS_ERR_RANGE
+    assert _batch(host_lib, scale=-top, temperature=0.5) == binding.CS_ERR_RANGE
+    assert _batch(host_lib, scale=float(np.finfo(np.float32).max), temperature=1.0) == binding.CS_ERR_RANGE
     B, K, D = 4, 8, 16
-    assert _batch(host_lib, B=B, K=K, D=D, scale=f32max, temperature=1.0, out=C_ADDR + 400) == binding.CS_ERR_ALIAS
-    assert _batch(host_lib, B=B, K=K, D=D, scale=1e-30, temperature=1e30, out=C_ADDR + 400) == binding.CS_ERR_ALIAS
+    for scale, T in ((top, 1.0), (-top, 1.0), (1e-30, 1e30)):
+        assert _batch(host_lib, B=B, K=K, D=D, scale=scale, temperature=T, out=C_ADDR + 400) == binding.CS_ERR_ALIAS
 
 
 def test_first_failing_check_wins(host_lib):
@@ -244,7 +246,7 @@ def test_ragged_rejects(host_lib):
     assert _ragged(host_lib, normalize=3) == E.CS_ERR_BAD_SIMILARITY
     assert _ragged(host_lib, scale=0.0) == E.CS_ERR_BAD_SCALE
     assert _ragged(host_lib, temperature=-2.0) == E.CS_ERR_BAD_TEMPERATURE
-    assert _ragged(host_lib, scale=14.2857, temperature=1e-38) == E.CS_ERR_RANGE
+    assert _ragged(host_lib, scale=14.2857, temperature=1e-37) == E.CS_ERR_RANGE
     assert _ragged(host_lib, out=OFF_ADDR + 8) == E.CS_ERR_ALIAS         # out over the offsets
     assert _ragged(host_lib, out=C_ADDR + 4 * 512 * 39) == E.CS_ERR_ALIAS
     assert host_lib.cs_score_candidates_ragged_bf16(Q_ADDR, C_ADDR, OFF_ADDR, 4, 40, 512, 1, 2.0, 1.0,
@@ -280,7 +282,7 @@ def test_project_rejects(host_lib):
     assert call(B=(1 << 31) // 200, K=255) == E.CS_ERR_BAD_BATCH  # B*K > CS_PROJ_MAX_ROWS
     assert call(s=0.0) == E.CS_ERR_BAD_SCALE
     assert call(t=-1.0) == E.CS_ERR_BAD_TEMPERATURE
-    assert call(s=14.2857, t=1e-38) == E.CS_ERR_RANGE
+    assert call(s=14.2857, t=1e-37) == E.CS_ERR_RANGE
     assert call(n=5) == E.CS_ERR_BAD_SIMILARITY
     assert call(D=128) == E.CS_ERR_BAD_PLAN
     assert call(out=C_ADDR) == E.CS_ERR_ALIAS

@@ -6,14 +6,15 @@ the arguments are bad. Here that rule meets float32: the fp64 oracle scores
 any finite input, the kernels accumulate in float32. So:
 
   * inputs inside the documented range get the oracle's distribution, also
-    where a naive float32 logit would overflow: a logit factor near
-    FLT_MAX, a query so short that scale / |q| overflows, dots whose
+    where a naive float32 logit would overflow: a logit factor near the
+    2^126 limit, a query so short that scale / |q| overflows, dots whose
     differences exceed FLT_MAX, a factor that underflows to 0;
   * a question whose dots or squared norms leave float32's range, or that
     holds a NaN or an infinity, is skipped: its rows of out keep what they
     held, the other questions are scored, and CS_DEVERR_RANGE is set;
   * a factor scale / temperature beyond FLT_MAX is refused on the host
-    (tests/test_abi_host.py) -- here, that no launch happened.
+    (2^126 and above: tests/test_abi_host.py) -- here, that no launch
+    happened.
 
 Every plan and entry point is run, since each forms its logits in its own
 code.
@@ -142,14 +143,14 @@ def _one_hot_case(normalize, B=2, K=40, D=512, qscale=1.0):
 
 @pytest.mark.parametrize("plan", PLANS)
 @pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
-def test_factor_near_float32_max(cuda_lib, plan, normalize):
-    """scale / temperature = 3e38 (and -3e38): accepted, and the softmax of
-    such logits puts all the weight on the largest (smallest) similarity,
-    shared between the two equal rows. For the cosine the query is short
-    (times 1e-3), so that scale / (T |q|) -- the factor a plain float32
-    kernel would form -- overflows."""
+def test_factor_near_its_limit(cuda_lib, plan, normalize):
+    """scale / temperature = 8e37 (and -8e37), just under the 2^126 limit:
+    accepted, and the softmax of such logits puts all the weight on the
+    largest (smallest) similarity, shared between the two equal rows. For
+    the cosine the query is short (times 1e-3), so that scale / (T |q|) --
+    the factor a plain float32 kernel would form -- overflows."""
     Q, C = _one_hot_case(normalize, qscale=1e-3 if normalize else 1.0)
-    for scale in (3e38, -3e38):
+    for scale in (8e37, -8e37):
         out, status = _run(plan, Q, C, normalize, scale, 1.0)
         assert status == 0
         ref = _ref(plan, Q, C, normalize, scale, 1.0)
@@ -176,6 +177,13 @@ def test_dot_differences_beyond_float32_max(cuda_lib, plan):
     ref = _ref(plan, Q, C, 0, scale, 1.0)
     assert ref[0, 1] > 1e-3  # the oracle's answer is not a one-hot
     assert_parity(out, ref, plan)
+    # at scale 1e-20 the same dots make logits of +-3e18: all the weight on
+    # row 0, although the difference of the two dots is beyond FLT_MAX
+    out, status = _run(plan, Q, C, 0, 1e-20, 1.0)
+    assert status == 0
+    ref = _ref(plan, Q, C, 0, 1e-20, 1.0)
+    assert np.allclose(ref[:, 0], 1.0)
+    assert_parity(out, ref, plan + " scale 1e-20")
 
 
 @pytest.mark.parametrize("plan", PLANS)
@@ -194,7 +202,7 @@ def test_refused_factor_launches_nothing(cuda_lib):
     wl = workloads.random_case(2, 40, 512, 1, 1.0, 66, DEV)
     out = torch.full((2, 40), SENTINEL, device=DEV)
     with pytest.raises(binding.CSError) as e:
-        binding.cs_score_candidates_batch(wl.Q, wl.C, 1, 14.2857, 1e-38, out=out)
+        binding.cs_score_candidates_batch(wl.Q, wl.C, 1, 14.2857, 1e-37, out=out)
     assert e.value.status == binding.CS_ERR_RANGE
     torch.cuda.synchronize()
     assert torch.all(out == SENTINEL)
