@@ -92,7 +92,8 @@ typedef enum {
     CS_ERR_TOO_LARGE = 11,     /* B*K*D elements do not fit the 64-bit index space */
     CS_ERR_BAD_PLAN = 12,      /* cs_score_candidates_batch_plan: plan not feasible */
     CS_ERR_SCRATCH_TOO_SMALL = 13,/* B*K above CS_NOALLOC_MAX_ROWS (no-allocation entry) */
-    CS_ERR_RANGE = 14          /* |scale / temperature| exceeds 2^126 (about 8.5e37) */
+    CS_ERR_RANGE = 14,         /* |scale / temperature| exceeds 2^126 (about 8.5e37) */
+    CS_ERR_MISALIGNED = 15     /* a pointer is not aligned to its element size */
 } cs_status;
 
 /* ABI version of this header and library: 1. The page's manifest records

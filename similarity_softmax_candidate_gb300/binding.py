@@ -26,7 +26,7 @@ STATUS = {
     0: "CS_OK", 1: "CS_ERR_NULL_POINTER", 2: "CS_ERR_K_ZERO", 3: "CS_ERR_K_TOO_LARGE",
     4: "CS_ERR_D_ZERO", 5: "CS_ERR_BAD_SCALE", 6: "CS_ERR_BAD_TEMPERATURE", 7: "CS_ERR_BAD_BATCH",
     8: "CS_ERR_BAD_SIMILARITY", 9: "CS_ERR_LAUNCH", 10: "CS_ERR_ALIAS", 11: "CS_ERR_TOO_LARGE",
-    12: "CS_ERR_BAD_PLAN", 13: "CS_ERR_SCRATCH_TOO_SMALL", 14: "CS_ERR_RANGE",
+    12: "CS_ERR_BAD_PLAN", 13: "CS_ERR_SCRATCH_TOO_SMALL", 14: "CS_ERR_RANGE", 15: "CS_ERR_MISALIGNED",
 }
 CS_NOALLOC_MAX_ROWS = 1 << 20
 CS_PROJ_MAX_ROWS = (1 << 31) - 256

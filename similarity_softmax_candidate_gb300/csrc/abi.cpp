@@ -84,6 +84,11 @@ int validate(const float* Q, const void* C, long long B, int K, int D, int norma
         const int r = logit_form(scale, temperature, normalize, nullptr, nullptr);
         if (r != CS_OK) return r;
     }
+    // Elements are read as float32 (bfloat16 for C in the _bf16 entry
+    // points): pointers must be aligned to them.
+    if ((reinterpret_cast<uintptr_t>(Q) & 3u) || (reinterpret_cast<uintptr_t>(C) & (c_bytes - 1)) ||
+        (has_out && (reinterpret_cast<uintptr_t>(out) & 3u)))
+        return CS_ERR_MISALIGNED;
     // B*K*D elements, as bytes, must fit comfortably in 64 bits.
     const unsigned long long bk = static_cast<unsigned long long>(B) * static_cast<unsigned long long>(K);
     if (bk > (1ull << 60) / static_cast<unsigned long long>(D)) return CS_ERR_TOO_LARGE;
@@ -146,8 +151,9 @@ int cached_generic_clusters(DeviceState& d, int cluster, int normalize, int c_bf
 }
 
 int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows) {
-    const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) | (nq4 << 2) |
-                           (c_bf16 << 1) | normalize;
+    // nq4 + 1 in bits 2..5 (nq4 is kNqcUnaligned = -1, 0, 1, 2, 4 or 8)
+    const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) |
+                           (static_cast<long long>(nq4 + 1) << 2) | (c_bf16 << 1) | normalize;
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = d.clusters.find({cluster, key2});
     if (it != d.clusters.end()) return it->second;
@@ -189,15 +195,16 @@ int stage_rows(long long row_bytes) {
 // to warp g % kConsumerWarps, so with NS a multiple of the warp count every
 // slot always has the same owner, which consumes its uses in order: a
 // parity wait on a slot can then never see a phase two uses old.
-int max_stages(const DeviceState& d, int R, int D, int c_bytes) {
-    const long long stage_bytes = static_cast<long long>(c_bytes) * R * D;
-    const size_t fixed = cs::smem_layout(0, R, D, c_bytes).total;
+int max_stages(const DeviceState& d, int R, int D, int c_bytes, bool ua) {
+    const long long stage_bytes = static_cast<long long>(cs::smem_layout(1, R, D, c_bytes, ua).slot_bytes);
+    const size_t fixed = cs::smem_layout(0, R, D, c_bytes, ua).total;
     if (fixed >= static_cast<size_t>(d.smem_optin)) return 0;
     long long ns = static_cast<long long>(d.smem_optin - fixed) / stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     ns -= ns % cs::kConsumerWarps;
     // The barrier array grows by 16 bytes per stage as well.
-    while (ns > 0 && cs::smem_layout(static_cast<int>(ns), R, D, c_bytes).total > static_cast<size_t>(d.smem_optin))
+    while (ns > 0 &&
+           cs::smem_layout(static_cast<int>(ns), R, D, c_bytes, ua).total > static_cast<size_t>(d.smem_optin))
         ns -= cs::kConsumerWarps;
     return ns > 0 ? static_cast<int>(ns) : 0;
 }
@@ -211,13 +218,16 @@ int ring_stages(long long need, int max_ns) {
 
 // STREAM plan with `ctas` persistent CTAs (0 = one per SM, at most B).
 // Picks rows per stage R <= stage_rows(D) that keeps the most bytes in
-// flight (larger R on ties). Returns false if no ring fits.
+// flight (larger R on ties). Rows the bulk copies cannot take whole (not
+// tma_eligible) are copied as aligned spans (nq4 = kNqcUnaligned). Returns
+// false if no ring fits.
 bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     const int cb = cs::c_elem_bytes(p);
+    const bool ua = !tma_eligible(p);
     int R = 0, max_ns = 0;
     long long best = 0;
     for (int r = stage_rows(static_cast<long long>(cb) * p.D); r >= 1; --r) {
-        const int ns = max_stages(d, r, p.D, cb);
+        const int ns = max_stages(d, r, p.D, cb, ua);
         const long long bytes = static_cast<long long>(cb) * r * p.D * ns;
         if (bytes > best) {
             best = bytes;
@@ -234,7 +244,7 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     // every consumer warp gets a stage instead of one warp doing them all.
     if (!p.offsets && qpc * p.K < static_cast<long long>(cs::kConsumerWarps) * R) {
         const int r = static_cast<int>((qpc * p.K + cs::kConsumerWarps - 1) / cs::kConsumerWarps);
-        const int ns = max_stages(d, r, p.D, cb);
+        const int ns = max_stages(d, r, p.D, cb, ua);
         if (ns > 0) {
             R = r;
             max_ns = ns;
@@ -246,8 +256,8 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     plan->ctas = ctas;
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = nq4_for(p);
-    plan->smem = cs::smem_layout(ns, R, p.D, cb).total;
+    plan->nq4 = ua ? cs::kNqcUnaligned : nq4_for(p);
+    plan->smem = cs::smem_layout(ns, R, p.D, cb, ua).total;
     return true;
 }
 
@@ -255,12 +265,13 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
 // consumer warps (one stage each) when the ring holds them.
 bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     const int cb = cs::c_elem_bytes(p);
+    const bool ua = !tma_eligible(p);
     const int rows = (p.K + G - 1) / G;
     int R = (rows + cs::kConsumerWarps - 1) / cs::kConsumerWarps;
     const int Rmax = stage_rows(static_cast<long long>(cb) * p.D);
     if (R > Rmax) R = Rmax;
-    while (R > 1 && max_stages(d, R, p.D, cb) == 0) --R;  // a ring of 8 stages must fit
-    const int max_ns = max_stages(d, R, p.D, cb);
+    while (R > 1 && max_stages(d, R, p.D, cb, ua) == 0) --R;  // a ring of 8 stages must fit
+    const int max_ns = max_stages(d, R, p.D, cb, ua);
     if (max_ns == 0) return false;
     const int ns = ring_stages((rows + R - 1) / R, max_ns);
     plan->kind = cs::kPlanCluster;
@@ -268,8 +279,8 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     plan->ctas = G * static_cast<int>(p.B);
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = nq4_for(p);
-    plan->smem = cs::smem_layout(ns, R, p.D, cb).total;
+    plan->nq4 = ua ? cs::kNqcUnaligned : nq4_for(p);
+    plan->smem = cs::smem_layout(ns, R, p.D, cb, ua).total;
     return true;
 }
 
@@ -338,12 +349,13 @@ void generic_plan(const Problem& p, Plan* plan, int G = 1) {
     plan->smem = 0;
 }
 
-// Chooses (or checks a forced) plan. Returns a cs_status. direct: the fused
-// readout may take the DIRECT plan (the unfused baseline's passes may not).
-int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas, Plan* plan, bool direct = true) {
+// Chooses (or checks a forced) plan. Returns a cs_status. fused: the fused
+// readout, which may take the DIRECT plan and copy unaligned rows as aligned
+// spans (the unfused baseline's passes may do neither).
+int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas, Plan* plan, bool fused = true) {
     const bool aligned = tma_eligible(p);
     if (kind == cs::kPlanDirect) {
-        if (!direct) return CS_ERR_BAD_PLAN;
+        if (!fused) return CS_ERR_BAD_PLAN;
         if (cluster == 0) {  // fewest CTAs per question that keep each within the row limit
             int max_rows = 0;
             direct_form(p, &max_rows);
@@ -366,11 +378,11 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         return CS_OK;
     }
     if (kind == cs::kPlanStream) {
-        if (!aligned || ctas < 0 || ctas > p.B) return CS_ERR_BAD_PLAN;
+        if ((!aligned && !fused) || ctas < 0 || ctas > p.B) return CS_ERR_BAD_PLAN;
         return stream_plan(d, p, ctas, plan) ? CS_OK : CS_ERR_BAD_PLAN;
     }
     if (kind == cs::kPlanCluster) {
-        if (!aligned || p.B > 65535 || cluster < 0 || cluster > cs::kMaxCluster || cluster > p.K)
+        if ((!aligned && !fused) || p.B > 65535 || cluster < 0 || cluster > cs::kMaxCluster || cluster > p.K)
             return CS_ERR_BAD_PLAN;
         if (cluster == 0) {
             cluster = 1;
@@ -396,7 +408,7 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         // Short questions (at most kDirectMaxRows rows per CTA): the DIRECT
         // plan, one trip to memory and no ring.
         int max_rows = 0;
-        if (direct && direct_form(p, &max_rows) != 0) {
+        if (fused && direct_form(p, &max_rows) != 0) {
             int g = G;
             const int kmax = p.offsets ? CS_MAX_K : p.K;
             while ((kmax + g - 1) / g > max_rows && g * 2 <= cs::kMaxCluster && g * 2 <= p.K &&
@@ -412,9 +424,18 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
                 return CS_OK;
         }
     }
-    if (aligned && stream_plan(d, p, 0, plan)) return CS_OK;
-    // Rows the bulk copies cannot take: the scalar plan, each of few
-    // questions spread over a cluster.
+    // A few questions whose rows the bulk copies cannot take whole: the
+    // scalar plan, each question spread over a cluster (latency-bound; the
+    // DIRECT plan needs aligned rows).
+    if (!aligned && p.B * 2 <= d.sms && !p.offsets) {
+        generic_plan(p, plan, generic_cluster_size(d, p));
+        return CS_OK;
+    }
+    // Many questions: the bulk-copy stream, aligned rows whole, others as
+    // aligned spans (fused readout only: the unfused passes have no
+    // unaligned build).
+    if ((aligned || fused) && stream_plan(d, p, 0, plan)) return CS_OK;
+    // Rows too long for the ring: the scalar plan.
     generic_plan(p, plan, generic_cluster_size(d, p));
     return CS_OK;
 }
@@ -468,6 +489,9 @@ int run_ragged(const float* Q, const void* C, const long long* offsets, long lon
     float w0, kexp;
     if (logit_form(scale, temperature, normalize, &w0, &kexp) != CS_OK) return CS_ERR_RANGE;
     const unsigned long long cb = c_bf16 ? 2ull : 4ull, rows = static_cast<unsigned long long>(total_rows);
+    if ((reinterpret_cast<uintptr_t>(Q) & 3u) || (reinterpret_cast<uintptr_t>(C) & (cb - 1)) ||
+        (reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(offsets) & 7u))
+        return CS_ERR_MISALIGNED;
     if (rows > (1ull << 60) / static_cast<unsigned long long>(D)) return CS_ERR_TOO_LARGE;
     const unsigned long long out_b = rows * 4ull, q_b = static_cast<unsigned long long>(B) * D * 4ull,
                              c_b = rows * D * cb, o_b = (static_cast<unsigned long long>(B) + 1ull) * 8ull;
@@ -489,6 +513,7 @@ int run_unfused(const float* Q, const float* C, long long B, int K, int D, int n
     const int v = validate(Q, C, B, K, D, normalize, out, true, true, scale, temperature);
     if (v != CS_OK) return v;
     if (!staged) return CS_ERR_NULL_POINTER;
+    if (reinterpret_cast<uintptr_t>(staged) & 3u) return CS_ERR_MISALIGNED;
     const unsigned long long bk4 = static_cast<unsigned long long>(B) * K * 4ull;
     if (overlaps(staged, bk4, out, bk4) || overlaps(staged, bk4, Q, static_cast<unsigned long long>(B) * D * 4ull) ||
         overlaps(staged, bk4, C, bk4 * static_cast<unsigned long long>(D)))
@@ -530,6 +555,7 @@ const char* cs_status_string(int status) {
         case CS_ERR_TOO_LARGE: return "B*K*D is too large";
         case CS_ERR_BAD_PLAN: return "requested plan cannot run these arguments";
         case CS_ERR_RANGE: return "|scale / temperature| exceeds 2^126";
+        case CS_ERR_MISALIGNED: return "a pointer is not aligned to its element size";
         case CS_ERR_SCRATCH_TOO_SMALL:
             return "B*K exceeds the built-in scratch of the no-allocation entry point (1048576 rows)";
         default: return "unknown status";

@@ -73,29 +73,44 @@ struct Plan {
     int ctas;          // CTAs launched in total
     int rows_per_stage;// candidate rows per bulk-copy stage
     int stages;        // stages in the shared-memory ring
-    int nq4;           // 16-byte chunks of a C row per lane whose q sits in registers (0: q read from smem)
+    int nq4;           // 16-byte chunks of a C row per lane whose q sits in registers (0: q read from
+                       // smem; kNqcUnaligned: unaligned rows)
     size_t smem;       // dynamic shared memory per CTA
 };
 
 // Shared-memory carve-up of the streaming kernels. All offsets are bytes
 // from the (128-byte aligned) dynamic shared-memory base.
 struct SmemLayout {
-    size_t ring;     // stages * rows_per_stage * D elements of C
-    size_t qbuf;     // 2 slots of D floats
-    size_t tn;       // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
-    size_t xch;      // kMaxCluster float2 (max, sum) received from the cluster's CTAs
-    size_t bars;     // full[stages], empty[stages], qfull[2], qempty[2], xbar (8 B each)
-    size_t range;    // two long longs: this CTA's question range (ragged STREAM plan)
-    size_t flag;     // int: this CTA gave up waiting
+    size_t ring;        // stages slots of slot_bytes each
+    size_t slot_bytes;  // one ring slot: rows_per_stage rows of C
+    size_t qbuf;        // 2 slots of qslot_bytes: the query rows
+    size_t qslot_bytes;
+    size_t tn;          // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
+    size_t xch;         // kMaxCluster float2 (max, sum) received from the cluster's CTAs
+    size_t bars;        // full[stages], empty[stages], qfull[2], qempty[2], xbar (8 B each)
+    size_t range;       // two long longs: this CTA's question range (ragged STREAM plan)
+    size_t flag;        // int: this CTA gave up waiting
     size_t total;
 };
 
-// c_bytes: bytes of one element of C (4 float32, 2 bfloat16).
-__host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage, int D, int c_bytes) {
+// Bulk copies of rows that do not start on a 16-byte boundary (or whose
+// length is not a multiple of 16 bytes) copy the 16-byte aligned span
+// around them: up to 15 bytes before and after, within the same 16-byte
+// granules as the rows' own bytes. A slot holds that span.
+__host__ __device__ inline size_t span_bytes(size_t bytes) { return (bytes + 15) / 16 * 16 + 32; }
+
+// c_bytes: bytes of one element of C (4 float32, 2 bfloat16). unaligned:
+// slots sized for the aligned spans of rows at any 4-byte (float32) or
+// 2-byte (bfloat16) offset.
+__host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage, int D, int c_bytes,
+                                                  bool unaligned = false) {
     SmemLayout L;
     size_t off = 0;
-    L.ring = off;   off += (size_t)stages * rows_per_stage * D * c_bytes;
-    L.qbuf = off;   off += 2 * (size_t)D * sizeof(float);
+    const size_t stage = (size_t)rows_per_stage * D * c_bytes, q = (size_t)D * sizeof(float);
+    L.slot_bytes = unaligned ? span_bytes(stage) : stage;
+    L.qslot_bytes = unaligned ? span_bytes(q) : q;
+    L.ring = off;   off += (size_t)stages * L.slot_bytes;
+    L.qbuf = off;   off += 2 * L.qslot_bytes;
     L.tn = off;     off += 4 * (size_t)kLogitSlots * sizeof(float);
     L.xch = off;    off += (size_t)kMaxCluster * 8;
     L.bars = off;   off += (2 * (size_t)stages + 5) * 8;
@@ -104,6 +119,11 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
     L.total = off;
     return L;
 }
+
+// Plan.nq4 of the streaming kernels for rows the bulk copies take as
+// aligned spans (D not a multiple of 16 bytes' worth of elements, or Q or C
+// off a 16-byte boundary): scalar shared-memory reads, q in shared memory.
+constexpr int kNqcUnaligned = -1;
 
 // What one launch of the streaming kernel computes.
 enum StreamMode {

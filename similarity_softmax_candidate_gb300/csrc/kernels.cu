@@ -117,6 +117,7 @@ struct Elem<float> {
         f[0] = make_float4(__uint_as_float(c.x), __uint_as_float(c.y), __uint_as_float(c.z), __uint_as_float(c.w));
     }
     __device__ __forceinline__ static float value(const float* row, int d) { return __ldg(row + d); }
+    __device__ __forceinline__ static float widen1(float x) { return x; }
 };
 template <>
 struct Elem<uint16_t> {  // bfloat16: the high half of a float32
@@ -131,6 +132,7 @@ struct Elem<uint16_t> {  // bfloat16: the high half of a float32
     __device__ __forceinline__ static float value(const uint16_t* row, int d) {
         return __uint_as_float(static_cast<uint32_t>(__ldg(row + d)) << 16);
     }
+    __device__ __forceinline__ static float widen1(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 };
 
 // ------------------------------------------------------------------ PTX
@@ -592,6 +594,55 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
     for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
 }
 
+// The same sums for a stage whose rows sit at any element-aligned offset in
+// their slot (unaligned plans): row r's element d is st[r * D + d], read as a
+// scalar, and q comes from shared memory. Lane takes elements lane,
+// lane + 32, ... two at a time (d and d + 32), so each sum still runs as a
+// packed pair; q is loaded once per element for all the stage's rows.
+template <int MODE, typename T, int MR, typename Release>
+__device__ __forceinline__ void stage_dots_scalar(const T* __restrict__ st, int nr, int D,
+                                                  const float* __restrict__ q, int lane,
+                                                  float (&v)[values_per_row(MODE) * MR], Release&& release) {
+    constexpr int VPR = values_per_row(MODE);
+    unsigned long long acc[VPR * MR];
+#pragma unroll
+    for (int i = 0; i < VPR * MR; ++i) acc[i] = 0ull;
+    auto accumulate = [&](unsigned long long c, unsigned long long qq, int r) {
+        if (acc_dot(MODE)) acc[VPR * r] = fma2(c, qq, acc[VPR * r]);
+        if (acc_norm(MODE)) acc[VPR * r + VPR - 1] = fma2(c, c, acc[VPR * r + VPR - 1]);
+    };
+    int d = lane;
+    for (; d + 32 < D; d += 64) {
+        const unsigned long long qq = pack2(q[d], q[d + 32]);
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+            if (r < nr) {
+                const T* row = st + r * D;
+                accumulate(pack2(Elem<T>::widen1(row[d]), Elem<T>::widen1(row[d + 32])), qq, r);
+            }
+    }
+    if (d < D) {
+        const unsigned long long qq = pack2(q[d], 0.f);
+#pragma unroll
+        for (int r = 0; r < MR; ++r)
+            if (r < nr) accumulate(pack2(Elem<T>::widen1(st[r * D + d]), 0.f), qq, r);
+    }
+    release();
+#pragma unroll
+    for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
+}
+
+// Global address of `bytes` bytes at src, widened to whole 16-byte granules
+// for a bulk copy: returns the aligned start and sets *shift (the offset of
+// src in it) and *span (the copy's length, a multiple of 16).
+__device__ __forceinline__ const void* aligned_span(const void* src, uint32_t bytes, uint32_t* shift,
+                                                    uint32_t* span) {
+    const unsigned long long a = reinterpret_cast<unsigned long long>(src);
+    *shift = static_cast<uint32_t>(a & 15u);
+    *span = (*shift + bytes + 15u) & ~15u;
+    return reinterpret_cast<const void*>(a & ~15ull);
+}
+
 // MR: most rows per stage this instantiation handles (kMaxRowsPerStage, or
 // kSmallStageRows for the fused modes when the plan's stages are that short:
 // the per-stage code a batch-1 launch fetches is then a quarter as long).
@@ -619,10 +670,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         return;
     }
 
-    const SmemLayout L = smem_layout(NS, R, D, static_cast<int>(sizeof(T)));
+    // UA: rows and queries need not start on 16-byte boundaries; each copy
+    // takes their aligned span and readers index from the offset in it.
+    constexpr bool UA = NQC == kNqcUnaligned;
+    const SmemLayout L = smem_layout(NS, R, D, static_cast<int>(sizeof(T)), UA);
     unsigned char* ring = smem + L.ring;
-    const uint32_t stage_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(D) * sizeof(T);
-    float* qbuf = reinterpret_cast<float*>(smem + L.qbuf);
+    const uint32_t slot_bytes = static_cast<uint32_t>(L.slot_bytes);
+    unsigned char* qbuf = smem + L.qbuf;
+    const uint32_t qslot_bytes = static_cast<uint32_t>(L.qslot_bytes);
     float* tn = reinterpret_cast<float*>(smem + L.tn);
     float2* xch = reinterpret_cast<float2*>(smem + L.xch);
     volatile int* give_up = reinterpret_cast<volatile int*>(smem + L.flag);
@@ -665,14 +720,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             row0 = (static_cast<long long>(c) * args.q_per_cta + min(c, args.q_rem)) * p.K;
             nrows = static_cast<long long>(args.q_per_cta + (c < args.q_rem ? 1 : 0)) * p.K;
         }
-        const long long rb = static_cast<long long>(D) * sizeof(T);  // a multiple of 16 (aligned plans)
+        const long long rb = static_cast<long long>(D) * sizeof(T);
         const long long total = min(nrows, static_cast<long long>(NS) * R) * rb;
         const long long piece = ((total + kConsumerWarps * 16 - 1) / (kConsumerWarps * 16)) * 16;
         const long long off = lane * piece;
         if (off < total) {
             const uint32_t bytes = static_cast<uint32_t>(min(piece, total - off));
             const unsigned char* src = reinterpret_cast<const unsigned char*>(Cg) + row0 * rb + off;
-            if (CS_IN_BOUNDS(src, bytes, p.C, rows_total(p) * rb, kSitePrefetchC)) bulk_prefetch_l2(src, bytes);
+            uint32_t shift, span;  // aligned plans: shift 0, span = bytes
+            const void* from = aligned_span(src, bytes, &shift, &span);
+            if (CS_IN_BOUNDS(src, bytes, p.C, rows_total(p) * rb, kSitePrefetchC)) bulk_prefetch_l2(from, span);
         }
     }
     wait_prior_grid();  // no global access before this point (prefetch hints aside)
@@ -745,11 +802,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;
                 const uint32_t bytes = static_cast<uint32_t>(min(R, qr.n - k0)) * row_bytes;
                 const T* src = Cg + static_cast<size_t>(qr.row0 + k0) * D;
-                unsigned char* dst = ring + static_cast<size_t>(slot) * stage_bytes;
+                unsigned char* dst = ring + static_cast<size_t>(slot) * slot_bytes;
+                // UA: the rows' aligned span (the same granules as the rows'
+                // own bytes, so no page they do not touch); aligned plans copy
+                // exactly the rows
+                uint32_t shift = 0, span = bytes;
+                const void* from = UA ? aligned_span(src, bytes, &shift, &span) : src;
                 const bool inb = CS_IN_BOUNDS(src, bytes, p.C, rows_total(p) * row_bytes, kSiteCopyC) &&
-                                 CS_IN_BOUNDS(dst, bytes, ring, static_cast<size_t>(NS) * stage_bytes, kSiteRing);
-                mbar_arrive_expect_tx(bar_f, inb ? bytes : 0u);
-                if (inb) bulk_g2s(smem_u32(dst), src, bytes, bar_f);
+                                 CS_IN_BOUNDS(dst, span, ring, static_cast<size_t>(NS) * slot_bytes, kSiteRing);
+                mbar_arrive_expect_tx(bar_f, inb ? span : 0u);
+                if (inb) bulk_g2s(smem_u32(dst), from, span, bar_f);
                 slot += kConsumerWarps;
                 if (slot >= static_cast<uint32_t>(NS)) {
                     slot -= NS;
@@ -784,10 +846,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
                 if (nq >= 2 && !wait_phase(qempty0 + 8u * qs, qpar ^ 1u, give_up)) break;
                 const float* src = p.Q + static_cast<size_t>(b) * D;
+                unsigned char* dst = qbuf + qs * qslot_bytes;
+                uint32_t shift = 0, span = q_bytes;
+                const void* from = UA ? aligned_span(src, q_bytes, &shift, &span) : src;
                 const bool inb = CS_IN_BOUNDS(src, q_bytes, p.Q, p.B * q_bytes, kSiteCopyQ) &&
-                                 CS_IN_BOUNDS(qbuf + qs * D, q_bytes, qbuf, 2 * q_bytes, kSiteQbuf);
-                mbar_arrive_expect_tx(qfull0 + 8u * qs, inb ? q_bytes : 0u);
-                if (inb) bulk_g2s(smem_u32(qbuf + qs * D), src, q_bytes, qfull0 + 8u * qs);
+                                 CS_IN_BOUNDS(dst, span, qbuf, 2 * qslot_bytes, kSiteQbuf);
+                mbar_arrive_expect_tx(qfull0 + 8u * qs, inb ? span : 0u);
+                if (inb) bulk_g2s(smem_u32(dst), from, span, qfull0 + 8u * qs);
             }
             if (*give_up) {
                 const unsigned long long deadline = globaltimer() + kWaitLimitNs;
@@ -812,10 +877,20 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             if (qr.bad && warp == 0 && lane == 0) atomicOr(&g_status, 4u);
             const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
             bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
-            const float4* q4 = reinterpret_cast<const float4*>(qbuf + qs * D);
+            unsigned char* qslot = qbuf + qs * qslot_bytes;
+            const float4* q4 = reinterpret_cast<const float4*>(qslot);
+            // UA: q at its offset in the aligned span the producer copied
+            const float* qf = reinterpret_cast<const float*>(
+                qslot + (reinterpret_cast<unsigned long long>(p.Q + static_cast<size_t>(b) * D) & 15u));
             float4 qv[(NQC > 0 ? NQC : 1) * QF4];
             float qsq = 0.f;  // |q|^2 (cosine)
-            if constexpr (NQC > 0) {
+            if constexpr (UA) {
+                if (COS) {
+                    float sq = 0.f;
+                    for (int i = lane; i < D; i += 32) sq = fmaf(qf[i], qf[i], sq);
+                    qsq = warp_sum(sq);
+                }
+            } else if constexpr (NQC > 0) {
                 float sq = 0.f;
 #pragma unroll
                 for (int j = 0; j < NQC; ++j) {
@@ -853,12 +928,21 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 const int k0 = s * R;  // relative to klo
                 const int nr = min(R, nrows - k0);
                 float v[V];
-                stage_dots<NQC, MODE, T, MR>(
-                    reinterpret_cast<const uint4*>(ring + static_cast<size_t>(slot) * stage_bytes), nr, DC, qv, q4,
-                    lane, v, [&] {
-                        __syncwarp();  // every lane's reads of the slot are done
-                        if (lane == 0) mbar_arrive(bar_e);
-                    });
+                unsigned char* st = ring + static_cast<size_t>(slot) * slot_bytes;
+                auto release = [&] {
+                    __syncwarp();  // every lane's reads of the slot are done
+                    if (lane == 0) mbar_arrive(bar_e);
+                };
+                if constexpr (UA) {
+                    // the rows at their offset in the aligned span
+                    const T* src = Cg + static_cast<size_t>(qr.row0 + k0) * D;
+                    stage_dots_scalar<MODE, T, MR>(
+                        reinterpret_cast<const T*>(st + (reinterpret_cast<unsigned long long>(src) & 15u)), nr, D,
+                        qf, lane, v, release);
+                } else {
+                    stage_dots<NQC, MODE, T, MR>(reinterpret_cast<const uint4*>(st), nr, DC, qv, q4, lane, v,
+                                                 release);
+                }
                 int idx;
                 const float sum = transpose_reduce<V>(v, lane, &idx);
                 if ((lane & (32 / V - 1)) == 0) {
@@ -878,7 +962,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     phase ^= 1u;
                 }
             }
-            if constexpr (NQC == 0) {
+            if constexpr (NQC <= 0) {  // q was read from shared memory by every stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
             }
@@ -1342,6 +1426,11 @@ cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t 
 template <int MODE, typename T, int MR>
 cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     switch (plan.nq4) {
+        case kNqcUnaligned:  // built for the fused modes at the full stage size only
+            if constexpr ((MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage)
+                return launch_stream_t<kNqcUnaligned, MODE, T, MR>(a, plan, stream);
+            else
+                return cudaErrorInvalidValue;
         case 1: return launch_stream_t<1, MODE, T, MR>(a, plan, stream);
         case 2: return launch_stream_t<2, MODE, T, MR>(a, plan, stream);
         case 4: return launch_stream_t<4, MODE, T, MR>(a, plan, stream);
@@ -1354,6 +1443,11 @@ cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t 
 template <int MODE, typename T, int MR>
 const void* stream_fn_m(int nqc) {
     switch (nqc) {
+        case kNqcUnaligned:
+            if constexpr ((MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage)
+                return reinterpret_cast<const void*>(stream_kernel<kNqcUnaligned, MODE, T, MR>);
+            else
+                return nullptr;
         case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE, T, MR>);
         case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE, T, MR>);
         case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE, T, MR>);
@@ -1363,16 +1457,21 @@ const void* stream_fn_m(int nqc) {
     return nullptr;
 }
 
-// The row limit of the instantiation that runs stages of R rows in `mode`.
-constexpr int rows_limit(int mode, int R) {
-    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows ? kSmallStageRows : kMaxRowsPerStage;
+// The row limit of the instantiation that runs stages of R rows in `mode`
+// (unaligned plans have only the full-size build).
+constexpr int rows_limit(int mode, int R, int nqc) {
+    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows && nqc != kNqcUnaligned
+               ? kSmallStageRows
+               : kMaxRowsPerStage;
 }
 
 // Kernels exist for every mode over float32 C, and for the fused modes over
 // bfloat16 C (nqc 8 is never planned for bfloat16: q would take 64 registers);
-// the fused modes also in a short-stage form (mr = kSmallStageRows).
+// the fused modes also in a short-stage form (mr = kSmallStageRows) and, at
+// the full stage size, for unaligned rows (nqc = kNqcUnaligned).
 const void* stream_fn_for(int nqc, int mode, int c_bf16, int mr) {
     const bool fused = mode == kFusedCos || mode == kFusedDot;
+    if (nqc == kNqcUnaligned && (!fused || mr != kMaxRowsPerStage)) return nullptr;
     if (mr == kSmallStageRows) {
         if (!fused || (c_bf16 && nqc == 8)) return nullptr;
         if (c_bf16)
@@ -1411,7 +1510,7 @@ cudaError_t launch_stream(const Problem& p, const Plan& plan, int mode, cudaStre
     const long long ctas = plan.kind == kPlanCluster ? 1 : plan.ctas;
     a.q_per_cta = static_cast<int>(p.B / ctas);
     a.q_rem = static_cast<int>(p.B % ctas);
-    const bool small = rows_limit(mode, plan.rows_per_stage) == kSmallStageRows;
+    const bool small = rows_limit(mode, plan.rows_per_stage, plan.nq4) == kSmallStageRows;
     if (p.c_bf16) {
         if (plan.nq4 == 8) return cudaErrorInvalidValue;
         switch (mode) {
@@ -1572,10 +1671,10 @@ cudaError_t configure_device_kernels(int smem_optin) {
                     cudaFuncSetAttribute(direct_fn_for(nqc, cos, bf), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (e != cudaSuccess) return e;
             }
-    const int nq4s[5] = {1, 2, 4, 8, 0};
+    const int nq4s[6] = {1, 2, 4, 8, 0, kNqcUnaligned};
     for (int bf = 0; bf < 2; ++bf) {
         for (int m = kFusedCos; m <= kStagedCos; ++m) {
-            for (int i = 0; i < 5; ++i) {
+            for (int i = 0; i < 6; ++i) {
                 for (int mr : {kSmallStageRows, kMaxRowsPerStage}) {
                     const void* f = stream_fn_for(nq4s[i], m, bf, mr);
                     if (!f) continue;
@@ -1592,7 +1691,7 @@ cudaError_t configure_device_kernels(int smem_optin) {
 
 int max_active_clusters(int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows_per_stage) {
     const int mode = normalize ? kFusedCos : kFusedDot;
-    const void* f = stream_fn_for(nq4, mode, c_bf16, rows_limit(mode, rows_per_stage));
+    const void* f = stream_fn_for(nq4, mode, c_bf16, rows_limit(mode, rows_per_stage, nq4));
     if (!f) return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

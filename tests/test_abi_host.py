@@ -144,6 +144,26 @@ def test_largest_factor_is_checked_in_double_precision(host_lib):
         assert _batch(host_lib, B=B, K=K, D=D, scale=scale, temperature=T, out=C_ADDR + 400) == binding.CS_ERR_ALIAS
 
 
+def test_rejects_pointers_off_their_element_size(host_lib):
+    """Elements are read as float32 (bfloat16 for the _bf16 candidates): a
+    pointer off its element size is refused before any CUDA call. Offsets
+    from a 16-byte boundary that keep the element alignment are accepted by
+    validation (an aliasing out then stops those calls at the later overlap
+    check)."""
+    E = binding
+    assert _batch(host_lib, Q=Q_ADDR + 2) == E.CS_ERR_MISALIGNED
+    assert _batch(host_lib, C=C_ADDR + 1) == E.CS_ERR_MISALIGNED
+    assert _batch(host_lib, out=OUT_ADDR + 3) == E.CS_ERR_MISALIGNED
+    assert _single(host_lib, q=Q_ADDR + 6) == E.CS_ERR_MISALIGNED
+    bf = host_lib.cs_score_candidates_batch_bf16
+    assert bf(Q_ADDR, C_ADDR + 1, 1, 5, 512, 1, 1.0, 1.0, OUT_ADDR, None) == E.CS_ERR_MISALIGNED
+    B, K, D = 4, 8, 16
+    assert bf(Q_ADDR, C_ADDR + 2, B, K, D, 1, 1.0, 1.0, C_ADDR + 400, None) == E.CS_ERR_ALIAS
+    assert _batch(host_lib, B=B, K=K, D=D, Q=Q_ADDR + 4, C=C_ADDR + 12, out=C_ADDR + 400) == E.CS_ERR_ALIAS
+    assert _ragged(host_lib, offsets=OFF_ADDR + 4) == E.CS_ERR_MISALIGNED
+    assert _unfused(host_lib, staged=STAGED_ADDR + 2) == E.CS_ERR_MISALIGNED
+
+
 def test_first_failing_check_wins(host_lib):
     # the page lists each reject on its own; with several bad arguments the
     # library reports pointers, then B, K, D, similarity, scale, temperature

@@ -207,7 +207,7 @@ def test_every_plan_every_tempered_pair(cuda_lib, plan, normalize):
                           f"{plan[0]} B={B} K={K} D={D} scale={wl.scale} T={wl.temperature}")
 
 
-def test_unaligned_and_odd_shapes_use_scalar_path(cuda_lib):
+def test_few_unaligned_or_odd_questions_use_the_scalar_plan(cuda_lib):
     for normalize in (0, 1):
         # odd D
         wl = workloads.random_case(3, 255, 513, normalize, 2.0, 21)
@@ -226,8 +226,13 @@ def test_unaligned_and_odd_shapes_use_scalar_path(cuda_lib):
         p = binding.cs_score_candidates_batch(Q, C, normalize, 2.0, 1.0)
         torch.cuda.synchronize()
         assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "unaligned")
+        # the stream plan takes them too, copying the rows' aligned spans
+        p = binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_STREAM)
+        torch.cuda.synchronize()
+        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "unaligned, stream plan")
+        # the DIRECT plan loads 16-byte chunks and refuses them
         with pytest.raises(binding.CSError):
-            binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_STREAM)
+            binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_DIRECT)
 
 
 @pytest.mark.parametrize("misaligned", [False, True], ids=["odd_d", "misaligned"])
@@ -303,8 +308,10 @@ def test_automatic_plans(cuda_lib):
     assert plan(1, 64, 1001)["cluster"] == 8     # limited by rows: one per warp
     assert plan(1, 12, 511)["cluster"] == 1      # fewer rows than two CTAs' warps
     assert plan(1, 255, 3)["cluster"] == 1       # 3 KB of rows: not worth splitting
-    many = plan(100, 255, 511)                   # too many questions for clusters
-    assert many["plan"] == "generic" and many["cluster"] == 1 and many["ctas"] == 100, many
+    many = plan(100, 255, 511)  # too many questions for clusters: the stream plan copies aligned spans
+    assert many["plan"] == "stream" and many["ctas"] == 100, many
+    assert plan(4096, 255, 510)["plan"] == "stream"
+    assert plan(2, 9, 20000)["plan"] == "generic"  # rows too long for the ring
 
 
 def test_throughput_workload_full_size(cuda_lib):
