@@ -389,6 +389,8 @@ def main():
     ap.add_argument("--questions", type=int, default=B_TOTAL,
                     help="questions per step (default 16384; smaller only for profiling captures)")
     ap.add_argument("--chunk", type=int, default=CHUNK, help="questions per launch (default 4096)")
+    ap.add_argument("--only-unaligned", action="store_true",
+                    help="profiling aid: time only the unaligned-row workloads and print their record")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
                     help="profiling aid: time only the projected readout on B questions and print its record")
     ap.add_argument("--plan-sweep", action="store_true",
@@ -424,6 +426,10 @@ def main():
     if args.plan_sweep:
         if rank == 0:
             print(json.dumps(plan_sweep(cs, dev)), flush=True)
+        return 0
+    if args.only_unaligned:
+        if rank == 0:
+            print(json.dumps(unaligned_rows(cs, dev, args.steps, args.warmup)), flush=True)
         return 0
     if args.only_projected:
         if rank == 0:
@@ -530,6 +536,7 @@ def main():
 
     if not args.skip_extra:
         line["extra"]["projected_readout"] = projected_readout(cs, dev, 20, args.warmup)
+        line["extra"]["unaligned_rows"] = unaligned_rows(cs, dev, 20, args.warmup)
         line["extra"]["latency_b1"] = latency_table(cs, workloads, dev, args.latency_calls)
         line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
     del wls, wl_cos, wl_dot
@@ -633,6 +640,58 @@ def extras(cs, workloads, wl_cos, wl_dot, out, dev, stream, args, world, barrier
     del staged
 
     return bf16, ragged_info, unfused
+
+
+def unaligned_rows(cs, dev, steps, warmup, B=4096):
+    """Rows the bulk copies cannot take whole, at throughput size: B
+    questions of K=255 with D=510 (rows of 2040 bytes), and with D=512 but
+    Q and C one float past a 16-byte boundary; each against the aligned
+    D=512 readout on the same buffer, and against the scalar plan forced on
+    the same rows. One launch per call over 2.1 GB (larger than L2)."""
+    import torch
+    flatC = torch.empty(B * K * 512 + 64, device=dev)
+    flatQ = torch.empty(B * 512 + 64, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(31)
+    flatC.normal_(generator=g)
+    flatQ.normal_(generator=g)
+    out = torch.empty(B, K, device=dev)
+    s = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(steps):
+            fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    res = {}
+    for name, d, off in (("aligned_d512", 512, 0), ("odd_d510", 510, 0), ("misaligned_d512", 512, 1)):
+        Q = flatQ[off:off + B * d].view(B, d)
+        C = flatC[off:off + B * K * d].view(B, K, d)
+        nbytes = B * 4 * (K * d + d + K)
+        row = {"plan": cs.cs_query_plan(Q, C, 1)["plan"]}
+        for normalize, scale in ((1, 14.285714), (0, 0.0625)):
+            tag = "cos" if normalize else "dot"
+            ms = timed(lambda: cs.cs_score_candidates_batch(Q, C, normalize, scale, 1.0, out=out, stream=s))
+            row[tag + "_gbs"] = nbytes / (ms / 1e3) / 1e9
+            row[tag + "_questions_per_s"] = B / (ms / 1e3)
+            if off or d % 4:
+                ms_g = timed(lambda: cs.cs_score_candidates_batch_plan(Q, C, normalize, scale, 1.0,
+                                                                       cs.CS_PLAN_GENERIC, 1, 0, out=out, stream=s))
+                row[tag + "_scalar_plan_gbs"] = nbytes / (ms_g / 1e3) / 1e9
+        res[name] = row
+    for name in ("odd_d510", "misaligned_d512"):
+        for tag in ("cos", "dot"):
+            res[name][tag + "_over_aligned"] = res[name][tag + "_gbs"] / res["aligned_d512"][tag + "_gbs"]
+    res["workload"] = f"{B} questions x K=255, fp32 N(0,1), one launch per call, {steps} calls"
+    del flatC, flatQ
+    return res
 
 
 def projected_readout(cs, dev, steps, warmup, B=4096):

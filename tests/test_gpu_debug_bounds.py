@@ -139,3 +139,27 @@ def test_projections_within_bounds(dbg):
         ref, got, status, site = _both(dbg, fn)
         assert site == 0 and status == 0, f"{name}: bounds site {site}, status {status}"
         _same(ref, got, name)
+
+
+def _placed(t, offset_elems):
+    flat = torch.empty(t.numel() + offset_elems + 64, dtype=t.dtype, device=DEV)
+    v = flat[offset_elems:offset_elems + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("B,K,D,oq,oc,bf16", [(300, 255, 510, 0, 0, False), (200, 64, 512, 1, 3, False),
+                                                (160, 33, 13, 0, 1, False), (170, 37, 21, 2, 5, True),
+                                                (3, 64, 509, 0, 3, False)])
+def test_unaligned_rows_within_bounds(dbg, B, K, D, oq, oc, bf16):
+    """Unaligned plans copy each stage's 16-byte aligned span; what the
+    kernels check and use is the rows' own range, which must stay inside C,
+    and the span must fit its ring slot."""
+    wl = workloads.random_case(B, K, D, 1, 3.0, 70 + B + D, DEV)
+    Q = _placed(wl.Q, oq)
+    C = _placed(wl.C.to(torch.bfloat16) if bf16 else wl.C, oc)
+    fn = binding.cs_score_candidates_batch_bf16 if bf16 else binding.cs_score_candidates_batch
+    for normalize in (1, 0):
+        ref, got, status, site = _both(dbg, lambda: fn(Q, C, normalize, 3.0, 1.0))
+        assert site == 0 and status == 0, f"bounds site {site}, status {status}"
+        _same(ref, got, f"unaligned B={B} K={K} D={D} q+{oq} c+{oc} bf16={bf16}")
