@@ -381,7 +381,7 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--latency-calls", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--skip-extra", action="store_true", help="only the headline throughput and its roofline")
@@ -391,6 +391,8 @@ def main():
     ap.add_argument("--chunk", type=int, default=CHUNK, help="questions per launch (default 4096)")
     ap.add_argument("--only-unaligned", action="store_true",
                     help="profiling aid: time only the unaligned-row workloads and print their record")
+    ap.add_argument("--only-unaligned-case", choices=[c[0] for c in UNALIGNED_CASES], default=None,
+                    help="profiling aid: W + K calls of one unaligned-row case (float32 cosine, 4096 questions)")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
                     help="profiling aid: time only the projected readout on B questions and print its record")
     ap.add_argument("--plan-sweep", action="store_true",
@@ -426,6 +428,11 @@ def main():
     if args.plan_sweep:
         if rank == 0:
             print(json.dumps(plan_sweep(cs, dev)), flush=True)
+        return 0
+    if args.only_unaligned_case:
+        if rank == 0:
+            print(json.dumps(unaligned_rows(cs, dev, args.steps, args.warmup, only=args.only_unaligned_case)),
+                  flush=True)
         return 0
     if args.only_unaligned:
         if rank == 0:
@@ -642,12 +649,17 @@ def extras(cs, workloads, wl_cos, wl_dot, out, dev, stream, args, world, barrier
     return bf16, ragged_info, unfused
 
 
-def unaligned_rows(cs, dev, steps, warmup, B=4096):
+UNALIGNED_CASES = (("aligned_d512", 512, 0), ("odd_d510", 510, 0), ("misaligned_d512", 512, 1))
+
+
+def unaligned_rows(cs, dev, steps, warmup, B=4096, only=None):
     """Rows the bulk copies cannot take whole, at throughput size: B
     questions of K=255 with D=510 (rows of 2040 bytes), and with D=512 but
-    Q and C one float past a 16-byte boundary; each against the aligned
+    Q and C one element past a 16-byte boundary; each against the aligned
     D=512 readout on the same buffer, and against the scalar plan forced on
-    the same rows. One launch per call over 2.1 GB (larger than L2)."""
+    the same rows; float32 and bfloat16 candidates. One launch per call
+    over 2.1 GB (larger than L2). only: time just that case's float32
+    cosine readout (a profiling aid)."""
     import torch
     flatC = torch.empty(B * K * 512 + 64, device=dev)
     flatQ = torch.empty(B * 512 + 64, device=dev)
@@ -657,6 +669,14 @@ def unaligned_rows(cs, dev, steps, warmup, B=4096):
     flatQ.normal_(generator=g)
     out = torch.empty(B, K, device=dev)
     s = torch.cuda.current_stream(dev)
+    if only is not None:
+        _, d, off = next(c for c in UNALIGNED_CASES if c[0] == only)
+        Q = flatQ[off:off + B * d].view(B, d)
+        C = flatC[off:off + B * K * d].view(B, K, d)
+        for _ in range(warmup + steps):
+            cs.cs_score_candidates_batch(Q, C, 1, 14.285714, 1.0, out=out, stream=s)
+        torch.cuda.synchronize()
+        return {"case": only, "calls": warmup + steps, "plan": cs.cs_query_plan(Q, C, 1)}
 
     def timed(fn):
         for _ in range(warmup):
@@ -671,26 +691,33 @@ def unaligned_rows(cs, dev, steps, warmup, B=4096):
         return a.elapsed_time(b) / steps
 
     res = {}
-    for name, d, off in (("aligned_d512", 512, 0), ("odd_d510", 510, 0), ("misaligned_d512", 512, 1)):
+    flatCb = flatC[:B * K * 512 + 64].to(torch.bfloat16)
+    for name, d, off in UNALIGNED_CASES:
         Q = flatQ[off:off + B * d].view(B, d)
-        C = flatC[off:off + B * K * d].view(B, K, d)
-        nbytes = B * 4 * (K * d + d + K)
-        row = {"plan": cs.cs_query_plan(Q, C, 1)["plan"]}
-        for normalize, scale in ((1, 14.285714), (0, 0.0625)):
-            tag = "cos" if normalize else "dot"
-            ms = timed(lambda: cs.cs_score_candidates_batch(Q, C, normalize, scale, 1.0, out=out, stream=s))
-            row[tag + "_gbs"] = nbytes / (ms / 1e3) / 1e9
-            row[tag + "_questions_per_s"] = B / (ms / 1e3)
-            if off or d % 4:
-                ms_g = timed(lambda: cs.cs_score_candidates_batch_plan(Q, C, normalize, scale, 1.0,
-                                                                       cs.CS_PLAN_GENERIC, 1, 0, out=out, stream=s))
-                row[tag + "_scalar_plan_gbs"] = nbytes / (ms_g / 1e3) / 1e9
+        row = {}
+        for dt, flat, eb in (("f32", flatC, 4), ("bf16", flatCb, 2)):
+            C = flat[off:off + B * K * d].view(B, K, d)
+            score = cs.cs_score_candidates_batch if dt == "f32" else cs.cs_score_candidates_batch_bf16
+            if dt == "f32":
+                row["plan"] = cs.cs_query_plan(Q, C, 1)["plan"]
+            nbytes = B * (eb * K * d + 4 * d + 4 * K)
+            for normalize, scale in ((1, 14.285714), (0, 0.0625)):
+                tag = dt + ("_cos" if normalize else "_dot")
+                ms = timed(lambda: score(Q, C, normalize, scale, 1.0, out=out, stream=s))
+                row[tag + "_gbs"] = nbytes / (ms / 1e3) / 1e9
+                row[tag + "_questions_per_s"] = B / (ms / 1e3)
+                if dt == "f32" and (off or d % 4):
+                    ms_g = timed(lambda: cs.cs_score_candidates_batch_plan(Q, C, normalize, scale, 1.0,
+                                                                           cs.CS_PLAN_GENERIC, 1, 0, out=out,
+                                                                           stream=s))
+                    row[tag + "_scalar_plan_gbs"] = nbytes / (ms_g / 1e3) / 1e9
         res[name] = row
     for name in ("odd_d510", "misaligned_d512"):
-        for tag in ("cos", "dot"):
+        for tag in ("f32_cos", "f32_dot", "bf16_cos", "bf16_dot"):
             res[name][tag + "_over_aligned"] = res[name][tag + "_gbs"] / res["aligned_d512"][tag + "_gbs"]
-    res["workload"] = f"{B} questions x K=255, fp32 N(0,1), one launch per call, {steps} calls"
-    del flatC, flatQ
+    res["workload"] = (f"{B} questions x K=255, N(0,1), float32 and bfloat16 candidates, one launch per call, "
+                       f"{steps} calls")
+    del flatC, flatQ, flatCb
     return res
 
 
@@ -964,10 +991,53 @@ def copy_ceiling(step_gbs, launch_gbs):
         return {"error": str(e)[:200]}
 
 
+def numa_placement(dev, ptrs):
+    """Host NUMA facts for the e2e buffers: the nodes with memory and CPUs,
+    the GPU's node (sysfs, from its PCI address) and the node of the first,
+    middle and last page of each pinned buffer (get_mempolicy on the
+    address). Linux only; fields it cannot read are left out."""
+    import ctypes
+    import glob
+    import platform
+    info = {}
+    try:
+        nodes = {}
+        for nd in sorted(glob.glob("/sys/devices/system/node/node[0-9]*")):
+            cpus = open(nd + "/cpulist").read().strip()
+            mem_kb = int(next(l for l in open(nd + "/meminfo") if "MemTotal" in l).split()[-2])
+            nodes[nd.rsplit("node", 1)[1]] = {"cpus": cpus, "mem_gb": round(mem_kb / 2 ** 20, 1)}
+        info["nodes"] = nodes
+        r = subprocess.run(["nvidia-smi", "-i", str(dev.index or 0), "--query-gpu=pci.bus_id",
+                            "--format=csv,noheader"], capture_output=True, text=True, timeout=30)
+        bus = r.stdout.strip().splitlines()[0].strip()
+        dom, rest = bus.split(":", 1)
+        info["gpu_pci"] = bus
+        info["gpu_node"] = int(open(f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest.lower()}/numa_node").read())
+    except Exception as e:  # not Linux, or no sysfs view
+        info["error"] = str(e)[:120]
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        sysno = {"aarch64": 236, "x86_64": 239}[platform.machine()]  # get_mempolicy
+
+        def node_of(addr):
+            mode = ctypes.c_int(-1)
+            rc = libc.syscall(sysno, ctypes.byref(mode), None, ctypes.c_ulong(0), ctypes.c_void_p(addr),
+                              ctypes.c_ulong(3))  # MPOL_F_NODE | MPOL_F_ADDR
+            return mode.value if rc == 0 else None
+        info["pinned_page_nodes"] = {name: sorted({node_of(p + o) for o in offs})
+                                     for name, (p, offs) in ptrs.items()}
+    except Exception as e:
+        info["pinned_page_nodes_error"] = str(e)[:120]
+    return info
+
+
 def e2e(cs, wl, dev, args, world, barrier, max_over_ranks):
     """questions/s with the inputs in pinned host memory: every step copies
     Q and C host->device (two chunk buffers, copies overlapped with compute
-    on a second stream) and the probabilities device->host."""
+    on a second stream) and the probabilities device->host. Beside it, the
+    host link measured the same way in the same run: the step's copies
+    alone, no kernel (link_ceiling); per-step rates show the steps the host
+    slowed down, and the NUMA placement of the pinned buffers."""
     import torch
     Qh = wl.Q.cpu().pin_memory()
     Ch = torch.empty(wl.C.shape, dtype=torch.float32, pin_memory=True)
@@ -982,7 +1052,7 @@ def e2e(cs, wl, dev, args, world, barrier, max_over_ranks):
     loaded = [torch.cuda.Event() for _ in range(2)]
     freed = [torch.cuda.Event() for _ in range(2)]
 
-    def one_step():
+    def one_step(score=True):
         n = B_TOTAL // CHUNK
         for i in range(n):
             j = i % 2
@@ -994,26 +1064,46 @@ def e2e(cs, wl, dev, args, world, barrier, max_over_ranks):
                 dC[j].copy_(Ch[b0:b0 + CHUNK], non_blocking=True)
                 loaded[j].record(copy)
             comp.wait_event(loaded[j])
-            cs.cs_score_candidates_batch(dQ[j], dC[j], wl.normalize, wl.scale, wl.temperature, out=dO[j],
-                                         stream=comp)
-            outh[b0:b0 + CHUNK].copy_(dO[j], non_blocking=True)
+            if score:
+                cs.cs_score_candidates_batch(dQ[j], dC[j], wl.normalize, wl.scale, wl.temperature, out=dO[j],
+                                             stream=comp)
+                outh[b0:b0 + CHUNK].copy_(dO[j], non_blocking=True)
             freed[j].record(comp)
         comp.synchronize()
 
-    for _ in range(2):
-        one_step()
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        one_step()
-    barrier()
-    dt = max_over_ranks(time.perf_counter() - t0)
     h2d = (Qh.numel() + Ch.numel()) * 4
     d2h = outh.numel() * 4
+
+    def timed(score):
+        for _ in range(2):
+            one_step(score)
+        barrier()
+        per = []
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            t = time.perf_counter()
+            one_step(score)
+            per.append(time.perf_counter() - t)
+        barrier()
+        return max_over_ranks(time.perf_counter() - t0), per
+
+    dt, per = timed(True)
+    ldt, lper = timed(False)
+    numa = numa_placement(dev, {"C": (Ch.data_ptr(), (0, h2d // 2, Ch.numel() * 4 - 4096)),
+                                "Q": (Qh.data_ptr(), (0,)), "out": (outh.data_ptr(), (0,))})
     del Ch, Qh, outh, dQ, dC, dO
+    link_gbs = h2d * args.e2e_steps / ldt / 1e9
+    e2e_gbs = h2d * args.e2e_steps / dt / 1e9
     return {"value": world * B_TOTAL * args.e2e_steps / dt, "unit": "questions/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "h2d_gbs": h2d * args.e2e_steps / dt / 1e9}
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "h2d_gbs": e2e_gbs,
+            "step_h2d_gbs": [round(h2d / t / 1e9, 1) for t in per],
+            "median_step_questions_per_s": world * B_TOTAL / statistics.median(per),
+            "link_ceiling": {"what": "the same steps' host-to-device copies, no kernel and no read-back",
+                             "h2d_gbs": link_gbs, "median_step_h2d_gbs": h2d / statistics.median(lper) / 1e9,
+                             "step_h2d_gbs": [round(h2d / t / 1e9, 1) for t in lper]},
+            "h2d_frac_of_link": e2e_gbs / link_gbs,
+            "median_step_frac_of_link": statistics.median(lper) / statistics.median(per),
+            "numa": numa}
 
 
 if __name__ == "__main__":

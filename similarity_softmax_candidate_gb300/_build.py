@@ -9,6 +9,7 @@ import glob
 import os
 import shutil
 import subprocess
+import sysconfig
 import tempfile
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +32,14 @@ CEILING_PATH = os.path.join(PKG, CEILING_NAME)
 CEILING_SRC = os.path.join(CSRC, "copy_ceiling_main.cu")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+# The binding's per-call marshalling in C (csrc/fastpath.c): a CPython
+# extension module next to the package, built with the host C compiler
+# against Python's headers. Optional: without it the binding marshals with
+# ctypes alone.
+FASTPATH_SRC = os.path.join(CSRC, "fastpath.c")
+FASTPATH_PATH = os.path.join(PKG, "_fastpath" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
 
 
 def _sources():
@@ -61,6 +70,8 @@ def build_library(force: bool = False, verbose: bool = False, debug_bounds: bool
     """Compile (if needed) and return the library path. Raises on failure.
     debug_bounds: the bounds-checked variant (DEBUG_LIB_PATH)."""
     path, name = (DEBUG_LIB_PATH, DEBUG_LIB_NAME) if debug_bounds else (LIB_PATH, LIB_NAME)
+    if not debug_bounds:
+        build_fastpath(force)
     if not force and not is_stale(path):
         return path
     nvcc = _nvcc()
@@ -91,6 +102,28 @@ def build_library(force: bool = False, verbose: bool = False, debug_bounds: bool
         shutil.copyfile(tmp_lib, staged)
         os.replace(staged, path)
     return path
+
+
+def build_fastpath(force: bool = False):
+    """Compile the binding's C marshalling module if it is missing or older
+    than its source. Returns its path, or None when it cannot be built (no
+    C compiler or no Python headers): the binding then uses ctypes alone."""
+    if not force and os.path.exists(FASTPATH_PATH) and \
+            os.path.getmtime(FASTPATH_PATH) >= os.path.getmtime(FASTPATH_SRC):
+        return FASTPATH_PATH
+    include = sysconfig.get_paths().get("include")
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc or not include or not os.path.exists(os.path.join(include, "Python.h")):
+        return None
+    staged = FASTPATH_PATH + f".tmp{os.getpid()}"
+    r = subprocess.run([cc, "-O2", "-shared", "-fPIC", "-Wall", "-I", include, FASTPATH_SRC, "-o", staged],
+                       stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+    if r.returncode != 0:
+        if os.path.exists(staged):
+            os.unlink(staged)
+        return None
+    os.replace(staged, FASTPATH_PATH)
+    return FASTPATH_PATH
 
 
 def _tool_jobs(force: bool):

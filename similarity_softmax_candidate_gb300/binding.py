@@ -7,6 +7,12 @@ passed as a device pointer faults the kernel, the first defect listed in
 PR #69 "cuda: add a fused candidate-scoring kernel for CLM and Kev",
 "Defects the GPU found, in order"; the binding refuses one up front).
 
+The readout calls (cs_score_candidates[_batch][_bf16]) with an `out` given
+marshal through a small C module (_fastpath, csrc/fastpath.c) when it was
+built: the same checks and the same library call, for well under the ~4 us
+ctypes takes per call. Anything it does not handle plainly falls back to the
+ctypes path below, which raises the precise error.
+
 If the library has not been built, every call raises: there is no CPU path.
 """
 from __future__ import annotations
@@ -35,6 +41,10 @@ globals().update({name: code for code, name in STATUS.items()})
 _lock = threading.Lock()
 _lib = None
 _debug_lib = None
+# The C marshalling module (_fastpath, built from csrc/fastpath.c) once set
+# up with the entry points of _fast_owner; False when it is unavailable.
+_fast = None
+_fast_owner = None
 CS_DEVERR_BOUNDS = 8
 CS_DEVERR_BAD_OFFSETS = 4
 CS_DEVERR_RANGE = 16
@@ -144,6 +154,29 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     return lib
 
 
+def _fastpath():
+    """The C marshalling module set up for the library in use, or None
+    (not built here, or another build of the library is in use)."""
+    global _fast, _fast_owner
+    lib = library()
+    if _fast_owner is lib:
+        return _fast
+    with _lock:
+        if _fast is None:
+            try:
+                from . import _fastpath as fp
+                import torch
+                addr = [ctypes.cast(f, ctypes.c_void_p).value for f in
+                        (lib.cs_score_candidates, lib.cs_score_candidates_batch, lib.cs_score_candidates_bf16,
+                         lib.cs_score_candidates_batch_bf16)]
+                fp.setup(*addr, torch.float32, torch.bfloat16, torch._C._cuda_getDevice,
+                         torch._C._cuda_getCurrentRawStream)
+                _fast, _fast_owner = fp, lib
+            except Exception:  # no C compiler or Python headers where it was built, or an older torch
+                _fast = False
+        return _fast if _fast_owner is lib else None
+
+
 def cs_abi_version() -> int:
     return int(library().cs_abi_version())
 
@@ -201,6 +234,14 @@ def _call(fn, device, args, stream):
 
 def cs_score_candidates(q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
     """One question: q[D], C[K,D] -> out[K] (float32, CUDA)."""
+    if out is not None:
+        fp = _fast if _fast_owner is _lib and _lib is not None else _fastpath()
+        if fp:
+            s = fp.score(q, C, out, normalize, scale, temperature, stream, False)
+            if s is not None:
+                if s != 0:
+                    raise CSError(s, "cs_score_candidates")
+                return out
     import torch
     qp = _check(q, "q", 1)
     cp = _check(C, "C", 2)
@@ -236,7 +277,14 @@ def _batch_ptrs(Q, C, out, c_dtype=None):
 
 def cs_score_candidates_batch(Q, C, normalize: int, scale: float, temperature: float, out=None, stream=None):
     """B questions: Q[B,D], C[B,K,D] -> out[B,K] (float32, CUDA), one launch."""
-    import torch
+    if out is not None:
+        fp = _fast if _fast_owner is _lib and _lib is not None else _fastpath()
+        if fp:
+            s = fp.score_batch(Q, C, out, normalize, scale, temperature, stream, False)
+            if s is not None:
+                if s != 0:
+                    raise CSError(s, "cs_score_candidates_batch")
+                return out
     qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out)
     s = _call(library().cs_score_candidates_batch, C.device,
               (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)
@@ -298,6 +346,14 @@ def cs_score_candidates_bf16(q, C, normalize: int, scale: float, temperature: fl
     """One question with bfloat16 candidates: q[D] float32, C[K,D] bfloat16
     -> out[K] float32 (CUDA)."""
     import torch
+    if out is not None and getattr(C, "dtype", None) == torch.bfloat16:
+        fp = _fast if _fast_owner is _lib and _lib is not None else _fastpath()
+        if fp:
+            s = fp.score(q, C, out, normalize, scale, temperature, stream, True)
+            if s is not None:
+                if s != 0:
+                    raise CSError(s, "cs_score_candidates_bf16")
+                return out
     qp = _check(q, "q", 1)
     cp = _check(C, "C", 2, torch.bfloat16)
     K, D = int(C.shape[0]), int(C.shape[1])
@@ -319,6 +375,14 @@ def cs_score_candidates_batch_bf16(Q, C, normalize: int, scale: float, temperatu
     """B questions with bfloat16 candidates: Q[B,D] float32, C[B,K,D]
     bfloat16 -> out[B,K] float32 (CUDA), one launch."""
     import torch
+    if out is not None and getattr(C, "dtype", None) == torch.bfloat16:
+        fp = _fast if _fast_owner is _lib and _lib is not None else _fastpath()
+        if fp:
+            s = fp.score_batch(Q, C, out, normalize, scale, temperature, stream, True)
+            if s is not None:
+                if s != 0:
+                    raise CSError(s, "cs_score_candidates_batch_bf16")
+                return out
     qp, cp, op, out, B, K, D = _batch_ptrs(Q, C, out, torch.bfloat16)
     s = _call(library().cs_score_candidates_batch_bf16, C.device,
               (qp, cp, B, K, D, int(normalize), float(scale), float(temperature), op), stream)

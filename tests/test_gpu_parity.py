@@ -436,3 +436,46 @@ def test_calls_without_a_stream_use_torchs_current_stream(cuda_lib):
         p = binding.cs_score_candidates_batch(wl.Q, wl.C, 1, 3.0, 1.0)
     side.synchronize()
     assert_parity(p, oracle_probs(wl.Q, wl.C, 1, 3.0, 1.0), "call on a side stream")
+
+
+def test_c_marshalling_matches_ctypes_marshalling(cuda_lib):
+    """The readout calls with `out` given go through the binding's C
+    marshalling module; the same calls without `out` go through ctypes.
+    Both reach the same library entry point, so the results are
+    bit-identical, errors come back as the same status, and what the C
+    module hands back (a wrong dtype, a non-contiguous tensor) raises the
+    ctypes path's error."""
+    fp = binding._fastpath()
+    assert fp, "the C marshalling module was not built or set up on this machine"
+    for B, K, D, normalize in ((1, 5, 512, 1), (1, 255, 2560, 0), (8, 255, 512, 1), (300, 33, 510, 0)):
+        wl = workloads.random_case(B, K, D, normalize, 3.0, 81 + B, DEV)
+        out = torch.empty(B, K, device=DEV)
+        if B == 1:
+            ref = binding.cs_score_candidates(wl.Q[0], wl.C[0], normalize, 3.0, 0.7)
+            got = binding.cs_score_candidates(wl.Q[0], wl.C[0], normalize, 3.0, 0.7, out=out[0])
+            Cb = wl.C[0].to(torch.bfloat16)
+            refb = binding.cs_score_candidates_bf16(wl.Q[0], Cb, normalize, 3.0, 0.7)
+            gotb = binding.cs_score_candidates_bf16(wl.Q[0], Cb, normalize, 3.0, 0.7,
+                                                    out=torch.empty(K, device=DEV))
+        else:
+            ref = binding.cs_score_candidates_batch(wl.Q, wl.C, normalize, 3.0, 0.7)
+            got = binding.cs_score_candidates_batch(wl.Q, wl.C, normalize, 3.0, 0.7, out=out)
+            Cb = wl.C.to(torch.bfloat16)
+            refb = binding.cs_score_candidates_batch_bf16(wl.Q, Cb, normalize, 3.0, 0.7)
+            gotb = binding.cs_score_candidates_batch_bf16(wl.Q, Cb, normalize, 3.0, 0.7,
+                                                          out=torch.empty(B, K, device=DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(ref, got) and torch.equal(refb, gotb), (B, K, D)
+    # an error status from the library, through the C module
+    q, C = torch.randn(512, device=DEV), torch.randn(256, 512, device=DEV)
+    with pytest.raises(binding.CSError) as e:
+        binding.cs_score_candidates(q, C, 1, 1.0, 1.0, out=torch.empty(256, device=DEV))
+    assert e.value.status == binding.CS_ERR_K_TOO_LARGE
+    # handed back to ctypes, which raises its own errors
+    C5 = torch.randn(5, 512, device=DEV)
+    with pytest.raises(TypeError):
+        binding.cs_score_candidates_bf16(q, C5, 1, 1.0, 1.0, out=torch.empty(5, device=DEV))
+    with pytest.raises(ValueError, match="contiguous"):
+        binding.cs_score_candidates(q, torch.randn(512, 5, device=DEV).t(), 1, 1.0, 1.0,
+                                    out=torch.empty(5, device=DEV))
+    assert fp.score(q, C5, torch.empty(5, device=DEV), 1, 1.0, 1.0, None, True) is None
