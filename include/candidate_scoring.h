@@ -19,7 +19,12 @@
  * Conventions shared by every entry point below:
  *   - All array pointers are CUDA DEVICE pointers to float32 data the caller
  *     owns (cudaMalloc, or a torch CUDA tensor). Host pointers are not
- *     detected; passing one is undefined (the kernel faults).
+ *     detected; passing one is undefined (the kernel faults). Each pointer
+ *     must be aligned to its element (4 bytes; 2 for bfloat16 candidates);
+ *     CS_ERR_MISALIGNED otherwise. Any offset from a 16-byte boundary is
+ *     fine: rows that do not start on one, or whose length is not a multiple
+ *     of 16 bytes, are copied as the aligned span around them (the bytes of
+ *     the same 16-byte granules, never used).
  *   - Layout is dense row-major: Q is [B][D], C is [B][K][D], out is [B][K].
  *     out must not overlap Q or C. Inputs are only read.
  *   - The work is queued on `stream` (a cudaStream_t; NULL = the legacy
@@ -28,8 +33,11 @@
  *     it captures into a CUDA graph as one node (PR #69, "Through a CUDA
  *     Graph" and "Verified on hardware").
  *   - The first call on a device does one-time set-up (kernel attributes and
- *     an occupancy query); make one ordinary call per device before starting
- *     a stream capture.
+ *     an occupancy query, and the device addresses of the library's own
+ *     status words) and caches it for the life of the process; make one
+ *     ordinary call per device before starting a stream capture. The cache
+ *     does not survive cudaDeviceReset: do not use the library on a device
+ *     after resetting it in the same process.
  *   - Invalid arguments return a nonzero status BEFORE any CUDA call: nothing
  *     is launched and out is untouched (PR #69, "Verified on hardware", the
  *     rejected-arguments group). A failed launch returns CS_ERR_LAUNCH.
@@ -138,8 +146,9 @@ int cs_score_candidates_batch(const float *Q, const float *C, int B, int K,
  * layout on a path whose time is the reading of C. Each element is widened
  * exactly to float32 and accumulated in float32, so the result is the
  * float32 readout of the bfloat16-rounded candidates. q and out stay
- * float32. The fast plans need D % 8 == 0 and 16-byte aligned Q and C;
- * other shapes take the scalar plan. Arguments, errors and conventions as
+ * float32. Rows with D % 8 != 0 or off a 16-byte boundary stream as
+ * aligned spans like float32 ones (a few such questions take the scalar
+ * plan). Arguments, errors and conventions as
  * cs_score_candidates / cs_score_candidates_batch. (bfloat16 storage is our
  * extension; the page's kernel reads float32.)
  */
@@ -211,11 +220,14 @@ int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,
 
 /* Execution plans (kernel choices) the library picks between. */
 #define CS_PLAN_AUTO 0
-#define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions */
+#define CS_PLAN_STREAM 1   /* persistent CTAs, each streams a run of questions
+                              (bulk copies; unaligned rows as aligned spans) */
 #define CS_PLAN_CLUSTER 2  /* one thread-block cluster per question, rows split */
 #define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment (one CTA per
                               question, or a cluster of CTAs per question
-                              when a uniform-K batch has few questions) */
+                              when a uniform-K batch has few questions): a
+                              few unaligned questions, or rows too long for
+                              the shared-memory ring */
 #define CS_PLAN_DIRECT 4   /* one CTA (or cluster) per short question: at most 32
                               rows per CTA, q and rows loaded straight into
                               registers, no shared-memory ring */
@@ -241,8 +253,10 @@ int cs_query_plan(const float *Q, const float *C, int B, int K, int D,
  * 2..16 (at most K) spreads each question's rows over a cluster of that many
  * CTAs.
  * Returns CS_ERR_BAD_PLAN when the plan cannot run these arguments (e.g.
- * CS_PLAN_STREAM or CS_PLAN_CLUSTER with D % 4 != 0 or unaligned pointers).
- * The result equals the automatic plan's within float32 rounding.
+ * CS_PLAN_DIRECT with D % 4 != 0 or Q or C off a 16-byte boundary, or a
+ * ring that does not fit shared memory for CS_PLAN_STREAM/CLUSTER; these
+ * two take unaligned rows as aligned spans). The result equals the
+ * automatic plan's within float32 rounding.
  */
 int cs_score_candidates_batch_plan(const float *Q, const float *C, int B,
                                    int K, int D, int normalize, float scale,
@@ -263,7 +277,8 @@ int cs_score_candidates_batch_plan(const float *Q, const float *C, int B,
  * rounding), plus `staged`: a caller-owned device buffer of B*K floats that
  * must not overlap Q, C or out; its contents on return are pass 1's values.
  * Two kernels are enqueued on `stream` (two graph nodes when captured).
- * Needs D % 4 == 0 and 16-byte aligned Q and C (CS_ERR_BAD_PLAN otherwise).
+ * Needs D % 4 == 0 and 16-byte aligned Q and C (CS_ERR_BAD_PLAN otherwise:
+ * the baseline's passes have no unaligned build).
  */
 int cs_score_candidates_batch_unfused(const float *Q, const float *C, int B,
                                       int K, int D, int normalize, float scale,
