@@ -151,9 +151,9 @@ int cached_generic_clusters(DeviceState& d, int cluster, int normalize, int c_bf
 }
 
 int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows) {
-    // nq4 + 2 in bits 2..5 (nq4 is kNqcUnalignedVec = -2, kNqcUnaligned = -1, 0, 1, 2, 4 or 8)
+    // nq4 + 1 in bits 2..5 (nq4 is kNqcUnaligned = -1, 0, 1, 2, 4 or 8)
     const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) |
-                           (static_cast<long long>(nq4 + 2) << 2) | (c_bf16 << 1) | normalize;
+                           (static_cast<long long>(nq4 + 1) << 2) | (c_bf16 << 1) | normalize;
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = d.clusters.find({cluster, key2});
     if (it != d.clusters.end()) return it->second;
@@ -195,16 +195,16 @@ int stage_rows(long long row_bytes) {
 // to warp g % kConsumerWarps, so with NS a multiple of the warp count every
 // slot always has the same owner, which consumes its uses in order: a
 // parity wait on a slot can then never see a phase two uses old.
-int max_stages(const DeviceState& d, int R, int D, int c_bytes, int form) {
-    const long long stage_bytes = static_cast<long long>(cs::smem_layout(1, R, D, c_bytes, form).slot_bytes);
-    const size_t fixed = cs::smem_layout(0, R, D, c_bytes, form).total;
+int max_stages(const DeviceState& d, int R, int D, int c_bytes, bool ua) {
+    const long long stage_bytes = static_cast<long long>(cs::smem_layout(1, R, D, c_bytes, ua).slot_bytes);
+    const size_t fixed = cs::smem_layout(0, R, D, c_bytes, ua).total;
     if (fixed >= static_cast<size_t>(d.smem_optin)) return 0;
     long long ns = static_cast<long long>(d.smem_optin - fixed) / stage_bytes;
     if (ns > kMaxStages) ns = kMaxStages;
     ns -= ns % cs::kConsumerWarps;
     // The barrier array grows by 16 bytes per stage as well.
     while (ns > 0 &&
-           cs::smem_layout(static_cast<int>(ns), R, D, c_bytes, form).total > static_cast<size_t>(d.smem_optin))
+           cs::smem_layout(static_cast<int>(ns), R, D, c_bytes, ua).total > static_cast<size_t>(d.smem_optin))
         ns -= cs::kConsumerWarps;
     return ns > 0 ? static_cast<int>(ns) : 0;
 }
@@ -216,28 +216,6 @@ int ring_stages(long long need, int max_ns) {
     return ns < max_ns ? static_cast<int>(ns) : max_ns;
 }
 
-// Ring bytes below which the vector form of unaligned rows (whose shifted
-// copies of q take shared memory from the ring) gives way to the scalar form.
-constexpr long long kVectorMinRing = 96 * 1024;
-
-// How the stream and cluster plans copy and read these rows (cs::RowForm):
-// whole when the bulk copies can take them as they are; otherwise as aligned
-// spans, read as 16-byte chunks against shifted copies of q when those
-// leave the ring at least kVectorMinRing bytes, else as scalars.
-int row_form(const DeviceState& d, const Problem& p) {
-    if (tma_eligible(p)) return cs::kRowsWhole;
-    const int cb = cs::c_elem_bytes(p);
-    const int R = stage_rows(static_cast<long long>(cb) * p.D);
-    const long long ring = static_cast<long long>(max_stages(d, R, p.D, cb, cs::kRowsSpanVector)) *
-                           static_cast<long long>(cs::smem_layout(1, R, p.D, cb, cs::kRowsSpanVector).slot_bytes);
-    return ring >= kVectorMinRing ? cs::kRowsSpanVector : cs::kRowsSpanScalar;
-}
-
-int form_nq4(const Problem& p, int form) {
-    return form == cs::kRowsSpanVector ? cs::kNqcUnalignedVec : form == cs::kRowsSpanScalar ? cs::kNqcUnaligned
-                                                                                             : nq4_for(p);
-}
-
 // STREAM plan with `ctas` persistent CTAs (0 = one per SM, at most B).
 // Picks rows per stage R <= stage_rows(D) that keeps the most bytes in
 // flight (larger R on ties). Rows the bulk copies cannot take whole (not
@@ -245,11 +223,11 @@ int form_nq4(const Problem& p, int form) {
 // false if no ring fits.
 bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     const int cb = cs::c_elem_bytes(p);
-    const int form = row_form(d, p);
+    const bool ua = !tma_eligible(p);
     int R = 0, max_ns = 0;
     long long best = 0;
     for (int r = stage_rows(static_cast<long long>(cb) * p.D); r >= 1; --r) {
-        const int ns = max_stages(d, r, p.D, cb, form);
+        const int ns = max_stages(d, r, p.D, cb, ua);
         const long long bytes = static_cast<long long>(cb) * r * p.D * ns;
         if (bytes > best) {
             best = bytes;
@@ -266,7 +244,7 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     // every consumer warp gets a stage instead of one warp doing them all.
     if (!p.offsets && qpc * p.K < static_cast<long long>(cs::kConsumerWarps) * R) {
         const int r = static_cast<int>((qpc * p.K + cs::kConsumerWarps - 1) / cs::kConsumerWarps);
-        const int ns = max_stages(d, r, p.D, cb, form);
+        const int ns = max_stages(d, r, p.D, cb, ua);
         if (ns > 0) {
             R = r;
             max_ns = ns;
@@ -278,8 +256,8 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     plan->ctas = ctas;
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = form_nq4(p, form);
-    plan->smem = cs::smem_layout(ns, R, p.D, cb, form).total;
+    plan->nq4 = ua ? cs::kNqcUnaligned : nq4_for(p);
+    plan->smem = cs::smem_layout(ns, R, p.D, cb, ua).total;
     return true;
 }
 
@@ -287,13 +265,13 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
 // consumer warps (one stage each) when the ring holds them.
 bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     const int cb = cs::c_elem_bytes(p);
-    const int form = row_form(d, p);
+    const bool ua = !tma_eligible(p);
     const int rows = (p.K + G - 1) / G;
     int R = (rows + cs::kConsumerWarps - 1) / cs::kConsumerWarps;
     const int Rmax = stage_rows(static_cast<long long>(cb) * p.D);
     if (R > Rmax) R = Rmax;
-    while (R > 1 && max_stages(d, R, p.D, cb, form) == 0) --R;  // a ring of 8 stages must fit
-    const int max_ns = max_stages(d, R, p.D, cb, form);
+    while (R > 1 && max_stages(d, R, p.D, cb, ua) == 0) --R;  // a ring of 8 stages must fit
+    const int max_ns = max_stages(d, R, p.D, cb, ua);
     if (max_ns == 0) return false;
     const int ns = ring_stages((rows + R - 1) / R, max_ns);
     plan->kind = cs::kPlanCluster;
@@ -301,8 +279,8 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     plan->ctas = G * static_cast<int>(p.B);
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = form_nq4(p, form);
-    plan->smem = cs::smem_layout(ns, R, p.D, cb, form).total;
+    plan->nq4 = ua ? cs::kNqcUnaligned : nq4_for(p);
+    plan->smem = cs::smem_layout(ns, R, p.D, cb, ua).total;
     return true;
 }
 

@@ -74,7 +74,7 @@ struct Plan {
     int rows_per_stage;// candidate rows per bulk-copy stage
     int stages;        // stages in the shared-memory ring
     int nq4;           // 16-byte chunks of a C row per lane whose q sits in registers (0: q read from
-                       // smem; kNqcUnaligned, kNqcUnalignedVec: unaligned rows)
+                       // smem; kNqcUnaligned: unaligned rows)
     size_t smem;       // dynamic shared memory per CTA
 };
 
@@ -86,8 +86,6 @@ struct SmemLayout {
     size_t qbuf;        // 2 slots of qslot_bytes: the query rows
     size_t qslot_bytes;
     size_t tn;          // 2 buffers x (dot[kLogitSlots], squared norm[kLogitSlots]) floats
-    size_t qcopy;       // vector row form: qready[2] mbarriers, then 2 buffers of qcopy_bytes
-    size_t qcopy_bytes; // one question's shifted copies of q (0 unless the vector form)
     size_t xch;         // kMaxCluster float2 (max, sum) received from the cluster's CTAs
     size_t bars;        // full[stages], empty[stages], qfull[2], qempty[2], xbar (8 B each)
     size_t range;       // two long longs: this CTA's question range (ragged STREAM plan)
@@ -101,39 +99,19 @@ struct SmemLayout {
 // granules as the rows' own bytes. A slot holds that span.
 __host__ __device__ inline size_t span_bytes(size_t bytes) { return (bytes + 15) / 16 * 16 + 32; }
 
-// How the streaming kernels read rows (Plan.nq4 tells them apart):
-//   kNqcUnaligned     aligned spans, read as scalars, q from shared memory;
-//   kNqcUnalignedVec  aligned spans, read as 16-byte chunks against copies
-//                     of q shifted to each element offset a row can start
-//                     at within a 16-byte granule (16 / c_bytes copies,
-//                     built once per question by the query-producer warp).
-constexpr int kNqcUnaligned = -1;
-constexpr int kNqcUnalignedVec = -2;
-enum RowForm { kRowsWhole = 0, kRowsSpanScalar = 1, kRowsSpanVector = 2 };
-
-// Chunks of 16 bytes a row of D elements spans at most, and the floats of
-// one shifted copy of q covering them.
-__host__ __device__ inline int qcopy_chunks(int D, int c_bytes) { return (D * c_bytes + 15) / 16 + 1; }
-__host__ __device__ inline int qcopy_floats(int D, int c_bytes) { return qcopy_chunks(D, c_bytes) * (16 / c_bytes); }
-
-// c_bytes: bytes of one element of C (4 float32, 2 bfloat16). form: how rows
-// are copied and read (RowForm); the vector form adds, after the per-row
-// arrays, two mbarriers (a question's copies of q are ready) and two
-// buffers of 16 / c_bytes shifted copies of q.
+// c_bytes: bytes of one element of C (4 float32, 2 bfloat16). unaligned:
+// slots sized for the aligned spans of rows at any 4-byte (float32) or
+// 2-byte (bfloat16) offset.
 __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage, int D, int c_bytes,
-                                                  int form = kRowsWhole) {
+                                                  bool unaligned = false) {
     SmemLayout L;
     size_t off = 0;
-    const bool span = form != kRowsWhole;
     const size_t stage = (size_t)rows_per_stage * D * c_bytes, q = (size_t)D * sizeof(float);
-    L.slot_bytes = span ? span_bytes(stage) : stage;
-    L.qslot_bytes = span ? span_bytes(q) : q;
+    L.slot_bytes = unaligned ? span_bytes(stage) : stage;
+    L.qslot_bytes = unaligned ? span_bytes(q) : q;
     L.ring = off;   off += (size_t)stages * L.slot_bytes;
     L.qbuf = off;   off += 2 * L.qslot_bytes;
     L.tn = off;     off += 4 * (size_t)kLogitSlots * sizeof(float);
-    L.qcopy = off;
-    L.qcopy_bytes = form == kRowsSpanVector ? (size_t)(16 / c_bytes) * qcopy_floats(D, c_bytes) * sizeof(float) : 0;
-    off += form == kRowsSpanVector ? 16 + 2 * L.qcopy_bytes : 0;
     L.xch = off;    off += (size_t)kMaxCluster * 8;
     L.bars = off;   off += (2 * (size_t)stages + 5) * 8;
     L.range = off;  off += 16;
@@ -141,6 +119,11 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
     L.total = off;
     return L;
 }
+
+// Plan.nq4 of the streaming kernels for rows the bulk copies take as
+// aligned spans (D not a multiple of 16 bytes' worth of elements, or Q or C
+// off a 16-byte boundary): scalar shared-memory reads, q in shared memory.
+constexpr int kNqcUnaligned = -1;
 
 // What one launch of the streaming kernel computes.
 enum StreamMode {

@@ -632,72 +632,6 @@ __device__ __forceinline__ void stage_dots_scalar(const T* __restrict__ st, int 
     for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
 }
 
-// Zero the elements of a widened 16-byte chunk whose row index e0 + m lies
-// outside [0, D) (the neighbouring bytes an aligned span carries).
-template <int QF4>
-__device__ __forceinline__ void mask_chunk(float4 (&c)[QF4], int e0, int D) {
-#pragma unroll
-    for (int h = 0; h < QF4; ++h) {
-        const int e = e0 + 4 * h;
-        if (e < 0 || e >= D) c[h].x = 0.f;
-        if (e + 1 < 0 || e + 1 >= D) c[h].y = 0.f;
-        if (e + 2 < 0 || e + 2 >= D) c[h].z = 0.f;
-        if (e + 3 < 0 || e + 3 >= D) c[h].w = 0.f;
-    }
-}
-
-// The same sums for a stage of unaligned rows read as 16-byte chunks (vector
-// row form). Row r starts `shift + r D` elements' worth of bytes into the
-// slot, u elements into its first 16-byte granule; its chunks are read
-// whole, and q comes from the copy shifted by u (qc + u Dq: element k of it
-// is q[k - u], zero outside), so chunk i meets q for exactly its elements.
-// Elements of the first and last chunk outside the row are zeroed.
-template <int MODE, typename T, int MR, typename Release>
-__device__ __forceinline__ void stage_dots_vec(const unsigned char* __restrict__ slot, uint32_t shift, int nr, int D,
-                                               const float* __restrict__ qc, int Dq, int lane,
-                                               float (&v)[values_per_row(MODE) * MR], Release&& release) {
-    constexpr int VPR = values_per_row(MODE);
-    constexpr int QF4 = Elem<T>::kQF4;
-    constexpr int EPC = Elem<T>::kPerChunk;
-    constexpr uint32_t ES = sizeof(T);
-    unsigned long long acc[VPR * MR];
-#pragma unroll
-    for (int i = 0; i < VPR * MR; ++i) acc[i] = 0ull;
-    auto accumulate = [&](const float4& c, const float4& q, int r) {
-        const unsigned long long c01 = pack2(c.x, c.y), c23 = pack2(c.z, c.w);
-        if (acc_dot(MODE)) {
-            unsigned long long& t = acc[VPR * r];
-            t = fma2(c01, pack2(q.x, q.y), t);
-            t = fma2(c23, pack2(q.z, q.w), t);
-        }
-        if (acc_norm(MODE)) {
-            unsigned long long& n = acc[VPR * r + VPR - 1];
-            n = fma2(c01, c01, n);
-            n = fma2(c23, c23, n);
-        }
-    };
-#pragma unroll
-    for (int r = 0; r < MR; ++r) {
-        if (r < nr) {
-            const uint32_t ro = shift + static_cast<uint32_t>(r) * static_cast<uint32_t>(D) * ES;
-            const int u = static_cast<int>((ro & 15u) / ES);
-            const uint4* rc = reinterpret_cast<const uint4*>(slot + (ro & ~15u));
-            const float4* q4 = reinterpret_cast<const float4*>(qc + u * Dq);
-            const int nch = (u * static_cast<int>(ES) + D * static_cast<int>(ES) + 15) / 16;
-            for (int i = lane; i < nch; i += 32) {
-                float4 c[QF4];
-                Elem<T>::widen(rc[i], c);
-                if (i == 0 || i == nch - 1) mask_chunk<QF4>(c, i * EPC - u, D);
-#pragma unroll
-                for (int h = 0; h < QF4; ++h) accumulate(c[h], q4[i * QF4 + h], r);
-            }
-        }
-    }
-    release();
-#pragma unroll
-    for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
-}
-
 // Global address of `bytes` bytes at src, widened to whole 16-byte granules
 // for a bulk copy: returns the aligned start and sets *shift (the offset of
 // src in it) and *span (the copy's length, a multiple of 16).
@@ -737,16 +671,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     }
 
     // UA: rows and queries need not start on 16-byte boundaries; each copy
-    // takes their aligned span and readers index from the offset in it,
-    // with scalar reads or (UAV) 16-byte reads against shifted copies of q.
-    constexpr bool UAV = NQC == kNqcUnalignedVec;
-    constexpr bool UA = NQC == kNqcUnaligned || UAV;
-    constexpr int NSH = 16 / static_cast<int>(sizeof(T));  // element offsets within a 16-byte granule
-    const SmemLayout L =
-        smem_layout(NS, R, D, static_cast<int>(sizeof(T)), UAV ? kRowsSpanVector : UA ? kRowsSpanScalar : kRowsWhole);
-    const uint32_t qready0 = smem_u32(smem + L.qcopy);  // UAV: a question's copies of q are ready
-    float* qcopy = reinterpret_cast<float*>(smem + L.qcopy + 16);
-    const int Dq = qcopy_floats(D, static_cast<int>(sizeof(T)));
+    // takes their aligned span and readers index from the offset in it.
+    constexpr bool UA = NQC == kNqcUnaligned;
+    const SmemLayout L = smem_layout(NS, R, D, static_cast<int>(sizeof(T)), UA);
     unsigned char* ring = smem + L.ring;
     const uint32_t slot_bytes = static_cast<uint32_t>(L.slot_bytes);
     unsigned char* qbuf = smem + L.qbuf;
@@ -772,7 +699,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const uint32_t count = (i >= 2 * NS + 2 && i < 2 * NS + 4) ? kConsumerWarps : 1u;
             mbar_init(full0 + 8u * i, count);
         }
-        if (UAV && lane < 2) mbar_init(qready0 + 8u * lane, 1);
         if (lane == 0) *give_up = 0;
         fence_mbar_init();
         __syncwarp();
@@ -914,47 +840,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         __syncwarp();
     } else if (warp == kConsumerWarps + 1) {
         // ---------------- query producer: one lane issues every question's q
-        if constexpr (UAV) {
-            // The whole warp: lane 0 copies each question's q span into its
-            // staging slot; once it lands, every lane helps build the
-            // question's NSH copies of q shifted by 0 .. NSH-1 elements
-            // (zero outside the row) into its copy buffer, and lane 0 marks
-            // them ready. Slots and buffers alternate by question; one is
-            // reused once the consumers have finished the question two before.
-            long long nq = 0, issued = 0;
-            for (long long b = qb; b < qe; ++b, ++nq) {
-                const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
-                const float* src = p.Q + static_cast<size_t>(b) * D;
-                uint32_t shift = 0, span = q_bytes;
-                const void* from = aligned_span(src, q_bytes, &shift, &span);
-                // every lane waits (each then reads or overwrites what the
-                // barrier guards); the vote keeps the warp together
-                if (!__all_sync(0xffffffffu, nq < 2 || wait_phase(qempty0 + 8u * qs, qpar ^ 1u, give_up))) break;
-                if (lane == 0) {
-                    unsigned char* dst = qbuf + qs * qslot_bytes;
-                    const bool inb = CS_IN_BOUNDS(src, q_bytes, p.Q, p.B * q_bytes, kSiteCopyQ) &&
-                                     CS_IN_BOUNDS(dst, span, qbuf, 2 * qslot_bytes, kSiteQbuf);
-                    mbar_arrive_expect_tx(qfull0 + 8u * qs, inb ? span : 0u);
-                    if (inb) bulk_g2s(smem_u32(dst), from, span, qfull0 + 8u * qs);
-                }
-                ++issued;
-                if (!__all_sync(0xffffffffu, wait_phase(qfull0 + 8u * qs, qpar, give_up))) break;
-                const float* qf = reinterpret_cast<const float*>(qbuf + qs * qslot_bytes + shift);
-                float* copies = qcopy + static_cast<size_t>(qs) * NSH * Dq;
-                for (int i = lane; i < NSH * Dq; i += 32) {
-                    const int u = i / Dq, e = i - u * Dq - u;
-                    copies[i] = e >= 0 && e < D ? qf[e] : 0.f;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(qready0 + 8u * qs);
-            }
-            if (lane == 0 && *give_up) {
-                const unsigned long long deadline = globaltimer() + kWaitLimitNs;
-                for (long long u = issued > 2 ? issued - 2 : 0; u < issued; ++u)
-                    wait_phase_until(qfull0 + 8u * static_cast<uint32_t>(u & 1),
-                                     static_cast<uint32_t>((u >> 1) & 1), deadline);
-            }
-        } else if (lane == 0) {
+        if (lane == 0) {
             long long nq = 0;
             for (long long b = qb; b < qe; ++b, ++nq) {
                 const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
@@ -990,9 +876,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const int nst = (nrows + R - 1) / R;
             if (qr.bad && warp == 0 && lane == 0) atomicOr(&g_status, 4u);
             const uint32_t qs = static_cast<uint32_t>(nq & 1), qpar = static_cast<uint32_t>((nq >> 1) & 1);
-            bool good = wait_phase((UAV ? qready0 : qfull0) + 8u * qs, qpar, give_up);
+            bool good = wait_phase(qfull0 + 8u * qs, qpar, give_up);
             unsigned char* qslot = qbuf + qs * qslot_bytes;
-            const float* qcopies = qcopy + static_cast<size_t>(qs) * NSH * Dq;  // UAV: copy 0 is q itself
             const float4* q4 = reinterpret_cast<const float4*>(qslot);
             // UA: q at its offset in the aligned span the producer copied
             const float* qf = reinterpret_cast<const float*>(
@@ -1001,9 +886,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             float qsq = 0.f;  // |q|^2 (cosine)
             if constexpr (UA) {
                 if (COS) {
-                    const float* qn = UAV ? qcopies : qf;
                     float sq = 0.f;
-                    for (int i = lane; i < D; i += 32) sq = fmaf(qn[i], qn[i], sq);
+                    for (int i = lane; i < D; i += 32) sq = fmaf(qf[i], qf[i], sq);
                     qsq = warp_sum(sq);
                 }
             } else if constexpr (NQC > 0) {
@@ -1052,12 +936,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 if constexpr (UA) {
                     // the rows at their offset in the aligned span
                     const T* src = Cg + static_cast<size_t>(qr.row0 + k0) * D;
-                    const uint32_t shift = static_cast<uint32_t>(reinterpret_cast<unsigned long long>(src) & 15u);
-                    if constexpr (UAV)
-                        stage_dots_vec<MODE, T, MR>(st, shift, nr, D, qcopies, Dq, lane, v, release);
-                    else
-                        stage_dots_scalar<MODE, T, MR>(reinterpret_cast<const T*>(st + shift), nr, D, qf, lane, v,
-                                                       release);
+                    stage_dots_scalar<MODE, T, MR>(
+                        reinterpret_cast<const T*>(st + (reinterpret_cast<unsigned long long>(src) & 15u)), nr, D,
+                        qf, lane, v, release);
                 } else {
                     stage_dots<NQC, MODE, T, MR>(reinterpret_cast<const uint4*>(st), nr, DC, qv, q4, lane, v,
                                                  release);
@@ -1550,11 +1431,6 @@ cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t 
                 return launch_stream_t<kNqcUnaligned, MODE, T, MR>(a, plan, stream);
             else
                 return cudaErrorInvalidValue;
-        case kNqcUnalignedVec:
-            if constexpr ((MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage)
-                return launch_stream_t<kNqcUnalignedVec, MODE, T, MR>(a, plan, stream);
-            else
-                return cudaErrorInvalidValue;
         case 1: return launch_stream_t<1, MODE, T, MR>(a, plan, stream);
         case 2: return launch_stream_t<2, MODE, T, MR>(a, plan, stream);
         case 4: return launch_stream_t<4, MODE, T, MR>(a, plan, stream);
@@ -1572,11 +1448,6 @@ const void* stream_fn_m(int nqc) {
                 return reinterpret_cast<const void*>(stream_kernel<kNqcUnaligned, MODE, T, MR>);
             else
                 return nullptr;
-        case kNqcUnalignedVec:
-            if constexpr ((MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage)
-                return reinterpret_cast<const void*>(stream_kernel<kNqcUnalignedVec, MODE, T, MR>);
-            else
-                return nullptr;
         case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE, T, MR>);
         case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE, T, MR>);
         case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE, T, MR>);
@@ -1589,8 +1460,9 @@ const void* stream_fn_m(int nqc) {
 // The row limit of the instantiation that runs stages of R rows in `mode`
 // (unaligned plans have only the full-size build).
 constexpr int rows_limit(int mode, int R, int nqc) {
-    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows && nqc >= 0 ? kSmallStageRows
-                                                                                         : kMaxRowsPerStage;
+    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows && nqc != kNqcUnaligned
+               ? kSmallStageRows
+               : kMaxRowsPerStage;
 }
 
 // Kernels exist for every mode over float32 C, and for the fused modes over
@@ -1599,7 +1471,7 @@ constexpr int rows_limit(int mode, int R, int nqc) {
 // the full stage size, for unaligned rows (nqc = kNqcUnaligned).
 const void* stream_fn_for(int nqc, int mode, int c_bf16, int mr) {
     const bool fused = mode == kFusedCos || mode == kFusedDot;
-    if (nqc < 0 && (!fused || mr != kMaxRowsPerStage)) return nullptr;
+    if (nqc == kNqcUnaligned && (!fused || mr != kMaxRowsPerStage)) return nullptr;
     if (mr == kSmallStageRows) {
         if (!fused || (c_bf16 && nqc == 8)) return nullptr;
         if (c_bf16)
@@ -1799,10 +1671,10 @@ cudaError_t configure_device_kernels(int smem_optin) {
                     cudaFuncSetAttribute(direct_fn_for(nqc, cos, bf), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (e != cudaSuccess) return e;
             }
-    const int nq4s[7] = {1, 2, 4, 8, 0, kNqcUnaligned, kNqcUnalignedVec};
+    const int nq4s[6] = {1, 2, 4, 8, 0, kNqcUnaligned};
     for (int bf = 0; bf < 2; ++bf) {
         for (int m = kFusedCos; m <= kStagedCos; ++m) {
-            for (int i = 0; i < 7; ++i) {
+            for (int i = 0; i < 6; ++i) {
                 for (int mr : {kSmallStageRows, kMaxRowsPerStage}) {
                     const void* f = stream_fn_for(nq4s[i], m, bf, mr);
                     if (!f) continue;
