@@ -161,6 +161,8 @@ def _fastpath():
     lib = library()
     if _fast_owner is lib:
         return _fast
+    if _fast is False:
+        return None
     with _lock:
         if _fast is None:
             try:
