@@ -554,7 +554,27 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
                 }
             }
         }
+    } else if constexpr (NQC > 0 && std::is_same<T, float>::value) {
+        // float32: chunks outer, the stage's rows inner (1.4 % more
+        // throughput than rows outer for the cosine and the dot)
+#pragma unroll
+        for (int j = 0; j < NQC; ++j) {
+            const int i = lane + 32 * j;
+            if (i < DC) {
+#pragma unroll
+                for (int r = 0; r < MR; ++r) {
+                    if (r < nr) {
+                        float4 c[QF4];
+                        Elem<T>::widen(st[r * DC + i], c);
+#pragma unroll
+                        for (int h = 0; h < QF4; ++h) accumulate(c[h], qv[j * QF4 + h], r);
+                    }
+                }
+            }
+        }
+        release();
     } else if constexpr (NQC > 0) {
+        // bfloat16: rows outer (chunks outer was 0.9 % slower for the dot)
 #pragma unroll
         for (int r = 0; r < MR; ++r) {
             if (r < nr) {
