@@ -469,28 +469,27 @@ def main():
     clocks.start()
 
     def timed(wl):
+        """K steps between two CUDA events on the launching stream. Nothing
+        else enters the stream between the launches: an event recorded
+        between two launches makes the second wait for the first's full
+        completion, which takes away the dependent-launch overlap a caller's
+        back-to-back calls get (about 3 % of the step). The step is nothing
+        but these launches, so its time over the launches is the mean launch
+        time the roofline uses."""
         for _ in range(args.warmup):
             step(wl)
         barrier()
         n_launch = args.steps * (B_TOTAL // CHUNK)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_launch)]
         t_wall = time.time()
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-        i = 0
         for _ in range(args.steps):
-            for b0 in range(0, B_TOTAL, CHUNK):
-                ev[i].record(stream)
-                cs.cs_score_candidates_batch(wl.Q[b0:b0 + CHUNK], wl.C[b0:b0 + CHUNK], wl.normalize, wl.scale,
-                                             wl.temperature, out=out[b0:b0 + CHUNK], stream=stream)
-                ev[i + 1].record(stream)
-                i += 2
+            step(wl)
         stop.record(stream)
         barrier()
         clocks.window(t_wall, time.time())
         ms = max_over_ranks(start.elapsed_time(stop))
-        launch_ms = [ev[j].elapsed_time(ev[j + 1]) for j in range(0, 2 * n_launch, 2)]
-        return ms, launch_ms, n_launch
+        return ms, [ms / n_launch] * n_launch, n_launch
 
     ms_cos, launches_cos, n_launch = timed(wl_cos)
     ms_dot, launches_dot, _ = timed(wl_dot)
@@ -527,6 +526,8 @@ def main():
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": f"stream_kernel (STREAM plan), one launch = {CHUNK} questions",
                      "algorithmic_bytes_per_launch": launch_bytes, "mean_launch_ms": mean_launch_ms,
+                     "mean_launch_ms_from": "the timed steps' CUDA events over their launches (the step is "
+                                            "only this kernel's launches, back to back)",
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
         "clocks": clock_info,
         "extra": {
@@ -791,8 +792,8 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
 
 def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32):
     """us per call, cosine K=255 D=512, of the automatic plan and of every
-    forced plan (STREAM; CLUSTER with 2..16 CTAs per question; DIRECT over 16
-    CTAs where it fits), each as n calls on consecutive slices of a
+    forced plan (STREAM; CLUSTER with 2..16 CTAs per question; DIRECT over 8
+    and 16 CTAs where it fits), each as n calls on consecutive slices of a
     4096-question buffer captured in one CUDA graph after a read of a
     256 MiB buffer (which leaves L2 holding none of the slices), minus the
     same graph without the calls: device time per call, every call reading
@@ -806,7 +807,7 @@ def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32)
     out = torch.empty(Bmax, K, device=dev)
     flush = torch.ones(64 << 20, device=dev)  # 256 MiB, read only
     plans = [("stream", cs.CS_PLAN_STREAM, 0)] + [(f"cluster{G}", cs.CS_PLAN_CLUSTER, G) for G in (2, 4, 8, 16)] + \
-        [("direct16", cs.CS_PLAN_DIRECT, 16)]
+        [("direct8", cs.CS_PLAN_DIRECT, 8), ("direct16", cs.CS_PLAN_DIRECT, 16)]
 
     def timed(B, plan, G):
         nsl = Bmax // B
