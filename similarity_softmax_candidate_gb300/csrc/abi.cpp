@@ -406,16 +406,23 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
                q_bytes / (G * 2) >= kSplitMinBytes)
             G *= 2;
         // Short questions (at most kDirectMaxRows rows per CTA): the DIRECT
-        // plan, one trip to memory and no ring.
+        // plan, one trip to memory and no ring. The fewest CTAs per question
+        // that keep each within the row limit, doubled while the grid stays
+        // within half the SMs and each CTA keeps kSplitMinBytes of rows; taken
+        // while its clusters run in at most 1.5 waves (the plan sweep on
+        // K=255, D=512: 8-CTA clusters beat the cluster plans up to 48
+        // questions, 16-CTA ones are best up to 4).
         int max_rows = 0;
         if (fused && direct_form(p, &max_rows) != 0) {
-            int g = G;
             const int kmax = p.offsets ? CS_MAX_K : p.K;
-            while ((kmax + g - 1) / g > max_rows && g * 2 <= cs::kMaxCluster && g * 2 <= p.K &&
-                   (g * 2) * p.B <= d.sms)
+            int g = 1;
+            while ((kmax + g - 1) / g > max_rows && g * 2 <= cs::kMaxCluster && g * 2 <= p.K) g *= 2;
+            while (g * 2 <= cs::kMaxCluster && g * 2 <= avg_k && (g * 2) * p.B * 2 <= d.sms &&
+                   q_bytes / (g * 2) >= kSplitMinBytes)
                 g *= 2;
             if (direct_plan(p, g, plan) &&
-                (g == 1 || cached_direct_clusters(d, g, plan->nq4, p.normalize, p.c_bf16) >= p.B))
+                (g == 1 ||
+                 3ll * cached_direct_clusters(d, g, plan->nq4, p.normalize, p.c_bf16) >= 2ll * p.B))
                 return CS_OK;
         }
         for (; G > 1; G /= 2) {
