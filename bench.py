@@ -392,7 +392,9 @@ def main():
     ap.add_argument("--only-unaligned", action="store_true",
                     help="profiling aid: time only the unaligned-row workloads and print their record")
     ap.add_argument("--only-unaligned-case", choices=[c[0] for c in UNALIGNED_CASES], default=None,
-                    help="profiling aid: W + K calls of one unaligned-row case (float32 cosine, 4096 questions)")
+                    help="profiling aid: W + K calls of one unaligned-row case (cosine, 4096 questions)")
+    ap.add_argument("--only-unaligned-dtype", choices=["f32", "bf16"], default="f32",
+                    help="candidate type of --only-unaligned-case")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
                     help="profiling aid: time only the projected readout on B questions and print its record")
     ap.add_argument("--plan-sweep", action="store_true",
@@ -431,7 +433,8 @@ def main():
         return 0
     if args.only_unaligned_case:
         if rank == 0:
-            print(json.dumps(unaligned_rows(cs, dev, args.steps, args.warmup, only=args.only_unaligned_case)),
+            print(json.dumps(unaligned_rows(cs, dev, args.steps, args.warmup, only=args.only_unaligned_case,
+                                            only_dtype=args.only_unaligned_dtype)),
                   flush=True)
         return 0
     if args.only_unaligned:
@@ -650,34 +653,46 @@ def extras(cs, workloads, wl_cos, wl_dot, out, dev, stream, args, world, barrier
     return bf16, ragged_info, unfused
 
 
-UNALIGNED_CASES = (("aligned_d512", 512, 0), ("odd_d510", 510, 0), ("misaligned_d512", 512, 1))
+# (name, D, element offset of Q and C from a 16-byte boundary, questions,
+# the aligned case it is compared with)
+UNALIGNED_CASES = (("aligned_d512", 512, 0, 4096, None), ("odd_d510", 510, 0, 4096, "aligned_d512"),
+                   ("misaligned_d512", 512, 1, 4096, "aligned_d512"), ("aligned_d2560", 2560, 0, 1024, None),
+                   ("misaligned_d2560", 2560, 1, 1024, "aligned_d2560"))
 
 
-def unaligned_rows(cs, dev, steps, warmup, B=4096, only=None):
-    """Rows the bulk copies cannot take whole, at throughput size: B
+def unaligned_rows(cs, dev, steps, warmup, only=None, only_dtype="f32"):
+    """Rows the bulk copies cannot take whole, at throughput size: 4096
     questions of K=255 with D=510 (rows of 2040 bytes), and with D=512 but
-    Q and C one element past a 16-byte boundary; each against the aligned
-    D=512 readout on the same buffer, and against the scalar plan forced on
-    the same rows; float32 and bfloat16 candidates. One launch per call
-    over 2.1 GB (larger than L2). only: time just that case's float32
-    cosine readout (a profiling aid)."""
+    Q and C one element past a 16-byte boundary, each against the aligned
+    D=512 readout on the same buffer; and 1024 questions of D=2560 one
+    element off, against aligned D=2560. Float32 cases also against the
+    scalar plan forced on the same rows; float32 and bfloat16 candidates.
+    One launch per call over at least 2.1 GB (larger than L2). only: time
+    just that case's cosine readout with only_dtype candidates (a profiling
+    aid)."""
     import torch
-    flatC = torch.empty(B * K * 512 + 64, device=dev)
-    flatQ = torch.empty(B * 512 + 64, device=dev)
+    n_c = max(B * K * d for _, d, _, B, _ in UNALIGNED_CASES) + 64
+    n_q = max(B * d for _, d, _, B, _ in UNALIGNED_CASES) + 64
+    flatC = torch.empty(n_c, device=dev)
+    flatQ = torch.empty(n_q, device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(31)
     flatC.normal_(generator=g)
     flatQ.normal_(generator=g)
-    out = torch.empty(B, K, device=dev)
     s = torch.cuda.current_stream(dev)
     if only is not None:
-        _, d, off = next(c for c in UNALIGNED_CASES if c[0] == only)
+        _, d, off, B, _ = next(c for c in UNALIGNED_CASES if c[0] == only)
+        out = torch.empty(B, K, device=dev)
         Q = flatQ[off:off + B * d].view(B, d)
-        C = flatC[off:off + B * K * d].view(B, K, d)
+        bf = only_dtype == "bf16"
+        flat = flatC[:B * K * d + 64].to(torch.bfloat16) if bf else flatC
+        C = flat[off:off + B * K * d].view(B, K, d)
+        score = cs.cs_score_candidates_batch_bf16 if bf else cs.cs_score_candidates_batch
         for _ in range(warmup + steps):
-            cs.cs_score_candidates_batch(Q, C, 1, 14.285714, 1.0, out=out, stream=s)
+            score(Q, C, 1, 14.285714, 1.0, out=out, stream=s)
         torch.cuda.synchronize()
-        return {"case": only, "calls": warmup + steps, "plan": cs.cs_query_plan(Q, C, 1)}
+        return {"case": only, "dtype": only_dtype, "calls": warmup + steps,
+                "plan": None if bf else cs.cs_query_plan(Q, C, 1)}
 
     def timed(fn):
         for _ in range(warmup):
@@ -692,10 +707,11 @@ def unaligned_rows(cs, dev, steps, warmup, B=4096, only=None):
         return a.elapsed_time(b) / steps
 
     res = {}
-    flatCb = flatC[:B * K * 512 + 64].to(torch.bfloat16)
-    for name, d, off in UNALIGNED_CASES:
+    flatCb = flatC.to(torch.bfloat16)
+    for name, d, off, B, _ in UNALIGNED_CASES:
+        out = torch.empty(B, K, device=dev)
         Q = flatQ[off:off + B * d].view(B, d)
-        row = {}
+        row = {"questions": B, "D": d}
         for dt, flat, eb in (("f32", flatC, 4), ("bf16", flatCb, 2)):
             C = flat[off:off + B * K * d].view(B, K, d)
             score = cs.cs_score_candidates_batch if dt == "f32" else cs.cs_score_candidates_batch_bf16
@@ -713,11 +729,12 @@ def unaligned_rows(cs, dev, steps, warmup, B=4096, only=None):
                                                                            stream=s))
                     row[tag + "_scalar_plan_gbs"] = nbytes / (ms_g / 1e3) / 1e9
         res[name] = row
-    for name in ("odd_d510", "misaligned_d512"):
-        for tag in ("f32_cos", "f32_dot", "bf16_cos", "bf16_dot"):
-            res[name][tag + "_over_aligned"] = res[name][tag + "_gbs"] / res["aligned_d512"][tag + "_gbs"]
-    res["workload"] = (f"{B} questions x K=255, N(0,1), float32 and bfloat16 candidates, one launch per call, "
-                       f"{steps} calls")
+    for name, _, _, _, ref in UNALIGNED_CASES:
+        if ref:
+            for tag in ("f32_cos", "f32_dot", "bf16_cos", "bf16_dot"):
+                res[name][tag + "_over_aligned"] = res[name][tag + "_gbs"] / res[ref][tag + "_gbs"]
+    res["workload"] = (f"K=255, N(0,1), float32 and bfloat16 candidates, one launch per call, {steps} calls; "
+                       f"each unaligned case against the aligned case of its D and question count")
     del flatC, flatQ, flatCb
     return res
 

@@ -298,8 +298,7 @@ int cs_score_candidates_batch_unfused(const float *Q, const float *C, int B,
  *   - The buffer takes 4 MiB of device memory on every GPU that loads the
  *     library, until the process exits.
  *   - The first call on a device looks up the buffer's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before
- *     starting any stream capture on that device.
+ *     (cudaGetSymbolAddress) and caches it for the life of the process.
  *   - Every call shares the one buffer and leaves its own pass-1 values in
  *     it. Nothing in it needs to start at zero (pass 1 writes every row that
  *     pass 2 reads), but calls that overlap on the GPU -- e.g. on two streams

@@ -151,9 +151,9 @@ int cached_generic_clusters(DeviceState& d, int cluster, int normalize, int c_bf
 }
 
 int cached_max_clusters(DeviceState& d, int cluster, size_t smem, int nq4, int normalize, int c_bf16, int rows) {
-    // nq4 + 1 in bits 2..5 (nq4 is kNqcUnaligned = -1, 0, 1, 2, 4 or 8)
+    // nq4 + 16 in bits 2..6 (nq4 is -16, -8, -4, kNqcUnaligned = -1, 0, 1, 2, 4 or 8)
     const long long key2 = (static_cast<long long>(smem) << 12) | (static_cast<long long>(rows) << 8) |
-                           (static_cast<long long>(nq4 + 1) << 2) | (c_bf16 << 1) | normalize;
+                           (static_cast<long long>(nq4 + 16) << 2) | (c_bf16 << 1) | normalize;
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = d.clusters.find({cluster, key2});
     if (it != d.clusters.end()) return it->second;
@@ -179,6 +179,17 @@ int nq4_for(const Problem& p) {
     for (int n = 1; n <= max_nqc; n *= 2)
         if (dc <= 32 * n) return n;
     return 0;
+}
+
+// Plan.nq4 for rows the bulk copies take as aligned spans: the unit-wise
+// form with the fewest units a lane that covers the row (units: float32
+// elements, or whole bfloat16 pairs), else the scalar form with q in shared
+// memory.
+int unaligned_nq4_for(const Problem& p) {
+    const int units = p.c_bf16 ? p.D / 2 : p.D;
+    for (int nu : cs::kUnalignedUnits)
+        if (units <= 32 * nu) return cs::unaligned_nqc(nu);
+    return cs::kNqcUnaligned;
 }
 
 // Rows per stage that make a stage of about kStageTargetBytes (1..8).
@@ -219,7 +230,7 @@ int ring_stages(long long need, int max_ns) {
 // STREAM plan with `ctas` persistent CTAs (0 = one per SM, at most B).
 // Picks rows per stage R <= stage_rows(D) that keeps the most bytes in
 // flight (larger R on ties). Rows the bulk copies cannot take whole (not
-// tma_eligible) are copied as aligned spans (nq4 = kNqcUnaligned). Returns
+// tma_eligible) are copied as aligned spans (nq4 < 0). Returns
 // false if no ring fits.
 bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     const int cb = cs::c_elem_bytes(p);
@@ -256,7 +267,7 @@ bool stream_plan(const DeviceState& d, const Problem& p, int ctas, Plan* plan) {
     plan->ctas = ctas;
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = ua ? cs::kNqcUnaligned : nq4_for(p);
+    plan->nq4 = ua ? unaligned_nq4_for(p) : nq4_for(p);
     plan->smem = cs::smem_layout(ns, R, p.D, cb, ua).total;
     return true;
 }
@@ -279,7 +290,7 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
     plan->ctas = G * static_cast<int>(p.B);
     plan->rows_per_stage = R;
     plan->stages = ns;
-    plan->nq4 = ua ? cs::kNqcUnaligned : nq4_for(p);
+    plan->nq4 = ua ? unaligned_nq4_for(p) : nq4_for(p);
     plan->smem = cs::smem_layout(ns, R, p.D, cb, ua).total;
     return true;
 }

@@ -74,7 +74,7 @@ struct Plan {
     int rows_per_stage;// candidate rows per bulk-copy stage
     int stages;        // stages in the shared-memory ring
     int nq4;           // 16-byte chunks of a C row per lane whose q sits in registers (0: q read from
-                       // smem; kNqcUnaligned: unaligned rows)
+                       // smem); negative for unaligned rows (kNqcUnaligned, unaligned_nqc)
     size_t smem;       // dynamic shared memory per CTA
 };
 
@@ -122,8 +122,16 @@ __host__ __device__ inline SmemLayout smem_layout(int stages, int rows_per_stage
 
 // Plan.nq4 of the streaming kernels for rows the bulk copies take as
 // aligned spans (D not a multiple of 16 bytes' worth of elements, or Q or C
-// off a 16-byte boundary): scalar shared-memory reads, q in shared memory.
+// off a 16-byte boundary). kNqcUnaligned: scalar shared-memory reads, q in
+// shared memory, any D. unaligned_nqc(NU) = -NU, NU in {4, 8, 16}: rows read
+// in 4-byte units (one float32 element, or a pair of bfloat16 elements), NU
+// units a lane with q for them in registers; the plan takes the smallest NU
+// with 32 NU >= the row's units (D float32, floor(D / 2) bfloat16), so that
+// for NU > 4 a lane's first NU / 2 units are always inside the row.
 constexpr int kNqcUnaligned = -1;
+constexpr int kUnalignedUnits[3] = {4, 8, 16};
+__host__ __device__ constexpr int unaligned_nqc(int nu) { return -nu; }
+__host__ __device__ constexpr int unaligned_units(int nqc) { return nqc < -1 ? -nqc : 0; }
 
 // What one launch of the streaming kernel computes.
 enum StreamMode {
@@ -207,6 +215,7 @@ enum BoundsSite : unsigned {
     kSiteStagedSoftmaxOut = 15,
     kSitePeer = 16,        // cluster exchange slot in a peer CTA
     kSitePrefetchC = 17,   // stream prologue: L2 prefetch of the first rows
+    kSiteUnitSlot = 18,    // unaligned unit-wise reads: the stage's extent in its ring slot
     kSiteProjQ = 20,       // projected readout: projected query
     kSiteProjOut = 21,     // projected readout: probabilities
     kSiteSelftest = 99,

@@ -614,16 +614,51 @@ __device__ __forceinline__ void stage_dots(const uint4* __restrict__ st, int nr,
     for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
 }
 
+// Packed q of the unaligned plans with q in registers (unaligned_units(NQC)
+// = NU > 0): NU / 2 pairs a lane for float32 (elements lane + 64 u and
+// lane + 64 u + 32), NU for bfloat16 (elements 2k and 2k + 1, k = lane + 32 u;
+// or 2k - 1 and 2k for rows read from the word before them, see
+// stage_dots_units).
+template <typename T, int NU>
+struct UnitQ {
+    static constexpr int kPairs = NU == 0 ? 1 : (std::is_same<T, float>::value ? NU / 2 : NU);
+};
+
+// bfloat16 rows of an even D whose first element is the high half of a
+// 4-byte word (C on an odd 2-byte boundary): every row of the launch then
+// starts so, and is read from that word on -- unit k holds elements 2k - 1
+// and 2k -- against q shifted by one element; element -1 (another row's, or
+// bytes of the span) is masked and element D - 1 added apart.
+__device__ __forceinline__ bool bf16_rows_from_word_before(const void* C, int D) {
+    return !(D & 1) && ((reinterpret_cast<unsigned long long>(C) >> 1) & 1u);
+}
+
 // The same sums for a stage whose rows sit at any element-aligned offset in
-// their slot (unaligned plans): row r's element d is st[r * D + d], read as a
-// scalar, and q comes from shared memory. Lane takes elements lane,
-// lane + 32, ... two at a time (d and d + 32), so each sum still runs as a
-// packed pair; q is loaded once per element for all the stage's rows.
-template <int MODE, typename T, int MR, typename Release>
-__device__ __forceinline__ void stage_dots_scalar(const T* __restrict__ st, int nr, int D,
-                                                  const float* __restrict__ q, int lane,
-                                                  float (&v)[values_per_row(MODE) * MR], Release&& release) {
+// their slot, read in 4-byte units with q in registers (qpk, UnitQ): lane
+// takes units lane, lane + 32, ... of each row -- float32 elements, or
+// bfloat16 pairs -- so consecutive lanes read consecutive words of shared
+// memory. Except for the float32 cosine (row by row), the words of RG rows
+// at a time are loaded before any arithmetic (all the stage's rows for
+// NU <= 8) and the slot is released after the last loads (group sizes and
+// orders as measured fastest on 4096 x 255 x 510 and on 4096 x 255 x 512 off
+// by one element). Units past the row's end read as zero (for NU > 4 a
+// lane's first NU / 2 units are always inside it: the plan picks NU so).
+// bfloat16: rows of an even D all start at the parity of C; on an odd
+// 2-byte boundary they are read from the word before
+// (bf16_rows_from_word_before). Rows of an odd D alternate: a row on an odd
+// boundary takes each pair from two words (the high half of one, the low
+// half of the next). Either way an element past the last whole unit --
+// element D - 1 -- is added by lane 0 (qlast its q). st: the slot, shift:
+// the stage's first row's byte offset in it.
+template <int NU, int MODE, typename T, int MR, typename Release>
+__device__ __forceinline__ void stage_dots_units(const unsigned char* __restrict__ st, uint32_t shift, int nr, int D,
+                                                 bool from_word_before,
+                                                 const unsigned long long (&qpk)[UnitQ<T, NU>::kPairs], float qlast,
+                                                 int lane, float (&v)[values_per_row(MODE) * MR], Release&& release) {
     constexpr int VPR = values_per_row(MODE);
+    constexpr int GV = NU > 4 ? NU / 2 : 0;               // units always inside the row
+    constexpr int RG = MR * NU <= 64 ? MR : 64 / NU;      // rows loaded at a time
+    static_assert(MR % RG == 0, "row groups must tile the stage");
     unsigned long long acc[VPR * MR];
 #pragma unroll
     for (int i = 0; i < VPR * MR; ++i) acc[i] = 0ull;
@@ -631,25 +666,201 @@ __device__ __forceinline__ void stage_dots_scalar(const T* __restrict__ st, int 
         if (acc_dot(MODE)) acc[VPR * r] = fma2(c, qq, acc[VPR * r]);
         if (acc_norm(MODE)) acc[VPR * r + VPR - 1] = fma2(c, c, acc[VPR * r + VPR - 1]);
     };
-    int d = lane;
-    for (; d + 32 < D; d += 64) {
-        const unsigned long long qq = pack2(q[d], q[d + 32]);
+    if constexpr (std::is_same<T, float>::value && !acc_norm(MODE)) {
+        // float32 dot: a group's rows loaded first (1-2 % faster than row by row)
+        const float* __restrict__ base = reinterpret_cast<const float*>(st + shift);
 #pragma unroll
-        for (int r = 0; r < MR; ++r)
-            if (r < nr) {
-                const T* row = st + r * D;
-                accumulate(pack2(Elem<T>::widen1(row[d]), Elem<T>::widen1(row[d + 32])), qq, r);
+        for (int g = 0; g < MR; g += RG) {
+            float c[RG][NU];
+#pragma unroll
+            for (int i = 0; i < RG; ++i) {
+                const float* __restrict__ row = base + (g + i) * D;
+#pragma unroll
+                for (int u = 0; u < NU; ++u) {
+                    const int k = lane + 32 * u;
+                    c[i][u] = g + i < nr && (u < GV || k < D) ? row[k] : 0.f;
+                }
             }
-    }
-    if (d < D) {
-        const unsigned long long qq = pack2(q[d], 0.f);
+            if (g + RG >= MR) release();
 #pragma unroll
-        for (int r = 0; r < MR; ++r)
-            if (r < nr) accumulate(pack2(Elem<T>::widen1(st[r * D + d]), 0.f), qq, r);
+            for (int i = 0; i < RG; ++i)
+                if (g + i < nr) {
+#pragma unroll
+                    for (int u = 0; u < NU / 2; ++u) accumulate(pack2(c[i][2 * u], c[i][2 * u + 1]), qpk[u], g + i);
+                }
+        }
+    } else if constexpr (std::is_same<T, float>::value) {
+        // float32 cosine: row by row (loading a group's rows first measured
+        // 2 % slower)
+        const float* __restrict__ base = reinterpret_cast<const float*>(st + shift);
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+            if (r < nr) {
+                const float* __restrict__ row = base + r * D;
+#pragma unroll
+                for (int u = 0; u < NU / 2; ++u) {
+                    const int k0 = lane + 64 * u, k1 = k0 + 32;
+                    const float c0 = 2 * u < GV || k0 < D ? row[k0] : 0.f;
+                    const float c1 = 2 * u + 1 < GV || k1 < D ? row[k1] : 0.f;
+                    accumulate(pack2(c0, c1), qpk[u], r);
+                }
+            }
+        }
+        release();
+    } else {
+        const uint32_t* __restrict__ words = reinterpret_cast<const uint32_t*>(st);
+        const uint16_t* __restrict__ halves = reinterpret_cast<const uint16_t*>(st);
+        const int np = D >> 1;
+        const uint32_t hb0 = shift >> 1;  // 2-byte index of the stage's element 0
+        if (!(D & 1)) {
+#pragma unroll
+            for (int g = 0; g < MR; g += RG) {
+                uint32_t w[RG][NU];
+                uint16_t tail[RG];
+#pragma unroll
+                for (int i = 0; i < RG; ++i) {
+                    const uint32_t hb = hb0 + static_cast<uint32_t>((g + i) * D);
+                    const uint32_t* __restrict__ row = words + (hb >> 1);
+#pragma unroll
+                    for (int u = 0; u < NU; ++u) {
+                        const int k = lane + 32 * u;
+                        w[i][u] = g + i < nr && (u < GV || k < np) ? row[k] : 0u;
+                    }
+                    if (from_word_before && lane == 0) w[i][0] &= 0xffff0000u;  // element -1
+                    tail[i] = from_word_before && lane == 0 && g + i < nr ? halves[hb + D - 1] : uint16_t(0);
+                }
+                if (g + RG >= MR) release();
+#pragma unroll
+                for (int i = 0; i < RG; ++i)
+                    if (g + i < nr) {
+#pragma unroll
+                        for (int u = 0; u < NU; ++u)
+                            accumulate(pack2(__uint_as_float(w[i][u] << 16), __uint_as_float(w[i][u] & 0xffff0000u)),
+                                       qpk[u], g + i);
+                        if (from_word_before)
+                            accumulate(pack2(Elem<uint16_t>::widen1(tail[i]), 0.f), pack2(qlast, 0.f), g + i);
+                    }
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < MR; ++r) {
+                if (r < nr) {
+                    const uint32_t hb = hb0 + static_cast<uint32_t>(r * D);
+                    const uint32_t* __restrict__ row = words + (hb >> 1);
+                    if (hb & 1u) {
+#pragma unroll
+                        for (int u = 0; u < NU; ++u) {
+                            const int k = lane + 32 * u;
+                            const bool in = u < GV || k < np;
+                            const uint32_t a = in ? row[k] : 0u, b = in ? row[k + 1] : 0u;
+                            accumulate(pack2(__uint_as_float(a & 0xffff0000u), __uint_as_float(b << 16)), qpk[u], r);
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < NU; ++u) {
+                            const int k = lane + 32 * u;
+                            const uint32_t x = u < GV || k < np ? row[k] : 0u;
+                            accumulate(pack2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u)), qpk[u], r);
+                        }
+                    }
+                    const uint16_t e = lane == 0 ? halves[hb + D - 1] : uint16_t(0);
+                    accumulate(pack2(Elem<uint16_t>::widen1(e), 0.f), pack2(qlast, 0.f), r);
+                }
+            }
+            release();
+        }
     }
-    release();
 #pragma unroll
     for (int i = 0; i < VPR * MR; ++i) v[i] = sum2(acc[i]);
+}
+
+// stage_dots_units for rows too long for q in registers (the plan's
+// kNqcUnaligned, any D): the same 4-byte units and the same bfloat16 forms,
+// q read from shared memory (qf: q at its offset in the q slot). Such rows
+// are long and their stages short (16 KB of rows: 1 to 7 rows), so the rows
+// are taken one at a time -- nothing is spent on rows a short stage lacks --
+// in blocks of kUnitBlock units a lane, all of a block's loads before its
+// arithmetic; q is read again for each row.
+constexpr int kUnitBlock = 8;
+
+template <int MODE, typename T, int MR, typename Release>
+__device__ __forceinline__ void stage_dots_units_shared_q(const unsigned char* __restrict__ st, uint32_t shift,
+                                                          int nr, int D, bool from_word_before,
+                                                          const float* __restrict__ qf, float qlast, int lane,
+                                                          float (&v)[values_per_row(MODE) * MR], Release&& release) {
+    constexpr int VPR = values_per_row(MODE);
+    constexpr int NB = kUnitBlock;
+#pragma unroll
+    for (int i = 0; i < VPR * MR; ++i) v[i] = 0.f;
+    const uint32_t* __restrict__ words = reinterpret_cast<const uint32_t*>(st);
+    const uint16_t* __restrict__ halves = reinterpret_cast<const uint16_t*>(st);
+    const int np = D >> 1;
+    const int sh = from_word_before ? 1 : 0;  // bfloat16 q pairs (2k - sh, 2k + 1 - sh)
+    for (int r = 0; r < nr; ++r) {
+        unsigned long long dot = 0ull, nrm = 0ull;
+        auto accumulate = [&](unsigned long long c, unsigned long long qq) {
+            if (acc_dot(MODE)) dot = fma2(c, qq, dot);
+            if (acc_norm(MODE)) nrm = fma2(c, c, nrm);
+        };
+        const uint32_t hb = (shift >> 1) + static_cast<uint32_t>(r * D);  // bfloat16: 2-byte index of element 0
+        if constexpr (std::is_same<T, float>::value) {
+            const float* __restrict__ row = reinterpret_cast<const float*>(st + shift) + r * D;
+            for (int k0 = lane; k0 - lane < D; k0 += 32 * NB) {
+                float c[NB], q[NB];
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const bool in = k0 + 32 * j < D;
+                    c[j] = in ? row[k0 + 32 * j] : 0.f;
+                    q[j] = in ? qf[k0 + 32 * j] : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < NB; j += 2) accumulate(pack2(c[j], c[j + 1]), pack2(q[j], q[j + 1]));
+            }
+        } else {
+            const uint32_t* __restrict__ row = words + (hb >> 1);
+            // an odd 2-byte start takes each pair from two words, unless every
+            // row is read from the word before (even D, from_word_before)
+            auto pairs = [&](auto split_tag) {
+                constexpr bool SPLIT = decltype(split_tag)::value;
+                for (int k0 = lane; k0 - lane < np; k0 += 32 * NB) {
+                    uint32_t x[NB], y[NB];
+                    float qa[NB], qb[NB];
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        const int k = k0 + 32 * j, e = 2 * k - sh;
+                        const bool in = k < np;
+                        x[j] = in ? row[k] : 0u;
+                        if (SPLIT) y[j] = in ? row[k + 1] : 0u;
+                        qa[j] = in && e >= 0 ? qf[e] : 0.f;
+                        qb[j] = in ? qf[e + 1] : 0.f;
+                    }
+                    if (from_word_before && k0 == 0) x[0] &= 0xffff0000u;  // element -1
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        const float lo = __uint_as_float(SPLIT ? x[j] & 0xffff0000u : x[j] << 16);
+                        const float hi = __uint_as_float(SPLIT ? y[j] << 16 : x[j] & 0xffff0000u);
+                        accumulate(pack2(lo, hi), pack2(qa[j], qb[j]));
+                    }
+                }
+            };
+            if ((hb & 1u) && !from_word_before)
+                pairs(std::true_type{});
+            else
+                pairs(std::false_type{});
+            if ((D & 1) || from_word_before) {
+                const uint16_t e = lane == 0 ? halves[hb + D - 1] : uint16_t(0);
+                accumulate(pack2(Elem<uint16_t>::widen1(e), 0.f), pack2(qlast, 0.f));
+            }
+        }
+        // row r's partial sums into their static places for the reduction
+#pragma unroll
+        for (int i = 0; i < MR; ++i)
+            if (i == r) {
+                if (acc_dot(MODE)) v[VPR * i] = sum2(dot);
+                if (acc_norm(MODE)) v[VPR * i + VPR - 1] = sum2(nrm);
+            }
+    }
+    release();
 }
 
 // Global address of `bytes` bytes at src, widened to whole 16-byte granules
@@ -691,8 +902,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
     }
 
     // UA: rows and queries need not start on 16-byte boundaries; each copy
-    // takes their aligned span and readers index from the offset in it.
-    constexpr bool UA = NQC == kNqcUnaligned;
+    // takes their aligned span and readers index from the offset in it
+    // (NU > 0: rows read in 4-byte units, q in registers).
+    constexpr bool UA = NQC < 0;
+    constexpr int NU = unaligned_units(NQC);
+    const bool from_word_before = !std::is_same<T, float>::value && bf16_rows_from_word_before(p.C, D);
     const SmemLayout L = smem_layout(NS, R, D, static_cast<int>(sizeof(T)), UA);
     unsigned char* ring = smem + L.ring;
     const uint32_t slot_bytes = static_cast<uint32_t>(L.slot_bytes);
@@ -903,8 +1117,41 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
             const float* qf = reinterpret_cast<const float*>(
                 qslot + (reinterpret_cast<unsigned long long>(p.Q + static_cast<size_t>(b) * D) & 15u));
             float4 qv[(NQC > 0 ? NQC : 1) * QF4];
+            unsigned long long qpk[UnitQ<T, NU>::kPairs];
+            float qlast = 0.f;
             float qsq = 0.f;  // |q|^2 (cosine)
-            if constexpr (UA) {
+            if constexpr (NU > 0) {
+                // unit u of q as packed pairs (UnitQ), zero past the row
+                float sq = 0.f;
+#pragma unroll
+                for (int u = 0; u < UnitQ<T, NU>::kPairs; ++u) {
+                    int k0, k1;
+                    bool in0, in1;
+                    if constexpr (std::is_same<T, float>::value) {
+                        k0 = lane + 64 * u;
+                        k1 = k0 + 32;
+                        in0 = k0 < D;
+                        in1 = k1 < D;
+                    } else {
+                        // pairs (2k, 2k + 1), or (2k - 1, 2k) for rows read from the word before
+                        k0 = 2 * (lane + 32 * u) - (from_word_before ? 1 : 0);
+                        k1 = k0 + 1;
+                        in1 = lane + 32 * u < (D >> 1);
+                        in0 = in1 && k0 >= 0;
+                    }
+                    const float a = in0 ? qf[k0] : 0.f, c = in1 ? qf[k1] : 0.f;
+                    qpk[u] = pack2(a, c);
+                    if (COS) sq += a * a + c * c;
+                }
+                if (!std::is_same<T, float>::value && ((D & 1) || from_word_before)) {
+                    qlast = qf[D - 1];
+                    if (COS && lane == 0) sq += qlast * qlast;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
+                if (COS) qsq = warp_sum(sq);
+            } else if constexpr (UA) {
+                if (!std::is_same<T, float>::value && ((D & 1) || from_word_before)) qlast = qf[D - 1];
                 if (COS) {
                     float sq = 0.f;
                     for (int i = lane; i < D; i += 32) sq = fmaf(qf[i], qf[i], sq);
@@ -956,9 +1203,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                 if constexpr (UA) {
                     // the rows at their offset in the aligned span
                     const T* src = Cg + static_cast<size_t>(qr.row0 + k0) * D;
-                    stage_dots_scalar<MODE, T, MR>(
-                        reinterpret_cast<const T*>(st + (reinterpret_cast<unsigned long long>(src) & 15u)), nr, D,
-                        qf, lane, v, release);
+                    const uint32_t shift = static_cast<uint32_t>(reinterpret_cast<unsigned long long>(src) & 15u);
+                    // the unit reads end at most one word past the stage's rows
+                    if (!CS_IN_BOUNDS(st, shift + nr * row_bytes + 4u, st, slot_bytes, kSiteUnitSlot)) {
+                        release();
+#pragma unroll
+                        for (int i = 0; i < V; ++i) v[i] = 0.f;
+                    } else if constexpr (NU > 0) {
+                        stage_dots_units<NU, MODE, T, MR>(st, shift, nr, D, from_word_before, qpk, qlast, lane, v,
+                                                          release);
+                    } else {
+                        stage_dots_units_shared_q<MODE, T, MR>(st, shift, nr, D, from_word_before, qf, qlast, lane, v,
+                                                               release);
+                    }
                 } else {
                     stage_dots<NQC, MODE, T, MR>(reinterpret_cast<const uint4*>(st), nr, DC, qv, q4, lane, v,
                                                  release);
@@ -982,7 +1239,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
                     phase ^= 1u;
                 }
             }
-            if constexpr (NQC <= 0) {  // q was read from shared memory by every stage
+            if constexpr (NQC == 0 || NQC == kNqcUnaligned) {  // q was read from shared memory by every stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(qempty0 + 8u * qs);
             }
@@ -1443,14 +1700,35 @@ cudaError_t launch_stream_t(const StreamArgs& a, const Plan& plan, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, stream_kernel<NQC, MODE, T, MR>, a);
 }
 
+// Unaligned rows: built for the fused modes at the full stage size only.
+template <int MODE, int MR>
+constexpr bool has_unaligned_build() {
+    return (MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage;
+}
+
+template <int NQC, int MODE, typename T, int MR>
+cudaError_t launch_stream_ua(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
+    if constexpr (has_unaligned_build<MODE, MR>())
+        return launch_stream_t<NQC, MODE, T, MR>(a, plan, stream);
+    else
+        return cudaErrorInvalidValue;
+}
+
+template <int NQC, int MODE, typename T, int MR>
+const void* stream_fn_ua() {
+    if constexpr (has_unaligned_build<MODE, MR>())
+        return reinterpret_cast<const void*>(stream_kernel<NQC, MODE, T, MR>);
+    else
+        return nullptr;
+}
+
 template <int MODE, typename T, int MR>
 cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t stream) {
     switch (plan.nq4) {
-        case kNqcUnaligned:  // built for the fused modes at the full stage size only
-            if constexpr ((MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage)
-                return launch_stream_t<kNqcUnaligned, MODE, T, MR>(a, plan, stream);
-            else
-                return cudaErrorInvalidValue;
+        case kNqcUnaligned: return launch_stream_ua<kNqcUnaligned, MODE, T, MR>(a, plan, stream);
+        case unaligned_nqc(4): return launch_stream_ua<unaligned_nqc(4), MODE, T, MR>(a, plan, stream);
+        case unaligned_nqc(8): return launch_stream_ua<unaligned_nqc(8), MODE, T, MR>(a, plan, stream);
+        case unaligned_nqc(16): return launch_stream_ua<unaligned_nqc(16), MODE, T, MR>(a, plan, stream);
         case 1: return launch_stream_t<1, MODE, T, MR>(a, plan, stream);
         case 2: return launch_stream_t<2, MODE, T, MR>(a, plan, stream);
         case 4: return launch_stream_t<4, MODE, T, MR>(a, plan, stream);
@@ -1463,11 +1741,10 @@ cudaError_t launch_stream_m(const StreamArgs& a, const Plan& plan, cudaStream_t 
 template <int MODE, typename T, int MR>
 const void* stream_fn_m(int nqc) {
     switch (nqc) {
-        case kNqcUnaligned:
-            if constexpr ((MODE == kFusedCos || MODE == kFusedDot) && MR == kMaxRowsPerStage)
-                return reinterpret_cast<const void*>(stream_kernel<kNqcUnaligned, MODE, T, MR>);
-            else
-                return nullptr;
+        case kNqcUnaligned: return stream_fn_ua<kNqcUnaligned, MODE, T, MR>();
+        case unaligned_nqc(4): return stream_fn_ua<unaligned_nqc(4), MODE, T, MR>();
+        case unaligned_nqc(8): return stream_fn_ua<unaligned_nqc(8), MODE, T, MR>();
+        case unaligned_nqc(16): return stream_fn_ua<unaligned_nqc(16), MODE, T, MR>();
         case 1: return reinterpret_cast<const void*>(stream_kernel<1, MODE, T, MR>);
         case 2: return reinterpret_cast<const void*>(stream_kernel<2, MODE, T, MR>);
         case 4: return reinterpret_cast<const void*>(stream_kernel<4, MODE, T, MR>);
@@ -1480,7 +1757,7 @@ const void* stream_fn_m(int nqc) {
 // The row limit of the instantiation that runs stages of R rows in `mode`
 // (unaligned plans have only the full-size build).
 constexpr int rows_limit(int mode, int R, int nqc) {
-    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows && nqc != kNqcUnaligned
+    return (mode == kFusedCos || mode == kFusedDot) && R <= kSmallStageRows && nqc >= 0
                ? kSmallStageRows
                : kMaxRowsPerStage;
 }
@@ -1488,10 +1765,10 @@ constexpr int rows_limit(int mode, int R, int nqc) {
 // Kernels exist for every mode over float32 C, and for the fused modes over
 // bfloat16 C (nqc 8 is never planned for bfloat16: q would take 64 registers);
 // the fused modes also in a short-stage form (mr = kSmallStageRows) and, at
-// the full stage size, for unaligned rows (nqc = kNqcUnaligned).
+// the full stage size, for unaligned rows (nqc < 0).
 const void* stream_fn_for(int nqc, int mode, int c_bf16, int mr) {
     const bool fused = mode == kFusedCos || mode == kFusedDot;
-    if (nqc == kNqcUnaligned && (!fused || mr != kMaxRowsPerStage)) return nullptr;
+    if (nqc < 0 && (!fused || mr != kMaxRowsPerStage)) return nullptr;
     if (mr == kSmallStageRows) {
         if (!fused || (c_bf16 && nqc == 8)) return nullptr;
         if (c_bf16)
@@ -1691,10 +1968,10 @@ cudaError_t configure_device_kernels(int smem_optin) {
                     cudaFuncSetAttribute(direct_fn_for(nqc, cos, bf), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                 if (e != cudaSuccess) return e;
             }
-    const int nq4s[6] = {1, 2, 4, 8, 0, kNqcUnaligned};
+    const int nq4s[9] = {1, 2, 4, 8, 0, kNqcUnaligned, unaligned_nqc(4), unaligned_nqc(8), unaligned_nqc(16)};
     for (int bf = 0; bf < 2; ++bf) {
         for (int m = kFusedCos; m <= kStagedCos; ++m) {
-            for (int i = 0; i < 6; ++i) {
+            for (int i = 0; i < 9; ++i) {
                 for (int mr : {kSmallStageRows, kMaxRowsPerStage}) {
                     const void* f = stream_fn_for(nq4s[i], m, bf, mr);
                     if (!f) continue;

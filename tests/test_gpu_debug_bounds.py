@@ -150,7 +150,10 @@ def _placed(t, offset_elems):
 
 @pytest.mark.parametrize("B,K,D,oq,oc,bf16", [(300, 255, 510, 0, 0, False), (200, 64, 512, 1, 3, False),
                                                 (160, 33, 13, 0, 1, False), (170, 37, 21, 2, 5, True),
-                                                (3, 64, 509, 0, 3, False)])
+                                                (3, 64, 509, 0, 3, False), (150, 255, 1025, 1, 3, True),
+                                                (200, 64, 512, 1, 1, True), (100, 31, 258, 0, 7, True),
+                                                (120, 255, 511, 3, 3, False), (60, 40, 2562, 1, 1, True),
+                                                (50, 40, 2563, 0, 2, True), (60, 40, 1030, 1, 3, False)])
 def test_unaligned_rows_within_bounds(dbg, B, K, D, oq, oc, bf16):
     """Unaligned plans copy each stage's 16-byte aligned span; what the
     kernels check and use is the rows' own range, which must stay inside C,

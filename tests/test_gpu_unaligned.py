@@ -97,6 +97,36 @@ def test_unaligned_bf16(cuda_lib, normalize):
     assert binding.cs_device_status() == 0
 
 
+# D either side of the unit-wise form's sizes (4, 8 or 16 four-byte units a
+# lane; float32 units are elements, bfloat16 units element pairs, an odd D's
+# last element added apart) and past its last one (the scalar form).
+UNIT_EDGES = {"f32": [1, 2, 127, 128, 129, 255, 256, 257, 511, 512, 513],
+              "bf16": [1, 2, 3, 255, 256, 257, 258, 511, 512, 513, 1023, 1024, 1025, 1026]}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_unit_form_sizes(cuda_lib, dtype, normalize):
+    """Unaligned rows at every D where the unit-wise form changes shape
+    (units a lane, the guaranteed-inside units, the odd bfloat16 element),
+    with rows starting on even and odd 2-byte offsets (bfloat16) and every
+    4-byte offset (float32); each question against the oracle."""
+    pairs = pairs_in_rotation(normalize)
+    bf16 = dtype == "bf16"
+    for i, D in enumerate(UNIT_EDGES[dtype]):
+        B, K = 40, 23 + i
+        wl = tempered_case(B, K, D, normalize, pairs[i % len(pairs)], 600 + D + (7 if bf16 else 0))
+        Cr = wl.C.to(torch.bfloat16) if bf16 else wl.C
+        ref = oracle_probs(wl.Q, Cr.float(), normalize, wl.scale, wl.temperature)
+        for oq, oc in ((1, 1), (0, 3), (3, 2), (2, 5) if bf16 else (2, 0)):
+            Q, C = _placed(wl.Q.to(DEV), oq), _placed(Cr.to(DEV), oc)
+            fn = binding.cs_score_candidates_batch_bf16 if bf16 else binding.cs_score_candidates_batch
+            p = fn(Q, C, normalize, wl.scale, wl.temperature)
+            torch.cuda.synchronize()
+            assert_parity(p, ref, f"{dtype} B={B} K={K} D={D} q+{oq} c+{oc}")
+    assert binding.cs_device_status() == 0
+
+
 def test_unaligned_ragged(cuda_lib):
     """A ragged batch of odd D, and one whose C is off a 16-byte boundary."""
     for B, D, oc in ((400, 513, 0), (300, 512, 1), (12, 255, 3)):
