@@ -143,6 +143,26 @@ def test_unaligned_ragged(cuda_lib):
     assert binding.cs_device_status() == 0
 
 
+def test_unaligned_ragged_bf16(cuda_lib):
+    """Ragged bfloat16 batches off 16-byte boundaries: C one element off with
+    an even D (every row read from the word before), an odd D (rows
+    alternating between whole-word and split pairs), and D past the
+    register form (q from shared memory)."""
+    for B, D, oc, normalize in ((300, 512, 1, 1), (250, 255, 0, 0), (200, 777, 3, 1), (60, 2562, 1, 0)):
+        wl = workloads.ragged(B, D, normalize, 14.2857 if normalize else 0.0625, 80 + B + D, "cpu")
+        Cb = wl.C.to(torch.bfloat16)
+        Q, C = wl.Q.to(DEV), _placed(Cb.to(DEV), oc)
+        p = binding.cs_score_candidates_ragged(Q, C, wl.offsets.to(DEV), normalize, wl.scale, 1.0)
+        torch.cuda.synchronize()
+        p = p.cpu()
+        off = wl.offsets.tolist()
+        for b in range(0, B, max(1, B // 30)):
+            o0, o1 = off[b], off[b + 1]
+            ref = oracle_probs(wl.Q[b:b + 1], Cb[o0:o1].float()[None], normalize, wl.scale, 1.0)
+            assert_parity(p[o0:o1][None], ref, f"ragged bf16 D={D} c+{oc} question {b}")
+    assert binding.cs_device_status() == 0
+
+
 @pytest.mark.parametrize("case", ["odd_d", "misaligned"])
 def test_unaligned_throughput_workloads_full_size(cuda_lib, case):
     """The two unaligned throughput workloads the benchmark times, 4096
