@@ -395,6 +395,8 @@ def main():
                     help="profiling aid: W + K calls of one unaligned-row case (cosine, 4096 questions)")
     ap.add_argument("--only-unaligned-dtype", choices=["f32", "bf16"], default="f32",
                     help="candidate type of --only-unaligned-case")
+    ap.add_argument("--only-unaligned-b1", action="store_true",
+                    help="profiling aid: time only one-question calls on unaligned rows and print their record")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
                     help="profiling aid: time only the projected readout on B questions and print its record")
     ap.add_argument("--plan-sweep", action="store_true",
@@ -440,6 +442,10 @@ def main():
     if args.only_unaligned:
         if rank == 0:
             print(json.dumps(unaligned_rows(cs, dev, args.steps, args.warmup)), flush=True)
+        return 0
+    if args.only_unaligned_b1:
+        if rank == 0:
+            print(json.dumps(unaligned_latency(cs, dev)), flush=True)
         return 0
     if args.only_projected:
         if rank == 0:
@@ -548,6 +554,7 @@ def main():
     if not args.skip_extra:
         line["extra"]["projected_readout"] = projected_readout(cs, dev, 20, args.warmup)
         line["extra"]["unaligned_rows"] = unaligned_rows(cs, dev, 20, args.warmup)
+        line["extra"]["unaligned_b1"] = unaligned_latency(cs, dev)
         line["extra"]["latency_b1"] = latency_table(cs, workloads, dev, args.latency_calls)
         line["e2e"] = e2e(cs, wl_cos, dev, args, world, barrier, max_over_ranks)
     del wls, wl_cos, wl_dot
@@ -875,6 +882,69 @@ def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32)
         row["auto_over_best"] = row["auto_us"] / best
         rows.append(row)
     return {"plan_sweep": rows, "workload": "cosine, K=255, D=512, inputs in HBM (larger than L2 across the graph)"}
+
+
+def unaligned_latency(cs, dev, n=32):
+    """us per call for one question of K=255 whose rows the bulk copies
+    cannot take whole (D=510, and D=512 with Q and C one element off a
+    16-byte boundary; float32 and bfloat16, cosine): the automatic plan
+    against the scalar plan (one question over a 16-CTA cluster) forced on
+    the same rows. Device time per call as in the plan sweep: n calls on
+    consecutive slices of a 2.1 GB buffer in one CUDA graph after a read of
+    256 MiB, minus the same graph without the calls (every call from HBM)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    n_elem = 4096 * K * 512
+    flatC = torch.randn(n_elem + 64, device=dev, generator=g)
+    flatCb = flatC.to(torch.bfloat16)
+    flatQ = torch.randn(4096 * 512 + 64, device=dev, generator=g)
+    out = torch.empty(K, device=dev)
+    flush = torch.ones(64 << 20, device=dev)  # 256 MiB, read only
+
+    def timed(score):
+        for i in range(4):
+            score(i)
+        torch.cuda.synchronize()
+
+        def graph_ms(calls):
+            graph, st = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(graph, stream=st):
+                    flush.sum()
+                    for i in range(calls):
+                        score(i)
+            graph.replay()
+            torch.cuda.synchronize()
+            best = float("inf")
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(10):
+                    graph.replay()
+                b.record()
+                torch.cuda.synchronize()
+                best = min(best, a.elapsed_time(b) / 10)
+            return best
+        return 1e3 * (graph_ms(n) - graph_ms(0)) / n
+
+    rows = []
+    for name, d, off in (("odd_d510", 510, 0), ("misaligned_d512", 512, 1)):
+        nsl = n_elem // (K * d) - 1
+        views = [(flatQ[off + (i % 4096) * d:off + (i % 4096) * d + d],
+                  flatC[off + (i % nsl) * K * d:off + ((i % nsl) + 1) * K * d].view(K, d),
+                  flatCb[off + (i % nsl) * K * d:off + ((i % nsl) + 1) * K * d].view(K, d)) for i in range(n)]
+        plan = cs.cs_query_plan(views[0][0][None], views[0][1][None], 1)
+        row = {"case": name, "K": K, "D": d, "auto_plan": f"{plan['plan']}{plan['cluster']}"}
+        row["f32_auto_us"] = timed(lambda i: cs.cs_score_candidates(views[i][0], views[i][1], 1, 14.285714, 1.0,
+                                                                    out=out))
+        row["f32_scalar16_us"] = timed(lambda i: cs.cs_score_candidates_batch_plan(
+            views[i][0][None], views[i][1][None], 1, 14.285714, 1.0, cs.CS_PLAN_GENERIC, 16, 0, out=out[None]))
+        row["bf16_auto_us"] = timed(lambda i: cs.cs_score_candidates_bf16(views[i][0], views[i][2], 1, 14.285714,
+                                                                          1.0, out=out))
+        rows.append(row)
+    del flatC, flatCb, flatQ, flush
+    return {"rows": rows, "workload": "one question, K=255, cosine, inputs in HBM (larger than L2 across the graph)"}
 
 
 def single_shape(cs, workloads, dev, name, calls, warmup):

@@ -226,11 +226,12 @@ int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,
 #define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment (one CTA per
                               question, or a cluster of CTAs per question
                               when a uniform-K batch has few questions): a
-                              few unaligned questions, or rows too long for
-                              the shared-memory ring */
+                              few unaligned questions with long rows, or
+                              rows too long for the shared-memory ring */
 #define CS_PLAN_DIRECT 4   /* one CTA (or cluster) per short question: at most 32
-                              rows per CTA, q and rows loaded straight into
-                              registers, no shared-memory ring */
+                              rows per CTA (16 for long rows), q and rows
+                              loaded straight into registers, no
+                              shared-memory ring */
 
 /*
  * The plan cs_score_candidates_batch would use for these arguments.
@@ -246,17 +247,18 @@ int cs_query_plan(const float *Q, const float *C, int B, int K, int D,
 /*
  * cs_score_candidates_batch with the plan chosen by the caller, for tests
  * and tuning. plan is CS_PLAN_*; cluster (CS_PLAN_CLUSTER and
- * CS_PLAN_DIRECT: 1..16, at most K; CS_PLAN_DIRECT also needs
- * ceil(K / cluster) <= 32, D <= 512 for float32 and D <= 1024 for bfloat16
- * candidates) and ctas (CS_PLAN_STREAM: 1..B) may be 0 for the automatic
- * choice. For CS_PLAN_GENERIC, cluster 0 or 1 means one CTA per question and
- * 2..16 (at most K) spreads each question's rows over a cluster of that many
- * CTAs.
+ * CS_PLAN_DIRECT: 1..16, at most K) and ctas (CS_PLAN_STREAM: 1..B) may be 0
+ * for the automatic choice. CS_PLAN_DIRECT also needs ceil(K / cluster) <=
+ * 32 for D <= 512 and ceil(K / cluster) <= 16 for 512 < D <= 2560; rows
+ * that do not start on 16-byte boundaries or whose length is not a
+ * multiple of 16 bytes only up to D = 512 (read in 4-byte units). For
+ * CS_PLAN_GENERIC, cluster 0 or 1 means one CTA per question and 2..16 (at
+ * most K) spreads each question's rows over a cluster of that many CTAs.
  * Returns CS_ERR_BAD_PLAN when the plan cannot run these arguments (e.g.
- * CS_PLAN_DIRECT with D % 4 != 0 or Q or C off a 16-byte boundary, or a
- * ring that does not fit shared memory for CS_PLAN_STREAM/CLUSTER; these
- * two take unaligned rows as aligned spans). The result equals the
- * automatic plan's within float32 rounding.
+ * CS_PLAN_DIRECT on rows longer than its forms take, or a ring that does
+ * not fit shared memory for CS_PLAN_STREAM/CLUSTER; these two take
+ * unaligned rows as aligned spans). The result equals the automatic plan's
+ * within float32 rounding.
  */
 int cs_score_candidates_batch_plan(const float *Q, const float *C, int B,
                                    int K, int D, int normalize, float scale,

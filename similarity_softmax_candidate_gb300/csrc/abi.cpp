@@ -131,7 +131,8 @@ cudaError_t device_state(DeviceState** st) {
 }
 
 int cached_direct_clusters(DeviceState& d, int cluster, int nq4, int normalize, int c_bf16) {
-    const long long key2 = (1ll << 62) | (nq4 << 2) | (c_bf16 << 1) | normalize;  // apart from the stream keys
+    // nq4 + 16 in bits 2..7 (nq4 is -16, -8, -4, 1, 2, 4 or kDirectWideChunks); bit 62: apart from the stream keys
+    const long long key2 = (1ll << 62) | (static_cast<long long>(nq4 + 16) << 2) | (c_bf16 << 1) | normalize;
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = d.clusters.find({cluster, key2});
     if (it != d.clusters.end()) return it->second;
@@ -296,11 +297,23 @@ bool cluster_plan(const DeviceState& d, const Problem& p, int G, Plan* plan) {
 }
 
 // The DIRECT kernel form these rows take: narrow (q in registers, nq4 in
-// 1, 2, 4, at most kDirectMaxRows rows per CTA) or wide (q in shared memory,
+// 1, 2, 4, at most kDirectMaxRows rows per CTA), wide (q in shared memory,
 // at most kDirectWideChunks 16-byte chunks of a row per lane, at most
-// kDirectWideMaxRows rows per CTA). Returns the chunks per lane the kernel is
-// built for (0: no DIRECT form) and the row limit.
+// kDirectWideMaxRows rows per CTA), or for rows the bulk copies cannot take
+// whole the 4-byte-unit form (unaligned_nqc, q in registers, at most
+// kDirectMaxRows rows per CTA). Returns the plan's nq4 for the form (0: no
+// DIRECT form) and the row limit.
 int direct_form(const Problem& p, int* max_rows) {
+    if (!tma_eligible(p)) {
+        // rows in 4-byte units with q in registers (no odd-D bfloat16 form)
+        const int nq = unaligned_nq4_for(p);
+        if (nq < cs::kNqcUnaligned && !(p.c_bf16 && (p.D & 1))) {
+            *max_rows = cs::kDirectMaxRows;
+            return nq;
+        }
+        *max_rows = 0;
+        return 0;
+    }
     const int nq4 = nq4_for(p);
     if (nq4 == 1 || nq4 == 2 || nq4 == 4) {
         *max_rows = cs::kDirectMaxRows;
@@ -321,7 +334,7 @@ int direct_form(const Problem& p, int* max_rows) {
 bool direct_plan(const Problem& p, int G, Plan* plan) {
     int max_rows = 0;
     const int nq4 = direct_form(p, &max_rows);
-    if (!tma_eligible(p) || p.B > 65535 || G < 1 || G > cs::kMaxCluster || G > p.K || nq4 == 0) return false;
+    if (p.B > 65535 || G < 1 || G > cs::kMaxCluster || G > p.K || nq4 == 0) return false;
     const int kmax = p.offsets ? CS_MAX_K : p.K;
     if ((kmax + G - 1) / G > max_rows) return false;
     plan->kind = cs::kPlanDirect;
@@ -407,7 +420,7 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
         return CS_OK;
     }
     // automatic choice
-    if (aligned && p.B * 2 <= d.sms) {
+    if (p.B * 2 <= d.sms) {
         // Few questions: split each over a cluster so one question is not
         // confined to one SM (the page's 256-thread lesson, "What it is worth").
         const long long avg_k = p.offsets ? (p.total_rows + p.B - 1) / p.B : p.K;
@@ -436,15 +449,15 @@ int make_plan(DeviceState& d, const Problem& p, int kind, int cluster, int ctas,
                  3ll * cached_direct_clusters(d, g, plan->nq4, p.normalize, p.c_bf16) >= 2ll * p.B))
                 return CS_OK;
         }
-        for (; G > 1; G /= 2) {
+        for (; aligned && G > 1; G /= 2) {
             if (cluster_plan(d, p, G, plan) &&
                 cached_max_clusters(d, G, plan->smem, plan->nq4, p.normalize, p.c_bf16, plan->rows_per_stage) >= p.B)
                 return CS_OK;
         }
     }
-    // A few questions whose rows the bulk copies cannot take whole: the
-    // scalar plan, each question spread over a cluster (latency-bound; the
-    // DIRECT plan needs aligned rows).
+    // A few questions whose rows the bulk copies cannot take whole and the
+    // DIRECT plan does not take: the scalar plan, each question spread over a
+    // cluster (latency-bound).
     if (!aligned && p.B * 2 <= d.sms && !p.offsets) {
         generic_plan(p, plan, generic_cluster_size(d, p));
         return CS_OK;

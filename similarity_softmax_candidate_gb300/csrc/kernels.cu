@@ -249,6 +249,12 @@ __device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
+// The two halves of a packed pair.
+__device__ __forceinline__ float2 unpack2(unsigned long long x) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+    return make_float2(lo, hi);
+}
 // The two halves of a packed pair, added: the value its partial sums make.
 __device__ __forceinline__ float sum2(unsigned long long x) {
     float lo, hi;
@@ -1369,16 +1375,54 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
     wait_prior_grid();  // no global access before this point
     allow_next_grid();
 
+    // NU > 0: rows that do not start on 16-byte boundaries (or whose length
+    // is not a multiple of 16 bytes), read in 4-byte units as the stream
+    // kernel's unaligned plans read them from shared memory (stage_dots_units):
+    // lane takes units lane, lane + 32, ... -- float32 elements or bfloat16
+    // pairs, bfloat16 rows of an even D on an odd 2-byte boundary from the
+    // word before (bf16_rows_from_word_before); no odd-D bfloat16 form.
+    constexpr int NU = unaligned_units(NQC);
+    constexpr bool F32 = std::is_same<T, float>::value;
+    constexpr int GV = NU > 4 ? NU / 2 : 0;  // units always inside the row (the plan picks NU so)
+    const bool from_word_before = !F32 && bf16_rows_from_word_before(p.C, D);
+
     const QRows qr = question_rows(p, b, rank, G);
     const int n = qr.n;
-    const bool skip = qr.bad || n > ROWS || (QSH && D > 4 * kDirectMaxQ4);  // the host plans neither
+    const bool skip = qr.bad || n > ROWS || (QSH && D > 4 * kDirectMaxQ4) ||
+                      (NU > 0 && !F32 && (D & 1));  // the host plans none of these
     if (threadIdx.x == 0 && qr.bad) atomicOr(&g_status, 4u);
     if (threadIdx.x == 0 && !qr.bad && skip) atomicOr(&g_status, 2u);
 
     // this warp's rows, then q: every load issued before any arithmetic
-    uint4 cv[RPW][NQC];
+    uint4 cv[RPW][NQC > 0 ? NQC : 1];
+    uint32_t cw[RPW][NU > 0 ? NU : 1];
+    uint16_t ctail[RPW];
+    if constexpr (NU > 0) {
 #pragma unroll
-    for (int m = 0; m < RPW; ++m) {
+        for (int m = 0; m < RPW; ++m) {
+            const int r = warp + 8 * m;
+            const T* row = static_cast<const T*>(p.C) + static_cast<size_t>(qr.row0 + (r < n ? r : 0)) * D;
+            const bool ok = !skip && r < n &&
+                            CS_IN_BOUNDS(row, static_cast<long long>(D) * sizeof(T), p.C,
+                                         rows_total(p) * D * static_cast<long long>(sizeof(T)), kSiteGenericC);
+            // float32: the row's own words; bfloat16: from the word holding
+            // element -1 when the row starts on an odd 2-byte boundary
+            const uint32_t* wr = reinterpret_cast<const uint32_t*>(reinterpret_cast<const unsigned char*>(row) -
+                                                                   (from_word_before ? 2 : 0));
+            const int units = F32 ? D : D >> 1;
+#pragma unroll
+            for (int u = 0; u < NU; ++u) {
+                const int k = lane + 32 * u;
+                cw[m][u] = ok && (u < GV || k < units) ? __ldg(wr + k) : 0u;
+            }
+            if (from_word_before && lane == 0) cw[m][0] &= 0xffff0000u;  // element -1
+            ctail[m] = 0;
+            if constexpr (!F32)
+                if (from_word_before && lane == 0 && ok) ctail[m] = __ldg(reinterpret_cast<const uint16_t*>(row) + D - 1);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < (NU > 0 ? 0 : RPW); ++m) {
         const int r = warp + 8 * m;
         const uint4* row = reinterpret_cast<const uint4*>(static_cast<const T*>(p.C) +
                                                           static_cast<size_t>(qr.row0 + (r < n ? r : 0)) * D);
@@ -1393,8 +1437,30 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
     }
     const float4* q4 = reinterpret_cast<const float4*>(p.Q + b * D);
     const bool q_ok = !skip && CS_IN_BOUNDS(q4, D * 4ll, p.Q, p.B * D * 4ll, kSiteGenericQ);
-    float4 qv[QSH ? 1 : NQC * QF4];
-    if constexpr (QSH) {
+    float4 qv[QSH || NU > 0 ? 1 : NQC * QF4];
+    unsigned long long qpk[UnitQ<T, NU>::kPairs];  // NU > 0: q of the lane's units (UnitQ)
+    float qlast = 0.f;                             // bfloat16 read from the word before: q[D - 1]
+    if constexpr (NU > 0) {
+        const float* qg = p.Q + b * D;
+#pragma unroll
+        for (int u = 0; u < UnitQ<T, NU>::kPairs; ++u) {
+            int k0, k1;
+            bool in0, in1;
+            if constexpr (F32) {
+                k0 = lane + 64 * u;
+                k1 = k0 + 32;
+                in0 = q_ok && k0 < D;
+                in1 = q_ok && k1 < D;
+            } else {
+                k0 = 2 * (lane + 32 * u) - (from_word_before ? 1 : 0);
+                k1 = k0 + 1;
+                in1 = q_ok && lane + 32 * u < (D >> 1);
+                in0 = in1 && k0 >= 0;
+            }
+            qpk[u] = pack2(in0 ? __ldg(qg + k0) : 0.f, in1 ? __ldg(qg + k1) : 0.f);
+        }
+        if (!F32 && from_word_before && q_ok) qlast = __ldg(qg + D - 1);
+    } else if constexpr (QSH) {
         for (int i = threadIdx.x; i < D / 4; i += kDirectThreads)
             qsh[i] = q_ok ? __ldg(q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
     } else {
@@ -1411,7 +1477,9 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
 
     // q's chunk (j, h) of this lane
     auto qchunk = [&](int j, int h) -> float4 {
-        if constexpr (QSH) {
+        if constexpr (NU > 0) {  // not used: the unit form keeps q in qpk
+            return make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if constexpr (QSH) {
             const int i = lane + 32 * j;
             return i < DC ? qsh[i * QF4 + h] : make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
@@ -1421,13 +1489,22 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
     float qsq = 0.f;
     if (COS) {
         float sq = 0.f;
+        if constexpr (NU > 0) {
 #pragma unroll
-        for (int j = 0; j < NQC; ++j)
-#pragma unroll
-            for (int h = 0; h < QF4; ++h) {
-                const float4 x = qchunk(j, h);
-                sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+            for (int u = 0; u < UnitQ<T, NU>::kPairs; ++u) {
+                const float2 x = unpack2(qpk[u]);
+                sq += x.x * x.x + x.y * x.y;
             }
+            if (lane == 0) sq += qlast * qlast;
+        } else {
+#pragma unroll
+            for (int j = 0; j < NQC; ++j)
+#pragma unroll
+                for (int h = 0; h < QF4; ++h) {
+                    const float4 x = qchunk(j, h);
+                    sq += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                }
+        }
         qsq = warp_sum(sq);  // each warp covers all of q: never summed across warps
     }
     const float w = value_scale(p.w0, qsq, COS);
@@ -1437,8 +1514,29 @@ __global__ void __launch_bounds__(kDirectThreads, 1) direct_kernel(const Problem
     unsigned long long acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0ull;
+    if constexpr (NU > 0) {
+        auto accumulate = [&](unsigned long long c, unsigned long long qq, int m) {
+            if (acc_dot(MODE)) acc[VPR * m] = fma2(c, qq, acc[VPR * m]);
+            if (acc_norm(MODE)) acc[VPR * m + VPR - 1] = fma2(c, c, acc[VPR * m + VPR - 1]);
+        };
 #pragma unroll
-    for (int j = 0; j < NQC; ++j) {
+        for (int m = 0; m < RPW; ++m) {
+            if constexpr (F32) {
+#pragma unroll
+                for (int u = 0; u < NU / 2; ++u)
+                    accumulate(pack2(__uint_as_float(cw[m][2 * u]), __uint_as_float(cw[m][2 * u + 1])), qpk[u], m);
+            } else {
+#pragma unroll
+                for (int u = 0; u < NU; ++u)
+                    accumulate(pack2(__uint_as_float(cw[m][u] << 16), __uint_as_float(cw[m][u] & 0xffff0000u)),
+                               qpk[u], m);
+                if (from_word_before)
+                    accumulate(pack2(Elem<uint16_t>::widen1(ctail[m]), 0.f), pack2(qlast, 0.f), m);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < (NU > 0 ? 0 : NQC); ++j) {
         float4 q[QF4];
 #pragma unroll
         for (int h = 0; h < QF4; ++h) q[h] = qchunk(j, h);
@@ -1842,6 +1940,10 @@ const void* direct_fn_m(int nqc) {
         case 4: return reinterpret_cast<const void*>(direct_kernel<4, MODE, T, 4, false>);
         case kDirectWideNqc:
             return reinterpret_cast<const void*>(direct_kernel<kDirectWideNqc, MODE, T, 2, true>);
+        case unaligned_nqc(4): return reinterpret_cast<const void*>(direct_kernel<unaligned_nqc(4), MODE, T, 4, false>);
+        case unaligned_nqc(8): return reinterpret_cast<const void*>(direct_kernel<unaligned_nqc(8), MODE, T, 4, false>);
+        case unaligned_nqc(16):
+            return reinterpret_cast<const void*>(direct_kernel<unaligned_nqc(16), MODE, T, 4, false>);
     }
     return nullptr;
 }
@@ -1961,7 +2063,7 @@ cudaError_t configure_device_kernels(int smem_optin) {
                 cudaFuncSetAttribute(generic_fn_for(cos, bf, true), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
         }
-    for (int nqc : {1, 2, 4, kDirectWideNqc})
+    for (int nqc : {1, 2, 4, kDirectWideNqc, unaligned_nqc(4), unaligned_nqc(8), unaligned_nqc(16)})
         for (int cos = 0; cos < 2; ++cos)
             for (int bf = 0; bf < 2; ++bf) {
                 const cudaError_t e =

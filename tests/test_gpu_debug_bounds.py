@@ -153,11 +153,14 @@ def _placed(t, offset_elems):
                                                 (3, 64, 509, 0, 3, False), (150, 255, 1025, 1, 3, True),
                                                 (200, 64, 512, 1, 1, True), (100, 31, 258, 0, 7, True),
                                                 (120, 255, 511, 3, 3, False), (60, 40, 2562, 1, 1, True),
-                                                (50, 40, 2563, 0, 2, True), (60, 40, 1030, 1, 3, False)])
+                                                (50, 40, 2563, 0, 2, True), (60, 40, 1030, 1, 3, False),
+                                                (2, 255, 512, 1, 1, True), (3, 40, 258, 0, 2, True),
+                                                (1, 255, 511, 2, 1, False)])
 def test_unaligned_rows_within_bounds(dbg, B, K, D, oq, oc, bf16):
     """Unaligned plans copy each stage's 16-byte aligned span; what the
     kernels check and use is the rows' own range, which must stay inside C,
-    and the span must fit its ring slot."""
+    and the span must fit its ring slot. A few questions take the DIRECT
+    plan's 4-byte units instead, checked the same way."""
     wl = workloads.random_case(B, K, D, 1, 3.0, 70 + B + D, DEV)
     Q = _placed(wl.Q, oq)
     C = _placed(wl.C.to(torch.bfloat16) if bf16 else wl.C, oc)

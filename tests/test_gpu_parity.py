@@ -207,32 +207,93 @@ def test_every_plan_every_tempered_pair(cuda_lib, plan, normalize):
                           f"{plan[0]} B={B} K={K} D={D} scale={wl.scale} T={wl.temperature}")
 
 
-def test_few_unaligned_or_odd_questions_use_the_scalar_plan(cuda_lib):
+def _off_by_one(wl):
+    """Copies of wl's Q and C one float past a 16-byte boundary."""
+    Qb = torch.empty(wl.B * wl.D + 1, device=DEV)
+    Cb = torch.empty(wl.B * wl.K * wl.D + 1, device=DEV)
+    Q = Qb[1:].view(wl.B, wl.D)
+    C = Cb[1:].view(wl.B, wl.K, wl.D)
+    Q.copy_(wl.Q)
+    C.copy_(wl.C)
+    return Q, C
+
+
+def test_few_unaligned_or_odd_questions(cuda_lib):
+    """A few questions whose rows the bulk copies cannot take whole: the
+    DIRECT plan reads rows of up to 512 float32 elements in 4-byte units;
+    longer ones take the scalar plan. Every plan that takes them matches the
+    oracle."""
     for normalize in (0, 1):
-        # odd D
+        # odd D past the unit form: the scalar plan; DIRECT refuses it
         wl = workloads.random_case(3, 255, 513, normalize, 2.0, 21)
         Q, C = wl.Q.to(DEV), wl.C.to(DEV)
         assert binding.cs_query_plan(Q, C, normalize)["plan"] == "generic"
         assert_parity(_run(wl), oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "odd D")
-        # pointers 4 bytes past a 16-byte boundary, D a multiple of 4
-        wl = workloads.random_case(2, 64, 512, normalize, 2.0, 22)
-        Qb = torch.empty(wl.B * wl.D + 1, device=DEV)
-        Cb = torch.empty(wl.B * wl.K * wl.D + 1, device=DEV)
-        Q = Qb[1:].view(wl.B, wl.D)
-        C = Cb[1:].view(wl.B, wl.K, wl.D)
-        Q.copy_(wl.Q)
-        C.copy_(wl.C)
-        assert binding.cs_query_plan(Q, C, normalize)["plan"] == "generic"
-        p = binding.cs_score_candidates_batch(Q, C, normalize, 2.0, 1.0)
-        torch.cuda.synchronize()
-        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "unaligned")
-        # the stream plan takes them too, copying the rows' aligned spans
-        p = binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_STREAM)
-        torch.cuda.synchronize()
-        assert_parity(p, oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "unaligned, stream plan")
-        # the DIRECT plan loads 16-byte chunks and refuses them
         with pytest.raises(binding.CSError):
             binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_DIRECT)
+        # odd D and pointers 4 bytes past a 16-byte boundary, within the unit form
+        for D in (511, 512):
+            wl = workloads.random_case(2, 64, D, normalize, 2.0, 22 + D)
+            Q, C = _off_by_one(wl)
+            ref = oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0)
+            plan = binding.cs_query_plan(Q, C, normalize)
+            assert plan["plan"] == "direct", plan
+            p = binding.cs_score_candidates_batch(Q, C, normalize, 2.0, 1.0)
+            torch.cuda.synchronize()
+            assert_parity(p, ref, f"unaligned D={D}, DIRECT plan")
+            # the stream and scalar plans take them too
+            for kind in (binding.CS_PLAN_STREAM, binding.CS_PLAN_GENERIC):
+                p = binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, kind)
+                torch.cuda.synchronize()
+                assert_parity(p, ref, f"unaligned D={D}, plan {kind}")
+
+
+@pytest.mark.parametrize("normalize", [1, 0], ids=["cos", "dot"])
+def test_direct_plan_on_unaligned_rows(cuda_lib, normalize):
+    """The DIRECT plan's 4-byte-unit form at every cluster size, on rows off
+    16-byte boundaries and of odd length: float32 at D either side of its
+    unit counts, bfloat16 with C on even and odd 2-byte boundaries (rows
+    read from the word before). Each question against the oracle; a
+    ragged batch too."""
+    pairs = pairs_in_rotation(normalize)
+    cases = [(1, 255, 512, 1, 1, False), (3, 64, 511, 0, 0, False), (2, 37, 129, 2, 3, False),
+             (1, 200, 3, 0, 1, False), (1, 255, 512, 1, 1, True), (4, 100, 1024, 0, 3, True),
+             (2, 70, 258, 1, 2, True), (1, 31, 2, 0, 5, True)]
+    for i, (B, K, D, oq, oc, bf16) in enumerate(cases):
+        wl = tempered_case(B, K, D, normalize, pairs[i % len(pairs)], 900 + B + K + D)
+        Cr = wl.C.to(torch.bfloat16) if bf16 else wl.C
+        ref = oracle_probs(wl.Q, Cr.float(), normalize, wl.scale, wl.temperature)
+        Qb = torch.empty(B * D + oq + 8, device=DEV)
+        Cb = torch.empty(B * K * D + oc + 8, device=DEV, dtype=Cr.dtype)
+        Q, C = Qb[oq:oq + B * D].view(B, D), Cb[oc:oc + B * K * D].view(B, K, D)
+        Q.copy_(wl.Q)
+        C.copy_(Cr)
+        what = f"B={B} K={K} D={D} q+{oq} c+{oc} bf16={bf16}"
+        if bf16:
+            p = binding.cs_score_candidates_batch_bf16(Q, C, normalize, wl.scale, wl.temperature)
+            torch.cuda.synchronize()
+            assert_parity(p, ref, "auto " + what)
+            continue
+        assert binding.cs_query_plan(Q, C, normalize)["plan"] == "direct", what
+        for G in (0, 1, 2, 4, 8, 16):
+            if G > K or (G and (K + G - 1) // G > 32):
+                continue
+            p = binding.cs_score_candidates_batch_plan(Q, C, normalize, wl.scale, wl.temperature,
+                                                       binding.CS_PLAN_DIRECT, G)
+            torch.cuda.synchronize()
+            assert_parity(p, ref, f"DIRECT G={G} " + what)
+    rw = workloads.ragged(6, 300, 1, 14.2857, 77, "cpu", kmax=60)
+    Cb = torch.empty(rw.C.numel() + 8, device=DEV)
+    C = Cb[1:1 + rw.C.numel()].view(rw.C.shape)
+    C.copy_(rw.C)
+    p = binding.cs_score_candidates_ragged(rw.Q.to(DEV), C, rw.offsets.to(DEV), 1, rw.scale, 1.0)
+    torch.cuda.synchronize()
+    p = p.cpu()
+    off = rw.offsets.tolist()
+    for b in range(rw.B):
+        ref = oracle_probs(rw.Q[b:b + 1], rw.C[off[b]:off[b + 1]][None], 1, rw.scale, 1.0)
+        assert_parity(p[off[b]:off[b + 1]][None], ref, f"ragged unaligned DIRECT question {b}")
+    assert binding.cs_device_status() == 0
 
 
 @pytest.mark.parametrize("misaligned", [False, True], ids=["odd_d", "misaligned"])
@@ -301,13 +362,19 @@ def test_automatic_plans(cuda_lib):
     assert plan(1, 255, 4096)["plan"] == "cluster"  # rows too long for registers: the ring
     big = plan(4096, 255, 512)
     assert big["plan"] == "stream" and big["ctas"] == torch.cuda.get_device_properties(0).multi_processor_count
-    # rows the bulk copies cannot take: the scalar plan, a few questions each
-    # spread over a cluster (at least one row per warp, 16 KB per CTA)
+    # rows the bulk copies cannot take: up to 512 float32 elements the DIRECT
+    # plan's 4-byte-unit form, at most 32 rows per CTA
     odd = plan(2, 255, 511)
-    assert odd["plan"] == "generic" and odd["cluster"] == 16 and odd["ctas"] == 32, odd
+    assert odd["plan"] == "direct" and odd["cluster"] >= 8, odd
+    short = plan(1, 12, 511)
+    assert short["plan"] == "direct" and short["cluster"] == 1, short
+    assert plan(1, 255, 3)["plan"] == "direct" and plan(1, 255, 3)["cluster"] == 8  # the row limit
+    # longer ones: the scalar plan, a few questions each spread over a
+    # cluster (at least one row per warp, 16 KB per CTA)
+    long_odd = plan(2, 255, 1001)
+    assert long_odd["plan"] == "generic" and long_odd["cluster"] == 16 and long_odd["ctas"] == 32, long_odd
     assert plan(1, 64, 1001)["cluster"] == 8     # limited by rows: one per warp
-    assert plan(1, 12, 511)["cluster"] == 1      # fewer rows than two CTAs' warps
-    assert plan(1, 255, 3)["cluster"] == 1       # 3 KB of rows: not worth splitting
+    assert plan(1, 12, 1001)["cluster"] == 1     # fewer rows than two CTAs' warps
     many = plan(100, 255, 511)  # too many questions for clusters: the stream plan copies aligned spans
     assert many["plan"] == "stream" and many["ctas"] == 100, many
     assert plan(4096, 255, 510)["plan"] == "stream"
