@@ -826,8 +826,11 @@ __device__ __forceinline__ void stage_dots_units_shared_q(const unsigned char* _
             const uint32_t* __restrict__ row = words + (hb >> 1);
             // an odd 2-byte start takes each pair from two words, unless every
             // row is read from the word before (even D, from_word_before)
-            auto pairs = [&](auto split_tag) {
+            // q's pairs as one 8-byte read when they sit on 8-byte boundaries
+            // (two 4-byte reads of every other word take twice the wavefronts)
+            auto pairs = [&](auto split_tag, auto q8_tag) {
                 constexpr bool SPLIT = decltype(split_tag)::value;
+                constexpr bool Q8 = decltype(q8_tag)::value;
                 for (int k0 = lane; k0 - lane < np; k0 += 32 * NB) {
                     uint32_t x[NB], y[NB];
                     float qa[NB], qb[NB];
@@ -837,8 +840,14 @@ __device__ __forceinline__ void stage_dots_units_shared_q(const unsigned char* _
                         const bool in = k < np;
                         x[j] = in ? row[k] : 0u;
                         if (SPLIT) y[j] = in ? row[k + 1] : 0u;
-                        qa[j] = in && e >= 0 ? qf[e] : 0.f;
-                        qb[j] = in ? qf[e + 1] : 0.f;
+                        if (Q8) {
+                            const float2 qq = in ? *reinterpret_cast<const float2*>(qf + e) : make_float2(0.f, 0.f);
+                            qa[j] = e >= 0 ? qq.x : 0.f;
+                            qb[j] = qq.y;
+                        } else {
+                            qa[j] = in && e >= 0 ? qf[e] : 0.f;
+                            qb[j] = in ? qf[e + 1] : 0.f;
+                        }
                     }
                     if (from_word_before && k0 == 0) x[0] &= 0xffff0000u;  // element -1
 #pragma unroll
@@ -849,10 +858,12 @@ __device__ __forceinline__ void stage_dots_units_shared_q(const unsigned char* _
                     }
                 }
             };
-            if ((hb & 1u) && !from_word_before)
-                pairs(std::true_type{});
+            const bool q8 = ((reinterpret_cast<unsigned long long>(qf) - 4u * sh) & 7u) == 0;
+            const bool split = (hb & 1u) && !from_word_before;
+            if (split)
+                q8 ? pairs(std::true_type{}, std::true_type{}) : pairs(std::true_type{}, std::false_type{});
             else
-                pairs(std::false_type{});
+                q8 ? pairs(std::false_type{}, std::true_type{}) : pairs(std::false_type{}, std::false_type{});
             if ((D & 1) || from_word_before) {
                 const uint16_t e = lane == 0 ? halves[hb + D - 1] : uint16_t(0);
                 accumulate(pack2(Elem<uint16_t>::widen1(e), 0.f), pack2(qlast, 0.f));
