@@ -736,16 +736,31 @@ __device__ __forceinline__ void stage_dots_units(const unsigned char* __restrict
                     tail[i] = from_word_before && lane == 0 && g + i < nr ? halves[hb + D - 1] : uint16_t(0);
                 }
                 if (g + RG >= MR) release();
+                auto widened = [&](uint32_t x) {
+                    return pack2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+                };
+                if constexpr (acc_norm(MODE)) {
+                    // cosine: units outer, every row of the group inner (rows a
+                    // short stage lacks hold zeros), so that consecutive packed
+                    // FMAs feed different rows' sums: 0.87 -> 0.97 of the aligned
+                    // rate, against 2 % less for the dot
 #pragma unroll
-                for (int i = 0; i < RG; ++i)
-                    if (g + i < nr) {
+                    for (int u = 0; u < NU; ++u)
 #pragma unroll
-                        for (int u = 0; u < NU; ++u)
-                            accumulate(pack2(__uint_as_float(w[i][u] << 16), __uint_as_float(w[i][u] & 0xffff0000u)),
-                                       qpk[u], g + i);
-                        if (from_word_before)
-                            accumulate(pack2(Elem<uint16_t>::widen1(tail[i]), 0.f), pack2(qlast, 0.f), g + i);
-                    }
+                        for (int i = 0; i < RG; ++i) accumulate(widened(w[i][u]), qpk[u], g + i);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < RG; ++i)
+                        if (g + i < nr) {
+#pragma unroll
+                            for (int u = 0; u < NU; ++u) accumulate(widened(w[i][u]), qpk[u], g + i);
+                        }
+                }
+                if (from_word_before) {
+#pragma unroll
+                    for (int i = 0; i < RG; ++i)
+                        accumulate(pack2(Elem<uint16_t>::widen1(tail[i]), 0.f), pack2(qlast, 0.f), g + i);
+                }
             }
         } else {
 #pragma unroll
