@@ -184,8 +184,8 @@ int nq4_for(const Problem& p) {
 
 // Plan.nq4 for rows the bulk copies take as aligned spans: the unit-wise
 // form with the fewest units a lane that covers the row (units: float32
-// elements, or whole bfloat16 pairs), else the scalar form with q in shared
-// memory.
+// elements, or whole bfloat16 pairs) with q in registers, else the unit-wise
+// form with q in shared memory (kNqcUnaligned).
 int unaligned_nq4_for(const Problem& p) {
     const int units = p.c_bf16 ? p.D / 2 : p.D;
     for (int nu : cs::kUnalignedUnits)

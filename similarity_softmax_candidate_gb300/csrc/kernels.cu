@@ -28,11 +28,15 @@
 //         peer's shared memory with st.async, completing on the peer's
 //         mbarrier, so one question uses up to 16 SMs.
 //     Dots and norms accumulate as packed float32 pairs (fma.rn.f32x2);
-//     plans of at most 2 rows per stage run a short-stage build.
+//     plans of at most 2 rows per stage run a short-stage build. Rows that
+//     do not start on 16-byte boundaries (or whose length is not a multiple
+//     of 16 bytes) are copied as the aligned span around them and read from
+//     shared memory in 4-byte units (stage_dots_units).
 //   * direct_kernel -- DIRECT plan, one or a few short questions: one CTA or
 //     cluster per question, at most 32 rows per CTA (16 for long rows), q
 //     and the rows loaded straight into registers (q in shared memory for
-//     long rows), one trip to memory, the same cluster exchange.
+//     long rows; unaligned rows as 4-byte units), one trip to memory, the
+//     same cluster exchange.
 //   * generic_kernel -- scalar loads, any D and any alignment: one CTA per
 //     question, or, for a few questions of a uniform batch, one cluster per
 //     question with the same exchange as the DIRECT plan.
