@@ -788,6 +788,9 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
     Prows = torch.empty((B * Kq, Dp), device=dev)
     rows_ms = timed(lambda: cs.cs_project_rows(Hrows, Wc, out=Prows, stream=s))
     rows_bytes = 2.0 * B * Kq * Din + 2.0 * Dp * Din + 4.0 * B * Kq * Dp
+    # Writes alone: P filled (torch's fill_), the kernel's 2.14 GB of
+    # stores without its reads or arithmetic.
+    fill_ms = timed(lambda: Prows.fill_(1.0))
     hbm, hbm_src = _peak_hbm()
     flop = 2.0 * B * Kq * Din * Dp + 2.0 * B * Din * Dp
     peak, peak_src = _peak_bf16()
@@ -799,6 +802,9 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
     flop_unit = 2.0 * 128 * 256 * Din
     sm_mhz, sms = _sm_max_mhz(), torch.cuda.get_device_properties(dev).multi_processor_count
     smem_bound = flop_unit / (smem_bytes_unit / 128.0) * sms * sm_mhz * 1e6 / 1e12
+    rows_smem_unit = smem_bytes_unit + 2 * 128 * 256 * 4
+    rows_units = -(-(B * Kq) // 128) * (Dp // 256)
+    rows_smem_ms = -(-rows_units // sms) * rows_smem_unit / 128.0 / (sm_mhz * 1e6) * 1e3
     return {"workload": f"{B} questions x K=255, Din=512 -> D=512, bf16 features and heads, cosine",
             "questions_per_s": B / (fused_ms / 1e3), "ms_per_call": fused_ms,
             "tflops": flop / (fused_ms / 1e3) / 1e12, "peak_tflops": peak,
@@ -809,9 +815,17 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
             "composed_cublas_bf16_ms": composed_ms, "fused_over_composed": composed_ms / fused_ms,
             "project_rows": {"rows": B * Kq, "ms_per_call": rows_ms,
                              "tflops": 2.0 * B * Kq * Din * Dp / (rows_ms / 1e3) / 1e12,
-                             "bound": "hbm", "gbs": rows_bytes / (rows_ms / 1e3) / 1e9,
-                             "frac": rows_bytes / (rows_ms / 1e3) / 1e9 / hbm,
-                             "peak_source": f"hbm_gbs ({hbm_src})"}}
+                             "gbs": rows_bytes / (rows_ms / 1e3) / 1e9,
+                             "frac_of_copy": rows_bytes / (rows_ms / 1e3) / 1e9 / hbm,
+                             "peak_source": f"hbm_gbs ({hbm_src})",
+                             # each unit also stages its 128 x 256 float32 outputs through
+                             # shared memory (written by the epilogue, read by the TMA store)
+                             "smem_bound": {"bytes_per_unit": rows_smem_unit, "bytes_per_clock": 128,
+                                            "sm_mhz": sm_mhz, "ms": rows_smem_ms, "frac": rows_smem_ms / rows_ms},
+                             "writes_alone": {
+                                 "what": "torch fill_ of P (the kernel's stores, no reads, no arithmetic)",
+                                 "ms": fill_ms, "write_gbs": 4.0 * B * Kq * Dp / (fill_ms / 1e3) / 1e9,
+                                 "rows_ms_over_fill_ms": rows_ms / fill_ms}}}
 
 
 def plan_sweep(cs, dev, Bs=(1, 2, 4, 8, 16, 24, 32, 48, 64, 76, 100, 152), n=32):
