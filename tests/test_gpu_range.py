@@ -35,11 +35,26 @@ SENTINEL = 4242.0
 
 # (name, how a batch is scored); every form takes Q [B,D], C [B,K,D] float32
 # on the device and writes out [B,K].
-PLANS = ["auto", "direct", "cluster4", "stream", "generic", "generic4", "unfused", "bf16", "ragged"]
+PLANS = ["auto", "direct", "cluster4", "stream", "generic", "generic4", "unfused", "bf16", "ragged",
+         "auto_off", "stream_off", "bf16_off"]
+
+
+def _one_off(t):
+    """A copy of t one element past a 16-byte boundary (rows the bulk copies
+    cannot take whole: the 4-byte-unit forms)."""
+    flat = torch.empty(t.numel() + 8, device=DEV, dtype=t.dtype)
+    v = flat[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
 
 
 def _score(plan, Q, C, normalize, scale, T, out):
     b = binding
+    if plan.endswith("_off"):  # the same plan on copies of Q and C one element off
+        if plan == "bf16_off":
+            Q, Cb = _one_off(Q), _one_off(C.to(torch.bfloat16))
+            return b.cs_score_candidates_batch_bf16(Q, Cb, normalize, scale, T, out=out)
+        return _score(plan[:-4], _one_off(Q), _one_off(C), normalize, scale, T, out)
     if plan == "auto":
         return b.cs_score_candidates_batch(Q, C, normalize, scale, T, out=out)
     if plan == "direct":
@@ -65,7 +80,7 @@ def _score(plan, Q, C, normalize, scale, T, out):
 
 
 def _ref(plan, Q, C, normalize, scale, T):
-    if plan == "bf16":
+    if plan in ("bf16", "bf16_off"):
         C = C.to(torch.bfloat16).float()
     return oracle_probs(Q.cpu().double(), C.cpu().double(), normalize, scale, T)
 
