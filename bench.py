@@ -903,7 +903,8 @@ def unaligned_latency(cs, dev, n=32):
     cannot take whole (D=510, and D=512 with Q and C one element off a
     16-byte boundary; float32 and bfloat16, cosine): the automatic plan
     against the scalar plan (one question over a 16-CTA cluster) forced on
-    the same rows. Device time per call as in the plan sweep: n calls on
+    the same rows, and the stream kernel's cluster plan (16 CTAs, rows copied
+    as aligned spans). Device time per call as in the plan sweep: n calls on
     consecutive slices of a 2.1 GB buffer in one CUDA graph after a read of
     256 MiB, minus the same graph without the calls (every call from HBM)."""
     import torch
@@ -943,7 +944,7 @@ def unaligned_latency(cs, dev, n=32):
         return 1e3 * (graph_ms(n) - graph_ms(0)) / n
 
     rows = []
-    for name, d, off in (("odd_d510", 510, 0), ("misaligned_d512", 512, 1)):
+    for name, d, off in (("odd_d510", 510, 0), ("misaligned_d512", 512, 1), ("misaligned_d2560", 2560, 1)):
         nsl = n_elem // (K * d) - 1
         views = [(flatQ[off + (i % 4096) * d:off + (i % 4096) * d + d],
                   flatC[off + (i % nsl) * K * d:off + ((i % nsl) + 1) * K * d].view(K, d),
@@ -954,6 +955,8 @@ def unaligned_latency(cs, dev, n=32):
                                                                     out=out))
         row["f32_scalar16_us"] = timed(lambda i: cs.cs_score_candidates_batch_plan(
             views[i][0][None], views[i][1][None], 1, 14.285714, 1.0, cs.CS_PLAN_GENERIC, 16, 0, out=out[None]))
+        row["f32_cluster16_us"] = timed(lambda i: cs.cs_score_candidates_batch_plan(
+            views[i][0][None], views[i][1][None], 1, 14.285714, 1.0, cs.CS_PLAN_CLUSTER, 16, 0, out=out[None]))
         row["bf16_auto_us"] = timed(lambda i: cs.cs_score_candidates_bf16(views[i][0], views[i][2], 1, 14.285714,
                                                                           1.0, out=out))
         rows.append(row)

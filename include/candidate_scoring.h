@@ -225,8 +225,7 @@ int cs_project_score_batch(const uint16_t *Hq, const uint16_t *Wq,
 #define CS_PLAN_CLUSTER 2  /* one thread-block cluster per question, rows split */
 #define CS_PLAN_GENERIC 3  /* scalar loads; any D, any alignment (one CTA per
                               question, or a cluster of CTAs per question
-                              when a uniform-K batch has few questions): a
-                              few unaligned questions with long rows, or
+                              when a uniform-K batch has few questions):
                               rows too long for the shared-memory ring */
 #define CS_PLAN_DIRECT 4   /* one CTA (or cluster) per short question: at most 32
                               rows per CTA (16 for long rows), q and rows

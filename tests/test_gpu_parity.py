@@ -221,16 +221,20 @@ def _off_by_one(wl):
 def test_few_unaligned_or_odd_questions(cuda_lib):
     """A few questions whose rows the bulk copies cannot take whole: the
     DIRECT plan reads rows of up to 512 float32 elements in 4-byte units;
-    longer ones take the scalar plan. Every plan that takes them matches the
-    oracle."""
+    longer ones take the stream kernel's cluster plan (aligned spans). Every
+    plan that takes them matches the oracle."""
     for normalize in (0, 1):
-        # odd D past the unit form: the scalar plan; DIRECT refuses it
+        # odd D past the unit form: a cluster plan; DIRECT refuses it
         wl = workloads.random_case(3, 255, 513, normalize, 2.0, 21)
         Q, C = wl.Q.to(DEV), wl.C.to(DEV)
-        assert binding.cs_query_plan(Q, C, normalize)["plan"] == "generic"
-        assert_parity(_run(wl), oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0), "odd D")
+        assert binding.cs_query_plan(Q, C, normalize)["plan"] == "cluster"
+        ref = oracle_probs(wl.Q, wl.C, normalize, 2.0, 1.0)
+        assert_parity(_run(wl), ref, "odd D")
         with pytest.raises(binding.CSError):
             binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_DIRECT)
+        p = binding.cs_score_candidates_batch_plan(Q, C, normalize, 2.0, 1.0, binding.CS_PLAN_GENERIC, 4)
+        torch.cuda.synchronize()
+        assert_parity(p, ref, "odd D, scalar plan")
         # odd D and pointers 4 bytes past a 16-byte boundary, within the unit form
         for D in (511, 512):
             wl = workloads.random_case(2, 64, D, normalize, 2.0, 22 + D)
@@ -369,16 +373,17 @@ def test_automatic_plans(cuda_lib):
     short = plan(1, 12, 511)
     assert short["plan"] == "direct" and short["cluster"] == 1, short
     assert plan(1, 255, 3)["plan"] == "direct" and plan(1, 255, 3)["cluster"] == 8  # the row limit
-    # longer ones: the scalar plan, a few questions each spread over a
-    # cluster (at least one row per warp, 16 KB per CTA)
+    # longer ones: the stream kernel's cluster plan, rows copied as aligned
+    # spans (at most 16 CTAs a question, 16 KB of rows each)
     long_odd = plan(2, 255, 1001)
-    assert long_odd["plan"] == "generic" and long_odd["cluster"] == 16 and long_odd["ctas"] == 32, long_odd
-    assert plan(1, 64, 1001)["cluster"] == 8     # limited by rows: one per warp
-    assert plan(1, 12, 1001)["cluster"] == 1     # fewer rows than two CTAs' warps
+    assert long_odd["plan"] == "cluster" and long_odd["cluster"] == 16 and long_odd["ctas"] == 32, long_odd
+    assert plan(1, 12, 1001)["cluster"] == 2     # 48 KB of rows: two CTAs of 24 KB
     many = plan(100, 255, 511)  # too many questions for clusters: the stream plan copies aligned spans
     assert many["plan"] == "stream" and many["ctas"] == 100, many
     assert plan(4096, 255, 510)["plan"] == "stream"
     assert plan(2, 9, 20000)["plan"] == "generic"  # rows too long for the ring
+    # rows too long for the ring's stages: the scalar plan over a cluster
+    assert plan(1, 64, 20001)["plan"] == "generic" and plan(1, 64, 20001)["cluster"] == 8
 
 
 def test_throughput_workload_full_size(cuda_lib):

@@ -128,8 +128,10 @@ def test_unit_form_sizes(cuda_lib, dtype, normalize):
 
 
 def test_unaligned_ragged(cuda_lib):
-    """A ragged batch of odd D, and one whose C is off a 16-byte boundary."""
-    for B, D, oc in ((400, 513, 0), (300, 512, 1), (12, 255, 3)):
+    """A ragged batch of odd D, and one whose C is off a 16-byte boundary:
+    many questions (the stream plan), a few short ones (DIRECT) and a few
+    long ones (a cluster plan)."""
+    for B, D, oc in ((400, 513, 0), (300, 512, 1), (12, 255, 3), (8, 1001, 1)):
         wl = workloads.ragged(B, D, 1, 14.2857, 60 + B, "cpu")
         Q, C = wl.Q.to(DEV), _placed(wl.C.to(DEV), oc)
         p = binding.cs_score_candidates_ragged(Q, C, wl.offsets.to(DEV), 1, wl.scale, 1.0)

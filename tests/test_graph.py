@@ -60,17 +60,30 @@ def _capture(rt, stream, fn):
     return graph
 
 
-# (B, K, D, normalize, scale, temperature): the page's shapes, a large batch,
-# odd D, and two calls with a temperature other than 1 and a negative scale.
-CASES = [(1, 5, 512, 1, 14.2857, 1.0), (1, 255, 512, 1, 14.2857, 1.0), (8, 255, 512, 1, 14.2857, 1.0),
-         (1, 255, 2560, 0, 0.0625, 1.0), (700, 255, 512, 0, 0.0625, 1.0), (3, 33, 513, 1, 14.2857, 1.0),
-         (4, 255, 512, 1, -14.2857, 0.7), (300, 64, 256, 0, -0.0625, 3.0)]
+# (B, K, D, normalize, scale, temperature, off): the page's shapes, a large
+# batch, odd D, two calls with a temperature other than 1 and a negative
+# scale, and Q and C `off` elements past a 16-byte boundary (the DIRECT and
+# stream plans' 4-byte-unit forms, and the scalar plan for long rows).
+CASES = [(1, 5, 512, 1, 14.2857, 1.0, 0), (1, 255, 512, 1, 14.2857, 1.0, 0), (8, 255, 512, 1, 14.2857, 1.0, 0),
+         (1, 255, 2560, 0, 0.0625, 1.0, 0), (700, 255, 512, 0, 0.0625, 1.0, 0), (3, 33, 513, 1, 14.2857, 1.0, 0),
+         (4, 255, 512, 1, -14.2857, 0.7, 0), (300, 64, 256, 0, -0.0625, 3.0, 0),
+         (1, 255, 512, 1, 14.2857, 1.0, 1), (700, 255, 510, 1, 14.2857, 0.7, 1), (2, 64, 2560, 0, 0.0625, 1.0, 3)]
 
 
-@pytest.mark.parametrize("B,K,D,normalize,scale,temperature", CASES)
-def test_one_node_and_bitwise_replay(cuda_lib, B, K, D, normalize, scale, temperature):
+def _off(t, off):
+    if not off:
+        return t
+    flat = torch.empty(t.numel() + off + 8, device=t.device, dtype=t.dtype)
+    v = flat[off:off + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("B,K,D,normalize,scale,temperature,off", CASES)
+def test_one_node_and_bitwise_replay(cuda_lib, B, K, D, normalize, scale, temperature, off):
     rt = _cudart()
     wl = workloads.random_case(B, K, D, normalize, scale, 71, "cuda:0", temperature=temperature)
+    wl.Q, wl.C = _off(wl.Q, off), _off(wl.C, off)
     s = torch.cuda.Stream()
     direct = torch.empty(B, K, device="cuda:0")
     replay = torch.full((B, K), -1.0, device="cuda:0")
