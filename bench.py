@@ -802,7 +802,7 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
     flop_unit = 2.0 * 128 * 256 * Din
     sm_mhz, sms = _sm_max_mhz(), torch.cuda.get_device_properties(dev).multi_processor_count
     smem_bound = flop_unit / (smem_bytes_unit / 128.0) * sms * sm_mhz * 1e6 / 1e12
-    rows_smem_unit = smem_bytes_unit + 2 * 128 * 256 * 4
+    rows_smem_unit = smem_bytes_unit  # the outputs go from registers to global memory
     rows_units = -(-(B * Kq) // 128) * (Dp // 256)
     rows_smem_ms = -(-rows_units // sms) * rows_smem_unit / 128.0 / (sm_mhz * 1e6) * 1e3
     return {"workload": f"{B} questions x K=255, Din=512 -> D=512, bf16 features and heads, cosine",
@@ -818,8 +818,6 @@ def projected_readout(cs, dev, steps, warmup, B=4096):
                              "gbs": rows_bytes / (rows_ms / 1e3) / 1e9,
                              "frac_of_copy": rows_bytes / (rows_ms / 1e3) / 1e9 / hbm,
                              "peak_source": f"hbm_gbs ({hbm_src})",
-                             # each unit also stages its 128 x 256 float32 outputs through
-                             # shared memory (written by the epilogue, read by the TMA store)
                              "smem_bound": {"bytes_per_unit": rows_smem_unit, "bytes_per_clock": 128,
                                             "sm_mhz": sm_mhz, "ms": rows_smem_ms, "frac": rows_smem_ms / rows_ms},
                              "writes_alone": {

@@ -218,6 +218,7 @@ enum BoundsSite : unsigned {
     kSiteUnitSlot = 18,    // unaligned unit-wise reads: the stage's extent in its ring slot
     kSiteProjQ = 20,       // projected readout: projected query
     kSiteProjOut = 21,     // projected readout: probabilities
+    kSiteProjRows = 22,    // projected rows: a 32-byte row segment of P
     kSiteSelftest = 99,
 };
 bool debug_bounds_build();

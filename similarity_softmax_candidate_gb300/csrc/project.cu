@@ -24,10 +24,10 @@
 // tensor memory as two 256-column accumulators and (one lane) issues
 // tcgen05.mma (M=128, N=256, K=16) into them in turn; tcgen05.commit frees a
 // ring stage when its MMAs finish and hands a finished accumulator to the
-// epilogue. Warps 2-5 (128 threads, one accumulator row each) read a unit
-// back with tcgen05.ld while the tensor cores fill the other accumulator,
-// and either store it or fold it into dot, norm and softmax. Every wait is
-// bounded.
+// epilogue. Warps 2-5 (128 threads, each warp the 32 accumulator rows of its
+// TMEM lane quarter) read a unit back with tcgen05.ld while the tensor cores
+// fill the other accumulator, and either store it or fold it into dot, norm
+// and softmax. Every wait is bounded.
 #include "internal.h"
 #include "softmax_form.cuh"
 
@@ -44,11 +44,8 @@ constexpr int kTileM = 128;        // accumulator rows (TMEM lanes)
 constexpr int kTileK = 64;         // Din columns per ring stage: 128 bytes of bf16, one swizzle row
 constexpr int kMmaN = 256;         // N of one tcgen05.mma
 constexpr int kMmaK = 16;          // K of one tcgen05.mma (bf16)
-// Ring stages of 48 KB; the plain kernel's output boxes (32 KB) take the
-// room of the scoring kernel's query and logits.
+// Ring stages of 48 KB.
 constexpr int kProjStages = 4;
-constexpr int kOutBox = 32;                    // output box: 32 rows x 32 float32 columns (128-byte rows)
-constexpr int kOutBoxBytes = kOutBox * kOutBox * 4;
 constexpr int kAccCols = 2 * kMmaN;  // two accumulators of kMmaN columns: all of tensor memory
 constexpr int kProjThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpiThreads = 128;
@@ -143,20 +140,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
         : "memory");
 }
 
-// 2-D tiled TMA store of a shared-memory box at (x = column, y = row); rows
-// and columns outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// At most one committed store group of this thread still reading shared memory.
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-// Every committed store group of this thread complete.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -195,6 +178,24 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 128 columns of 16 TMEM lanes (taddr's lane the first), as the .16x256b
+// shape spreads them: repetition i gives thread t the columns 8 i + 2 (t % 4)
+// and + 1 of lanes t / 4 (v[4 i], v[4 i + 1]) and t / 4 + 8 (v[4 i + 2],
+// v[4 i + 3]), so a quad of threads holds 8 consecutive columns of a lane.
+__device__ __forceinline__ void tmem_ld_16x256b_x16(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x16.b32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
+        "}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 128 consecutive accumulator columns of this thread's TMEM lane.
@@ -248,18 +249,17 @@ __device__ __forceinline__ float wmax(float v) {
 }
 
 // Shared memory, from a 1024-byte aligned base: ring stages (A tile, then
-// the unit's kMmaN rows of W), output staging (plain kernel: two boxes per
-// epilogue warp), q (D floats), 2 x 256 logits, barriers, TMEM address.
+// the unit's kMmaN rows of W), q (D floats) and 2 x 256 logits (scoring
+// kernel only), barriers, TMEM address.
 struct ProjLayout {
-    uint32_t stage_bytes, a_bytes, ring, out, q, logits, bars, tmem, flag, total;
+    uint32_t stage_bytes, a_bytes, ring, q, logits, bars, tmem, flag, total;
 };
 __host__ __device__ inline ProjLayout proj_layout(int D, int mode) {
     ProjLayout L;
     L.a_bytes = kTileM * kTileK * 2;
     L.stage_bytes = L.a_bytes + kMmaN * kTileK * 2;
     L.ring = 0;
-    L.out = L.ring + kProjStages * L.stage_bytes;
-    L.q = L.out + (mode == 1 ? 0u : (kEpiThreads / 32) * 2u * kOutBoxBytes);
+    L.q = L.ring + kProjStages * L.stage_bytes;
     L.logits = L.q + (mode == 1 ? static_cast<uint32_t>(D) * 4 : 0u);  // q and logits: scoring kernel only
     L.bars = L.logits + (mode == 1 ? 2u * 256u * 4u : 0u);
     L.tmem = L.bars + (2 * kProjStages + 4) * 8;
@@ -271,7 +271,7 @@ __host__ __device__ inline ProjLayout proj_layout(int D, int mode) {
 template <int MODE>
 __global__ void __launch_bounds__(kProjThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmP, const ProjArgs a) {
+                const ProjArgs a) {
     extern __shared__ unsigned char smem_raw[];
     const int D = a.D, nk = a.Din / kTileK, nhalf = D / kMmaN;
     const ProjLayout L = proj_layout(D, MODE);
@@ -393,9 +393,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         const int et = threadIdx.x - 64;                  // 0..127
         const int row = 32 * (warp & 3) + lane;           // TMEM lane this warp may read
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        uint32_t unit = 0, nbox = 0;
-        unsigned char* stage_out = sm + L.out + (warp - 2) * 2 * kOutBoxBytes;  // plain kernel only
-        const uint32_t stage_out_s = base + L.out + static_cast<uint32_t>(warp - 2) * 2u * kOutBoxBytes;
+        uint32_t unit = 0;
         long long nq = 0;
         for (long long item = blockIdx.x; item < items; item += gridDim.x, ++nq) {
             float w = 1.f;  // SCORE: the question's value scale (softmax_form.cuh)
@@ -420,10 +418,10 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < kMmaN; c += 128) {
-                        float v[128];
-                        tmem_ld128(lane_addr + acc * kMmaN + static_cast<uint32_t>(c), v);
-                        const int col = n * kMmaN + c;  // output feature of v[0]
-                        if (MODE == kProjScore) {
+                        const int col = n * kMmaN + c;  // output feature of the chunk's first column
+                        if constexpr (MODE == kProjScore) {
+                            float v[128];
+                            tmem_ld128(lane_addr + acc * kMmaN + static_cast<uint32_t>(c), v);
                             const float4* q4 = reinterpret_cast<const float4*>(qs + col);
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
@@ -438,31 +436,28 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                                 nrm = fmaf(v[4 * j + 3], v[4 * j + 3], nrm);
                             }
                         } else {
-                            // 4 boxes of 32 rows x 32 columns through this warp's two
-                            // staging buffers (128-byte swizzle: 16-byte chunk j of row
-                            // r sits at chunk j ^ (r & 7), so the lanes' stores hit
-                            // distinct banks), each written out by one TMA store
+                            // the warp's 32 lanes as two halves of 16 read with the
+                            // .16x256b shape: a quad of threads holds 8 consecutive
+                            // columns of a row, so every store instruction writes
+                            // whole 32-byte segments of 8 rows straight from registers
+#pragma unroll 1
+                            for (int hh = 0; hh < 2; ++hh) {
+                                float v[64];
+                                tmem_ld_16x256b_x16(lane_addr + (static_cast<uint32_t>(16 * hh) << 16) +
+                                                        acc * kMmaN + static_cast<uint32_t>(c),
+                                                    v);
+                                const long long r0 = item * kTileM + 32 * (warp & 3) + 16 * hh + (lane >> 2);
+                                float* p0 = a.out + r0 * D + col + 2 * (lane & 3);
+                                float* p1 = p0 + 8ll * D;  // row r0 + 8
+                                const bool in0 = r0 < a.rows, in1 = r0 + 8 < a.rows;
 #pragma unroll
-                            for (int bx = 0; bx < 4; ++bx, ++nbox) {
-                                const uint32_t buf = nbox & 1u;
-                                if (nbox >= 2) {
-                                    if (lane == 0) bulk_wait_read1();  // this buffer's last store has read it
-                                    __syncwarp();
-                                }
-                                unsigned char* box = stage_out + buf * kOutBoxBytes + lane * 128;
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    const int e = 32 * bx + 4 * j;
-                                    *reinterpret_cast<float4*>(box + ((j ^ (lane & 7)) << 4)) =
-                                        ok ? make_float4(v[e], v[e + 1], v[e + 2], v[e + 3])
-                                           : make_float4(NAN, NAN, NAN, NAN);
-                                }
-                                fence_proxy_async();
-                                __syncwarp();
-                                if (lane == 0) {
-                                    tma_store_2d(&tmP, stage_out_s + buf * kOutBoxBytes, col + 32 * bx,
-                                                 static_cast<int>(item * kTileM + 32 * (warp & 3)));
-                                    bulk_commit();
+                                for (int i = 0; i < 16; ++i) {
+                                    if (in0 && CS_IN_BOUNDS(p0 + 8 * i, 8, a.out, a.rows * D * 4ll, kSiteProjRows))
+                                        *reinterpret_cast<float2*>(p0 + 8 * i) =
+                                            ok ? make_float2(v[4 * i], v[4 * i + 1]) : make_float2(NAN, NAN);
+                                    if (in1 && CS_IN_BOUNDS(p1 + 8 * i, 8, a.out, a.rows * D * 4ll, kSiteProjRows))
+                                        *reinterpret_cast<float2*>(p1 + 8 * i) =
+                                            ok ? make_float2(v[4 * i + 2], v[4 * i + 3]) : make_float2(NAN, NAN);
                                 }
                             }
                         }
@@ -511,7 +506,6 @@ __global__ void __launch_bounds__(kProjThreads, 1)
                 }
             }
         }
-        if (MODE == kProjPlain && lane == 0) bulk_wait_all();  // stores done before shared memory goes away
         __syncwarp();
     }
 
@@ -542,7 +536,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // Tensor map of a row-major matrix [rows][cols] with boxes of box_rows x
 // box_cols elements and 128-byte swizzle (box_cols x element size = 128
-// bytes); loads read rows past the end as zero, stores skip them.
+// bytes); loads read rows past the end as zero.
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, int elem_bytes, const void* ptr, unsigned long long rows,
               unsigned long long cols, int box_cols, int box_rows) {
     auto fn = encode_fn();
@@ -577,9 +571,8 @@ cudaError_t configure_proj_kernels(int smem_optin) {
 
 cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long rows, int Din, int D, float* P,
                                 int sms, unsigned* status, unsigned* bounds, cudaStream_t stream) {
-    CUtensorMap ma, mw, mp;
-    if (!make_bf16_map(&ma, H, rows, Din, kTileM) || !make_bf16_map(&mw, W, D, Din, kMmaN) ||
-        !make_map(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, P, rows, D, kOutBox, kOutBox))
+    CUtensorMap ma, mw;
+    if (!make_bf16_map(&ma, H, rows, Din, kTileM) || !make_bf16_map(&mw, W, D, Din, kMmaN))
         return cudaErrorInvalidValue;
     ProjArgs a{};
     a.rows = rows;
@@ -590,7 +583,7 @@ cudaError_t launch_project_rows(const uint16_t* H, const uint16_t* W, long long 
     a.bounds = bounds;
     const long long tiles = (rows + kTileM - 1) / kTileM;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    proj_kernel<kProjPlain><<<grid, kProjThreads, proj_layout(D, kProjPlain).total, stream>>>(ma, mw, mp, a);
+    proj_kernel<kProjPlain><<<grid, kProjThreads, proj_layout(D, kProjPlain).total, stream>>>(ma, mw, a);
     return cudaGetLastError();
 }
 
@@ -615,8 +608,7 @@ cudaError_t launch_project_score(const uint16_t* Hc, const uint16_t* Wc, const f
     a.status = status;
     a.bounds = bounds;
     const unsigned grid = static_cast<unsigned>(B < sms ? B : sms);
-    // the scoring kernel stores no rows: its output map is never used
-    proj_kernel<kProjScore><<<grid, kProjThreads, proj_layout(D, kProjScore).total, stream>>>(ma, mw, ma, a);
+    proj_kernel<kProjScore><<<grid, kProjThreads, proj_layout(D, kProjScore).total, stream>>>(ma, mw, a);
     return cudaGetLastError();
 }
 
