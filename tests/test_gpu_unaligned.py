@@ -3,7 +3,8 @@
 
 Such rows stream through the same bulk-copy ring as aligned ones, each copy
 widened to the 16-byte granules around them (unaligned plans); the kernel
-reads them as scalars from where they landed. The page's float4 rules
+reads them in 4-byte units (float32 elements, bfloat16 pairs) from where
+they landed, and a few questions take the DIRECT kernel's unit form. The page's float4 rules
 ("weighted RMS with float4 loads", on the page set's RMS-norm page) say
 when 16-byte accesses are allowed; here they decide only the copy's span,
 not the path. Each case is compared with the fp64 oracle (1e-4 per
@@ -99,7 +100,7 @@ def test_unaligned_bf16(cuda_lib, normalize):
 
 # D either side of the unit-wise form's sizes (4, 8 or 16 four-byte units a
 # lane; float32 units are elements, bfloat16 units element pairs, an odd D's
-# last element added apart) and past its last one (the scalar form).
+# last element added apart) and past its last one (q from shared memory).
 UNIT_EDGES = {"f32": [1, 2, 127, 128, 129, 255, 256, 257, 511, 512, 513],
               "bf16": [1, 2, 3, 255, 256, 257, 258, 511, 512, 513, 1023, 1024, 1025, 1026]}
 
