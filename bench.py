@@ -395,6 +395,8 @@ def main():
                     help="profiling aid: W + K calls of one unaligned-row case (cosine, 4096 questions)")
     ap.add_argument("--only-unaligned-dtype", choices=["f32", "bf16"], default="f32",
                     help="candidate type of --only-unaligned-case")
+    ap.add_argument("--only-unaligned-plan", choices=["auto", "generic"], default="auto",
+                    help="plan of --only-unaligned-case (generic: the scalar plan forced, float32)")
     ap.add_argument("--only-unaligned-b1", action="store_true",
                     help="profiling aid: time only one-question calls on unaligned rows and print their record")
     ap.add_argument("--only-projected", type=int, default=0, metavar="B",
@@ -436,7 +438,7 @@ def main():
     if args.only_unaligned_case:
         if rank == 0:
             print(json.dumps(unaligned_rows(cs, dev, args.steps, args.warmup, only=args.only_unaligned_case,
-                                            only_dtype=args.only_unaligned_dtype)),
+                                            only_dtype=args.only_unaligned_dtype, only_plan=args.only_unaligned_plan)),
                   flush=True)
         return 0
     if args.only_unaligned:
@@ -667,7 +669,7 @@ UNALIGNED_CASES = (("aligned_d512", 512, 0, 4096, None), ("odd_d510", 510, 0, 40
                    ("misaligned_d2560", 2560, 1, 1024, "aligned_d2560"))
 
 
-def unaligned_rows(cs, dev, steps, warmup, only=None, only_dtype="f32"):
+def unaligned_rows(cs, dev, steps, warmup, only=None, only_dtype="f32", only_plan="auto"):
     """Rows the bulk copies cannot take whole, at throughput size: 4096
     questions of K=255 with D=510 (rows of 2040 bytes), and with D=512 but
     Q and C one element past a 16-byte boundary, each against the aligned
@@ -675,8 +677,9 @@ def unaligned_rows(cs, dev, steps, warmup, only=None, only_dtype="f32"):
     element off, against aligned D=2560. Float32 cases also against the
     scalar plan forced on the same rows; float32 and bfloat16 candidates.
     One launch per call over at least 2.1 GB (larger than L2). only: time
-    just that case's cosine readout with only_dtype candidates (a profiling
-    aid)."""
+    just that case's cosine readout with only_dtype candidates and the
+    automatic plan, or with only_plan "generic" the scalar plan forced
+    (float32; profiling aids)."""
     import torch
     n_c = max(B * K * d for _, d, _, B, _ in UNALIGNED_CASES) + 64
     n_q = max(B * d for _, d, _, B, _ in UNALIGNED_CASES) + 64
@@ -695,10 +698,17 @@ def unaligned_rows(cs, dev, steps, warmup, only=None, only_dtype="f32"):
         flat = flatC[:B * K * d + 64].to(torch.bfloat16) if bf else flatC
         C = flat[off:off + B * K * d].view(B, K, d)
         score = cs.cs_score_candidates_batch_bf16 if bf else cs.cs_score_candidates_batch
+        if only_plan == "generic":
+            if bf:
+                raise SystemExit("--only-unaligned-plan generic takes float32 candidates")
+
+            def score(Q, C, normalize, scale, T, out, stream):
+                return cs.cs_score_candidates_batch_plan(Q, C, normalize, scale, T, cs.CS_PLAN_GENERIC, 1, 0,
+                                                         out=out, stream=stream)
         for _ in range(warmup + steps):
             score(Q, C, 1, 14.285714, 1.0, out=out, stream=s)
         torch.cuda.synchronize()
-        return {"case": only, "dtype": only_dtype, "calls": warmup + steps,
+        return {"case": only, "dtype": only_dtype, "plan_forced": only_plan, "calls": warmup + steps,
                 "plan": None if bf else cs.cs_query_plan(Q, C, 1)}
 
     def timed(fn):
